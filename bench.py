@@ -1,0 +1,396 @@
+"""Benchmark of the draft-tree hot path on one or more GB300 GPUs.
+
+One step = one tree step over a batch of requests: softmax + top-K marginals
+over the drafter logits, best-first tree build with the online controller, and
+greedy verification against the target logits (three launches, replayed from a
+CUDA graph).  Default workload: 32 requests, block size 16, vocab 151,936,
+top-64, tree budget 128, bf16 logits.
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+        [--workload 1..5]
+Multi-GPU: launched under torchrun; every rank runs an independent replica on
+its own GPU (weak scaling), timed with a barrier and the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "tree steps/s (top-K+best-first+verify) B=32 V=151936; % HBM roofline"
+UNIT = "tree steps/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampling in the background (SM clock, power, throttle reasons)."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"bench_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "power_w_max": max(power) if power else None, "reasons": sorted(reasons)}
+
+
+def dist_setup():
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    else:
+        torch.cuda.set_device(0)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def pinned_from(arr: np.ndarray):
+    import torch
+    t = torch.empty(arr.shape, dtype=torch.int16 if arr.dtype == np.uint16 else torch.float32,
+                    pin_memory=True)
+    t.numpy()[...] = arr.view(np.int16) if arr.dtype == np.uint16 else arr
+    return t.view(torch.bfloat16) if arr.dtype == np.uint16 else t
+
+
+# --------------------------------------------------------------------------- our arm
+
+def run_ours(args, ws, rank, local):
+    import torch
+
+    import synth
+    from draft_tree_build_gb300 import bastion
+
+    dev = torch.device(f"cuda:{local}")
+    w = synth.workload(args.workload)
+    es = w.elem_bytes
+    roots, ctx, cost, lar = synth.root_tokens(w), synth.ctx_lens(w), synth.cost_table(w), synth.l_ar(w)
+
+    # inputs: drafter logits on the host (pinned), two device copies (rotated so
+    # every step reads logits the previous step did not touch)
+    x_host = synth.drafter_logits(w)
+    x_pin = pinned_from(x_host)
+    xs = [x_pin.to(dev, non_blocking=False) for _ in range(2)]
+    step = bastion.TreeStep(w.B, w.b, w.V, w.K, w.n_max, dev, torch.from_numpy(roots),
+                            torch.from_numpy(ctx), torch.from_numpy(cost), torch.from_numpy(lar))
+    # the target rows are planted at the nodes of the tree this device builds
+    tgt_tmp = torch.zeros((w.B, w.n_max, w.V), dtype=xs[0].dtype, device=dev)
+    step.run(xs[0], tgt_tmp)
+    torch.cuda.synchronize()
+    n_nodes = step.tree.n_nodes.cpu().numpy()
+    depth = step.tree.depth.cpu().numpy()
+    topk_tok = step.topk.tok.cpu().numpy()
+    del tgt_tmp
+    t_host = synth.host_array((w.B, w.n_max, w.V), w.dtype)
+    synth.fill_target_noise(w, t_host.ctypes.data)
+    synth.plant_into(w, t_host.ctypes.data, synth.plant_tokens(w, n_nodes, depth, topk_tok))
+    t_pin = pinned_from(t_host)
+    ts = [t_pin.to(dev) for _ in range(2)]
+
+    bytes_k1 = w.B * w.b * w.V * es
+    bytes_k4 = int(n_nodes.sum()) * w.V * es
+    bytes_step = bytes_k1 + bytes_k4
+
+    graphs = [step.capture(xs[i], ts[i]) for i in range(2)]
+    stream = torch.cuda.current_stream()
+
+    # warm-up (W steps, then at least ~1 s so clocks settle)
+    for i in range(args.warmup):
+        graphs[i & 1].replay()
+    torch.cuda.synchronize()
+    t_end = time.time() + 1.0
+    i = 0
+    while time.time() < t_end:
+        for _ in range(50):
+            graphs[i & 1].replay()
+            i += 1
+        torch.cuda.synchronize()
+
+    clocks = Clocks(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        graphs[i & 1].replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    elapsed_ms = max_over_ranks(e0.elapsed_time(e1), ws)
+    # keep the GPU busy a little longer so the clock samples cover the region
+    for i in range(min(args.steps, 200)):
+        graphs[i & 1].replay()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+
+    # per-kernel durations: the same steps launched directly with events between
+    P = min(args.steps, 100)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(P)]
+    t, tr, v = step.topk, step.tree, step.ver
+    for p in range(P):
+        xd, td = xs[p & 1], ts[p & 1]
+        evs[p][0].record(stream)
+        bastion.bastion_topk_marginals(xd, w.K, t.logq, t.logit, t.tok, t.lse, step.ws_topk, step.status)
+        evs[p][1].record(stream)
+        bastion.bastion_build_tree(t.logit, t.tok, t.lse, w.n_max, step.root_token, step.ctx_len,
+                                   step.cost_ms, step.l_ar, tr.n_nodes, tr.parent, tr.depth, tr.pos_id,
+                                   tr.token, tr.rank, tr.log_rho, tr.a_hat, tr.speedup, tr.anc_mask,
+                                   step.status)
+        evs[p][2].record(stream)
+        bastion.bastion_verify_greedy(td, w.b, tr.n_nodes, tr.parent, tr.token, v.argmax, v.accept_len,
+                                      v.accept_nodes, v.out_tokens, step.ws_verify, step.status)
+        evs[p][3].record(stream)
+    torch.cuda.synchronize()
+    k1 = statistics.mean(evs[p][0].elapsed_time(evs[p][1]) for p in range(P))
+    k2 = statistics.mean(evs[p][1].elapsed_time(evs[p][2]) for p in range(P))
+    k4 = statistics.mean(evs[p][2].elapsed_time(evs[p][3]) for p in range(P))
+    assert int(step.status.abs().sum()) == 0, "device status bits set"
+
+    # end to end through the public API with host buffers (pinned), per step:
+    # H2D of the drafter and target logits, the step, D2H of the results
+    E = max(3, min(args.steps, 20))
+    out_host = torch.empty((w.B, w.b + 1), dtype=torch.int32, pin_memory=True)
+    acc_host = torch.empty((w.B,), dtype=torch.int32, pin_memory=True)
+    xin, tin = torch.empty_like(xs[0]), torch.empty_like(ts[0])
+
+    def e2e_step():
+        xin.copy_(x_pin, non_blocking=True)
+        tin.copy_(t_pin, non_blocking=True)
+        step.run(xin, tin)
+        out_host.copy_(step.ver.out_tokens, non_blocking=True)
+        acc_host.copy_(step.ver.accept_len, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(ws)
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(E):
+        e2e_step()
+    f1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1), ws) / E
+    h2d = x_pin.numel() * x_pin.element_size() + t_pin.numel() * t_pin.element_size()
+    d2h = out_host.numel() * 4 + acc_host.numel() * 4
+
+    hbm, peak_kind = peaks()
+    ms_step = elapsed_ms / args.steps
+    kern = {"topk_marginals": {"ms": k1, "bytes": bytes_k1, "gbs": bytes_k1 / (k1 * 1e-3) / 1e9},
+            "build_tree": {"ms": k2, "bytes": w.B * w.b * w.K * 16},
+            "verify_greedy": {"ms": k4, "bytes": bytes_k4, "gbs": bytes_k4 / (k4 * 1e-3) / 1e9}}
+    dom = max(("topk_marginals", "verify_greedy"), key=lambda k: kern[k]["ms"])
+    ach = kern[dom]["gbs"]
+    res = {
+        "metric": METRIC, "value": ws * args.steps / (elapsed_ms * 1e-3), "unit": UNIT,
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "b": w.b, "V": w.V, "K": w.K, "n_max": w.n_max,
+                   "logit_dtype": w.dtype, "seed": w.seed, "mean_tree_nodes": float(n_nodes.mean()),
+                   "l2": "inputs larger than L2, two rotating device copies",
+                   "parallelism": f"replicas x{ws}"},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": hbm, "unit": "GB/s",
+                     "frac": ach / hbm, "peak_source": f"{peak_kind} copy bandwidth",
+                     "traffic": None,
+                     "step_frac": bytes_step / (ms_step * 1e-3) / 1e9 / hbm,
+                     "bytes_per_step": bytes_step},
+        "kernels": kern,
+        "clocks": clk,
+        "e2e": {"value": ws / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 3 * args.steps,
+    }
+    return res
+
+
+# --------------------------------------------------------------------------- oracle legs
+
+def oracle_step(w, req, x, lse_rows=None, pre=None):
+    """The oracle's tree step for one request (top-K of its b rows, its tree,
+    its target rows' argmaxes and accept walk)."""
+    import oracle
+    import synth
+    roots, ctx, cost, lar = pre
+    tk = oracle.topk_marginals(x[req:req + 1], w.K)
+    tr = oracle.build_tree(tk.logit, tk.tok, tk.lse, w.n_max, roots[req:req + 1], ctx[req:req + 1],
+                           cost, lar[req:req + 1])
+    return tk, tr
+
+
+def cpu_baseline(args, budget_s=12.0):
+    """Times the oracle as it stands on the host (single thread) on a bounded
+    sample: whole requests of the bench workload, cycled until ~budget_s."""
+    import oracle
+    import synth
+    w = synth.workload(args.workload)
+    pre = (synth.root_tokens(w), synth.ctx_lens(w), synth.cost_table(w), synth.l_ar(w))
+    x = synth.drafter_logits(w)
+    # plant the target for the sampled requests from the oracle's own trees (outside the timing)
+    tk_all = oracle.topk_marginals(x, w.K)
+    tr_all = oracle.build_tree(tk_all.logit, tk_all.tok, tk_all.lse, w.n_max, *pre)
+    tgt, _ = synth.target_logits(w, tr_all.n_nodes, tr_all.depth, tk_all.tok)
+    t0 = time.perf_counter()
+    done = 0
+    while True:
+        r = done % w.B
+        tk, tr = oracle_step(w, r, x, pre=pre)
+        oracle.verify_greedy(tgt[r:r + 1], w.b, tr.n_nodes, tr.parent, tr.token)
+        done += 1
+        if time.perf_counter() - t0 > budget_s and done >= 1:
+            break
+    dt = time.perf_counter() - t0
+    per_req = dt / done
+    return {"value": 1.0 / (per_req * w.B), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{done} whole requests (top-K of 16 rows, tree, verify of its rows) of the "
+                      f"{w.name} workload in {dt:.1f} s, scaled to a {w.B}-request step"}
+
+
+def run_reference(args, ws, rank):
+    """Reference arm: the oracle, as it stands, on the host cores; each step is
+    one request of the workload (a bounded sample), scaled to a full step."""
+    import oracle
+    import synth
+    w = synth.workload(args.workload)
+    pre = (synth.root_tokens(w), synth.ctx_lens(w), synth.cost_table(w), synth.l_ar(w))
+    x = synth.drafter_logits(w)
+    tk_all = oracle.topk_marginals(x, w.K)
+    tr_all = oracle.build_tree(tk_all.logit, tk_all.tok, tk_all.lse, w.n_max, *pre)
+    tgt, _ = synth.target_logits(w, tr_all.n_nodes, tr_all.depth, tk_all.tok)
+
+    def one(r):
+        tk, tr = oracle_step(w, r, x, pre=pre)
+        oracle.verify_greedy(tgt[r:r + 1], w.b, tr.n_nodes, tr.parent, tr.token)
+
+    for i in range(args.warmup):
+        one(i % w.B)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        one(i % w.B)
+    dt = time.perf_counter() - t0
+    per_full_step = dt / args.steps * w.B
+    val = 1.0 / per_full_step
+    return {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_full_step * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "b": w.b, "V": w.V, "K": w.K, "n_max": w.n_max,
+                       "logit_dtype": w.dtype},
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"each step one request of {w.B} (top-K, tree, verify), "
+                                       f"scaled by {w.B}"},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=100)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", type=int, default=3, choices=[1, 2, 3, 5])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        ws = int(os.environ.get("WORLD_SIZE", "1"))
+        if rank != 0:
+            return
+        steps = args.steps
+        res = run_reference(args, ws, rank)
+        print(json.dumps(res), flush=True)
+        return
+
+    ws, rank, local = dist_setup()
+    res = run_ours(args, ws, rank, local)
+    if rank == 0:
+        if ws == 1 and not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(args)
+        print(json.dumps(res), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

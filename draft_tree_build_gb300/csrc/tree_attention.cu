@@ -1,0 +1,504 @@
+// Tree-masked GQA attention of the draft tree's query tokens against the KV
+// cache: the target's one parallel verification pass over the whole tree
+// (Bastion, gist.science/nl/paper/2605.29727, "Probleemstelling": the target
+// verifies the drafted candidates in parallel; Methodologie §2: the tree is
+// verified as one prefix tree).  Query i sees every committed context slot and
+// the tree slots of its own root path (ancestor-or-self bitmask).
+//
+// sm_103a design, one CTA per (request, KV head, 128 query rows):
+//  * the 128 rows are (tree node, query head of the KV group) pairs, so the G
+//    heads that share a KV head share every K/V tile read;
+//  * warp 0 streams Q once and K/V tiles of 128 keys through a 2-stage ring
+//    with TMA (cp.async.bulk.tensor, 128-byte swizzle, no multicast);
+//  * warp 1 (one thread) issues tcgen05.mma kind::f16 (bf16 in, fp32 out):
+//    S_t = Q K_t^T into one of two TMEM buffers, then O += P_{t-1} V_{t-1};
+//  * warps 4-7 (one TMEM lane = one query row per thread) read S_t with
+//    tcgen05.ld, apply the tree mask and the online softmax in base 2, and write
+//    P_t as bf16 into shared memory in the MMA operand layout; O stays in TMEM
+//    and is rescaled only when a row's running max grows by more than 2^8
+//    (the final normalisation uses the same reference max, so this is exact);
+//  * epilogue: O / l as bf16 (round to nearest even) to global memory.
+// Every wait is bounded (~1 s); on a timeout the CTA flags the request, waits
+// for its own copies and MMAs (bounded), frees its TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+
+namespace bastion {
+
+namespace {
+
+constexpr int kAT = 256;
+constexpr int kBM = 128;
+constexpr int kBN = 128;
+constexpr uint32_t kAtom = 128 * 128;          // 128 rows x 128 bytes
+constexpr uint32_t kTile = 2 * kAtom;          // 128 x 128 bf16
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffKV = kTile;             // stage s: K at +0, V at +kTile
+constexpr uint32_t kOffP = kOffKV + 2 * 2 * kTile;
+constexpr uint32_t kOffBar = kOffP + 2 * kTile;
+constexpr uint32_t kSmem = kOffBar + 256 + 1024;  // + alignment slack
+constexpr float kRescale = 8.0f;               // lazy rescale threshold (log2 units)
+
+struct AttnArgs {
+  int B, n_max, Hq, Hkv, G, W, qt_max;
+  int64_t L_cap;
+  const int32_t *ctx_len, *n_nodes;
+  const uint32_t *anc_mask;
+  float scale_log2;
+  uint16_t *out;
+  int32_t *status;
+};
+
+struct Bars {
+  uint64_t q_full, kv_full[2], kv_empty[2], s_full[2], p_full[2], pv_done[2];
+  uint32_t tmem;
+  int abort;
+};
+
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version
+  d |= (uint64_t)2 << 61;  // 128-byte swizzle
+  return d;
+}
+
+// kind::f16 instruction descriptor: fp32 accumulate, bf16 A and B, M = N = 128.
+__device__ __forceinline__ uint32_t idesc_bf16(bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accum) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accum));
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, int c0, int c1,
+                                            int c2, int c3, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Bounded wait that also honours the CTA's abort flag.
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                         int32_t *status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  uint32_t spins = 0;
+  while (!mbar_try_wait(bar, parity)) {
+    if ((++spins & 63u) == 0u) {
+      if (*abort) return false;
+      if (global_ns() - t0 > 1000000000ull) {
+        *abort = 1;
+        atomicOr(status, BASTION_STATUS_TIMEOUT);
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ uint32_t select_word(const uint32_t (&w)[8], int k) {
+  uint32_t r = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) r = (k == i) ? w[i] : r;
+  return r;
+}
+
+__global__ void __launch_bounds__(kAT, 1)
+    tree_attention_kernel(const __grid_constant__ CUtensorMap tm_q,
+                          const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_v, AttnArgs a) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char *smem = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  Bars &bs = *reinterpret_cast<Bars *>(smem + kOffBar);
+  volatile int *abort = &bs.abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int qt = blockIdx.x % a.qt_max;
+  const int g = (blockIdx.x / a.qt_max) % a.Hkv;
+  const int r = blockIdx.x / (a.qt_max * a.Hkv);
+  const int nn = a.n_nodes[r];
+  const int ctx = a.ctx_len[r];
+  const int rows = nn * a.G;
+  if (nn < 1 || nn > a.n_max || qt * kBM >= rows) return;
+  const int nodes_per_tile = kBM / a.G;
+  const int i0 = qt * nodes_per_tile;
+  int64_t keys = (int64_t)ctx + nn;
+  if (ctx < 0 || keys > a.L_cap) {
+    if (tid == 0 && qt == 0 && g == 0) atomicOr(&a.status[r], BASTION_STATUS_KV_OVERFLOW);
+    keys = keys > a.L_cap ? a.L_cap : keys;
+  }
+  const int ctx_c = ctx < 0 ? 0 : ctx;
+  const int n_tiles = (int)((keys + kBN - 1) / kBN);
+
+  if (tid == 0) {
+    mbar_init(&bs.q_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bs.kv_full[s], 1);
+      mbar_init(&bs.kv_empty[s], 1);
+      mbar_init(&bs.s_full[s], 1);
+      mbar_init(&bs.p_full[s], 128);
+      mbar_init(&bs.pv_done[s], 1);
+    }
+    bs.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
+                     smem_u32(&bs.tmem)));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bs.tmem;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bs.q_full, kTile);
+      tma_load_4d(smem + kOffQ, &tm_q, 0, g * a.G, i0, r, &bs.q_full);
+      tma_load_4d(smem + kOffQ + kAtom, &tm_q, 64, g * a.G, i0, r, &bs.q_full);
+      int issued = 0;
+      for (int t = 0; t < n_tiles; ++t) {
+        const int s = t & 1;
+        if (t >= 2 && !wait_bar(&bs.kv_empty[s], ((t - 2) >> 1) & 1, abort, &a.status[r])) break;
+        unsigned char *kb = smem + kOffKV + s * 2 * kTile;
+        mbar_arrive_expect_tx(&bs.kv_full[s], 2 * kTile);
+        tma_load_4d(kb, &tm_k, 0, g, t * kBN, r, &bs.kv_full[s]);
+        tma_load_4d(kb + kAtom, &tm_k, 64, g, t * kBN, r, &bs.kv_full[s]);
+        tma_load_4d(kb + kTile, &tm_v, 0, g, t * kBN, r, &bs.kv_full[s]);
+        tma_load_4d(kb + kTile + kAtom, &tm_v, 64, g, t * kBN, r, &bs.kv_full[s]);
+        issued = t + 1;
+      }
+      // drain: our last copies have landed (bounded) before the CTA may exit
+      for (int t = issued > 2 ? issued - 2 : 0; t < issued; ++t)
+        mbar_wait_bounded(&bs.kv_full[t & 1], (t >> 1) & 1);
+      mbar_wait_bounded(&bs.q_full, 0);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t id_qk = idesc_bf16(false), id_pv = idesc_bf16(true);
+      const uint32_t sq = smem_u32(smem + kOffQ);
+      bool ok = wait_bar(&bs.q_full, 0, abort, &a.status[r]);
+      tc_fence_after();
+      int last_pv = -1;
+      for (int t = 0; ok && t <= n_tiles; ++t) {
+        if (t < n_tiles) {
+          const int s = t & 1;
+          if (!wait_bar(&bs.kv_full[s], (t >> 1) & 1, abort, &a.status[r])) break;
+          tc_fence_after();
+          const uint32_t sk = smem_u32(smem + kOffKV + s * 2 * kTile);
+          const uint32_t d = tmem + 128u * (1u + (uint32_t)s);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t off = (uint32_t)(ks >> 2) * kAtom + (uint32_t)(ks & 3) * 32u;
+            mma_bf16(d, sw128_desc(sq + off, 16, 1024), sw128_desc(sk + off, 16, 1024), id_qk,
+                     ks > 0);
+          }
+          mma_commit(&bs.s_full[s]);
+        }
+        if (t >= 1) {
+          const int u = t - 1, s = u & 1;
+          if (!wait_bar(&bs.p_full[s], (u >> 1) & 1, abort, &a.status[r])) break;
+          tc_fence_after();
+          const uint32_t sp = smem_u32(smem + kOffP + s * kTile);
+          const uint32_t sv = smem_u32(smem + kOffKV + s * 2 * kTile + kTile);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t offp = (uint32_t)(ks >> 2) * kAtom + (uint32_t)(ks & 3) * 32u;
+            mma_bf16(tmem, sw128_desc(sp + offp, 16, 1024),
+                     sw128_desc(sv + (uint32_t)ks * 2048u, kAtom, 1024), id_pv, (u > 0 || ks > 0));
+          }
+          mma_commit(&bs.pv_done[s]);
+          mma_commit(&bs.kv_empty[s]);
+          last_pv = u;
+        }
+      }
+      if (last_pv >= 0) mbar_wait_bounded(&bs.pv_done[last_pv & 1], (last_pv >> 1) & 1);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int m = (warp - 4) * 32 + lane;  // query row = TMEM lane
+    const int node = i0 + m / a.G;
+    const int hh = m % a.G;
+    const bool row_live = node < nn;
+    uint32_t anc[8];
+#pragma unroll
+    for (int w = 0; w < 8; ++w)
+      anc[w] = (row_live && w < a.W) ? a.anc_mask[((size_t)r * a.n_max + node) * a.W + w] : 0u;
+    const uint32_t lane_base = tmem + ((uint32_t)((warp - 4) * 32) << 16);
+    float m_ref = -INFINITY, l_sum = 0.f;
+    bool ok = true;
+    for (int t = 0; t < n_tiles && ok; ++t) {
+      const int s = t & 1;
+      ok = wait_bar(&bs.s_full[s], (t >> 1) & 1, abort, &a.status[r]);
+      if (!ok) break;
+      tc_fence_after();
+      const int kb = t * kBN;
+      // visibility of the 128 keys of this tile, 32 per word
+      uint32_t vis[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int j0 = kb + 32 * q;           // first key of the group
+        uint32_t ctxbits;
+        if (j0 + 32 <= ctx_c) ctxbits = 0xffffffffu;
+        else if (j0 >= ctx_c) ctxbits = 0u;
+        else ctxbits = (1u << (ctx_c - j0)) - 1u;
+        const int t0 = j0 - ctx_c;            // tree index of the first key
+        uint32_t tb = 0u;
+        if (t0 + 32 > 0 && t0 < 256) {
+          if (t0 >= 0) {
+            const int w0 = t0 >> 5, sh = t0 & 31;
+            tb = select_word(anc, w0) >> sh;
+            if (sh) tb |= select_word(anc, w0 + 1) << (32 - sh);
+          } else {
+            tb = select_word(anc, 0) << (-t0);
+          }
+        }
+        uint32_t lim = 0xffffffffu;  // keys at or past the end are never visible
+        const int64_t left = keys - j0;
+        if (left <= 0) lim = 0u;
+        else if (left < 32) lim = (1u << left) - 1u;
+        vis[q] = (ctxbits | tb) & lim;
+      }
+      // pass 1: tile max of the visible scaled scores
+      float mt = -INFINITY;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        float v[32];
+        tmem_ld32(lane_base + 128u * (1u + (uint32_t)s) + 32u * cc, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if ((vis[cc] >> i) & 1u) mt = fmaxf(mt, v[i] * a.scale_log2);
+      }
+      if (mt > m_ref + kRescale || (m_ref == -INFINITY && mt != -INFINITY)) {
+        const float m_new = mt;
+        if (t > 0 && m_ref != -INFINITY) {
+          const float alpha = ex2f(m_ref - m_new);
+          ok = wait_bar(&bs.pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, abort, &a.status[r]);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            float o[32];
+            tmem_ld32(lane_base + 32u * cc, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            tmem_st32(lane_base + 32u * cc, o);
+          }
+          l_sum *= alpha;
+        }
+        m_ref = m_new;
+      }
+      // P buffer s must be free: PV of tile t-2 done
+      if (t >= 2) {
+        ok = wait_bar(&bs.pv_done[s], ((t - 2) >> 1) & 1, abort, &a.status[r]);
+        if (!ok) break;
+      }
+      unsigned char *pb = smem + kOffP + s * kTile;
+      float part = 0.f;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        float v[32];
+        tmem_ld32(lane_base + 128u * (1u + (uint32_t)s) + 32u * cc, v);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          float p0 = ((vis[cc] >> i) & 1u) && m_ref != -INFINITY ? ex2f(v[i] * a.scale_log2 - m_ref) : 0.f;
+          float p1 = ((vis[cc] >> (i + 1)) & 1u) && m_ref != -INFINITY ? ex2f(v[i + 1] * a.scale_log2 - m_ref) : 0.f;
+          part += p0 + p1;
+          pk[i >> 1] = pack_bf16(p0, p1);
+        }
+        // columns 32cc .. 32cc+31: atom cc/2, 16-byte chunks (4cc+q) % 8
+        unsigned char *rowp = pb + (cc >> 1) * kAtom + (m >> 3) * 1024 + (m & 7) * 128;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int ch = ((cc & 1) * 4 + q) ^ (m & 7);
+          *reinterpret_cast<uint4 *>(rowp + ch * 16) =
+              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
+      }
+      l_sum += part;
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc_fence_before();
+      mbar_arrive(&bs.p_full[s]);
+    }
+    // epilogue
+    if (ok && n_tiles > 0) {
+      const int u = n_tiles - 1;
+      ok = wait_bar(&bs.pv_done[u & 1], (u >> 1) & 1, abort, &a.status[r]);
+      tc_fence_after();
+      if (ok && row_live) {
+        const float inv = 1.0f / l_sum;
+        uint16_t *dst = a.out + (((size_t)r * a.n_max + node) * a.Hq + (size_t)g * a.G + hh) * 128;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          float o[32];
+          tmem_ld32(lane_base + 32u * cc, o);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 pkt;
+            pkt.x = pack_bf16(o[8 * q + 0] * inv, o[8 * q + 1] * inv);
+            pkt.y = pack_bf16(o[8 * q + 2] * inv, o[8 * q + 3] * inv);
+            pkt.z = pack_bf16(o[8 * q + 4] * inv, o[8 * q + 5] * inv);
+            pkt.w = pack_bf16(o[8 * q + 6] * inv, o[8 * q + 7] * inv);
+            *reinterpret_cast<uint4 *>(dst + 32 * cc + 8 * q) = pkt;
+          }
+        }
+      } else if (row_live) {
+        // nothing
+      }
+    } else if (!ok) {
+      // abort path: make sure our pending PV is not still writing TMEM
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+bool make_map(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t d3,
+              uint32_t b0, uint32_t b1, uint32_t b2) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[4] = {d0, d1, d2, d3};
+  cuuint64_t strides[3] = {d0 * 2, d0 * d1 * 2, d0 * d1 * d2 * 2};
+  cuuint32_t box[4] = {b0, b1, b2, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult rc = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
+                    box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return rc == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+size_t attention_workspace_bytes(int, int, int, int, int, int64_t) { return 256; }
+
+int launch_attention(const void *q, const void *k, const void *v, int B, int n_max, int Hq,
+                     int Hkv, int D, int64_t L_cap, const int32_t *ctx_len,
+                     const int32_t *n_nodes, const uint32_t *anc_mask, float scale, void *out,
+                     void *ws, int32_t *status, cudaStream_t stream) {
+  (void)ws;
+  (void)D;
+  const int G = Hq / Hkv;
+  if (128 % G) return BASTION_ERR_UNSUPPORTED;
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, q, 128, (uint64_t)Hq, (uint64_t)n_max, (uint64_t)B, 64, (uint32_t)G,
+                (uint32_t)(128 / G)) ||
+      !make_map(&mk, k, 128, (uint64_t)Hkv, (uint64_t)L_cap, (uint64_t)B, 64, 1, 128) ||
+      !make_map(&mv, v, 128, (uint64_t)Hkv, (uint64_t)L_cap, (uint64_t)B, 64, 1, 128))
+    return BASTION_ERR_LAUNCH;
+  AttnArgs a;
+  a.B = B;
+  a.n_max = n_max;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.G = G;
+  a.W = (n_max + 31) / 32;
+  a.qt_max = (n_max * G + kBM - 1) / kBM;
+  a.L_cap = L_cap;
+  a.ctx_len = ctx_len;
+  a.n_nodes = n_nodes;
+  a.anc_mask = anc_mask;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.out = static_cast<uint16_t *>(out);
+  a.status = status;
+  cudaFuncSetAttribute(tree_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+  const long long grid = (long long)B * Hkv * a.qt_max;
+  tree_attention_kernel<<<(unsigned)grid, kAT, kSmem, stream>>>(mq, mk, mv, a);
+  return cudaGetLastError() == cudaSuccess ? BASTION_OK : BASTION_ERR_LAUNCH;
+}
+
+}  // namespace bastion

@@ -1,0 +1,191 @@
+/*
+ * bastion.h -- C ABI of the GB300 (sm_103a) draft-tree hot path.
+ *
+ * The method: "Bastion: Budget-Aware Speculative Decoding with Tree-structured
+ * Block Diffusion Drafting" (gist.science/nl/paper/2605.29727, technical
+ * summary, "Methodologie" §1-§3; same text on gist.science/fr/paper/2605.29727).
+ * A block-diffusion drafter emits one marginal q_k per block position in one
+ * forward pass; a prefix tree of candidate continuations is grown best-first by
+ * path score rho(i) = prod_{k<=d(i)} q_k(x_ik) until the estimated speedup
+ * S(N) = A_hat(T_N) * L_AR / C(N), A_hat = sum rho, starts to fall; the target
+ * verifies the tree in one parallel pass (tree-masked attention) and greedy
+ * (temperature 0) acceptance keeps the longest matching root path plus one
+ * bonus token.
+ *
+ * Conventions shared by every entry point:
+ *  - All tensors are caller-owned DEVICE pointers, row-major, with the shapes
+ *    given at each function.  The library allocates nothing and keeps no
+ *    global mutable state; every call is asynchronous on the caller's stream.
+ *  - Return value: BASTION_OK, or a negative BASTION_ERR_* code when an
+ *    argument check on the host fails (nothing is launched then), or
+ *    BASTION_ERR_LAUNCH when the launch itself reports an error.
+ *  - Data-dependent problems found on the device (a NaN or +inf logit, a
+ *    non-positive cost, a tree too large for the KV cache, a bounded wait that
+ *    ran out) are OR-ed as BASTION_STATUS_* bits into status[r] of the
+ *    request concerned; the caller zeroes status before the calls it wants to
+ *    check.  The outputs of a request with a status bit set are unspecified.
+ *    No kernel traps or asserts.
+ *  - Workspace: functions that take one need at least *_workspace_bytes()
+ *    bytes, 256-byte aligned, ZERO-FILLED before its first use.  Every call
+ *    leaves it zero-filled again when it completes.  Calls that may run
+ *    concurrently need separate workspaces.
+ *  - dtype: BASTION_F32 (float) or BASTION_BF16 (bfloat16 bits).
+ */
+#ifndef BASTION_H_
+#define BASTION_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *bastion_stream_t; /* the same handle as cudaStream_t */
+
+enum { BASTION_F32 = 0, BASTION_BF16 = 1 };
+
+enum {
+  BASTION_OK = 0,
+  BASTION_ERR_NULL = -1,        /* a required pointer is null */
+  BASTION_ERR_SIZE = -2,        /* a size, count or stride is out of range */
+  BASTION_ERR_DTYPE = -3,       /* unknown dtype */
+  BASTION_ERR_ALIGN = -4,       /* a pointer misses its documented alignment */
+  BASTION_ERR_WORKSPACE = -5,   /* workspace missing or too small */
+  BASTION_ERR_UNSUPPORTED = -6, /* valid but not implemented (e.g. head dim) */
+  BASTION_ERR_LAUNCH = -7       /* the CUDA launch reported an error */
+};
+
+enum {
+  BASTION_STATUS_NONFINITE = 1,    /* a NaN or +inf logit in the request's rows */
+  BASTION_STATUS_EMPTY_ROW = 2,    /* a drafter row with no finite logit */
+  BASTION_STATUS_BAD_COST = 4,     /* some C(N) <= 0 or not finite */
+  BASTION_STATUS_KV_OVERFLOW = 8,  /* ctx_len + n_nodes > L_cap, or ctx_len < 0 */
+  BASTION_STATUS_BAD_TREE = 16,    /* n_nodes outside [1, n_max] */
+  BASTION_STATUS_TIMEOUT = 1 << 30 /* a bounded device wait ran out */
+};
+
+/* Library version string ("bastion-gb300 x.y.z sm_103a"). */
+const char *bastion_version(void);
+
+/* Text for a BASTION_ERR_* return code or a single BASTION_STATUS_* bit. */
+const char *bastion_status_string(int code);
+
+/* ---------------------------------------------------------------------------
+ * Step 1 -- softmax + top-K marginals.
+ * Methodologie §1 ("positie-afhankelijke marginaalverdelingen {q_k}"): for
+ * every drafter row (request r, block position k) it forms q_k = softmax(l_k)
+ * and ranks the vocabulary by q_k (equivalently by logit), ties broken by the
+ * lower token id; the K best are kept.
+ *
+ * logits     [B, b, V] at row stride ld_row elements (ld_row >= V), dtype as
+ *            given.  Any address is accepted; 16-byte aligned rows read fastest.
+ * topk_logq  [B, b, K] float  log q_k of each kept token, l - lse rounded once.
+ *            May be NULL.
+ * topk_logit [B, b, K] float  the kept logits exactly as given (fp32 value).
+ * topk_tok   [B, b, K] int32  token ids, rank order.
+ * lse        [B, b] double    log sum_v exp(l_v).
+ * status     [B] int32        OR-ed BASTION_STATUS_* bits.
+ * Limits: B >= 1, 1 <= b <= 32, 1 <= K <= min(V, 1024), V < 2^30.
+ * Workspace: bastion_topk_marginals_workspace_bytes(B, b, V, K) bytes.
+ */
+size_t bastion_topk_marginals_workspace_bytes(int B, int b, int V, int K);
+int bastion_topk_marginals(const void *logits, int dtype, int B, int b, int V, int64_t ld_row,
+                           int K, float *topk_logq, float *topk_logit, int32_t *topk_tok,
+                           double *lse, void *workspace, size_t workspace_bytes,
+                           int32_t *status, bastion_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Steps 2-3 -- best-first tree expansion under the online budget controller,
+ * and the tree arrays.
+ * Methodologie §1 ("Pad-scoren": rho = prod q_k), §2 ("Surrogaat-schatting":
+ * A_hat = sum rho; "Optimale Constructie": always add the valid node with the
+ * highest rho), §3 ("Adaptief Stoppen": grow until S(N) = A_hat*L_AR/C(N)
+ * starts to decrease).
+ *
+ * Node 0 is the root (the last committed token, root_token[r]) at depth 0 with
+ * rho = 1, counted in N and A_hat.  The children of a depth-d node are the K
+ * ranked tokens of q_{d+1}; a node's next candidate child is its next-ranked
+ * token.  Candidates are ordered by log rho (descending), then depth, rank and
+ * parent index (ascending).  log rho of a depth-d node is evaluated in fp64 as
+ * (sum of its path's logits) - (lse_1 + ... + lse_d).  From N = 1 (root only),
+ * the best candidate is added as node N while S(N+1) >= S(N); the build stops
+ * at the first strict decrease, when no candidate is left, or at n_max nodes.
+ * One warp builds one request's tree.
+ *
+ * topk_logit, topk_tok [B, b, K], lse [B, b]: the outputs of step 1.
+ * root_token, ctx_len [B] int32.
+ * cost_ms    [Bc, n_max+1] float: entry N is C(N) = T_draft + T_verify(N) in
+ *            ms for a tree of N nodes; Bc = B when cost_per_request != 0, else 1.
+ * l_ar       [B] float: L_AR in ms (it scales S and does not move the stop).
+ * Outputs:   n_nodes [B]; per node [B, n_max] (rows >= n_nodes untouched):
+ *            parent (root -1), depth, pos_id (= ctx_len + depth), token, rank
+ *            (root -1), log_rho (float), a_hat (A_hat of nodes 0..n), speedup
+ *            (S at size n+1); anc_mask [B, n_max, W] uint32 with
+ *            W = ceil(n_max/32): bit t%32 of word t/32 of node i is set iff node
+ *            t is node i or one of its ancestors.  Node order is pop order
+ *            (parent[i] < i).
+ * Limits: B >= 1, 1 <= b <= 32, 1 <= K <= 1024, 1 <= n_max <= 256.
+ */
+int bastion_build_tree(const float *topk_logit, const int32_t *topk_tok, const double *lse,
+                       int B, int b, int K, int n_max, const int32_t *root_token,
+                       const int32_t *ctx_len, const float *cost_ms, int cost_per_request,
+                       const float *l_ar, int32_t *n_nodes, int32_t *parent, int32_t *depth,
+                       int32_t *pos_id, int32_t *token, int32_t *rank, float *log_rho,
+                       float *a_hat, float *speedup, uint32_t *anc_mask, int32_t *status,
+                       bastion_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Tree-masked GQA attention of the tree's query tokens against the KV cache
+ * (the target's parallel verification pass over the whole tree,
+ * "Probleemstelling" and Methodologie §2).
+ *
+ * O[r,i,h] = sum_j softmax_j(scale * Q[r,i,h] . K[r,j,h/G]) V[r,j,h/G],
+ * G = Hq/Hkv.  Key slot j < ctx_len[r] is visible to every query; tree slot
+ * ctx_len[r] + t (t < n_nodes[r]) is visible to query i iff bit t of
+ * anc_mask[r,i]; other slots are not visible.  Rows i >= n_nodes[r] of out
+ * are left untouched.  bf16 inputs, fp32 accumulation, bf16 output (RNE).
+ *
+ * q        [B, n_max, Hq, D] bf16; k_cache, v_cache [B, L_cap, Hkv, D] bf16,
+ *          with the tree's keys/values at slots ctx_len .. ctx_len+n_nodes-1;
+ *          all 16-byte aligned.
+ * out      [B, n_max, Hq, D] bf16.
+ * Limits: D = 128, Hq % Hkv == 0, Hq/Hkv <= 8, 1 <= n_max <= 256.
+ * Workspace: bastion_tree_attention_workspace_bytes(...) bytes.
+ */
+size_t bastion_tree_attention_workspace_bytes(int B, int n_max, int Hq, int Hkv, int D,
+                                              int64_t L_cap);
+int bastion_tree_attention(const void *q, const void *k_cache, const void *v_cache, int B,
+                           int n_max, int Hq, int Hkv, int D, int64_t L_cap,
+                           const int32_t *ctx_len, const int32_t *n_nodes,
+                           const uint32_t *anc_mask, float scale, void *out, void *workspace,
+                           size_t workspace_bytes, int32_t *status, bastion_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Step 4 -- greedy (temperature 0) verification ("Experimentele Resultaten":
+ * greedy decoding).  For every tree node i < n_nodes[r] the target's greedy
+ * token is argmax_v target[r,i,v] (ties: lowest v).  From the root, the child
+ * whose token equals the current node's greedy token is accepted and becomes
+ * the current node; the walk ends at the first node without such a child, and
+ * that node's greedy token is the bonus token.
+ *
+ * target_logits [B, n_max, V] at row stride ld_row elements, dtype as given.
+ * n_nodes [B], parent/token [B, n_max]: the tree of step 3.
+ * Outputs: argmax [B, n_max] (rows >= n_nodes untouched); accept_len [B]
+ *          (0..b); accept_nodes [B, b+1] (root 0, then the accepted nodes,
+ *          then -1); out_tokens [B, b+1] (accepted tokens, the bonus, then -1).
+ * Limits: 1 <= B <= 4096, 1 <= n_max <= 256, 1 <= b <= 32, V < 2^30.
+ * Workspace: bastion_verify_greedy_workspace_bytes(B, n_max, V) bytes.
+ */
+size_t bastion_verify_greedy_workspace_bytes(int B, int n_max, int V);
+int bastion_verify_greedy(const void *target_logits, int dtype, int B, int n_max, int V,
+                          int64_t ld_row, int b, const int32_t *n_nodes, const int32_t *parent,
+                          const int32_t *token, int32_t *argmax, int32_t *accept_len,
+                          int32_t *accept_nodes, int32_t *out_tokens, void *workspace,
+                          size_t workspace_bytes, int32_t *status, bastion_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BASTION_H_ */

@@ -176,7 +176,7 @@ int oracle_build_tree(const float* topk_logit, const int32_t* topk_tok, const do
     double* sp = speedup + (int64_t)r * n_max;
     uint32_t* mk = anc_mask + (int64_t)r * n_max * W;
     int st = 0;
-    for (int N = 0; N <= n_max; ++N)
+    for (int N = 1; N <= n_max; ++N)
       if (!(C[N] > 0.0f) || std::isinf(C[N])) st |= OR_BAD_COST;
 
     // tree = node 0 (root)

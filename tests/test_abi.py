@@ -1,0 +1,72 @@
+"""The C ABI library loads and exports every symbol the header declares, and
+rejects bad arguments on the host before any launch (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _header_functions():
+    src = open(os.path.join(ROOT, "include", "bastion.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return re.findall(r"\b(bastion_\w+)\s*\(", src)
+
+
+@pytest.fixture(scope="module")
+def L():
+    from draft_tree_build_gb300 import bastion
+    return bastion.lib()
+
+
+def test_exports_every_declared_symbol(L):
+    from draft_tree_build_gb300 import bastion
+    names = _header_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(bastion.SYMBOLS)
+
+
+def test_version_and_strings(L):
+    assert L.bastion_version().startswith(b"bastion-gb300")
+    for code in (0, -1, -2, -3, -4, -5, -6, -7, 1, 2, 4, 8, 16, 1 << 30):
+        assert L.bastion_status_string(code) != b"unknown code"
+
+
+def test_host_checks_reject_before_launch(L):
+    vp = ctypes.c_void_p
+    fake = vp(0x10000)  # never dereferenced: every call below fails a host check
+    ws = vp(0x100000)
+    # null pointers
+    assert L.bastion_topk_marginals(None, 1, 1, 1, 8, 8, 1, None, fake, fake, fake, ws, 1 << 20, fake, None) == -1
+    # bad dtype
+    assert L.bastion_topk_marginals(fake, 7, 1, 1, 8, 8, 1, None, fake, fake, fake, ws, 1 << 20, fake, None) == -3
+    # K > V, b > 32, ld < V
+    assert L.bastion_topk_marginals(fake, 1, 1, 1, 8, 8, 9, None, fake, fake, fake, ws, 1 << 20, fake, None) == -2
+    assert L.bastion_topk_marginals(fake, 1, 1, 33, 8, 8, 1, None, fake, fake, fake, ws, 1 << 20, fake, None) == -2
+    assert L.bastion_topk_marginals(fake, 1, 1, 1, 8, 7, 1, None, fake, fake, fake, ws, 1 << 20, fake, None) == -2
+    # misaligned logits / workspace
+    assert L.bastion_topk_marginals(vp(0x10001), 1, 1, 1, 8, 8, 1, None, fake, fake, fake, ws, 1 << 20, fake, None) == -4
+    assert L.bastion_topk_marginals(fake, 1, 1, 1, 8, 8, 1, None, fake, fake, fake, vp(0x100010), 1 << 20, fake, None) == -4
+    # workspace too small
+    assert L.bastion_topk_marginals(fake, 1, 1, 1, 8, 8, 1, None, fake, fake, fake, ws, 16, fake, None) == -5
+    # tree: n_max > 256
+    args = [fake] * 3 + [1, 4, 8, 257] + [fake] * 3 + [0, fake] + [fake] * 12 + [None]
+    assert L.bastion_build_tree(*args) == -2
+    # attention: D != 128 -> unsupported; Hq % Hkv -> size
+    base = [fake, fake, fake, 1, 16, 32, 8, 64, 256, fake, fake, fake, ctypes.c_float(0.1), fake, ws, 1 << 20, fake, None]
+    assert L.bastion_tree_attention(*base) == -6
+    base[6], base[7] = 5, 128
+    assert L.bastion_tree_attention(*base) == -2
+    # verify: B > 4096
+    assert L.bastion_verify_greedy(fake, 1, 5000, 4, 8, 8, 4, fake, fake, fake, fake, fake, fake, fake, ws, 1 << 20, fake, None) == -2
+
+
+def test_workspace_queries(L):
+    assert L.bastion_topk_marginals_workspace_bytes(32, 16, 151936, 64) > 0
+    assert L.bastion_topk_marginals_workspace_bytes(1, 1, 8, 9) == 0
+    assert L.bastion_verify_greedy_workspace_bytes(32, 128, 151936) >= 32 * 128 * 8
+    assert L.bastion_tree_attention_workspace_bytes(8, 64, 32, 8, 128, 4160) > 0
