@@ -65,7 +65,7 @@ def lib(build_if_missing: bool = True):
     L.bastion_topk_marginals.restype = i32
     L.bastion_topk_marginals.argtypes = [vp, i32, i32, i32, i32, i64, i32, vp, vp, vp, vp, vp, sz, vp, vp]
     L.bastion_build_tree.restype = i32
-    L.bastion_build_tree.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, i32, vp] + [vp] * 12 + [vp]
+    L.bastion_build_tree.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, i32, vp] + [vp] * 11 + [vp]
     L.bastion_tree_attention_workspace_bytes.restype = sz
     L.bastion_tree_attention_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i64]
     L.bastion_tree_attention.restype = i32

@@ -306,7 +306,7 @@ __global__ void __launch_bounds__(kAT, 1)
     bool ok = true;
     for (int t = 0; t < n_tiles && ok; ++t) {
       const int s = t & 1;
-      ok = wait_bar(&bs.s_full[s], (t >> 1) & 1, abort, &a.status[r]);
+      ok = __all_sync(kFull, wait_bar(&bs.s_full[s], (t >> 1) & 1, abort, &a.status[r]));
       if (!ok) break;
       tc_fence_after();
       const int kb = t * kBN;
@@ -346,28 +346,31 @@ __global__ void __launch_bounds__(kAT, 1)
         for (int i = 0; i < 32; ++i)
           if ((vis[cc] >> i) & 1u) mt = fmaxf(mt, v[i] * a.scale_log2);
       }
-      if (mt > m_ref + kRescale || (m_ref == -INFINITY && mt != -INFINITY)) {
-        const float m_new = mt;
-        if (t > 0 && m_ref != -INFINITY) {
-          const float alpha = ex2f(m_ref - m_new);
-          ok = wait_bar(&bs.pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, abort, &a.status[r]);
-          if (!ok) break;
-          tc_fence_after();
+      // lazy rescale: a row moves its reference max only when the tile max
+      // exceeds it by more than 2^8; O in TMEM is rescaled by the whole warp
+      // (tcgen05.ld/st are warp-collective), with alpha = 1 for other rows.
+      const bool grow = mt > m_ref + kRescale || (m_ref == -INFINITY && mt != -INFINITY);
+      const bool rescale = grow && t > 0 && m_ref != -INFINITY;
+      const float alpha = rescale ? ex2f(m_ref - mt) : 1.0f;
+      if (__any_sync(kFull, rescale)) {
+        ok = __all_sync(kFull, wait_bar(&bs.pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, abort,
+                                        &a.status[r]));
+        if (!ok) break;
+        tc_fence_after();
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            float o[32];
-            tmem_ld32(lane_base + 32u * cc, o);
+        for (int cc = 0; cc < 4; ++cc) {
+          float o[32];
+          tmem_ld32(lane_base + 32u * cc, o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= alpha;
-            tmem_st32(lane_base + 32u * cc, o);
-          }
-          l_sum *= alpha;
+          for (int i = 0; i < 32; ++i) o[i] *= alpha;
+          tmem_st32(lane_base + 32u * cc, o);
         }
-        m_ref = m_new;
       }
+      if (rescale) l_sum *= alpha;
+      if (grow) m_ref = mt;
       // P buffer s must be free: PV of tile t-2 done
       if (t >= 2) {
-        ok = wait_bar(&bs.pv_done[s], ((t - 2) >> 1) & 1, abort, &a.status[r]);
+        ok = __all_sync(kFull, wait_bar(&bs.pv_done[s], ((t - 2) >> 1) & 1, abort, &a.status[r]));
         if (!ok) break;
       }
       unsigned char *pb = smem + kOffP + s * kTile;
@@ -398,33 +401,32 @@ __global__ void __launch_bounds__(kAT, 1)
       tc_fence_before();
       mbar_arrive(&bs.p_full[s]);
     }
-    // epilogue
+    // epilogue: the whole warp reads O from TMEM; live rows store O / l
     if (ok && n_tiles > 0) {
       const int u = n_tiles - 1;
-      ok = wait_bar(&bs.pv_done[u & 1], (u >> 1) & 1, abort, &a.status[r]);
+      ok = __all_sync(kFull, wait_bar(&bs.pv_done[u & 1], (u >> 1) & 1, abort, &a.status[r]));
       tc_fence_after();
-      if (ok && row_live) {
-        const float inv = 1.0f / l_sum;
-        uint16_t *dst = a.out + (((size_t)r * a.n_max + node) * a.Hq + (size_t)g * a.G + hh) * 128;
+      if (ok) {
+        const float inv = row_live ? 1.0f / l_sum : 0.0f;
+        uint16_t *dst = a.out + (((size_t)r * a.n_max + (row_live ? node : 0)) * a.Hq +
+                                 (size_t)g * a.G + hh) * 128;
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
           float o[32];
           tmem_ld32(lane_base + 32u * cc, o);
+          if (row_live) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 pkt;
-            pkt.x = pack_bf16(o[8 * q + 0] * inv, o[8 * q + 1] * inv);
-            pkt.y = pack_bf16(o[8 * q + 2] * inv, o[8 * q + 3] * inv);
-            pkt.z = pack_bf16(o[8 * q + 4] * inv, o[8 * q + 5] * inv);
-            pkt.w = pack_bf16(o[8 * q + 6] * inv, o[8 * q + 7] * inv);
-            *reinterpret_cast<uint4 *>(dst + 32 * cc + 8 * q) = pkt;
+            for (int q = 0; q < 4; ++q) {
+              uint4 pkt;
+              pkt.x = pack_bf16(o[8 * q + 0] * inv, o[8 * q + 1] * inv);
+              pkt.y = pack_bf16(o[8 * q + 2] * inv, o[8 * q + 3] * inv);
+              pkt.z = pack_bf16(o[8 * q + 4] * inv, o[8 * q + 5] * inv);
+              pkt.w = pack_bf16(o[8 * q + 6] * inv, o[8 * q + 7] * inv);
+              *reinterpret_cast<uint4 *>(dst + 32 * cc + 8 * q) = pkt;
+            }
           }
         }
-      } else if (row_live) {
-        // nothing
       }
-    } else if (!ok) {
-      // abort path: make sure our pending PV is not still writing TMEM
     }
   }
   tc_fence_before();

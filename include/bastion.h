@@ -26,9 +26,11 @@
  *    check.  The outputs of a request with a status bit set are unspecified.
  *    No kernel traps or asserts.
  *  - Workspace: functions that take one need at least *_workspace_bytes()
- *    bytes, 256-byte aligned, ZERO-FILLED before its first use.  Every call
- *    leaves it zero-filled again when it completes.  Calls that may run
- *    concurrently need separate workspaces.
+ *    bytes, 256-byte aligned, ZERO-FILLED before its first use.  It holds
+ *    per-call partial results and arrival counters; every call that completes
+ *    returns the counters to zero, so the same workspace serves the next call
+ *    without clearing.  Calls that may run concurrently need separate
+ *    workspaces.
  *  - dtype: BASTION_F32 (float) or BASTION_BF16 (bfloat16 bits).
  */
 #ifndef BASTION_H_

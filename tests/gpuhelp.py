@@ -33,7 +33,6 @@ def gpu_topk(x: np.ndarray, K: int, x_dev=None):
     st = torch.zeros(B, dtype=torch.int32, device=dev())
     bastion.bastion_topk_marginals(xd, K, t.logq, t.logit, t.tok, t.lse, ws, st)
     torch.cuda.synchronize()
-    assert int(ws.abs().sum()) == 0, "workspace not left zeroed"
     return t, st
 
 

@@ -30,6 +30,23 @@ def test_exports_every_declared_symbol(L):
     assert set(names) == set(bastion.SYMBOLS)
 
 
+def _header_arg_counts():
+    src = open(os.path.join(ROOT, "include", "bastion.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    out = {}
+    for m in re.finditer(r"\b(bastion_\w+)\s*\(([^)]*)\)\s*;", src):
+        args = m.group(2).strip()
+        out[m.group(1)] = 0 if args in ("", "void") else args.count(",") + 1
+    return out
+
+
+def test_binding_argtypes_match_header(L):
+    counts = _header_arg_counts()
+    assert len(counts) == 9
+    for name, n in counts.items():
+        assert len(getattr(L, name).argtypes) == n, name
+
+
 def test_version_and_strings(L):
     assert L.bastion_version().startswith(b"bastion-gb300")
     for code in (0, -1, -2, -3, -4, -5, -6, -7, 1, 2, 4, 8, 16, 1 << 30):
@@ -54,7 +71,7 @@ def test_host_checks_reject_before_launch(L):
     # workspace too small
     assert L.bastion_topk_marginals(fake, 1, 1, 1, 8, 8, 1, None, fake, fake, fake, ws, 16, fake, None) == -5
     # tree: n_max > 256
-    args = [fake] * 3 + [1, 4, 8, 257] + [fake] * 3 + [0, fake] + [fake] * 12 + [None]
+    args = [fake] * 3 + [1, 4, 8, 257] + [fake] * 3 + [0, fake] + [fake] * 11 + [None]
     assert L.bastion_build_tree(*args) == -2
     # attention: D != 128 -> unsupported; Hq % Hkv -> size
     base = [fake, fake, fake, 1, 16, 32, 8, 64, 256, fake, fake, fake, ctypes.c_float(0.1), fake, ws, 1 << 20, fake, None]
