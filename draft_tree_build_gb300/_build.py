@@ -16,7 +16,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libbastion.so")
-SOURCES = ["api.cu", "topk_marginals.cu", "build_tree.cu", "verify_greedy.cu", "tree_attention.cu"]
+SOURCES = ["api.cu", "topk_marginals.cu", "build_tree.cu", "verify_greedy.cu", "tree_attention.cu",
+           "verify_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -31,6 +31,7 @@ SYMBOLS = (
     "bastion_build_tree",
     "bastion_tree_attention_workspace_bytes", "bastion_tree_attention",
     "bastion_verify_greedy_workspace_bytes", "bastion_verify_greedy",
+    "bastion_verify_greedy_noalloc",
 )
 
 
@@ -76,6 +77,9 @@ def lib(build_if_missing: bool = True):
     L.bastion_verify_greedy.restype = i32
     L.bastion_verify_greedy.argtypes = [vp, i32, i32, i32, i32, i64, i32, vp, vp, vp, vp, vp, vp, vp,
                                         vp, sz, vp, vp]
+    L.bastion_verify_greedy_noalloc.restype = i32
+    L.bastion_verify_greedy_noalloc.argtypes = [vp, i32, i32, i32, i32, i64, i32, vp, vp, vp, vp, vp,
+                                                vp, vp, vp, vp]
     _lib = L
     return L
 
@@ -189,6 +193,21 @@ def bastion_verify_greedy(target_logits, b, n_nodes, parent, token, argmax, acce
                                      _p(accept_nodes), _p(out_tokens), _p(workspace),
                                      workspace.numel() * workspace.element_size(), _p(status), _s(stream))
     _check(rc, "bastion_verify_greedy")
+
+
+def bastion_verify_greedy_noalloc(target_logits, b, n_nodes, parent, token, argmax, accept_len,
+                                  accept_nodes, out_tokens, status, stream=None):
+    """Same as bastion_verify_greedy without a workspace argument, for callers that
+    cannot allocate device memory: the library uses a fixed 144 KiB scratch array
+    of its own (B <= 4096, B * n_max <= 16384).  Calls that overlap on the GPU race
+    on that array."""
+    B, n_max, V = target_logits.shape
+    ld = _rows_view(target_logits, 3)
+    rc = lib().bastion_verify_greedy_noalloc(_p(target_logits), _dtype(target_logits), B, n_max, V, ld,
+                                             int(b), _p(n_nodes), _p(parent), _p(token), _p(argmax),
+                                             _p(accept_len), _p(accept_nodes), _p(out_tokens), _p(status),
+                                             _s(stream))
+    _check(rc, "bastion_verify_greedy_noalloc")
 
 
 # --------------------------------------------------------------------------- buffers

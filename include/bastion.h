@@ -186,6 +186,33 @@ int bastion_verify_greedy(const void *target_logits, int dtype, int B, int n_max
                           int32_t *accept_nodes, int32_t *out_tokens, void *workspace,
                           size_t workspace_bytes, int32_t *status, bastion_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * Greedy verification without a workspace, for callers that cannot allocate.
+ * The pages have no counterpart: this is a deployment variant of the call
+ * above, not a step of the method.
+ *
+ * Some callers cannot call cudaMalloc or have memory allocated for them (a
+ * serving loop that must not touch the allocator after start-up, code inside a
+ * framework that owns the allocator, a plug-in that only receives input and
+ * output pointers).  This entry point takes the same arguments and gives the
+ * same results as bastion_verify_greedy, but its scratch is a fixed 144 KiB
+ * array compiled into the library, which every GPU that loads the library
+ * holds until the process exits; it calls no cudaMalloc or cudaFree.
+ * Limits: B <= 4096 and B * n_max <= 16384 (e.g. 64 requests x 256 nodes);
+ * larger sizes return BASTION_ERR_SIZE without launching.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  Each call clears the part of the array it uses
+ * (cudaMemsetAsync on the caller's stream) and then launches the verify kernel.
+ * All calls share the one array: calls that can overlap on the GPU (other
+ * streams, other host threads) race on it and must be serialised by the caller.
+ */
+int bastion_verify_greedy_noalloc(const void *target_logits, int dtype, int B, int n_max, int V,
+                                  int64_t ld_row, int b, const int32_t *n_nodes,
+                                  const int32_t *parent, const int32_t *token, int32_t *argmax,
+                                  int32_t *accept_len, int32_t *accept_nodes, int32_t *out_tokens,
+                                  int32_t *status, bastion_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

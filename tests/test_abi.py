@@ -42,7 +42,7 @@ def _header_arg_counts():
 
 def test_binding_argtypes_match_header(L):
     counts = _header_arg_counts()
-    assert len(counts) == 9
+    assert len(counts) == 10
     for name, n in counts.items():
         assert len(getattr(L, name).argtypes) == n, name
 
