@@ -171,11 +171,11 @@ def run_ours(args, ws, rank, local):
     graphs = [step.capture(xs[i], ts[i]) for i in range(2)]
     stream = torch.cuda.current_stream()
 
-    # warm-up (W steps, then at least ~1 s so clocks settle)
+    # warm-up (W steps, then, for long runs, ~1 s more so the clocks settle)
     for i in range(args.warmup):
         graphs[i & 1].replay()
     torch.cuda.synchronize()
-    t_end = time.time() + 1.0
+    t_end = time.time() + (1.0 if args.steps >= 100 else 0.0)
     i = 0
     while time.time() < t_end:
         for _ in range(50):
@@ -282,6 +282,159 @@ def run_ours(args, ws, rank, local):
     return res
 
 
+def run_with_attention(args, ws, rank, local):
+    """Workload 4: one tree-masked GQA attention call per step (8 requests, 32/8
+    heads, d 128, ctx 4096, trees of 64 nodes).  Workload 5: the full serving
+    step, top-K + tree + attention + verify (64 requests, vocab 128,256, trees of
+    256 nodes over a 16,384-token cache)."""
+    import torch
+
+    import synth
+    from draft_tree_build_gb300 import bastion
+
+    dev = torch.device(f"cuda:{local}")
+    w = synth.workload(args.workload)
+    es = w.elem_bytes
+    roots, ctx, cost, lar = synth.root_tokens(w), synth.ctx_lens(w), synth.cost_table(w), synth.l_ar(w)
+    x_host = synth.drafter_logits(w)
+    x_pin = pinned_from(x_host)
+    xd = x_pin.to(dev)
+    step = bastion.TreeStep(w.B, w.b, w.V, w.K, w.n_max, dev, torch.from_numpy(roots),
+                            torch.from_numpy(ctx), torch.from_numpy(cost), torch.from_numpy(lar))
+    tgt_tmp = torch.zeros((w.B, w.n_max, 1 if args.workload == 4 else w.V), dtype=xd.dtype, device=dev)
+    if args.workload == 4:
+        # the tree only: run steps 1-3
+        t, tr = step.topk, step.tree
+        bastion.bastion_topk_marginals(xd, w.K, t.logq, t.logit, t.tok, t.lse, step.ws_topk, step.status)
+        bastion.bastion_build_tree(t.logit, t.tok, t.lse, w.n_max, step.root_token, step.ctx_len,
+                                   step.cost_ms, step.l_ar, tr.n_nodes, tr.parent, tr.depth, tr.pos_id,
+                                   tr.token, tr.rank, tr.log_rho, tr.a_hat, tr.speedup, tr.anc_mask,
+                                   step.status)
+    else:
+        step.run(xd, tgt_tmp)
+    torch.cuda.synchronize()
+    n_nodes = step.tree.n_nodes.cpu().numpy()
+    depth = step.tree.depth.cpu().numpy()
+    topk_tok = step.topk.tok.cpu().numpy()
+    del tgt_tmp
+    if args.workload == 5:
+        t_host = synth.host_array((w.B, w.n_max, w.V), w.dtype)
+        synth.fill_target_noise(w, t_host.ctypes.data)
+        synth.plant_into(w, t_host.ctypes.data, synth.plant_tokens(w, n_nodes, depth, topk_tok))
+        td = pinned_from(t_host).to(dev)
+        del t_host
+    q = torch.empty((w.B, w.n_max, w.Hq, w.D), dtype=torch.int16, pin_memory=True)
+    k = torch.empty((w.B, w.L_cap, w.Hkv, w.D), dtype=torch.int16, pin_memory=True)
+    v = torch.empty_like(k)
+    synth.fill_attention(w, q.data_ptr(), k.data_ptr(), v.data_ptr())
+    qd, kd, vd = (t.view(torch.bfloat16).to(dev) for t in (q, k, v))
+    del q, k, v
+    out = torch.empty((w.B, w.n_max, w.Hq, w.D), dtype=torch.bfloat16, device=dev)
+    ws_attn = bastion.workspace(bastion.bastion_tree_attention_workspace_bytes(
+        w.B, w.n_max, w.Hq, w.Hkv, w.D, w.L_cap), dev)
+    ctx_d = torch.from_numpy(ctx).to(dev)
+    scale = 1.0 / math.sqrt(w.D)
+    stream = torch.cuda.current_stream()
+    tr = step.tree
+
+    def attn():
+        bastion.bastion_tree_attention(qd, kd, vd, ctx_d, tr.n_nodes, tr.anc_mask, scale, out, ws_attn,
+                                       step.status)
+
+    def full():
+        t, v_ = step.topk, step.ver
+        bastion.bastion_topk_marginals(xd, w.K, t.logq, t.logit, t.tok, t.lse, step.ws_topk, step.status)
+        bastion.bastion_build_tree(t.logit, t.tok, t.lse, w.n_max, step.root_token, step.ctx_len,
+                                   step.cost_ms, step.l_ar, tr.n_nodes, tr.parent, tr.depth, tr.pos_id,
+                                   tr.token, tr.rank, tr.log_rho, tr.a_hat, tr.speedup, tr.anc_mask,
+                                   step.status)
+        attn()
+        bastion.bastion_verify_greedy(td, w.b, tr.n_nodes, tr.parent, tr.token, v_.argmax, v_.accept_len,
+                                      v_.accept_nodes, v_.out_tokens, step.ws_verify, step.status)
+
+    body = attn if args.workload == 4 else full
+    body()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        body()
+    for _ in range(args.warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    t_end = time.time() + (1.0 if args.steps >= 100 else 0.0)
+    while time.time() < t_end:
+        for _ in range(10):
+            g.replay()
+        torch.cuda.synchronize()
+    clocks = Clocks(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    elapsed_ms = max_over_ranks(e0.elapsed_time(e1), ws)
+    for _ in range(min(args.steps, 50)):
+        g.replay()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    # attention kernel alone, events around each launch
+    P = min(args.steps, 50)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(P)]
+    for a_, b_ in evs:
+        a_.record(stream)
+        attn()
+        b_.record(stream)
+    torch.cuda.synchronize()
+    t_attn = statistics.mean(a_.elapsed_time(b_) for a_, b_ in evs)
+    assert int(step.status.abs().sum()) == 0, "device status bits set"
+
+    hbm, peak_kind = peaks()
+    pk = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if peak_kind == "measured" else {}
+    tf_peak = float(pk.get("bf16_tflops", 1900.0))
+    G = w.Hq // w.Hkv
+    vis_pairs = 0  # visible (query row, key) pairs per KV head: context + own root path
+    for r in range(w.B):
+        n = int(n_nodes[r])
+        vis_pairs += n * int(ctx[r]) + int((depth[r, :n] + 1).sum())
+    flops = 4.0 * w.D * G * w.Hkv * vis_pairs
+    bytes_attn = (w.B * w.Hkv * (int(ctx.mean()) + w.n_max) * w.D * 2 * 2
+                  + 2 * w.B * w.n_max * w.Hq * w.D * 2)
+    t_mem = bytes_attn / (hbm * 1e9)
+    t_tc = flops / (tf_peak * 1e12)
+    bound = "hbm" if t_mem >= t_tc else "tensor"
+    ms_step = elapsed_ms / args.steps
+    if bound == "hbm":
+        roof = {"bound": "hbm", "kernel": "tree_attention", "achieved": bytes_attn / (t_attn * 1e-3) / 1e9,
+                "peak": hbm, "unit": "GB/s", "peak_source": f"{peak_kind} copy bandwidth"}
+    else:
+        roof = {"bound": "tensor", "kernel": "tree_attention", "achieved": flops / (t_attn * 1e-3) / 1e12,
+                "peak": tf_peak, "unit": "TFLOP/s", "peak_source": f"{peak_kind} bf16 (burst)"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["roofline_us"] = max(t_mem, t_tc) * 1e6
+    roof["attn_bytes"] = bytes_attn
+    roof["attn_flops"] = flops
+    metric = ("tree-attention calls/s (B=8, 32/8 heads, d=128, ctx 4096, N=64)" if args.workload == 4
+              else "full tree steps/s (top-K+best-first+attention+verify) B=64 V=128256 ctx 16384 N=256")
+    return {
+        "metric": metric, "value": ws * args.steps / (elapsed_ms * 1e-3),
+        "unit": "calls/s" if args.workload == 4 else "steps/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16-in/f32-acc", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "n_max": w.n_max, "ctx": w.ctx, "Hq": w.Hq, "Hkv": w.Hkv,
+                   "D": w.D, "mean_tree_nodes": float(n_nodes.mean()),
+                   "l2": "inputs larger than L2", "parallelism": f"replicas x{ws}"},
+        "roofline": roof, "kernels": {"tree_attention": {"ms": t_attn}}, "clocks": clk,
+        "gpu_launches": (1 if args.workload == 4 else 4) * args.steps,
+    }
+
+
 # --------------------------------------------------------------------------- oracle legs
 
 def oracle_step(w, req, x, lse_rows=None, pre=None):
@@ -366,7 +519,7 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=100)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", type=int, default=3, choices=[1, 2, 3, 5])
+    ap.add_argument("--workload", type=int, default=3, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -382,9 +535,12 @@ def main():
         return
 
     ws, rank, local = dist_setup()
-    res = run_ours(args, ws, rank, local)
+    if args.workload in (4, 5):
+        res = run_with_attention(args, ws, rank, local)
+    else:
+        res = run_ours(args, ws, rank, local)
     if rank == 0:
-        if ws == 1 and not args.no_cpu_baseline:
+        if ws == 1 and not args.no_cpu_baseline and args.workload not in (4, 5):
             res["cpu_baseline"] = cpu_baseline(args)
         print(json.dumps(res), flush=True)
     if ws > 1:
