@@ -198,7 +198,7 @@ def bastion_verify_greedy(target_logits, b, n_nodes, parent, token, argmax, acce
 def bastion_verify_greedy_noalloc(target_logits, b, n_nodes, parent, token, argmax, accept_len,
                                   accept_nodes, out_tokens, status, stream=None):
     """Same as bastion_verify_greedy without a workspace argument, for callers that
-    cannot allocate device memory: the library uses a fixed 144 KiB scratch array
+    cannot allocate device memory: the library uses a fixed 128 KiB scratch array
     of its own (B <= 4096, B * n_max <= 16384).  Calls that overlap on the GPU race
     on that array."""
     B, n_max, V = target_logits.shape

@@ -7,26 +7,32 @@
 // ("Adaptief Stoppen": grow until S(N) = A_hat(T_N) L_AR / C(N) starts to fall).
 //
 // One warp builds one request's tree; requests are independent CTAs.
-//  * Frontier: each tree node p has at most one pending candidate, its next
-//    ranked child (p, j).  Because the children's q are sorted, the best
-//    candidate of the full frontier is always among these.  The pending
-//    candidate of node p lives in register slot p/32 of lane p%32 as a 96-bit
-//    key: order-preserving image of log rho (fp64), then the tie bits
-//    0xFFFFFF - (depth<<18 | rank<<8 | parent), so that equal scores prefer the
-//    lower depth, rank and parent.  Each lane caches its best slot; a pop is
-//    three redux.sync max reductions over the warp.
-//  * log rho of a depth-d candidate = (fp64 sum of its path's logits, root
-//    down) - Lam[d], Lam[d] = lse_1 + ... + lse_d (fp64, in that order).
-//  * Stop test before adding the best candidate c to a tree of N nodes:
-//    S(N+1) < S(N)  <=>  rho_c C(N) < A_hat (C(N+1) - C(N))   (C > 0).
+//  * Scores: log rho of a depth-d node = L - Lam[d], L = the sum of its path's
+//    logits and Lam[d] = lse_1 + ... + lse_d.  L is carried as an unevaluated
+//    float pair (hi + lo), in which sums of bf16/fp32 logits are exact, so two
+//    paths of equal depth and equal logit sum get identical scores and the tie
+//    rule decides between them; log rho itself is a float pair (~2^-44
+//    relative), far inside the 1e-6 band where floating point may decide.
+//  * Frontier: node p has one pending candidate, its next-ranked child (p, j);
+//    with sorted ranks, the best of these is the best candidate overall.  The
+//    pending candidate of node p is held in lane p % 32, register slot p / 32,
+//    as a 96-bit key: order-preserving images of the hi and lo floats of log
+//    rho, then tie bits 0xFFFFFF - (depth<<18 | rank<<8 | parent) so equal
+//    scores prefer lower depth, rank and parent.  A pop is three redux.sync
+//    reductions over the lanes' cached best keys.
+//  * When node n is created its first 32 child keys (and their rho) are
+//    computed at once, one rank per lane, into shared memory; the next block of
+//    32 is computed when a node's rank pointer runs past its block.  A pop thus
+//    does no fp64 work and at most one parallel key computation.
+//  * Stop test before adding candidate c to a tree of N nodes (C > 0):
+//    S(N+1) < S(N)  <=>  rho_c C(N) < A_hat (C(N+1) - C(N)), in fp32 with
+//    A_hat summed with Kahan compensation.
 //  * Ancestor masks are built in shared memory and stored row by row.
 #include "common.cuh"
 
 namespace bastion {
 
 namespace {
-
-constexpr int kSlots = 8;  // 8 slots x 32 lanes = 256 nodes
 
 struct TreeArgs {
   const float *topk_logit;
@@ -43,6 +49,47 @@ struct TreeArgs {
   int32_t *status;
 };
 
+struct F2 {  // unevaluated sum hi + lo, |lo| <= ulp(hi)/2
+  float h, l;
+};
+
+// a + b (float) with the rounding error of the leading sum kept (TwoSum).
+__device__ __forceinline__ F2 f2_add(F2 a, float b) {
+  const float s = a.h + b;
+  if (!isfinite(s)) return {s, 0.f};
+  const float bb = s - a.h;
+  float e = (a.h - (s - bb)) + (b - bb);
+  e += a.l;
+  const float h = s + e;
+  return {h, e - (h - s)};
+}
+
+// a - b for two pairs.
+__device__ __forceinline__ F2 f2_sub(F2 a, F2 b) {
+  const float s = a.h - b.h;
+  if (!isfinite(s)) return {s, 0.f};
+  const float bb = s - a.h;
+  float e = (a.h - (s - bb)) + (-b.h - bb);
+  e += a.l - b.l;
+  const float h = s + e;
+  return {h, e - (h - s)};
+}
+
+struct KeyE {  // one candidate: key words and rho
+  uint32_t h, l, t;
+  float rho;
+};
+
+__device__ __forceinline__ KeyE make_cand(F2 lr, int d, int j, int p) {
+  KeyE k;
+  k.h = ord_f32(lr.h);
+  k.l = ord_f32(lr.l);
+  k.t = 0xFFFFFFu - (((uint32_t)d << 18) | ((uint32_t)j << 8) | (uint32_t)p);
+  const float e = lr.h < -104.f ? 0.f : expf(lr.h);
+  k.rho = fmaf(e, lr.l, e);
+  return k;
+}
+
 __device__ __forceinline__ bool key_gt(uint32_t ah, uint32_t al, uint32_t at, uint32_t bh,
                                        uint32_t bl, uint32_t bt) {
   if (ah != bh) return ah > bh;
@@ -50,36 +97,26 @@ __device__ __forceinline__ bool key_gt(uint32_t ah, uint32_t al, uint32_t at, ui
   return at > bt;
 }
 
-__device__ __forceinline__ void cand_key(double lr, int d, int j, int p, uint32_t &h, uint32_t &l,
-                                         uint32_t &t) {
-  const uint64_t o = ord_f64(lr);
-  h = (uint32_t)(o >> 32);
-  l = (uint32_t)o;
-  t = 0xFFFFFFu - (((uint32_t)d << 18) | ((uint32_t)j << 8) | (uint32_t)p);
-}
-
-// rho = exp(log rho) from an fp32 exp of the leading part times (1 + the
-// remainder): relative error a few fp32 ulps; 0 far below fp32 range.
-__device__ __forceinline__ double rho_of(double lr) {
-  if (lr < -150.0) return 0.0;
-  const float hi = (float)lr;
-  const float lo = (float)(lr - (double)hi);
-  return (double)expf(hi) * (1.0 + (double)lo);
-}
-
+template <int S>  // register slots per lane: S * 32 >= n_max
 __global__ void __launch_bounds__(32) build_tree_kernel(TreeArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
-  double *Lsum = reinterpret_cast<double *>(smem);         // [n_max] path logit sums
-  double *Lam = Lsum + a.n_max;                             // [33]
-  float *C = reinterpret_cast<float *>(Lam + 33);           // [n_max + 1]
-  uint32_t *mask = reinterpret_cast<uint32_t *>(C + a.n_max + 1);  // [n_max * W]
-  float *lg = reinterpret_cast<float *>(mask + a.n_max * a.W);     // [b * R]
+  uint4 *blk = reinterpret_cast<uint4 *>(smem);                    // [n_max][32] keys of children
+  F2 *Lnode = reinterpret_cast<F2 *>(blk + (size_t)a.n_max * 32);  // [n_max] path logit sums
+  F2 *Lam = Lnode + a.n_max;                                        // [33]
+  int *base = reinterpret_cast<int *>(Lam + 33);                    // [n_max] first rank in blk
+  float *C = reinterpret_cast<float *>(base + a.n_max);             // [n_max + 1]
+  uint32_t *mask = reinterpret_cast<uint32_t *>(C + a.n_max + 1);   // [n_max * W]
+  float *lg = reinterpret_cast<float *>(mask + a.n_max * a.W);      // [b * R]
+  int *tk = reinterpret_cast<int *>(lg + a.b * a.R);                 // [b * R]
 
   const int r = blockIdx.x, lane = threadIdx.x;
-  const int R = a.R, W = a.W;
-  for (int idx = lane; idx < a.b * R; idx += 32) {
+  const int R = a.R, W = a.W, b = a.b;
+  griddep_wait();
+  griddep_launch_dependents();
+  for (int idx = lane; idx < b * R; idx += 32) {
     const int d = idx / R, j = idx - d * R;
-    lg[idx] = a.topk_logit[((size_t)r * a.b + d) * a.K + j];
+    lg[idx] = a.topk_logit[((size_t)r * b + d) * a.K + j];
+    tk[idx] = a.topk_tok[((size_t)r * b + d) * a.K + j];
   }
   const float *cr = a.cost + (a.cost_per_request ? (size_t)r * (a.n_max + 1) : 0);
   bool bad = false;
@@ -90,15 +127,17 @@ __global__ void __launch_bounds__(32) build_tree_kernel(TreeArgs a) {
   }
   if (__any_sync(kFull, bad) && lane == 0) atomicOr(&a.status[r], BASTION_STATUS_BAD_COST);
   if (lane == 0) {
+    // Lam[d] = lse_1 + ... + lse_d in fp64, then as a float pair
     double acc = 0.0;
-    Lam[0] = 0.0;
-    for (int d = 1; d <= a.b; ++d) {
-      acc = acc + a.lse[(size_t)r * a.b + d - 1];
-      Lam[d] = acc;
+    Lam[0] = {0.f, 0.f};
+    for (int d = 1; d <= b; ++d) {
+      acc = acc + a.lse[(size_t)r * b + d - 1];
+      const float h = (float)acc;
+      Lam[d] = {h, (float)(acc - (double)h)};
     }
   }
   const int ctx = a.ctx_len[r];
-  const double L = (double)a.l_ar[r];
+  const float L_ar = a.l_ar[r];
   const size_t nb = (size_t)r * a.n_max;
   if (lane == 0) {
     a.parent[nb] = -1;
@@ -108,8 +147,9 @@ __global__ void __launch_bounds__(32) build_tree_kernel(TreeArgs a) {
     a.rank[nb] = -1;
     a.log_rho[nb] = 0.f;
     a.a_hat[nb] = 1.f;
-    a.speedup[nb] = a.n_max >= 1 ? (float)(L / (double)C[1]) : 0.f;
-    Lsum[0] = 0.0;
+    a.speedup[nb] = L_ar / C[1];
+    Lnode[0] = {0.f, 0.f};
+    base[0] = 0;
   }
   for (int w = lane; w < W; w += 32) {
     const uint32_t m = w == 0 ? 1u : 0u;
@@ -118,45 +158,84 @@ __global__ void __launch_bounds__(32) build_tree_kernel(TreeArgs a) {
   }
   __syncwarp();
 
-  uint32_t kh[kSlots], kl[kSlots], kt[kSlots];
-#pragma unroll
-  for (int s = 0; s < kSlots; ++s) kh[s] = kl[s] = kt[s] = 0u;
-  uint32_t bh = 0u, bl = 0u, bt = 0u;
-  if (lane == 0) {
-    cand_key((double)lg[0] - Lam[1], 1, 0, 0, kh[0], kl[0], kt[0]);
-    bh = kh[0]; bl = kl[0]; bt = kt[0];
+  // children of the root: ranks 0..31 at depth 1
+  {
+    const F2 lam = Lam[1];
+    KeyE k = {0u, 0u, 0u, 0.f};
+    if (lane < R) k = make_cand(f2_sub(f2_add({0.f, 0.f}, lg[lane]), lam), 1, lane, 0);
+    blk[lane] = make_uint4(k.h, k.l, k.t, __float_as_uint(k.rho));
   }
+  uint32_t kh[S], kl[S], kt[S];
+#pragma unroll
+  for (int s = 0; s < S; ++s) kh[s] = kl[s] = kt[s] = 0u;
+  __syncwarp();
+  if (lane == 0) {
+    const uint4 e = blk[0];
+    kh[0] = e.x; kl[0] = e.y; kt[0] = e.z;
+  }
+  uint32_t bh = kh[0], bl = kl[0], bt = kt[0];
 
-  double A = 1.0;
+  float A_hi = 1.f, A_lo = 0.f;  // A_hat with Kahan compensation
   int N = 1;
   while (N < a.n_max) {
     const uint32_t mh = __reduce_max_sync(kFull, bh);
     const uint32_t ml = __reduce_max_sync(kFull, bh == mh ? bl : 0u);
     const uint32_t mt = __reduce_max_sync(kFull, (bh == mh && bl == ml) ? bt : 0u);
     if ((mh | ml | mt) == 0u) break;  // no candidate left
-    const double lr = unord_f64(((uint64_t)mh << 32) | ml);
-    if (lr == -INFINITY) break;
+    const float lr_h = unord_f32(mh);
+    if (lr_h == -INFINITY) break;
     const uint32_t sec = 0xFFFFFFu - mt;
     const int d = (int)(sec >> 18), j = (int)((sec >> 8) & 1023u), p = (int)(sec & 255u);
-    const double rho = rho_of(lr);
-    const double Cp = (double)C[N], Cn = (double)C[N + 1];
-    if (rho * Cp < A * (Cn - Cp)) break;  // S would decrease: keep T_N
+    const int bp = base[p];
+    const float rho = __uint_as_float(blk[(size_t)p * 32 + (j - bp)].w);
+    const float Cp = C[N], Cn = C[N + 1];
+    if (rho * Cp < (A_hi + A_lo) * (Cn - Cp)) break;  // S would decrease: keep T_N
 
     const int n = N;
-    const double ls = Lsum[p] + (double)lg[(d - 1) * R + j];
-    A += rho;
     N = n + 1;
+    {
+      const float y = rho - A_lo;
+      const float t = A_hi + y;
+      A_lo = (t - A_hi) - y;
+      A_hi = t;
+    }
+    const F2 Ln = f2_add(Lnode[p], lg[(d - 1) * R + j]);
+    // children of the new node: ranks lane (and further blocks later)
+    uint32_t c0h = 0u, c0l = 0u, c0t = 0u;
+    if (d < b) {
+      const F2 lam = Lam[d + 1];
+      KeyE k = {0u, 0u, 0u, 0.f};
+      if (lane < R) k = make_cand(f2_sub(f2_add(Ln, lg[d * R + lane]), lam), d + 1, lane, n);
+      blk[(size_t)n * 32 + lane] = make_uint4(k.h, k.l, k.t, __float_as_uint(k.rho));
+      c0h = __shfl_sync(kFull, k.h, 0);
+      c0l = __shfl_sync(kFull, k.l, 0);
+      c0t = __shfl_sync(kFull, k.t, 0);
+    }
+    // node p's next-ranked child replaces (p, j); a new block when needed
+    const int jn = j + 1;
+    if (jn < R && jn - bp == 32) {
+      const F2 lam = Lam[d];
+      const F2 Lp = Lnode[p];
+      KeyE k = {0u, 0u, 0u, 0.f};
+      if (jn + lane < R) k = make_cand(f2_sub(f2_add(Lp, lg[(d - 1) * R + jn + lane]), lam), d, jn + lane, p);
+      blk[(size_t)p * 32 + lane] = make_uint4(k.h, k.l, k.t, __float_as_uint(k.rho));
+      __syncwarp();
+      if (lane == 0) base[p] = jn;
+    }
+    __syncwarp();
     if (lane == 0) {
-      Lsum[n] = ls;
+      Lnode[n] = Ln;
+      base[n] = 0;
       const size_t o = nb + n;
+      const float Ah = A_hi + A_lo;
       a.parent[o] = p;
       a.depth[o] = d;
       a.pos_id[o] = ctx + d;
-      a.token[o] = a.topk_tok[((size_t)r * a.b + d - 1) * a.K + j];
+      a.token[o] = tk[(d - 1) * R + j];
       a.rank[o] = j;
-      a.log_rho[o] = (float)lr;
-      a.a_hat[o] = (float)A;
-      a.speedup[o] = (float)(A * L / Cn);
+      a.log_rho[o] = lr_h;
+      a.a_hat[o] = Ah;
+      a.speedup[o] = Ah * L_ar / Cn;
     }
     for (int w = lane; w < W; w += 32) {
       const uint32_t m = mask[p * W + w] | (w == (n >> 5) ? (1u << (n & 31)) : 0u);
@@ -164,33 +243,38 @@ __global__ void __launch_bounds__(32) build_tree_kernel(TreeArgs a) {
       a.anc_mask[(nb + n) * W + w] = m;
     }
     bool touched = false;
-    if (lane == (p & 31)) {  // node p's next-ranked child replaces (p, j)
-      uint32_t h2 = 0u, l2 = 0u, t2 = 0u;
-      if (j + 1 < R) cand_key(Lsum[p] + (double)lg[(d - 1) * R + j + 1] - Lam[d], d, j + 1, p, h2, l2, t2);
+    if (lane == (p & 31)) {
+      uint4 e = make_uint4(0u, 0u, 0u, 0u);
+      if (jn < R) e = blk[(size_t)p * 32 + (jn - (jn - bp == 32 ? jn : bp))];
       const int s0 = p >> 5;
 #pragma unroll
-      for (int s = 0; s < kSlots; ++s)
-        if (s == s0) { kh[s] = h2; kl[s] = l2; kt[s] = t2; }
+      for (int s = 0; s < S; ++s)
+        if (s == s0) { kh[s] = e.x; kl[s] = e.y; kt[s] = e.z; }
       touched = true;
     }
-    if (d < a.b && lane == (n & 31)) {  // the new node's first child
-      uint32_t h3, l3, t3;
-      cand_key(ls + (double)lg[d * R] - Lam[d + 1], d + 1, 0, n, h3, l3, t3);
+    if (d < b && lane == (n & 31)) {
       const int s1 = n >> 5;
 #pragma unroll
-      for (int s = 0; s < kSlots; ++s)
-        if (s == s1) { kh[s] = h3; kl[s] = l3; kt[s] = t3; }
+      for (int s = 0; s < S; ++s)
+        if (s == s1) { kh[s] = c0h; kl[s] = c0l; kt[s] = c0t; }
       touched = true;
     }
     if (touched) {
       bh = kh[0]; bl = kl[0]; bt = kt[0];
 #pragma unroll
-      for (int s = 1; s < kSlots; ++s)
+      for (int s = 1; s < S; ++s)
         if (key_gt(kh[s], kl[s], kt[s], bh, bl, bt)) { bh = kh[s]; bl = kl[s]; bt = kt[s]; }
     }
     __syncwarp();
   }
   if (lane == 0) a.n_nodes[r] = N;
+}
+
+template <int S>
+void launch_s(const TreeArgs &a, size_t smem, cudaStream_t stream) {
+  if (smem > 48 * 1024)
+    cudaFuncSetAttribute(build_tree_kernel<S>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  launch_pdl(build_tree_kernel<S>, dim3(a.B), dim3(32), smem, stream, a);
 }
 
 }  // namespace
@@ -227,11 +311,12 @@ int launch_build_tree(const float *topk_logit, const int32_t *topk_tok, const do
   a.speedup = speedup;
   a.anc_mask = anc_mask;
   a.status = status;
-  const size_t smem = (size_t)n_max * 8 + 33 * 8 + (size_t)(n_max + 1) * 4 +
-                      (size_t)n_max * a.W * 4 + (size_t)b * a.R * 4;
-  if (smem > 48 * 1024)
-    cudaFuncSetAttribute(build_tree_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  build_tree_kernel<<<B, 32, smem, stream>>>(a);
+  const size_t smem = (size_t)n_max * 32 * 16 + (size_t)n_max * 8 + 33 * 8 + (size_t)n_max * 4 +
+                      (size_t)(n_max + 1) * 4 + (size_t)n_max * a.W * 4 + (size_t)b * a.R * 8;
+  if (n_max <= 32) launch_s<1>(a, smem, stream);
+  else if (n_max <= 64) launch_s<2>(a, smem, stream);
+  else if (n_max <= 128) launch_s<4>(a, smem, stream);
+  else launch_s<8>(a, smem, stream);
   return cudaGetLastError() == cudaSuccess ? BASTION_OK : BASTION_ERR_LAUNCH;
 }
 

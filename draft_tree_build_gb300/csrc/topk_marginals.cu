@@ -5,26 +5,29 @@
 // children of a depth-(k-1) tree node are the ranked tokens of q_k.
 //
 // Design (HBM-bound sweep, one read of every logit):
-//  * a row is cut into chunks of CL elements; one CTA per (row, chunk) stages
-//    its chunk in shared memory with one TMA bulk copy (cp.async.bulk), so the
-//    chunk is read from HBM once and swept twice from shared memory;
+//  * a row is cut into C equal chunks of at most 32 KB; one CTA per (row,
+//    chunk) stages its chunk in shared memory with one TMA bulk copy
+//    (cp.async.bulk), so the chunk is read from HBM once and swept twice from
+//    shared memory, while the other CTAs resident on the SM keep their copies
+//    in flight;
 //  * sweep 1: per-thread maxima.  The chunk max M_c comes from them, and so
-//    does a prefilter threshold T0: in each of the 8 warps the ceil(K/8)-th
-//    largest lane maximum is a value that at least ceil(K/8) distinct elements
-//    of that warp reach, so the minimum over warps is reached by >= K elements
-//    and every top-K element of the chunk is >= T0;
-//  * sweep 2: sum of exp(l - M_c) (fp32 per 8-element vector, Kahan-compensated
-//    per thread, fp64 across threads) and compaction of the few elements >= T0;
+//    does a prefilter threshold T0 = the K-th largest of the 256 thread maxima
+//    (found by counting in the 8 warp-sorted lists): at least K distinct
+//    elements reach T0, so every top-K element of the chunk is >= T0;
+//  * sweep 2: sum of exp(l - M_c) with packed f32x2 arithmetic and ex2, the
+//    log2(e) factor split in two parts so its rounding does not bias all terms
+//    alike, fp32 per 8-element vector and Kahan-compensated per thread, then a
+//    compensated (two-float) reduction; and compaction of the few elements
+//    >= T0 (about K of them);
 //  * the survivors are ranked exactly by counting (keys are unique: value desc,
 //    token asc); if they do not fit (heavy ties at T0) an exact radix select
 //    over the whole chunk takes over;
 //  * the last CTA of a row to finish (atomic arrival counter, no waiting)
-//    merges the chunk partials: M = max M_c, s = sum s_c exp(M_c - M) in fp64,
-//    lse = M + log s, and the top-K of the union of the sorted chunk lists by
-//    rank = own position + binary-search counts in the other lists.
+//    merges the chunk partials: M = max M_c, s = sum s_c exp(M_c - M) as a
+//    two-float sum, lse = M + log s in fp64, and the top-K of the union of the
+//    sorted chunk lists by rank = own position + binary-search counts in the
+//    other lists.
 #include <cuda_bf16.h>
-
-#include <type_traits>
 
 #include "common.cuh"
 
@@ -32,53 +35,91 @@ namespace bastion {
 
 namespace {
 
-constexpr int kT = 256;     // threads per CTA (8 warps)
-constexpr int kCap = 1024;  // survivor keys held in shared memory (>= max K)
-constexpr int kPad = 32;    // bytes in front of the staged chunk (head elements)
-constexpr float kL2eHi = 1.4426950216293335f;   // log2(e) rounded to float
+constexpr int kT = 256;       // threads per CTA (8 warps)
+constexpr int kPad = 32;      // bytes in front of the staged chunk
+constexpr float kL2eHi = 1.4426950216293335f;     // log2(e) rounded to float
 constexpr float kL2eLo = 1.925963033500011e-08f;  // log2(e) - kL2eHi
 
 struct TopkArgs {
   const unsigned char *logits;
-  int rows, b, V, K, CL, C;
+  int rows, b, V, K, CL, C, cap, chunk_bytes, lists_bytes;
   int64_t ld;  // elements
   float *topk_logq, *topk_logit;
   int32_t *topk_tok;
   double *lse;
   int32_t *status;
   float *part_m;
-  double *part_s;
+  float2 *part_s;  // (hi, lo) of the chunk's sum of exp(l - M_c)
   int32_t *part_n;
   uint64_t *part_keys;
   uint32_t *row_cnt;
 };
 
 struct Scratch {
-  float red_f[32];
-  double red_d[32];
+  float lanemax[kT];  // warp-sorted thread maxima (descending per warp)
+  float red_f[8];
+  float2 red_s[8];
+  float2 s_row;
   uint32_t hist[256];
+  uint32_t t0_ord;
   int n_surv;
   int last;
-  float M;
-  float T0;
   uint32_t digit_info[2];
   int scan[kT + 1];
 };
 
+// --------------------------------------------------------------------------- arithmetic
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 
-// exp(d) for d = l - M <= 0 with the log2(e) product split in two parts, so
-// the constant's rounding does not bias every term the same way.
-__device__ __forceinline__ float exp_shifted(float d) {
-  return ex2(fmaf(d, kL2eHi, d * kL2eLo));
+// exp(x0 - m) + exp(x1 - m), exp(x2 - m) + exp(x3 - m) as a pair, with the
+// subtraction and the split log2(e) product in packed f32x2 arithmetic.
+__device__ __forceinline__ void exp4(float x0, float x1, float x2, float x3, float m, float &s0,
+                                     float &s1) {
+  float t0, t1, t2, t3;
+  asm("{\n .reg .b64 d, e, mm, hh, ll, p, q;\n"
+      " mov.b64 d, {%4, %5};\n mov.b64 e, {%6, %7};\n mov.b64 mm, {%8, %8};\n"
+      " mov.b64 hh, {%9, %9};\n mov.b64 ll, {%10, %10};\n"
+      " sub.rn.f32x2 d, d, mm;\n sub.rn.f32x2 e, e, mm;\n"
+      " mul.rn.f32x2 p, d, ll;\n mul.rn.f32x2 q, e, ll;\n"
+      " fma.rn.f32x2 d, d, hh, p;\n fma.rn.f32x2 e, e, hh, q;\n"
+      " mov.b64 {%0, %1}, d;\n mov.b64 {%2, %3}, e;\n}\n"
+      : "=f"(t0), "=f"(t1), "=f"(t2), "=f"(t3)
+      : "f"(x0), "f"(x1), "f"(x2), "f"(x3), "f"(m), "f"(kL2eHi), "f"(kL2eLo));
+  const float e0 = ex2(t0), e1 = ex2(t1), e2 = ex2(t2), e3 = ex2(t3);
+  asm("{\n .reg .b64 a, c;\n mov.b64 a, {%2, %3};\n mov.b64 c, {%4, %5};\n"
+      " add.rn.f32x2 a, a, c;\n mov.b64 {%0, %1}, a;\n}\n"
+      : "=f"(s0), "=f"(s1)
+      : "f"(e0), "f"(e1), "f"(e2), "f"(e3));
+}
+
+__device__ __forceinline__ float exp_shifted(float d) { return ex2(fmaf(d, kL2eHi, d * kL2eLo)); }
+
+// Two-float sums: value = hi + lo.
+__device__ __forceinline__ float2 two_sum(float a, float b) {
+  const float s = a + b;
+  const float bb = s - a;
+  return make_float2(s, (a - (s - bb)) + (b - bb));
+}
+__device__ __forceinline__ float2 ff_add(float2 a, float2 b) {
+  float2 s = two_sum(a.x, b.x);
+  s.y += a.y + b.y;
+  return two_sum(s.x, s.y);
+}
+__device__ __forceinline__ float2 ff_warp_sum(float2 v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    float2 w = make_float2(__shfl_xor_sync(kFull, v.x, o), __shfl_xor_sync(kFull, v.y, o));
+    v = ff_add(v, w);
+  }
+  return v;
 }
 
 template <int ES>
-__device__ __forceinline__ float load_elem_smem(const unsigned char *p) {
+__device__ __forceinline__ float load_elem(const unsigned char *p) {
   if constexpr (ES == 4) {
     return *reinterpret_cast<const float *>(p);
   } else {
@@ -126,46 +167,66 @@ __device__ __forceinline__ float warp_sort_desc(float v, int lane) {
   return v;
 }
 
-// Append the elements of one lane that pass `pass[i]` as keys into surv[].
-template <int NE>
-__device__ __forceinline__ void append_keys(const float (&f)[NE], const bool (&pass)[NE],
-                                            uint32_t tok0, int lane, uint64_t *surv,
-                                            int *n_surv) {
-#pragma unroll
-  for (int i = 0; i < NE; ++i) {
-    unsigned bal = __ballot_sync(kFull, pass[i]);
-    if (bal) {
-      int leader = __ffs(bal) - 1;
-      int base = 0;
-      if (lane == leader) base = atomicAdd(n_surv, __popc(bal));
-      base = __shfl_sync(kFull, base, leader);
-      if (pass[i]) {
-        int idx = base + __popc(bal & ((1u << lane) - 1u));
-        if (idx < kCap) surv[idx] = make_key(f[i], tok0 + (uint32_t)i);
-      }
-    }
+// Number of entries >= c in a descending list of 32.
+__device__ __forceinline__ int count_ge(const float *list, float c) {
+  int lo = 0, hi = 32;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (list[mid] >= c) lo = mid + 1; else hi = mid;
   }
+  return lo;
+}
+
+// --------------------------------------------------------------------------- chunk geometry
+struct Item {
+  int row, c, e0, n, body, nh, t0, nvec;
+  const unsigned char *g0;
+  uintptr_t ga0;
+};
+
+template <int ES>
+__device__ __forceinline__ Item item_at(const TopkArgs &a, int it) {
+  Item m;
+  m.row = it / a.C;
+  m.c = it - m.row * a.C;
+  m.e0 = m.c * a.CL;
+  m.n = min(a.V - m.e0, a.CL);
+  m.g0 = a.logits + ((size_t)m.row * (size_t)a.ld + (size_t)m.e0) * ES;
+  m.ga0 = ((uintptr_t)m.g0 + 15) & ~(uintptr_t)15;
+  const uintptr_t ga1 = ((uintptr_t)m.g0 + (uintptr_t)m.n * ES) & ~(uintptr_t)15;
+  m.body = ga1 > m.ga0 ? (int)(ga1 - m.ga0) : 0;
+  const int h = m.body ? (int)(m.ga0 - (uintptr_t)m.g0) : m.n * ES;
+  m.nh = h / ES;
+  m.t0 = (h + m.body) / ES;
+  m.nvec = m.body / 16;
+  return m;
+}
+
+// Element e of the item: from the staged body, else from global memory.
+template <int ES>
+__device__ __forceinline__ float item_elem(const Item &m, const unsigned char *body, int e) {
+  if (e >= m.nh && e < m.t0) return load_elem<ES>(body + (size_t)(e - m.nh) * ES);
+  return load_elem<ES>(m.g0 + (size_t)e * ES);
 }
 
 // Exact top-min(K, n) of the chunk when the prefilter left too many survivors:
 // radix select of the K-th largest value (8-bit digits of the order-preserving
 // key), then every element above it plus the lowest-token elements equal to it.
 template <int ES>
-__device__ void chunk_topk_exact(const unsigned char *elem0, int n, int K, uint32_t tok_base,
-                                 uint64_t *surv, Scratch &sc) {
-  const int tid = threadIdx.x;
+__device__ void chunk_topk_exact(const Item &m, const unsigned char *body, int K, uint64_t *surv,
+                                 Scratch &sc) {
+  const int tid = threadIdx.x, n = m.n;
   int kk = min(K, n);
   uint32_t prefix = 0, pmask = 0;
   for (int shift = 24; shift >= 0; shift -= 8) {
     for (int i = tid; i < 256; i += kT) sc.hist[i] = 0;
     __syncthreads();
     for (int e = tid; e < n; e += kT) {
-      uint32_t o = ord_f32(load_elem_smem<ES>(elem0 + (size_t)e * ES));
+      const uint32_t o = ord_f32(item_elem<ES>(m, body, e));
       if ((o & pmask) == prefix) atomicAdd(&sc.hist[(o >> shift) & 255u], 1u);
     }
     __syncthreads();
     if (tid < 32) {
-      // bins 255 - 8*lane ... 255 - 8*lane - 7 (descending digits)
       uint32_t cnt[8], tot = 0;
 #pragma unroll
       for (int q = 0; q < 8; ++q) { cnt[q] = sc.hist[255 - 8 * tid - q]; tot += cnt[q]; }
@@ -175,9 +236,8 @@ __device__ void chunk_topk_exact(const unsigned char *elem0, int n, int K, uint3
         uint32_t y = __shfl_up_sync(kFull, incl, o);
         if (tid >= o) incl += y;
       }
-      uint32_t above = incl - tot;  // count in higher digit bins than this lane's
-      bool mine = above < (uint32_t)kk && incl >= (uint32_t)kk;
-      if (mine) {
+      const uint32_t above = incl - tot;
+      if (above < (uint32_t)kk && incl >= (uint32_t)kk) {
         uint32_t run = above;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
@@ -191,19 +251,17 @@ __device__ void chunk_topk_exact(const unsigned char *elem0, int n, int K, uint3
       }
     }
     __syncthreads();
-    uint32_t digit = sc.digit_info[0];
+    const uint32_t digit = sc.digit_info[0];
     kk -= (int)sc.digit_info[1];
     prefix |= digit << shift;
     pmask |= 255u << shift;
     __syncthreads();
   }
-  // prefix = order key of the K-th largest value; take kk elements equal to it
-  // in token order, and every element above it.
   if (tid == 0) sc.n_surv = 0;
   const int per = (n + kT - 1) / kT;
   const int lo = min(n, tid * per), hi = min(n, lo + per);
   int eq = 0;
-  for (int e = lo; e < hi; ++e) eq += ord_f32(load_elem_smem<ES>(elem0 + (size_t)e * ES)) == prefix;
+  for (int e = lo; e < hi; ++e) eq += ord_f32(item_elem<ES>(m, body, e)) == prefix;
   sc.scan[tid] = eq;
   __syncthreads();
   if (tid == 0) {
@@ -213,145 +271,143 @@ __device__ void chunk_topk_exact(const unsigned char *elem0, int n, int K, uint3
   __syncthreads();
   int rank_eq = sc.scan[tid];
   for (int e = lo; e < hi; ++e) {
-    float v = load_elem_smem<ES>(elem0 + (size_t)e * ES);
-    uint32_t o = ord_f32(v);
+    const float v = item_elem<ES>(m, body, e);
+    const uint32_t o = ord_f32(v);
     bool take = o > prefix;
     if (o == prefix) { take = rank_eq < kk; ++rank_eq; }
-    if (take) {
-      int idx = atomicAdd(&sc.n_surv, 1);
-      surv[idx] = make_key(v, tok_base + (uint32_t)e);
-    }
+    if (take) surv[atomicAdd(&sc.n_surv, 1)] = make_key(v, (uint32_t)(m.e0 + e));
   }
   __syncthreads();
 }
 
+// Append this lane's elements >= T0 of one vector (keys into surv).
+template <int NE>
+__device__ __forceinline__ void append_lane(const float (&f)[NE], float T0, uint32_t tok0,
+                                            uint64_t *surv, int *n_surv, int cap) {
+  uint32_t msk = 0;
+#pragma unroll
+  for (int i = 0; i < NE; ++i) msk |= (f[i] >= T0 ? 1u : 0u) << i;
+  int idx = atomicAdd(n_surv, __popc(msk));
+#pragma unroll
+  for (int i = 0; i < NE; ++i) {
+    if ((msk >> i) & 1u) {
+      if (idx < cap) surv[idx] = make_key(f[i], tok0 + (uint32_t)i);
+      ++idx;
+    }
+  }
+}
+
 template <int ES>
-__global__ void __launch_bounds__(kT, 4) topk_chunk_kernel(TopkArgs a) {
+__global__ void __launch_bounds__(kT, 4) topk_kernel(TopkArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem);
-  uint64_t *surv = reinterpret_cast<uint64_t *>(smem + 16);
-  Scratch &sc = *reinterpret_cast<Scratch *>(smem + 16 + kCap * 8);
-  unsigned char *buf = smem + 16 + kCap * 8 + ((sizeof(Scratch) + 127) / 128) * 128;
+  uint64_t *surv = reinterpret_cast<uint64_t *>(smem + 128);  // [cap]
+  Scratch &sc = *reinterpret_cast<Scratch *>(smem + 128 + (size_t)a.cap * 8);
+  uint64_t *lists = reinterpret_cast<uint64_t *>(smem + 128 + (size_t)a.cap * 8 +
+                                                 ((sizeof(Scratch) + 127) / 128) * 128);
+  unsigned char *chunk = reinterpret_cast<unsigned char *>(lists) + a.lists_bytes;
+  unsigned char *body = chunk + kPad;
 
-  constexpr int NE = 16 / ES;  // elements per 16-byte vector
+  constexpr int NE = 16 / ES;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int row = blockIdx.x / a.C, c = blockIdx.x % a.C;
-  const int req = row / a.b;
-  const int e0 = c * a.CL;
-  const int n = min(a.V - e0, a.CL);
-  const unsigned char *g0 = a.logits + ((size_t)row * (size_t)a.ld + (size_t)e0) * ES;
-  const uintptr_t ga0 = ((uintptr_t)g0 + 15) & ~(uintptr_t)15;
-  const uintptr_t ga1 = ((uintptr_t)g0 + (uintptr_t)n * ES) & ~(uintptr_t)15;
-  const int body = ga1 > ga0 ? (int)(ga1 - ga0) : 0;       // bytes copied in bulk
-  const int h = body ? (int)(ga0 - (uintptr_t)g0) : n * ES;  // head bytes
-  const int nh = h / ES;                                      // head elements
-  const int t0 = (h + body) / ES;                             // first tail element
-  const int nvec = body / 16;
-  unsigned char *elem0 = buf + kPad - h;  // chunk element e lives at elem0 + e*ES
+  const Item m = item_at<ES>(a, blockIdx.x);
+  const int req = m.row / a.b;
 
   if (tid == 0) {
     mbar_init(bar, 1);
     fence_mbar_init();
     sc.n_surv = 0;
+    sc.t0_ord = 0u;
   }
+  griddep_wait();
+  griddep_launch_dependents();
   __syncthreads();
-  if (tid == 0 && body) {
-    mbar_arrive_expect_tx(bar, (uint32_t)body);
-    bulk_g2s(buf + kPad, reinterpret_cast<const void *>(ga0), (uint32_t)body, bar);
+  if (tid == 0 && m.body) {
+    mbar_arrive_expect_tx(bar, (uint32_t)m.body);
+    bulk_g2s(body, reinterpret_cast<const void *>(m.ga0), (uint32_t)m.body, bar);
   }
-  // unaligned head and tail elements: plain loads
-  using ElemT = typename std::conditional<ES == 4, uint32_t, uint16_t>::type;
-  for (int e = tid; e < nh; e += kT)
-    reinterpret_cast<ElemT *>(elem0)[e] = reinterpret_cast<const ElemT *>(g0)[e];
-  for (int e = t0 + tid; e < n; e += kT)
-    reinterpret_cast<ElemT *>(elem0)[e] = reinterpret_cast<const ElemT *>(g0)[e];
-  if (body && !mbar_wait_bounded(bar, 0)) {
+  // unaligned head and tail elements: plain loads (read before the wait)
+  const int nscal = m.nh + (m.n - m.t0);
+  float tmax = -INFINITY;
+  for (int j = tid; j < nscal; j += kT) {
+    const int e = j < m.nh ? j : m.t0 + (j - m.nh);
+    tmax = fmaxf(tmax, load_elem<ES>(m.g0 + (size_t)e * ES));
+  }
+  if (m.body && !mbar_wait_bounded(bar, 0)) {
     if (lane == 0) atomicOr(&a.status[req], BASTION_STATUS_TIMEOUT);
   }
-  __syncthreads();
 
-  // ---- sweep 1: maxima
-  float tmax = -INFINITY;
-  for (int v = tid; v < nvec; v += kT) tmax = fmaxf(tmax, vmax<ES>(ld_shared_v4(buf + kPad + v * 16)));
-  for (int e = tid; e < nh; e += kT) tmax = fmaxf(tmax, load_elem_smem<ES>(elem0 + (size_t)e * ES));
-  for (int e = t0 + tid; e < n; e += kT) tmax = fmaxf(tmax, load_elem_smem<ES>(elem0 + (size_t)e * ES));
+  // ---- sweep 1: maxima, and T0 = K-th largest thread maximum
+  for (int v = tid; v < m.nvec; v += kT) tmax = fmaxf(tmax, vmax<ES>(ld_shared_v4(body + v * 16)));
   {
-    float wm = warp_max_f(tmax);
-    float sorted = warp_sort_desc(tmax, lane);
-    const int kw = (a.K + 7) / 8;
-    float tw = __shfl_sync(kFull, sorted, kw <= 32 ? kw - 1 : 0);
-    if (kw > 32) tw = -INFINITY;
-    if (lane == 0) { sc.red_f[warp] = wm; sc.red_f[8 + warp] = tw; }
+    const float wm = warp_max_f(tmax);
+    sc.lanemax[warp * 32 + lane] = warp_sort_desc(tmax, lane);
+    if (lane == 0) sc.red_f[warp] = wm;
   }
-  __syncthreads();
-  if (tid == 0) {
-    float m = -INFINITY, t = INFINITY;
-    for (int w = 0; w < kT / 32; ++w) { m = fmaxf(m, sc.red_f[w]); t = fminf(t, sc.red_f[8 + w]); }
-    sc.M = m;
-    sc.T0 = t;
+  __syncthreads();  // A
+  float M = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < kT / 32; ++w) M = fmaxf(M, sc.red_f[w]);
+  if (a.K <= kT) {
+    // candidate c = my sorted entry; T0 = the largest c with #(maxima >= c) >= K
+    const float c = sc.lanemax[tid];
+    int cnt = 0;
+#pragma unroll
+    for (int w = 0; w < kT / 32; ++w) cnt += count_ge(&sc.lanemax[w * 32], c);
+    uint32_t best = cnt >= a.K ? ord_f32(c) : 0u;
+    best = __reduce_max_sync(kFull, best);
+    if (lane == 0 && best) atomicMax(&sc.t0_ord, best);
   }
-  __syncthreads();
-  const float M = sc.M, T0 = sc.T0;
+  __syncthreads();  // A2
+  const float T0 = sc.t0_ord ? unord_f32(sc.t0_ord) : -INFINITY;
   const bool have_mass = M != -INFINITY;
 
   // ---- sweep 2: sum of exp(l - M) and survivors >= T0
-  float s = 0.f, comp = 0.f;
-  const uint32_t tok_vec0 = (uint32_t)(e0 + h / ES);  // token of the first body element
-  for (int base = warp * 32; base < nvec; base += kT) {
-    const int v = base + lane;
-    const bool valid = v < nvec;
+  float sum = 0.f, comp = 0.f;
+  const uint32_t tok_vec0 = (uint32_t)(m.e0 + m.nh);
+  for (int v = tid; v < m.nvec; v += kT) {
+    const uint4 x = ld_shared_v4(body + v * 16);
     float f[NE];
-    uint4 x = make_uint4(0, 0, 0, 0);
-    if (valid) x = ld_shared_v4(buf + kPad + v * 16);
     unpack<ES>(x, f);
-    float vs = 0.f;
-    bool any = false;
-    bool pass[NE];
-#pragma unroll
-    for (int i = 0; i < NE; ++i) {
-      vs += exp_shifted(f[i] - M);
-      pass[i] = valid && f[i] >= T0;
-      any |= pass[i];
+    float vs;
+    if constexpr (ES == 2) {
+      float p0, p1, q0, q1;
+      exp4(f[0], f[1], f[2], f[3], M, p0, p1);
+      exp4(f[4], f[5], f[6], f[7], M, q0, q1);
+      vs = (p0 + p1) + (q0 + q1);
+    } else {
+      float p0, p1;
+      exp4(f[0], f[1], f[2], f[3], M, p0, p1);
+      vs = p0 + p1;
     }
-    if (valid && have_mass) {
-      float y = vs - comp;
-      float t = s + y;
-      comp = (t - s) - y;
-      s = t;
-    }
-    if (__any_sync(kFull, any))
-      append_keys<NE>(f, pass, tok_vec0 + (uint32_t)(v * NE), lane, surv, &sc.n_surv);
+    const float y = vs - comp;
+    const float t = sum + y;
+    comp = (t - sum) - y;
+    sum = t;
+    if (vmax<ES>(x) >= T0) append_lane<NE>(f, T0, tok_vec0 + (uint32_t)(v * NE), surv, &sc.n_surv, a.cap);
   }
-  // head and tail scalars, by warp 0
-  if (warp == 0) {
-    const int nscal = nh + (n - t0);
-    for (int base = 0; base < nscal; base += 32) {
-      const int j = base + lane;
-      const bool valid = j < nscal;
-      const int e = j < nh ? j : t0 + (j - nh);
-      float f[1] = {valid ? load_elem_smem<ES>(elem0 + (size_t)e * ES) : -INFINITY};
-      bool pass[1] = {valid && f[0] >= T0};
-      if (valid && have_mass) {
-        float y = exp_shifted(f[0] - M) - comp;
-        float t = s + y;
-        comp = (t - s) - y;
-        s = t;
-      }
-      if (__any_sync(kFull, pass[0]))
-        append_keys<1>(f, pass, (uint32_t)(e0 + e), lane, surv, &sc.n_surv);
-    }
+  for (int j = tid; j < nscal; j += kT) {  // head and tail
+    const int e = j < m.nh ? j : m.t0 + (j - m.nh);
+    const float f[1] = {load_elem<ES>(m.g0 + (size_t)e * ES)};
+    const float y = exp_shifted(f[0] - M) - comp;
+    const float t = sum + y;
+    comp = (t - sum) - y;
+    sum = t;
+    if (f[0] >= T0) append_lane<1>(f, T0, (uint32_t)(m.e0 + e), surv, &sc.n_surv, a.cap);
   }
-  double sd = warp_sum_d((double)s - (double)comp);
-  if (lane == 0) sc.red_d[warp] = sd;
-  __syncthreads();
+  {
+    const float2 ws = ff_warp_sum(two_sum(sum, -comp));
+    if (lane == 0) sc.red_s[warp] = ws;
+  }
+  __syncthreads();  // B
 
   int n_s = sc.n_surv;
-  if (n_s > kCap) {
-    chunk_topk_exact<ES>(elem0, n, a.K, (uint32_t)e0, surv, sc);
+  if (n_s > a.cap) {
+    chunk_topk_exact<ES>(m, body, a.K, surv, sc);
     n_s = sc.n_surv;
   }
-  // ---- rank survivors exactly and write the chunk's sorted top list
-  const size_t part = (size_t)row * a.C + c;
+  // ---- rank survivors exactly and write the chunk's sorted list
+  const size_t part = (size_t)m.row * a.C + m.c;
   uint64_t *out_keys = a.part_keys + part * a.K;
   for (int i = tid; i < n_s; i += kT) {
     const uint64_t ki = surv[i];
@@ -360,40 +416,48 @@ __global__ void __launch_bounds__(kT, 4) topk_chunk_kernel(TopkArgs a) {
     if (rk < a.K) out_keys[rk] = ki;
   }
   if (tid == 0) {
-    double stot = 0.0;
-    for (int w = 0; w < kT / 32; ++w) stot += sc.red_d[w];
+    float2 st = make_float2(0.f, 0.f);
+    for (int w = 0; w < kT / 32; ++w) st = ff_add(st, sc.red_s[w]);
     a.part_m[part] = M;
-    a.part_s[part] = have_mass ? stot : 0.0;
+    a.part_s[part] = have_mass ? st : make_float2(0.f, 0.f);
     a.part_n[part] = min(n_s, a.K);
   }
   __threadfence();
-  __syncthreads();
-  if (tid == 0) sc.last = atomicAdd(&a.row_cnt[row], 1u) == (uint32_t)(a.C - 1);
-  __syncthreads();
+  __syncthreads();  // C
+  if (tid == 0) sc.last = atomicAdd(&a.row_cnt[m.row], 1u) == (uint32_t)(a.C - 1);
+  __syncthreads();  // D
   if (!sc.last) return;
   __threadfence();
 
   // ---- merge of the row's chunk partials (last arriving CTA)
-  const size_t part0 = (size_t)row * a.C;
-  // fp64 log-sum-exp over chunks
-  float Mrow = -INFINITY;
-  for (int q = 0; q < a.C; ++q) Mrow = fmaxf(Mrow, __ldcg(&a.part_m[part0 + q]));
-  double acc = 0.0;
-  if (warp == 0) {
-    for (int q = lane; q < a.C; q += 32) {
-      float mq = __ldcg(&a.part_m[part0 + q]);
-      double sq = __ldcg(&a.part_s[part0 + q]);
-      if (mq != -INFINITY) acc += sq * exp((double)mq - (double)Mrow);
-    }
-    acc = warp_sum_d(acc);
+  const size_t part0 = (size_t)m.row * a.C;
+  float *pm = sc.lanemax;  // [C] chunk maxima (C <= 256)
+  int *offs = sc.scan;     // [C + 1] list starts
+  if (tid < a.C) {
+    pm[tid] = __ldcg(&a.part_m[part0 + tid]);
+    offs[tid + 1] = __ldcg(&a.part_n[part0 + tid]);
   }
-  // stage the sorted chunk lists in shared memory (reusing the chunk buffer)
-  uint64_t *lists = reinterpret_cast<uint64_t *>(buf);
-  int *offs = sc.scan;  // offs[q] = start of list q, offs[C] = total
+  __syncthreads();
   if (tid == 0) {
-    int run = 0;
-    for (int q = 0; q < a.C; ++q) { offs[q] = run; run += __ldcg(&a.part_n[part0 + q]); }
-    offs[a.C] = run;
+    offs[0] = 0;
+    for (int q = 0; q < a.C; ++q) offs[q + 1] += offs[q];
+  }
+  float Mrow = -INFINITY;
+  for (int q = 0; q < a.C; ++q) Mrow = fmaxf(Mrow, pm[q]);
+  if (warp == 0) {
+    float2 acc = make_float2(0.f, 0.f);
+    for (int q = lane; q < a.C; q += 32) {
+      const float mq = pm[q];
+      if (mq != -INFINITY) {
+        const float2 sq = __ldcg(&a.part_s[part0 + q]);
+        const float e = expf(mq - Mrow);
+        const float ph = sq.x * e;
+        const float pl = fmaf(sq.x, e, -ph) + sq.y * e;
+        acc = ff_add(acc, make_float2(ph, pl));
+      }
+    }
+    acc = ff_warp_sum(acc);
+    if (lane == 0) sc.s_row = acc;
   }
   __syncthreads();
   const int total = offs[a.C];
@@ -403,7 +467,6 @@ __global__ void __launch_bounds__(kT, 4) topk_chunk_kernel(TopkArgs a) {
     lists[i] = __ldcg(&a.part_keys[(part0 + q) * a.K + (i - offs[q])]);
   }
   __syncthreads();
-  uint64_t *final_keys = surv;
   for (int i = tid; i < total; i += kT) {
     int q = 0;
     while (offs[q + 1] <= i) ++q;
@@ -413,29 +476,32 @@ __global__ void __launch_bounds__(kT, 4) topk_chunk_kernel(TopkArgs a) {
       if (o == q) continue;
       int lo = offs[o], hi = offs[o + 1];
       while (lo < hi) {
-        int mid = (lo + hi) >> 1;
+        const int mid = (lo + hi) >> 1;
         if (lists[mid] > key) lo = mid + 1; else hi = mid;
       }
       rk += lo - offs[o];
     }
-    if (rk < a.K) final_keys[rk] = key;
+    if (rk < a.K) surv[rk] = key;
   }
+  __shared__ double s_lse;
   if (tid == 0) {
-    double lse = (double)Mrow + log(acc);
-    sc.red_d[0] = lse;
+    const float2 s = sc.s_row;
+    const double acc = (double)s.x + (double)s.y;
+    const double lse = (double)Mrow + log(acc);
+    s_lse = lse;
     int st = 0;
     if (Mrow == INFINITY || !(acc == acc) || acc == INFINITY) st |= BASTION_STATUS_NONFINITE;
     if (Mrow == -INFINITY) st |= BASTION_STATUS_EMPTY_ROW;
     if (st) atomicOr(&a.status[req], st);
-    a.lse[row] = lse;
-    a.row_cnt[row] = 0u;
+    a.lse[m.row] = lse;
+    a.row_cnt[m.row] = 0u;
   }
   __syncthreads();
-  const double lse = sc.red_d[0];
+  const double lse = s_lse;
   for (int j = tid; j < a.K; j += kT) {
-    const uint64_t key = final_keys[j];
+    const uint64_t key = surv[j];
     const float v = key_value(key);
-    const size_t o = (size_t)row * a.K + j;
+    const size_t o = (size_t)m.row * a.K + j;
     a.topk_logit[o] = v;
     a.topk_tok[o] = (int32_t)key_token(key);
     if (a.topk_logq) a.topk_logq[o] = (float)((double)v - lse);
@@ -445,19 +511,25 @@ __global__ void __launch_bounds__(kT, 4) topk_chunk_kernel(TopkArgs a) {
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct TopkPlan {
-  int CL, C;
+  int CL, C, cap, chunk_bytes, lists_bytes;
   size_t smem;
 };
 
 TopkPlan plan_topk(int V, int K, int es) {
   TopkPlan p;
-  p.CL = es == 2 ? 16384 : 8192;
-  p.C = (V + p.CL - 1) / p.CL;
-  while (p.C > 256 || (size_t)p.C * K * 8 > (size_t)p.CL * es) {
-    p.CL *= 2;
-    p.C = (V + p.CL - 1) / p.CL;
+  int cl_max = es == 2 ? 16384 : 8192;  // 32 KB chunks
+  for (;;) {
+    p.C = (V + cl_max - 1) / cl_max;
+    p.CL = (V + p.C - 1) / p.C;
+    p.CL = (p.CL + 7) & ~7;
+    if (p.C <= 256 && (size_t)p.C * K * 8 <= (size_t)cl_max * es) break;
+    cl_max *= 2;
   }
-  p.smem = 16 + kCap * 8 + ((sizeof(Scratch) + 127) / 128) * 128 + kPad + (size_t)p.CL * es + 32;
+  p.cap = ((K > 512 ? K : 512) + 15) & ~15;  // keeps every later section 16-byte aligned
+  p.chunk_bytes = (int)(((size_t)kPad + (size_t)p.CL * es + 32 + 127) / 128 * 128);
+  p.lists_bytes = (int)(((size_t)p.C * K * 8 + 127) / 128 * 128);
+  p.smem = 128 + (size_t)p.cap * 8 + ((sizeof(Scratch) + 127) / 128) * 128 + p.lists_bytes +
+           p.chunk_bytes;
   return p;
 }
 
@@ -471,7 +543,7 @@ size_t topk_workspace_bytes(int B, int b, int V, int K, int es) {
 
 int topk_max_smem_ok(int V, int K, int es) {
   TopkPlan p = plan_topk(V, K, es);
-  return p.smem <= 200 * 1024;
+  return p.smem <= 227 * 1024;
 }
 
 int launch_topk(const void *logits, int dtype, int B, int b, int V, int64_t ld, int K,
@@ -487,6 +559,9 @@ int launch_topk(const void *logits, int dtype, int B, int b, int V, int64_t ld, 
   a.K = K;
   a.CL = p.CL;
   a.C = p.C;
+  a.cap = p.cap;
+  a.chunk_bytes = p.chunk_bytes;
+  a.lists_bytes = p.lists_bytes;
   a.ld = ld;
   a.topk_logq = topk_logq;
   a.topk_logit = topk_logit;
@@ -497,24 +572,18 @@ int launch_topk(const void *logits, int dtype, int B, int b, int V, int64_t ld, 
   unsigned char *w = static_cast<unsigned char *>(ws);
   a.part_m = reinterpret_cast<float *>(w);
   w += align256(P * 4);
-  a.part_s = reinterpret_cast<double *>(w);
+  a.part_s = reinterpret_cast<float2 *>(w);
   w += align256(P * 8);
   a.part_n = reinterpret_cast<int32_t *>(w);
   w += align256(P * 4);
   a.part_keys = reinterpret_cast<uint64_t *>(w);
   w += align256(P * K * 8);
   a.row_cnt = reinterpret_cast<uint32_t *>(w);
-  const unsigned grid = (unsigned)P;
-  if (es == 4) {
-    if (p.smem > 48 * 1024)
-      cudaFuncSetAttribute(topk_chunk_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
-    topk_chunk_kernel<4><<<grid, kT, p.smem, stream>>>(a);
-  } else {
-    if (p.smem > 48 * 1024)
-      cudaFuncSetAttribute(topk_chunk_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
-    topk_chunk_kernel<2><<<grid, kT, p.smem, stream>>>(a);
-  }
-  return cudaGetLastError() == cudaSuccess ? BASTION_OK : BASTION_ERR_LAUNCH;
+  auto kern = es == 4 ? topk_kernel<4> : topk_kernel<2>;
+  if (p.smem > 48 * 1024)
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
+  const cudaError_t e = launch_pdl(kern, dim3((unsigned)P), dim3(kT), p.smem, stream, a);
+  return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? BASTION_OK : BASTION_ERR_LAUNCH;
 }
 
 }  // namespace bastion

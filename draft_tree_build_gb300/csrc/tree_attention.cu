@@ -187,6 +187,8 @@ __global__ void __launch_bounds__(kAT, 1)
   volatile int *abort = &bs.abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  griddep_wait();
+  griddep_launch_dependents();
   const int qt = blockIdx.x % a.qt_max;
   const int g = (blockIdx.x / a.qt_max) % a.Hkv;
   const int r = blockIdx.x / (a.qt_max * a.Hkv);
@@ -499,8 +501,9 @@ int launch_attention(const void *q, const void *k, const void *v, int B, int n_m
   a.status = status;
   cudaFuncSetAttribute(tree_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
   const long long grid = (long long)B * Hkv * a.qt_max;
-  tree_attention_kernel<<<(unsigned)grid, kAT, kSmem, stream>>>(mq, mk, mv, a);
-  return cudaGetLastError() == cudaSuccess ? BASTION_OK : BASTION_ERR_LAUNCH;
+  const cudaError_t e = launch_pdl(tree_attention_kernel, dim3((unsigned)grid), dim3(kAT), kSmem,
+                                   stream, mq, mk, mv, a);
+  return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? BASTION_OK : BASTION_ERR_LAUNCH;
 }
 
 }  // namespace bastion

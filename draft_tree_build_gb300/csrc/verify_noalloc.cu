@@ -9,7 +9,7 @@
 // fixed array compiled into the library instead of a caller-provided workspace.
 //
 // The array below is a file-scope __device__ array: every GPU that loads the
-// library holds it (144 KiB) until the process exits.  Its name is only a
+// library holds it (128 KiB) until the process exits.  Its name is only a
 // host-side stand-in in host code, so the host looks up its device address
 // once per device with cudaGetSymbolAddress (with that device current) and
 // passes that address to the kernel.
@@ -31,10 +31,10 @@ int launch_verify(const void *target, int dtype, int B, int n_max, int V, int64_
 namespace {
 
 // Largest sizes the fixed scratch covers: B * n_max <= 16384 node rows (one
-// 8-byte key each) and B <= 4096 requests (one 4-byte counter each).
+// 8-byte key each) and B <= 4096 requests.
 constexpr int kMaxRows = 16384;
 constexpr int kMaxRequests = 4096;
-constexpr size_t kScratchBytes = (size_t)kMaxRows * 8 + (size_t)kMaxRequests * 4;
+constexpr size_t kScratchBytes = (size_t)kMaxRows * 8;
 
 static __device__ __align__(256) unsigned char g_verify_scratch[kScratchBytes];
 
@@ -80,8 +80,8 @@ extern "C" int bastion_verify_greedy_noalloc(const void *target_logits, int dtyp
   if (need > kScratchBytes) return BASTION_ERR_SIZE;
   void *scratch = scratch_for_current_device();
   if (!scratch) return BASTION_ERR_LAUNCH;
-  // The array keeps whatever the previous call left; the keys and counters this
-  // call uses must start at zero.
+  // The array keeps whatever the previous call left; the keys this call uses
+  // must start at zero.
   if (cudaMemsetAsync(scratch, 0, need, (cudaStream_t)stream) != cudaSuccess)
     return BASTION_ERR_LAUNCH;
   return bastion::launch_verify(target_logits, dtype, B, n_max, V, ld_row, b, n_nodes, parent,

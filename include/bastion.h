@@ -195,7 +195,7 @@ int bastion_verify_greedy(const void *target_logits, int dtype, int B, int n_max
  * serving loop that must not touch the allocator after start-up, code inside a
  * framework that owns the allocator, a plug-in that only receives input and
  * output pointers).  This entry point takes the same arguments and gives the
- * same results as bastion_verify_greedy, but its scratch is a fixed 144 KiB
+ * same results as bastion_verify_greedy, but its scratch is a fixed 128 KiB
  * array compiled into the library, which every GPU that loads the library
  * holds until the process exits; it calls no cudaMalloc or cudaFree.
  * Limits: B <= 4096 and B * n_max <= 16384 (e.g. 64 requests x 256 nodes);
