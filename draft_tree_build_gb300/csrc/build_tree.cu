@@ -20,10 +20,13 @@
 //    rho, then tie bits 0xFFFFFF - (depth<<18 | rank<<8 | parent) so equal
 //    scores prefer lower depth, rank and parent.  A pop is three redux.sync
 //    reductions over the lanes' cached best keys.
-//  * When node n is created its first 32 child keys (and their rho) are
-//    computed at once, one rank per lane, into shared memory; the next block of
-//    32 is computed when a node's rank pointer runs past its block.  A pop thus
-//    does no fp64 work and at most one parallel key computation.
+//  * Each slot keeps, in a shared-memory record, its next-ranked candidate
+//    (key and logit sum) and the first-child key of both its current and next
+//    candidate.  A pop reads the winner's record: the winner's slot moves to
+//    its next candidate and the new node's slot starts at the precomputed first
+//    child, so the pop itself does only integer work and one expf (rho of the
+//    winner, for the stop test).  The three records the pop invalidates are
+//    recomputed afterwards, one per lane in a single SIMT pass.
 //  * Stop test before adding candidate c to a tree of N nodes (C > 0):
 //    S(N+1) < S(N)  <=>  rho_c C(N) < A_hat (C(N+1) - C(N)), in fp32 with
 //    A_hat summed with Kahan compensation.
@@ -75,21 +78,6 @@ __device__ __forceinline__ F2 f2_sub(F2 a, F2 b) {
   return {h, e - (h - s)};
 }
 
-struct KeyE {  // one candidate: key words and rho
-  uint32_t h, l, t;
-  float rho;
-};
-
-__device__ __forceinline__ KeyE make_cand(F2 lr, int d, int j, int p) {
-  KeyE k;
-  k.h = ord_f32(lr.h);
-  k.l = ord_f32(lr.l);
-  k.t = 0xFFFFFFu - (((uint32_t)d << 18) | ((uint32_t)j << 8) | (uint32_t)p);
-  const float e = lr.h < -104.f ? 0.f : expf(lr.h);
-  k.rho = fmaf(e, lr.l, e);
-  return k;
-}
-
 __device__ __forceinline__ bool key_gt(uint32_t ah, uint32_t al, uint32_t at, uint32_t bh,
                                        uint32_t bl, uint32_t bt) {
   if (ah != bh) return ah > bh;
@@ -97,14 +85,50 @@ __device__ __forceinline__ bool key_gt(uint32_t ah, uint32_t al, uint32_t at, ui
   return at > bt;
 }
 
+// Record of a candidate (parent P, rank j, depth d): its key, its logit sum and
+// the key of its first child (whose parent index is filled in at pop time).
+struct Cand {
+  uint32_t h, l, t;    // key (0, 0, 0 = none)
+  F2 L;                // path logit sum
+  uint32_t ch, cl, ct; // first child key; ct lacks the child's parent index
+};
+
+__device__ __forceinline__ Cand cand_of(F2 Lp, int P, int d, int j, int b, int R, const float *lg,
+                                        const F2 *Lam) {
+  Cand c = {0u, 0u, 0u, {0.f, 0.f}, 0u, 0u, 0u};
+  if (j >= R) return c;
+  c.L = f2_add(Lp, lg[(d - 1) * R + j]);
+  const F2 lr = f2_sub(c.L, Lam[d]);
+  c.h = ord_f32(lr.h);
+  c.l = ord_f32(lr.l);
+  c.t = 0xFFFFFFu - (((uint32_t)d << 18) | ((uint32_t)j << 8) | (uint32_t)P);
+  if (d < b) {
+    const F2 lg2 = f2_sub(f2_add(c.L, lg[d * R]), Lam[d + 1]);
+    c.ch = ord_f32(lg2.h);
+    c.cl = ord_f32(lg2.l);
+    c.ct = 0xFFFFFFu - ((uint32_t)(d + 1) << 18);
+  }
+  return c;
+}
+
+// Shared-memory record of slot s: its current candidate's logit sum and first
+// child key, and its next candidate (key, logit sum, first child key).
+struct Rec {
+  F2 cL;
+  uint32_t ch, cl, ct;
+  uint32_t nh, nl, nt;
+  F2 nL;
+  uint32_t nch, ncl, nct;
+  uint32_t pad[3];
+};
+
 template <int S>  // register slots per lane: S * 32 >= n_max
 __global__ void __launch_bounds__(32) build_tree_kernel(TreeArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
-  uint4 *blk = reinterpret_cast<uint4 *>(smem);                    // [n_max][32] keys of children
-  F2 *Lnode = reinterpret_cast<F2 *>(blk + (size_t)a.n_max * 32);  // [n_max] path logit sums
-  F2 *Lam = Lnode + a.n_max;                                        // [33]
-  int *base = reinterpret_cast<int *>(Lam + 33);                    // [n_max] first rank in blk
-  float *C = reinterpret_cast<float *>(base + a.n_max);             // [n_max + 1]
+  Rec *rec = reinterpret_cast<Rec *>(smem);                         // [n_max]
+  F2 *Lam = reinterpret_cast<F2 *>(rec + a.n_max);                  // [33]
+  F2 *Lnode = Lam + 33;                                              // [n_max] node logit sums
+  float *C = reinterpret_cast<float *>(Lnode + a.n_max);             // [n_max + 1]
   uint32_t *mask = reinterpret_cast<uint32_t *>(C + a.n_max + 1);   // [n_max * W]
   float *lg = reinterpret_cast<float *>(mask + a.n_max * a.W);      // [b * R]
   int *tk = reinterpret_cast<int *>(lg + a.b * a.R);                 // [b * R]
@@ -126,15 +150,21 @@ __global__ void __launch_bounds__(32) build_tree_kernel(TreeArgs a) {
     if (i >= 1) bad |= !(c > 0.f) || isinf(c);
   }
   if (__any_sync(kFull, bad) && lane == 0) atomicOr(&a.status[r], BASTION_STATUS_BAD_COST);
-  if (lane == 0) {
-    // Lam[d] = lse_1 + ... + lse_d in fp64, then as a float pair
-    double acc = 0.0;
-    Lam[0] = {0.f, 0.f};
-    for (int d = 1; d <= b; ++d) {
-      acc = acc + a.lse[(size_t)r * b + d - 1];
-      const float h = (float)acc;
-      Lam[d] = {h, (float)(acc - (double)h)};
+  {
+    // Lam[d] = lse_1 + ... + lse_d: each lse as a float pair, then a prefix scan
+    F2 v = {0.f, 0.f};
+    if (lane < b) {
+      const double x = a.lse[(size_t)r * b + lane];
+      const float h = (float)x;
+      v = {h, (float)(x - (double)h)};
     }
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const F2 u = {__shfl_up_sync(kFull, v.h, o), __shfl_up_sync(kFull, v.l, o)};
+      if (lane >= o) v = f2_sub(v, F2{-u.h, -u.l});
+    }
+    if (lane < b) Lam[lane + 1] = v;
+    if (lane == 0) Lam[0] = {0.f, 0.f};
   }
   const int ctx = a.ctx_len[r];
   const float L_ar = a.l_ar[r];
@@ -149,7 +179,6 @@ __global__ void __launch_bounds__(32) build_tree_kernel(TreeArgs a) {
     a.a_hat[nb] = 1.f;
     a.speedup[nb] = L_ar / C[1];
     Lnode[0] = {0.f, 0.f};
-    base[0] = 0;
   }
   for (int w = lane; w < W; w += 32) {
     const uint32_t m = w == 0 ? 1u : 0u;
@@ -158,21 +187,24 @@ __global__ void __launch_bounds__(32) build_tree_kernel(TreeArgs a) {
   }
   __syncwarp();
 
-  // children of the root: ranks 0..31 at depth 1
-  {
-    const F2 lam = Lam[1];
-    KeyE k = {0u, 0u, 0u, 0.f};
-    if (lane < R) k = make_cand(f2_sub(f2_add({0.f, 0.f}, lg[lane]), lam), 1, lane, 0);
-    blk[lane] = make_uint4(k.h, k.l, k.t, __float_as_uint(k.rho));
-  }
+  // the root's slot: current candidate (0, 0), next (0, 1)
   uint32_t kh[S], kl[S], kt[S];
 #pragma unroll
   for (int s = 0; s < S; ++s) kh[s] = kl[s] = kt[s] = 0u;
-  __syncwarp();
-  if (lane == 0) {
-    const uint4 e = blk[0];
-    kh[0] = e.x; kl[0] = e.y; kt[0] = e.z;
+  {
+    const Cand c = cand_of({0.f, 0.f}, 0, 1, lane, b, R, lg, Lam);  // lanes 0, 1 used
+    const Cand c0 = {__shfl_sync(kFull, c.h, 0), __shfl_sync(kFull, c.l, 0), __shfl_sync(kFull, c.t, 0),
+                     {__shfl_sync(kFull, c.L.h, 0), __shfl_sync(kFull, c.L.l, 0)},
+                     __shfl_sync(kFull, c.ch, 0), __shfl_sync(kFull, c.cl, 0), __shfl_sync(kFull, c.ct, 0)};
+    if (lane == 1) {
+      Rec q;
+      q.cL = c0.L; q.ch = c0.ch; q.cl = c0.cl; q.ct = c0.ct;
+      q.nh = c.h; q.nl = c.l; q.nt = c.t; q.nL = c.L; q.nch = c.ch; q.ncl = c.cl; q.nct = c.ct;
+      rec[0] = q;
+    }
+    if (lane == 0) { kh[0] = c0.h; kl[0] = c0.l; kt[0] = c0.t; }
   }
+  __syncwarp();
   uint32_t bh = kh[0], bl = kl[0], bt = kt[0];
 
   float A_hi = 1.f, A_lo = 0.f;  // A_hat with Kahan compensation
@@ -182,12 +214,12 @@ __global__ void __launch_bounds__(32) build_tree_kernel(TreeArgs a) {
     const uint32_t ml = __reduce_max_sync(kFull, bh == mh ? bl : 0u);
     const uint32_t mt = __reduce_max_sync(kFull, (bh == mh && bl == ml) ? bt : 0u);
     if ((mh | ml | mt) == 0u) break;  // no candidate left
-    const float lr_h = unord_f32(mh);
+    const float lr_h = unord_f32(mh), lr_l = unord_f32(ml);
     if (lr_h == -INFINITY) break;
     const uint32_t sec = 0xFFFFFFu - mt;
     const int d = (int)(sec >> 18), j = (int)((sec >> 8) & 1023u), p = (int)(sec & 255u);
-    const int bp = base[p];
-    const float rho = __uint_as_float(blk[(size_t)p * 32 + (j - bp)].w);
+    const float e = lr_h < -104.f ? 0.f : expf(lr_h);
+    const float rho = fmaf(e, lr_l, e);
     const float Cp = C[N], Cn = C[N + 1];
     if (rho * Cp < (A_hi + A_lo) * (Cn - Cp)) break;  // S would decrease: keep T_N
 
@@ -199,33 +231,54 @@ __global__ void __launch_bounds__(32) build_tree_kernel(TreeArgs a) {
       A_lo = (t - A_hi) - y;
       A_hi = t;
     }
-    const F2 Ln = f2_add(Lnode[p], lg[(d - 1) * R + j]);
-    // children of the new node: ranks lane (and further blocks later)
-    uint32_t c0h = 0u, c0l = 0u, c0t = 0u;
-    if (d < b) {
-      const F2 lam = Lam[d + 1];
-      KeyE k = {0u, 0u, 0u, 0.f};
-      if (lane < R) k = make_cand(f2_sub(f2_add(Ln, lg[d * R + lane]), lam), d + 1, lane, n);
-      blk[(size_t)n * 32 + lane] = make_uint4(k.h, k.l, k.t, __float_as_uint(k.rho));
-      c0h = __shfl_sync(kFull, k.h, 0);
-      c0l = __shfl_sync(kFull, k.l, 0);
-      c0t = __shfl_sync(kFull, k.t, 0);
+    const Rec w = rec[p];
+    // critical path: the two slots that change
+    if (lane == (p & 31)) {
+      const int s0 = p >> 5;
+#pragma unroll
+      for (int s = 0; s < S; ++s)
+        if (s == s0) { kh[s] = w.nh; kl[s] = w.nl; kt[s] = w.nt; }
     }
-    // node p's next-ranked child replaces (p, j); a new block when needed
-    const int jn = j + 1;
-    if (jn < R && jn - bp == 32) {
-      const F2 lam = Lam[d];
-      const F2 Lp = Lnode[p];
-      KeyE k = {0u, 0u, 0u, 0.f};
-      if (jn + lane < R) k = make_cand(f2_sub(f2_add(Lp, lg[(d - 1) * R + jn + lane]), lam), d, jn + lane, p);
-      blk[(size_t)p * 32 + lane] = make_uint4(k.h, k.l, k.t, __float_as_uint(k.rho));
+    if (d < b && lane == (n & 31)) {
+      const int s1 = n >> 5;
+#pragma unroll
+      for (int s = 0; s < S; ++s)
+        if (s == s1) { kh[s] = w.ch; kl[s] = w.cl; kt[s] = w.ct - (uint32_t)n; }
+    }
+    if (lane == (p & 31) || (d < b && lane == (n & 31))) {
+      bh = kh[0]; bl = kl[0]; bt = kt[0];
+#pragma unroll
+      for (int s = 1; s < S; ++s)
+        if (key_gt(kh[s], kl[s], kt[s], bh, bl, bt)) { bh = kh[s]; bl = kl[s]; bt = kt[s]; }
+    }
+    // the records this pop invalidates, one per lane:
+    //   lane 0: slot p's new next candidate (p, j + 2)
+    //   lane 1: the new node's current candidate (n, 0) (logit sum, first child)
+    //   lane 2: the new node's next candidate (n, 1)
+    {
+      F2 Lpar = w.cL;  // the new node's logit sum
+      int P = n, dd = d + 1, jj = lane - 1;
+      if (lane == 0) { Lpar = Lnode[p]; P = p; dd = d; jj = j + 2; }
+      Cand c = {0u, 0u, 0u, {0.f, 0.f}, 0u, 0u, 0u};
+      if (lane < 3 && dd <= b) c = cand_of(Lpar, P, dd, jj, b, R, lg, Lam);
       __syncwarp();
-      if (lane == 0) base[p] = jn;
+      if (lane == 3) Lnode[n] = w.cL;
+      if (lane == 0) {
+        // slot p advances: current <- next, next <- (p, j + 2)
+        Rec q = w;
+        q.cL = w.nL; q.ch = w.nch; q.cl = w.ncl; q.ct = w.nct;
+        q.nh = c.h; q.nl = c.l; q.nt = c.t; q.nL = c.L; q.nch = c.ch; q.ncl = c.cl; q.nct = c.ct;
+        rec[p] = q;
+      }
+      if (d < b) {
+        if (lane == 1) { rec[n].cL = c.L; rec[n].ch = c.ch; rec[n].cl = c.cl; rec[n].ct = c.ct; }
+        if (lane == 2) {
+          rec[n].nh = c.h; rec[n].nl = c.l; rec[n].nt = c.t; rec[n].nL = c.L;
+          rec[n].nch = c.ch; rec[n].ncl = c.cl; rec[n].nct = c.ct;
+        }
+      }
     }
-    __syncwarp();
     if (lane == 0) {
-      Lnode[n] = Ln;
-      base[n] = 0;
       const size_t o = nb + n;
       const float Ah = A_hi + A_lo;
       a.parent[o] = p;
@@ -237,33 +290,10 @@ __global__ void __launch_bounds__(32) build_tree_kernel(TreeArgs a) {
       a.a_hat[o] = Ah;
       a.speedup[o] = Ah * L_ar / Cn;
     }
-    for (int w = lane; w < W; w += 32) {
-      const uint32_t m = mask[p * W + w] | (w == (n >> 5) ? (1u << (n & 31)) : 0u);
-      mask[n * W + w] = m;
-      a.anc_mask[(nb + n) * W + w] = m;
-    }
-    bool touched = false;
-    if (lane == (p & 31)) {
-      uint4 e = make_uint4(0u, 0u, 0u, 0u);
-      if (jn < R) e = blk[(size_t)p * 32 + (jn - (jn - bp == 32 ? jn : bp))];
-      const int s0 = p >> 5;
-#pragma unroll
-      for (int s = 0; s < S; ++s)
-        if (s == s0) { kh[s] = e.x; kl[s] = e.y; kt[s] = e.z; }
-      touched = true;
-    }
-    if (d < b && lane == (n & 31)) {
-      const int s1 = n >> 5;
-#pragma unroll
-      for (int s = 0; s < S; ++s)
-        if (s == s1) { kh[s] = c0h; kl[s] = c0l; kt[s] = c0t; }
-      touched = true;
-    }
-    if (touched) {
-      bh = kh[0]; bl = kl[0]; bt = kt[0];
-#pragma unroll
-      for (int s = 1; s < S; ++s)
-        if (key_gt(kh[s], kl[s], kt[s], bh, bl, bt)) { bh = kh[s]; bl = kl[s]; bt = kt[s]; }
+    for (int q = lane; q < W; q += 32) {
+      const uint32_t m = mask[p * W + q] | (q == (n >> 5) ? (1u << (n & 31)) : 0u);
+      mask[n * W + q] = m;
+      a.anc_mask[(nb + n) * W + q] = m;
     }
     __syncwarp();
   }
@@ -311,8 +341,8 @@ int launch_build_tree(const float *topk_logit, const int32_t *topk_tok, const do
   a.speedup = speedup;
   a.anc_mask = anc_mask;
   a.status = status;
-  const size_t smem = (size_t)n_max * 32 * 16 + (size_t)n_max * 8 + 33 * 8 + (size_t)n_max * 4 +
-                      (size_t)(n_max + 1) * 4 + (size_t)n_max * a.W * 4 + (size_t)b * a.R * 8;
+  const size_t smem = (size_t)n_max * 64 + 33 * 8 + (size_t)n_max * 8 + (size_t)(n_max + 1) * 4 +
+                      (size_t)n_max * a.W * 4 + (size_t)b * a.R * 8;
   if (n_max <= 32) launch_s<1>(a, smem, stream);
   else if (n_max <= 64) launch_s<2>(a, smem, stream);
   else if (n_max <= 128) launch_s<4>(a, smem, stream);

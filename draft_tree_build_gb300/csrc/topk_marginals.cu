@@ -10,23 +10,24 @@
 //    (cp.async.bulk), so the chunk is read from HBM once and swept twice from
 //    shared memory, while the other CTAs resident on the SM keep their copies
 //    in flight;
-//  * sweep 1: per-thread maxima.  The chunk max M_c comes from them, and so
-//    does a prefilter threshold T0 = the K-th largest of the 256 thread maxima
-//    (found by counting in the 8 warp-sorted lists): at least K distinct
-//    elements reach T0, so every top-K element of the chunk is >= T0;
+//  * sweep 1: the max of each 16-byte vector (packed bf16x2 max), kept in
+//    registers, and per-thread maxima.  The chunk max M_c comes from them, and
+//    so does a prefilter threshold T0: a two-pass radix select over the 16-bit
+//    prefixes of the 256 thread maxima finds the K-th largest prefix, and the
+//    smallest value with that prefix is reached by at least K distinct
+//    elements, so every top-K element of the chunk is >= T0;
 //  * sweep 2: sum of exp(l - M_c) with packed f32x2 arithmetic and ex2, the
 //    log2(e) factor split in two parts so its rounding does not bias all terms
-//    alike, fp32 per 8-element vector and Kahan-compensated per thread, then a
-//    compensated (two-float) reduction; and compaction of the few elements
-//    >= T0 (about K of them);
-//  * the survivors are ranked exactly by counting (keys are unique: value desc,
-//    token asc); if they do not fit (heavy ties at T0) an exact radix select
-//    over the whole chunk takes over;
+//    alike, then a compensated (two-float) reduction across threads; vectors
+//    whose max reaches T0 append their elements >= T0 (about K of them);
+//  * the survivors are sorted by one warp (register bitonic network on the
+//    64-bit keys value desc, token asc; counting rank beyond 256 survivors, an
+//    exact radix select over the chunk if they do not fit at all);
 //  * the last CTA of a row to finish (atomic arrival counter, no waiting)
 //    merges the chunk partials: M = max M_c, s = sum s_c exp(M_c - M) as a
-//    two-float sum, lse = M + log s in fp64, and the top-K of the union of the
-//    sorted chunk lists by rank = own position + binary-search counts in the
-//    other lists.
+//    two-float sum, lse = M + log s in fp64; the best chunk K-th key bounds
+//    the row's K-th key from below, so only list entries at or above it are
+//    sorted for the row's top-K.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -56,12 +57,14 @@ struct TopkArgs {
 };
 
 struct Scratch {
-  float lanemax[kT];  // warp-sorted thread maxima (descending per warp)
+  float lanemax[kT];  // chunk maxima during the merge
+  uint32_t hist2[256];
   float red_f[8];
   float2 red_s[8];
   float2 s_row;
   uint32_t hist[256];
-  uint32_t t0_ord;
+  unsigned long long kth;
+  int n_cand;
   int n_surv;
   int last;
   uint32_t digit_info[2];
@@ -165,6 +168,83 @@ __device__ __forceinline__ float warp_sort_desc(float v, int lane) {
     }
   }
   return v;
+}
+
+// Descending bitonic sort of NPL*32 64-bit keys, NPL per lane (element
+// e = i*32 + lane lives in v[i] of that lane).
+template <int NPL>
+__device__ __forceinline__ void warp_bitonic_desc(uint64_t (&v)[NPL], int lane) {
+  constexpr int N = NPL * 32;
+#pragma unroll
+  for (int k = 2; k <= N; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      if (j >= 32) {
+        const int jj = j >> 5;
+#pragma unroll
+        for (int i = 0; i < NPL; ++i) {
+          const int ip = i ^ jj;
+          if (ip > i) {
+            const bool desc = ((i * 32 + lane) & k) == 0;
+            const uint64_t x = v[i], y = v[ip];
+            const bool sw = desc ? (x < y) : (x > y);
+            v[i] = sw ? y : x;
+            v[ip] = sw ? x : y;
+          }
+        }
+      } else {
+        const bool lower = (lane & j) == 0;
+#pragma unroll
+        for (int i = 0; i < NPL; ++i) {
+          const uint64_t o = __shfl_xor_sync(kFull, v[i], j);
+          const bool desc = ((i * 32 + lane) & k) == 0;
+          const bool keep_max = desc == lower;
+          v[i] = keep_max ? (v[i] > o ? v[i] : o) : (v[i] < o ? v[i] : o);
+        }
+      }
+    }
+  }
+}
+
+// Sort n <= NPL*32 keys from src (descending) with warp 0 and write the first
+// min(n, K) of them to dst.
+template <int NPL>
+__device__ __forceinline__ void warp_sort_write(const uint64_t *src, int n, int K, uint64_t *dst,
+                                                int lane) {
+  uint64_t v[NPL];
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const int e = i * 32 + lane;
+    v[i] = e < n ? src[e] : 0ull;
+  }
+  warp_bitonic_desc<NPL>(v, lane);
+  const int lim = min(n, K);
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const int e = i * 32 + lane;
+    if (e < lim) dst[e] = v[i];
+  }
+}
+
+// Rank n unique keys of src exactly and write the first min(n, K), sorted
+// descending, to dst (all threads of the CTA call it; a barrier must follow
+// before dst is read when dst is shared memory).
+__device__ __forceinline__ void sort_top(const uint64_t *src, int n, int K, uint64_t *dst) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  if (n <= 64) {
+    if (tid < 32) warp_sort_write<2>(src, n, K, dst, lane);
+  } else if (n <= 128) {
+    if (tid < 32) warp_sort_write<4>(src, n, K, dst, lane);
+  } else if (n <= 256) {
+    if (tid < 32) warp_sort_write<8>(src, n, K, dst, lane);
+  } else {
+    for (int i = tid; i < n; i += kT) {
+      const uint64_t ki = src[i];
+      int rk = 0;
+      for (int j = 0; j < n; ++j) rk += src[j] > ki;
+      if (rk < K) dst[rk] = ki;
+    }
+  }
 }
 
 // Number of entries >= c in a descending list of 32.
@@ -288,13 +368,63 @@ __device__ __forceinline__ void append_lane(const float (&f)[NE], float T0, uint
 #pragma unroll
   for (int i = 0; i < NE; ++i) msk |= (f[i] >= T0 ? 1u : 0u) << i;
   int idx = atomicAdd(n_surv, __popc(msk));
+  while (msk) {
+    const int i = __ffs(msk) - 1;
+    msk &= msk - 1u;
+    float fi = f[0];
 #pragma unroll
-  for (int i = 0; i < NE; ++i) {
-    if ((msk >> i) & 1u) {
-      if (idx < cap) surv[idx] = make_key(f[i], tok0 + (uint32_t)i);
-      ++idx;
-    }
+    for (int q = 1; q < NE; ++q) fi = q == i ? f[q] : fi;
+    if (idx < cap) surv[idx] = make_key(fi, tok0 + (uint32_t)i);
+    ++idx;
   }
+}
+
+// Radix select of a threshold over the 16-bit prefixes of one value per
+// thread: returns the smallest float whose order key has the K-th largest
+// prefix (so >= K threads hold a value >= it).  All threads call it.
+__device__ __forceinline__ float kth_prefix_threshold(float v, int K, Scratch &sc) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  const uint32_t key = ord_f32(v) >> 16;
+  sc.hist[tid] = 0u;
+  sc.hist2[tid] = 0u;
+  __syncthreads();
+  atomicAdd(&sc.hist[key >> 8], 1u);
+  __syncthreads();
+  // digit d scanned from 255 down: lane owns digits 255-8*lane .. 255-8*lane-7
+  auto find = [&](const uint32_t *h, uint32_t need) {
+    uint32_t cnt[8], tot = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) { cnt[q] = h[255 - 8 * lane - q]; tot += cnt[q]; }
+    uint32_t incl = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const uint32_t above = incl - tot;
+    if (above < need && incl >= need) {
+      uint32_t run = above;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (run + cnt[q] >= need) {
+          sc.digit_info[0] = 255u - 8u * lane - q;
+          sc.digit_info[1] = run;
+          break;
+        }
+        run += cnt[q];
+      }
+    }
+  };
+  if (tid < 32) find(sc.hist, (uint32_t)K);
+  __syncthreads();
+  const uint32_t d1 = sc.digit_info[0], above1 = sc.digit_info[1];
+  if ((key >> 8) == d1) atomicAdd(&sc.hist2[key & 255u], 1u);
+  __syncthreads();
+  if (tid < 32) find(sc.hist2, (uint32_t)K - above1);
+  __syncthreads();
+  const uint32_t t16 = (d1 << 8) | sc.digit_info[0];
+  const float t = unord_f32(t16 << 16);
+  return t == t ? t : -INFINITY;  // the prefix of -inf maps to a NaN pattern
 }
 
 template <int ES>
@@ -309,6 +439,7 @@ __global__ void __launch_bounds__(kT, 4) topk_kernel(TopkArgs a) {
   unsigned char *body = chunk + kPad;
 
   constexpr int NE = 16 / ES;
+  constexpr int kVPT = 8;  // vectors per thread (chunks hold at most 8 * 256 vectors)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const Item m = item_at<ES>(a, blockIdx.x);
   const int req = m.row / a.b;
@@ -317,7 +448,6 @@ __global__ void __launch_bounds__(kT, 4) topk_kernel(TopkArgs a) {
     mbar_init(bar, 1);
     fence_mbar_init();
     sc.n_surv = 0;
-    sc.t0_ord = 0u;
   }
   griddep_wait();
   griddep_launch_dependents();
@@ -333,70 +463,62 @@ __global__ void __launch_bounds__(kT, 4) topk_kernel(TopkArgs a) {
     const int e = j < m.nh ? j : m.t0 + (j - m.nh);
     tmax = fmaxf(tmax, load_elem<ES>(m.g0 + (size_t)e * ES));
   }
-  if (m.body && !mbar_wait_bounded(bar, 0)) {
-    if (lane == 0) atomicOr(&a.status[req], BASTION_STATUS_TIMEOUT);
-  }
+  // one thread waits for the bulk copy; the barrier below releases the rest
+  // (spinning in every thread would take issue slots from the other CTAs)
+  if (tid == 0 && m.body && !mbar_wait_bounded(bar, 0)) atomicOr(&a.status[req], BASTION_STATUS_TIMEOUT);
+  __syncthreads();
 
-  // ---- sweep 1: maxima, and T0 = K-th largest thread maximum
-  for (int v = tid; v < m.nvec; v += kT) tmax = fmaxf(tmax, vmax<ES>(ld_shared_v4(body + v * 16)));
+  // ---- sweep 1: vector maxima (kept), thread maxima, chunk max, T0
+  float vm[kVPT];
+#pragma unroll
+  for (int u = 0; u < kVPT; ++u) {
+    const int v = tid + u * kT;
+    vm[u] = v < m.nvec ? vmax<ES>(ld_shared_v4(body + v * 16)) : -INFINITY;
+    tmax = fmaxf(tmax, vm[u]);
+  }
   {
     const float wm = warp_max_f(tmax);
-    sc.lanemax[warp * 32 + lane] = warp_sort_desc(tmax, lane);
     if (lane == 0) sc.red_f[warp] = wm;
   }
-  __syncthreads();  // A
+  float T0 = -INFINITY;
+  if (a.K <= kT) T0 = kth_prefix_threshold(tmax, a.K, sc);  // has barriers
+  else __syncthreads();                                     // the maxima above
   float M = -INFINITY;
 #pragma unroll
   for (int w = 0; w < kT / 32; ++w) M = fmaxf(M, sc.red_f[w]);
-  if (a.K <= kT) {
-    // candidate c = my sorted entry; T0 = the largest c with #(maxima >= c) >= K
-    const float c = sc.lanemax[tid];
-    int cnt = 0;
-#pragma unroll
-    for (int w = 0; w < kT / 32; ++w) cnt += count_ge(&sc.lanemax[w * 32], c);
-    uint32_t best = cnt >= a.K ? ord_f32(c) : 0u;
-    best = __reduce_max_sync(kFull, best);
-    if (lane == 0 && best) atomicMax(&sc.t0_ord, best);
-  }
-  __syncthreads();  // A2
-  const float T0 = sc.t0_ord ? unord_f32(sc.t0_ord) : -INFINITY;
   const bool have_mass = M != -INFINITY;
 
   // ---- sweep 2: sum of exp(l - M) and survivors >= T0
-  float sum = 0.f, comp = 0.f;
+  float sum = 0.f;
   const uint32_t tok_vec0 = (uint32_t)(m.e0 + m.nh);
-  for (int v = tid; v < m.nvec; v += kT) {
-    const uint4 x = ld_shared_v4(body + v * 16);
-    float f[NE];
-    unpack<ES>(x, f);
-    float vs;
-    if constexpr (ES == 2) {
-      float p0, p1, q0, q1;
-      exp4(f[0], f[1], f[2], f[3], M, p0, p1);
-      exp4(f[4], f[5], f[6], f[7], M, q0, q1);
-      vs = (p0 + p1) + (q0 + q1);
-    } else {
-      float p0, p1;
-      exp4(f[0], f[1], f[2], f[3], M, p0, p1);
-      vs = p0 + p1;
+#pragma unroll
+  for (int u = 0; u < kVPT; ++u) {
+    const int v = tid + u * kT;
+    if (v < m.nvec) {
+      const uint4 x = ld_shared_v4(body + v * 16);
+      float f[NE];
+      unpack<ES>(x, f);
+      if constexpr (ES == 2) {
+        float p0, p1, q0, q1;
+        exp4(f[0], f[1], f[2], f[3], M, p0, p1);
+        exp4(f[4], f[5], f[6], f[7], M, q0, q1);
+        sum += (p0 + p1) + (q0 + q1);
+      } else {
+        float p0, p1;
+        exp4(f[0], f[1], f[2], f[3], M, p0, p1);
+        sum += p0 + p1;
+      }
+      if (vm[u] >= T0) append_lane<NE>(f, T0, tok_vec0 + (uint32_t)(v * NE), surv, &sc.n_surv, a.cap);
     }
-    const float y = vs - comp;
-    const float t = sum + y;
-    comp = (t - sum) - y;
-    sum = t;
-    if (vmax<ES>(x) >= T0) append_lane<NE>(f, T0, tok_vec0 + (uint32_t)(v * NE), surv, &sc.n_surv, a.cap);
   }
   for (int j = tid; j < nscal; j += kT) {  // head and tail
     const int e = j < m.nh ? j : m.t0 + (j - m.nh);
     const float f[1] = {load_elem<ES>(m.g0 + (size_t)e * ES)};
-    const float y = exp_shifted(f[0] - M) - comp;
-    const float t = sum + y;
-    comp = (t - sum) - y;
-    sum = t;
+    sum += exp_shifted(f[0] - M);
     if (f[0] >= T0) append_lane<1>(f, T0, (uint32_t)(m.e0 + e), surv, &sc.n_surv, a.cap);
   }
   {
-    const float2 ws = ff_warp_sum(two_sum(sum, -comp));
+    const float2 ws = ff_warp_sum(make_float2(sum, 0.f));
     if (lane == 0) sc.red_s[warp] = ws;
   }
   __syncthreads();  // B
@@ -406,15 +528,9 @@ __global__ void __launch_bounds__(kT, 4) topk_kernel(TopkArgs a) {
     chunk_topk_exact<ES>(m, body, a.K, surv, sc);
     n_s = sc.n_surv;
   }
-  // ---- rank survivors exactly and write the chunk's sorted list
+  // ---- the chunk's sorted top list
   const size_t part = (size_t)m.row * a.C + m.c;
-  uint64_t *out_keys = a.part_keys + part * a.K;
-  for (int i = tid; i < n_s; i += kT) {
-    const uint64_t ki = surv[i];
-    int rk = 0;
-    for (int j = 0; j < n_s; ++j) rk += surv[j] > ki;
-    if (rk < a.K) out_keys[rk] = ki;
-  }
+  sort_top(surv, n_s, a.K, a.part_keys + part * a.K);
   if (tid == 0) {
     float2 st = make_float2(0.f, 0.f);
     for (int w = 0; w < kT / 32; ++w) st = ff_add(st, sc.red_s[w]);
@@ -437,7 +553,13 @@ __global__ void __launch_bounds__(kT, 4) topk_kernel(TopkArgs a) {
     pm[tid] = __ldcg(&a.part_m[part0 + tid]);
     offs[tid + 1] = __ldcg(&a.part_n[part0 + tid]);
   }
+  if (tid == 0) { sc.kth = 0ull; sc.n_cand = 0; }
   __syncthreads();
+  // the best chunk K-th key: every chunk holding K keys has K keys >= its K-th
+  if (tid < a.C && offs[tid + 1] == a.K) {
+    const uint64_t kth = __ldcg(&a.part_keys[(part0 + tid) * a.K + a.K - 1]);
+    atomicMax(reinterpret_cast<unsigned long long *>(&sc.kth), (unsigned long long)kth);
+  }
   if (tid == 0) {
     offs[0] = 0;
     for (int q = 0; q < a.C; ++q) offs[q + 1] += offs[q];
@@ -460,33 +582,21 @@ __global__ void __launch_bounds__(kT, 4) topk_kernel(TopkArgs a) {
     if (lane == 0) sc.s_row = acc;
   }
   __syncthreads();
+  // candidates: list entries at or above the bound (at least K of them)
   const int total = offs[a.C];
+  const uint64_t bound = sc.kth;
   for (int i = tid; i < total; i += kT) {
     int q = 0;
     while (offs[q + 1] <= i) ++q;
-    lists[i] = __ldcg(&a.part_keys[(part0 + q) * a.K + (i - offs[q])]);
+    const uint64_t key = __ldcg(&a.part_keys[(part0 + q) * a.K + (i - offs[q])]);
+    if (key >= bound) lists[atomicAdd(&sc.n_cand, 1)] = key;
   }
   __syncthreads();
-  for (int i = tid; i < total; i += kT) {
-    int q = 0;
-    while (offs[q + 1] <= i) ++q;
-    const uint64_t key = lists[i];
-    int rk = i - offs[q];
-    for (int o = 0; o < a.C && rk < a.K; ++o) {
-      if (o == q) continue;
-      int lo = offs[o], hi = offs[o + 1];
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (lists[mid] > key) lo = mid + 1; else hi = mid;
-      }
-      rk += lo - offs[o];
-    }
-    if (rk < a.K) surv[rk] = key;
-  }
+  sort_top(lists, sc.n_cand, a.K, surv);
   __shared__ double s_lse;
   if (tid == 0) {
-    const float2 s = sc.s_row;
-    const double acc = (double)s.x + (double)s.y;
+    const float2 sr = sc.s_row;
+    const double acc = (double)sr.x + (double)sr.y;
     const double lse = (double)Mrow + log(acc);
     s_lse = lse;
     int st = 0;
@@ -516,15 +626,13 @@ struct TopkPlan {
 };
 
 TopkPlan plan_topk(int V, int K, int es) {
+  // chunks of at most 32 KB (2048 vectors of 16 bytes, 8 per thread); the
+  // merge buffer holds C lists of K keys
   TopkPlan p;
-  int cl_max = es == 2 ? 16384 : 8192;  // 32 KB chunks
-  for (;;) {
-    p.C = (V + cl_max - 1) / cl_max;
-    p.CL = (V + p.C - 1) / p.C;
-    p.CL = (p.CL + 7) & ~7;
-    if (p.C <= 256 && (size_t)p.C * K * 8 <= (size_t)cl_max * es) break;
-    cl_max *= 2;
-  }
+  const int cl_max = es == 2 ? 16384 : 8192;
+  p.C = (V + cl_max - 1) / cl_max;
+  p.CL = (V + p.C - 1) / p.C;
+  p.CL = (p.CL + 7) & ~7;
   p.cap = ((K > 512 ? K : 512) + 15) & ~15;  // keeps every later section 16-byte aligned
   p.chunk_bytes = (int)(((size_t)kPad + (size_t)p.CL * es + 32 + 127) / 128 * 128);
   p.lists_bytes = (int)(((size_t)p.C * K * 8 + 127) / 128 * 128);
@@ -543,7 +651,7 @@ size_t topk_workspace_bytes(int B, int b, int V, int K, int es) {
 
 int topk_max_smem_ok(int V, int K, int es) {
   TopkPlan p = plan_topk(V, K, es);
-  return p.smem <= 227 * 1024;
+  return p.C <= 256 && p.smem <= 227 * 1024;
 }
 
 int launch_topk(const void *logits, int dtype, int B, int b, int V, int64_t ld, int K,

@@ -31,7 +31,8 @@ def test_topk_full_size_llama_vocab(cuda_lib):
 
 
 @pytest.mark.parametrize("V,K,dtype", [(1023, 8, "f32"), (151937, 64, "bf16"), (1023, 1023, "bf16"),
-                                       (5000, 1024, "f32"), (17, 3, "bf16"), (8, 8, "f32")])
+                                       (5000, 1024, "f32"), (17, 3, "bf16"), (8, 8, "f32"),
+                                       (151936, 1024, "bf16"), (40000, 200, "f32")])
 def test_topk_ragged_vocab_and_large_k(cuda_lib, V, K, dtype):
     w = synth.Workload(91, "ragged", B=2, b=3, V=V, K=min(K, V), n_max=8, dtype=dtype, l_ar_ms=1.0,
                        cost="flat", drafter="spike-geometric", p_agree="uniform", seed=1234 + V)
