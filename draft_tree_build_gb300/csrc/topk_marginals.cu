@@ -4,30 +4,32 @@
 // diffusion drafter emits position-wise marginals q_k = softmax(l_k); the
 // children of a depth-(k-1) tree node are the ranked tokens of q_k.
 //
-// Design (HBM-bound sweep, one read of every logit):
-//  * a row is cut into C equal chunks of at most 32 KB; one CTA per (row,
-//    chunk) stages its chunk in shared memory with one TMA bulk copy
-//    (cp.async.bulk), so the chunk is read from HBM once and swept twice from
-//    shared memory, while the other CTAs resident on the SM keep their copies
-//    in flight;
-//  * sweep 1: the max of each 16-byte vector (packed bf16x2 max), kept in
-//    registers, and per-thread maxima.  The chunk max M_c comes from them, and
-//    so does a prefilter threshold T0: a two-pass radix select over the 16-bit
-//    prefixes of the 256 thread maxima finds the K-th largest prefix, and the
-//    smallest value with that prefix is reached by at least K distinct
-//    elements, so every top-K element of the chunk is >= T0;
-//  * sweep 2: sum of exp(l - M_c) with packed f32x2 arithmetic and ex2, the
-//    log2(e) factor split in two parts so its rounding does not bias all terms
-//    alike, then a compensated (two-float) reduction across threads; vectors
-//    whose max reaches T0 append their elements >= T0 (about K of them);
-//  * the survivors are sorted by one warp (register bitonic network on the
-//    64-bit keys value desc, token asc; counting rank beyond 256 survivors, an
-//    exact radix select over the chunk if they do not fit at all);
-//  * the last CTA of a row to finish (atomic arrival counter, no waiting)
-//    merges the chunk partials: M = max M_c, s = sum s_c exp(M_c - M) as a
-//    two-float sum, lse = M + log s in fp64; the best chunk K-th key bounds
-//    the row's K-th key from below, so only list entries at or above it are
-//    sorted for the row's top-K.
+// Design (HBM-bound, one read of every logit):
+//  * one thread-block cluster of CS CTAs per row (CS <= 8; 16 for the widest
+//    rows).  CTA r stages slice r of the row in shared memory with one TMA
+//    bulk copy (cp.async.bulk);
+//  * pass A, per thread: the max of each of its 16-byte vectors (kept in
+//    registers) and the thread max m_t.  Each thread stores the 16-bit prefix
+//    of m_t's order key into the cluster leader's table (distributed shared
+//    memory) and the CTA arrives on a cluster barrier; while the other CTAs
+//    catch up it sums exp(l - m_t) over its elements with packed f32x2
+//    arithmetic and ex2 (the log2(e) factor split in two parts so its
+//    rounding does not bias all terms alike);
+//  * the row threshold T: every CTA copies the row's CS*256 prefixes back and
+//    runs a two-round radix select over them.  T is the smallest float with
+//    the K-th largest prefix, so at least K elements of the row reach it and
+//    the row's top K lies among the elements >= T (on logit rows, K plus a
+//    few);
+//  * pass B: each thread counts its elements >= T, reserves room in the
+//    leader's list with one remote atomic and stores them there as 64-bit
+//    keys (value desc, token asc); the CTA hands the leader its max and its
+//    two-float sum of exp(l - max), arrives on the cluster barrier and exits;
+//  * the leader waits, ranks the list by counting (the keys are unique),
+//    writes the top K and lse = M + log(sum) in fp64.  If the list overflows
+//    (long runs of equal values), it selects the row's top K exactly with a
+//    radix select over the row in global memory.
+// Rows too wide for 16 slices, and K > 256, take the exact path in a kernel
+// of their own.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -36,40 +38,36 @@ namespace bastion {
 
 namespace {
 
-constexpr int kT = 256;       // threads per CTA (8 warps)
-constexpr int kPad = 32;      // bytes in front of the staged chunk
+constexpr int kT = 256;      // threads per CTA (8 warps)
+constexpr int kMaxCS = 16;   // CTAs per row at most
 constexpr float kL2eHi = 1.4426950216293335f;     // log2(e) rounded to float
 constexpr float kL2eLo = 1.925963033500011e-08f;  // log2(e) - kL2eHi
+constexpr double kLn2 = 0.6931471805599453;       // ln 2
 
 struct TopkArgs {
   const unsigned char *logits;
-  int rows, b, V, K, CL, C, cap, chunk_bytes, lists_bytes;
+  int rows, b, V, K, CS, SL, cap, tab_bytes;
   int64_t ld;  // elements
   float *topk_logq, *topk_logit;
   int32_t *topk_tok;
   double *lse;
   int32_t *status;
-  float *part_m;
-  float2 *part_s;  // (hi, lo) of the chunk's sum of exp(l - M_c)
-  int32_t *part_n;
-  uint64_t *part_keys;
-  uint32_t *row_cnt;
 };
 
 struct Scratch {
-  float lanemax[kT];  // chunk maxima during the merge
-  uint32_t hist2[256];
+  uint32_t hist1[256];
+  uint32_t red_u[8];
   float red_f[8];
   float2 red_s[8];
-  float2 s_row;
-  uint32_t hist[256];
-  unsigned long long kth;
-  int n_cand;
-  int n_surv;
-  int last;
+  float part_m[kMaxCS];   // leader: each CTA's max
+  float2 part_s[kMaxCS];  // leader: each CTA's two-float sum of exp(l - max)
+  uint32_t n_surv;        // leader: keys pushed by the cluster
+  uint32_t n_exact;
   uint32_t digit_info[2];
-  int scan[kT + 1];
+  int warp_tot[8];
+  double lse;
 };
+constexpr int kScratchBytes = (int)((sizeof(Scratch) + 127) / 128 * 128);
 
 // --------------------------------------------------------------------------- arithmetic
 __device__ __forceinline__ float ex2(float x) {
@@ -155,542 +153,526 @@ __device__ __forceinline__ float vmax(const uint4 &x) {
   }
 }
 
-// Descending bitonic sort of one float per lane; returns this lane's value.
-__device__ __forceinline__ float warp_sort_desc(float v, int lane) {
-#pragma unroll
-  for (int k = 2; k <= 32; k <<= 1) {
-#pragma unroll
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      float o = __shfl_xor_sync(kFull, v, j);
-      bool desc = (lane & k) == 0;
-      bool lower = (lane & j) == 0;
-      v = (desc == lower) ? fmaxf(v, o) : fminf(v, o);
-    }
-  }
-  return v;
-}
-
-// Descending bitonic sort of NPL*32 64-bit keys, NPL per lane (element
-// e = i*32 + lane lives in v[i] of that lane).
-template <int NPL>
-__device__ __forceinline__ void warp_bitonic_desc(uint64_t (&v)[NPL], int lane) {
-  constexpr int N = NPL * 32;
-#pragma unroll
-  for (int k = 2; k <= N; k <<= 1) {
-#pragma unroll
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      if (j >= 32) {
-        const int jj = j >> 5;
-#pragma unroll
-        for (int i = 0; i < NPL; ++i) {
-          const int ip = i ^ jj;
-          if (ip > i) {
-            const bool desc = ((i * 32 + lane) & k) == 0;
-            const uint64_t x = v[i], y = v[ip];
-            const bool sw = desc ? (x < y) : (x > y);
-            v[i] = sw ? y : x;
-            v[ip] = sw ? x : y;
-          }
-        }
-      } else {
-        const bool lower = (lane & j) == 0;
-#pragma unroll
-        for (int i = 0; i < NPL; ++i) {
-          const uint64_t o = __shfl_xor_sync(kFull, v[i], j);
-          const bool desc = ((i * 32 + lane) & k) == 0;
-          const bool keep_max = desc == lower;
-          v[i] = keep_max ? (v[i] > o ? v[i] : o) : (v[i] < o ? v[i] : o);
-        }
-      }
-    }
-  }
-}
-
-// Sort n <= NPL*32 keys from src (descending) with warp 0 and write the first
-// min(n, K) of them to dst.
-template <int NPL>
-__device__ __forceinline__ void warp_sort_write(const uint64_t *src, int n, int K, uint64_t *dst,
-                                                int lane) {
-  uint64_t v[NPL];
-#pragma unroll
-  for (int i = 0; i < NPL; ++i) {
-    const int e = i * 32 + lane;
-    v[i] = e < n ? src[e] : 0ull;
-  }
-  warp_bitonic_desc<NPL>(v, lane);
-  const int lim = min(n, K);
-#pragma unroll
-  for (int i = 0; i < NPL; ++i) {
-    const int e = i * 32 + lane;
-    if (e < lim) dst[e] = v[i];
-  }
-}
-
-// Rank n unique keys of src exactly and write the first min(n, K), sorted
-// descending, to dst (all threads of the CTA call it; a barrier must follow
-// before dst is read when dst is shared memory).
-__device__ __forceinline__ void sort_top(const uint64_t *src, int n, int K, uint64_t *dst) {
-  const int tid = threadIdx.x, lane = tid & 31;
-  if (n <= 64) {
-    if (tid < 32) warp_sort_write<2>(src, n, K, dst, lane);
-  } else if (n <= 128) {
-    if (tid < 32) warp_sort_write<4>(src, n, K, dst, lane);
-  } else if (n <= 256) {
-    if (tid < 32) warp_sort_write<8>(src, n, K, dst, lane);
+// Sum of exp(x - m) over one 16-byte vector.
+template <int ES>
+__device__ __forceinline__ float vexp_sum(const uint4 &x, float m) {
+  float f[16 / ES];
+  unpack<ES>(x, f);
+  if constexpr (ES == 2) {
+    float p0, p1, q0, q1;
+    exp4(f[0], f[1], f[2], f[3], m, p0, p1);
+    exp4(f[4], f[5], f[6], f[7], m, q0, q1);
+    return (p0 + p1) + (q0 + q1);
   } else {
-    for (int i = tid; i < n; i += kT) {
-      const uint64_t ki = src[i];
-      int rk = 0;
-      for (int j = 0; j < n; ++j) rk += src[j] > ki;
-      if (rk < K) dst[rk] = ki;
+    float p0, p1;
+    exp4(f[0], f[1], f[2], f[3], m, p0, p1);
+    return p0 + p1;
+  }
+}
+
+// --------------------------------------------------------------------------- selection helpers
+// Warp 0: scanning the 256 bins of h from 255 down, the bin at which the
+// running count reaches need (0 < need <= total), and the count above it,
+// into info[0], info[1].
+__device__ __forceinline__ void find_digit(const uint32_t *h, uint32_t need, uint32_t *info,
+                                           int lane) {
+  uint32_t cnt[8], tot = 0;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) { cnt[q] = h[255 - 8 * lane - q]; tot += cnt[q]; }
+  uint32_t incl = tot;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const uint32_t above = incl - tot;
+  if (above < need && incl >= need) {
+    uint32_t run = above;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if (run + cnt[q] >= need) {
+        info[0] = 255u - 8u * lane - q;
+        info[1] = run;
+        break;
+      }
+      run += cnt[q];
     }
   }
 }
 
-// Number of entries >= c in a descending list of 32.
-__device__ __forceinline__ int count_ge(const float *list, float c) {
-  int lo = 0, hi = 32;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (list[mid] >= c) lo = mid + 1; else hi = mid;
-  }
-  return lo;
+// Adds 1 to h[bin] for every lane whose bin is < 256 (one atomic per distinct
+// bin of the warp).  All lanes call it.
+__device__ __forceinline__ void hist_add(uint32_t *h, uint32_t bin, int lane) {
+  const uint32_t peers = __match_any_sync(kFull, bin);
+  if (bin < 256u && lane == __ffs(peers) - 1) atomicAdd(&h[bin], (uint32_t)__popc(peers));
 }
 
-// --------------------------------------------------------------------------- chunk geometry
-struct Item {
-  int row, c, e0, n, body, nh, t0, nvec;
+// Exclusive prefix sum over the CTA of one int per thread.
+__device__ __forceinline__ int cta_exclusive_scan(int x, Scratch &sc) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int incl = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) sc.warp_tot[warp] = incl;
+  __syncthreads();
+  int before = 0;
+  for (int w = 0; w < warp; ++w) before += sc.warp_tot[w];
+  __syncthreads();
+  return before + incl - x;
+}
+
+// The row's top min(K, V) keys, exactly and unsorted, into dst: a radix select
+// of the K-th largest order key (8-bit digits) over the row in global memory,
+// then every element above it and the lowest-token elements equal to it.  All
+// threads of the CTA call it; returns the number of keys written.
+template <int ES>
+__device__ int row_topk_exact(const unsigned char *g, int V, int K, uint64_t *dst, Scratch &sc) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int want = min(K, V);
+  int kk = want;
+  uint32_t prefix = 0, pmask = 0;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    sc.hist1[tid] = 0u;
+    __syncthreads();
+    for (int e = tid; e < V; e += kT) {
+      const uint32_t o = ord_f32(load_elem<ES>(g + (size_t)e * ES));
+      if ((o & pmask) == prefix) atomicAdd(&sc.hist1[(o >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    if (tid < 32) find_digit(sc.hist1, (uint32_t)kk, sc.digit_info, lane);
+    __syncthreads();
+    prefix |= sc.digit_info[0] << shift;
+    pmask |= 255u << shift;
+    kk -= (int)sc.digit_info[1];
+  }
+  // kk elements equal to the threshold key are taken, lowest tokens first
+  const int per = (V + kT - 1) / kT;
+  const int lo = min(V, tid * per), hi = min(V, lo + per);
+  int eq = 0;
+  for (int e = lo; e < hi; ++e) eq += ord_f32(load_elem<ES>(g + (size_t)e * ES)) == prefix;
+  int rank_eq = cta_exclusive_scan(eq, sc);
+  if (tid == 0) sc.n_exact = 0u;
+  __syncthreads();
+  for (int e = lo; e < hi; ++e) {
+    const float v = load_elem<ES>(g + (size_t)e * ES);
+    const uint32_t o = ord_f32(v);
+    bool take = o > prefix;
+    if (o == prefix) take = rank_eq++ < kk;
+    if (take) dst[atomicAdd(&sc.n_exact, 1u)] = make_key(v, (uint32_t)e);
+  }
+  __syncthreads();
+  return want;
+}
+
+// Ranks n unique keys of list by counting, writes the top K's logits and
+// tokens and keeps each key's rank in rk (all threads call it; list[n] must be
+// readable and zero when n is odd).
+__device__ __forceinline__ void rank_keys(const TopkArgs &a, int row, const uint64_t *list, int n,
+                                          int *rk) {
+  const int K = a.K;
+  const ulonglong2 *l2 = reinterpret_cast<const ulonglong2 *>(list);
+  const int n2 = (n + 1) >> 1;
+  for (int i = threadIdx.x; i < n; i += kT) {
+    const uint64_t key = list[i];
+    int r = 0;
+#pragma unroll 4
+    for (int j = 0; j < n2; ++j) {
+      const ulonglong2 p = l2[j];
+      r += (p.x > key) + (p.y > key);
+    }
+    rk[i] = r;
+    if (r < K) {
+      const size_t o = (size_t)row * K + r;
+      a.topk_logit[o] = key_value(key);
+      a.topk_tok[o] = (int32_t)key_token(key);
+    }
+  }
+}
+
+// log q = logit - lse for the ranked keys (after rank_keys and a barrier).
+__device__ __forceinline__ void write_logq(const TopkArgs &a, int row, const uint64_t *list, int n,
+                                           const int *rk, double lse) {
+  if (!a.topk_logq) return;
+  for (int i = threadIdx.x; i < n; i += kT) {
+    const int r = rk[i];
+    if (r < a.K) a.topk_logq[(size_t)row * a.K + r] = (float)((double)key_value(list[i]) - lse);
+  }
+}
+
+// --------------------------------------------------------------------------- slice geometry
+struct Slice {
+  int e0, n, nh, t0, nvec, body;  // body: bytes of the 16-byte aligned middle
   const unsigned char *g0;
   uintptr_t ga0;
 };
 
 template <int ES>
-__device__ __forceinline__ Item item_at(const TopkArgs &a, int it) {
-  Item m;
-  m.row = it / a.C;
-  m.c = it - m.row * a.C;
-  m.e0 = m.c * a.CL;
-  m.n = min(a.V - m.e0, a.CL);
-  m.g0 = a.logits + ((size_t)m.row * (size_t)a.ld + (size_t)m.e0) * ES;
-  m.ga0 = ((uintptr_t)m.g0 + 15) & ~(uintptr_t)15;
-  const uintptr_t ga1 = ((uintptr_t)m.g0 + (uintptr_t)m.n * ES) & ~(uintptr_t)15;
-  m.body = ga1 > m.ga0 ? (int)(ga1 - m.ga0) : 0;
-  const int h = m.body ? (int)(m.ga0 - (uintptr_t)m.g0) : m.n * ES;
-  m.nh = h / ES;
-  m.t0 = (h + m.body) / ES;
-  m.nvec = m.body / 16;
-  return m;
+__device__ __forceinline__ Slice slice_at(const TopkArgs &a, int row, int r) {
+  Slice s;
+  s.e0 = r * a.SL;
+  s.n = max(0, min(a.V - s.e0, a.SL));
+  s.g0 = a.logits + ((size_t)row * (size_t)a.ld + (size_t)s.e0) * ES;
+  s.ga0 = ((uintptr_t)s.g0 + 15) & ~(uintptr_t)15;
+  const uintptr_t ga1 = ((uintptr_t)s.g0 + (uintptr_t)s.n * ES) & ~(uintptr_t)15;
+  s.body = ga1 > s.ga0 ? (int)(ga1 - s.ga0) : 0;
+  const int h = s.body ? (int)(s.ga0 - (uintptr_t)s.g0) : s.n * ES;
+  s.nh = h / ES;
+  s.t0 = (h + s.body) / ES;
+  s.nvec = s.body / 16;
+  return s;
 }
 
-// Element e of the item: from the staged body, else from global memory.
-template <int ES>
-__device__ __forceinline__ float item_elem(const Item &m, const unsigned char *body, int e) {
-  if (e >= m.nh && e < m.t0) return load_elem<ES>(body + (size_t)(e - m.nh) * ES);
-  return load_elem<ES>(m.g0 + (size_t)e * ES);
-}
-
-// Exact top-min(K, n) of the chunk when the prefilter left too many survivors:
-// radix select of the K-th largest value (8-bit digits of the order-preserving
-// key), then every element above it plus the lowest-token elements equal to it.
-template <int ES>
-__device__ void chunk_topk_exact(const Item &m, const unsigned char *body, int K, uint64_t *surv,
-                                 Scratch &sc) {
-  const int tid = threadIdx.x, n = m.n;
-  int kk = min(K, n);
-  uint32_t prefix = 0, pmask = 0;
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = tid; i < 256; i += kT) sc.hist[i] = 0;
-    __syncthreads();
-    for (int e = tid; e < n; e += kT) {
-      const uint32_t o = ord_f32(item_elem<ES>(m, body, e));
-      if ((o & pmask) == prefix) atomicAdd(&sc.hist[(o >> shift) & 255u], 1u);
-    }
-    __syncthreads();
-    if (tid < 32) {
-      uint32_t cnt[8], tot = 0;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) { cnt[q] = sc.hist[255 - 8 * tid - q]; tot += cnt[q]; }
-      uint32_t incl = tot;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        uint32_t y = __shfl_up_sync(kFull, incl, o);
-        if (tid >= o) incl += y;
-      }
-      const uint32_t above = incl - tot;
-      if (above < (uint32_t)kk && incl >= (uint32_t)kk) {
-        uint32_t run = above;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          if (run + cnt[q] >= (uint32_t)kk) {
-            sc.digit_info[0] = 255u - 8u * tid - q;
-            sc.digit_info[1] = run;
-            break;
-          }
-          run += cnt[q];
-        }
-      }
-    }
-    __syncthreads();
-    const uint32_t digit = sc.digit_info[0];
-    kk -= (int)sc.digit_info[1];
-    prefix |= digit << shift;
-    pmask |= 255u << shift;
-    __syncthreads();
+// lse of the row from per-CTA (max, two-float sum) pairs; sets status bits.
+__device__ __forceinline__ double row_lse(const TopkArgs &a, int row, const float *pm,
+                                          const float2 *ps, int n) {
+  float M = -INFINITY;
+  for (int q = 0; q < n; ++q) M = fmaxf(M, pm[q]);
+  float2 acc = make_float2(0.f, 0.f);
+  for (int q = 0; q < n; ++q) {
+    if (pm[q] == -INFINITY) continue;
+    const float e = expf(pm[q] - M);
+    const float ph = ps[q].x * e;
+    const float pl = fmaf(ps[q].x, e, -ph) + ps[q].y * e;
+    acc = ff_add(acc, make_float2(ph, pl));
   }
-  if (tid == 0) sc.n_surv = 0;
-  const int per = (n + kT - 1) / kT;
-  const int lo = min(n, tid * per), hi = min(n, lo + per);
-  int eq = 0;
-  for (int e = lo; e < hi; ++e) eq += ord_f32(item_elem<ES>(m, body, e)) == prefix;
-  sc.scan[tid] = eq;
-  __syncthreads();
-  if (tid == 0) {
-    int run = 0;
-    for (int t = 0; t < kT; ++t) { int v = sc.scan[t]; sc.scan[t] = run; run += v; }
-  }
-  __syncthreads();
-  int rank_eq = sc.scan[tid];
-  for (int e = lo; e < hi; ++e) {
-    const float v = item_elem<ES>(m, body, e);
-    const uint32_t o = ord_f32(v);
-    bool take = o > prefix;
-    if (o == prefix) { take = rank_eq < kk; ++rank_eq; }
-    if (take) surv[atomicAdd(&sc.n_surv, 1)] = make_key(v, (uint32_t)(m.e0 + e));
-  }
-  __syncthreads();
+  const double s = (double)acc.x + (double)acc.y;
+  // log s = e ln 2 + log m + log(1 + lo/hi) with hi = m 2^e, m in [0.5, 1):
+  // |log m| < 0.7, so the single-precision log is accurate to ~1e-7 absolute
+  int e2 = 0;
+  const float mant = frexpf(acc.x, &e2);
+  const double corr = (acc.x > 0.f && acc.x < INFINITY) ? (double)(acc.y / acc.x) : 0.0;
+  const double lse = (double)M + ((double)e2 * kLn2 + (double)logf(mant) + corr);
+  int st = 0;
+  if (M == INFINITY || !(s == s) || s == INFINITY) st |= BASTION_STATUS_NONFINITE;
+  if (M == -INFINITY) st |= BASTION_STATUS_EMPTY_ROW;
+  if (st) atomicOr(&a.status[row / a.b], st);
+  a.lse[row] = lse;
+  return lse;
 }
 
-// Append this lane's elements >= T0 of one vector (keys into surv).
-template <int NE>
-__device__ __forceinline__ void append_lane(const float (&f)[NE], float T0, uint32_t tok0,
-                                            uint64_t *surv, int *n_surv, int cap) {
-  uint32_t msk = 0;
-#pragma unroll
-  for (int i = 0; i < NE; ++i) msk |= (f[i] >= T0 ? 1u : 0u) << i;
-  int idx = atomicAdd(n_surv, __popc(msk));
-  while (msk) {
-    const int i = __ffs(msk) - 1;
-    msk &= msk - 1u;
-    float fi = f[0];
-#pragma unroll
-    for (int q = 1; q < NE; ++q) fi = q == i ? f[q] : fi;
-    if (idx < cap) surv[idx] = make_key(fi, tok0 + (uint32_t)i);
-    ++idx;
-  }
-}
-
-// Radix select of a threshold over the 16-bit prefixes of one value per
-// thread: returns the smallest float whose order key has the K-th largest
-// prefix (so >= K threads hold a value >= it).  All threads call it.
-__device__ __forceinline__ float kth_prefix_threshold(float v, int K, Scratch &sc) {
-  const int tid = threadIdx.x, lane = tid & 31;
-  const uint32_t key = ord_f32(v) >> 16;
-  sc.hist[tid] = 0u;
-  sc.hist2[tid] = 0u;
-  __syncthreads();
-  atomicAdd(&sc.hist[key >> 8], 1u);
-  __syncthreads();
-  // digit d scanned from 255 down: lane owns digits 255-8*lane .. 255-8*lane-7
-  auto find = [&](const uint32_t *h, uint32_t need) {
-    uint32_t cnt[8], tot = 0;
-#pragma unroll
-    for (int q = 0; q < 8; ++q) { cnt[q] = h[255 - 8 * lane - q]; tot += cnt[q]; }
-    uint32_t incl = tot;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(kFull, incl, o);
-      if (lane >= o) incl += y;
-    }
-    const uint32_t above = incl - tot;
-    if (above < need && incl >= need) {
-      uint32_t run = above;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        if (run + cnt[q] >= need) {
-          sc.digit_info[0] = 255u - 8u * lane - q;
-          sc.digit_info[1] = run;
-          break;
-        }
-        run += cnt[q];
-      }
-    }
-  };
-  if (tid < 32) find(sc.hist, (uint32_t)K);
-  __syncthreads();
-  const uint32_t d1 = sc.digit_info[0], above1 = sc.digit_info[1];
-  if ((key >> 8) == d1) atomicAdd(&sc.hist2[key & 255u], 1u);
-  __syncthreads();
-  if (tid < 32) find(sc.hist2, (uint32_t)K - above1);
-  __syncthreads();
-  const uint32_t t16 = (d1 << 8) | sc.digit_info[0];
-  const float t = unord_f32(t16 << 16);
-  return t == t ? t : -INFINITY;  // the prefix of -inf maps to a NaN pattern
-}
-
-template <int ES>
-__global__ void __launch_bounds__(kT, 4) topk_kernel(TopkArgs a) {
+// --------------------------------------------------------------------------- kernels
+template <int ES, int NV>
+__global__ void __launch_bounds__(kT, 5) topk_cluster_kernel(TopkArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem);
-  uint64_t *surv = reinterpret_cast<uint64_t *>(smem + 128);  // [cap]
-  Scratch &sc = *reinterpret_cast<Scratch *>(smem + 128 + (size_t)a.cap * 8);
-  uint64_t *lists = reinterpret_cast<uint64_t *>(smem + 128 + (size_t)a.cap * 8 +
-                                                 ((sizeof(Scratch) + 127) / 128) * 128);
-  unsigned char *chunk = reinterpret_cast<unsigned char *>(lists) + a.lists_bytes;
-  unsigned char *body = chunk + kPad;
+  Scratch &sc = *reinterpret_cast<Scratch *>(smem + 128);
+  // the row's thread-max prefixes [CS * 256] (the leader's copy is the table)
+  uint16_t *keys = reinterpret_cast<uint16_t *>(smem + 128 + kScratchBytes);
+  uint64_t *list = reinterpret_cast<uint64_t *>(smem + 128 + kScratchBytes + a.tab_bytes);  // [cap], leader
+  unsigned char *body = reinterpret_cast<unsigned char *>(list + a.cap);
 
   constexpr int NE = 16 / ES;
-  constexpr int kVPT = 8;  // vectors per thread (chunks hold at most 8 * 256 vectors)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const Item m = item_at<ES>(a, blockIdx.x);
-  const int req = m.row / a.b;
+  const uint32_t rank = cluster_rank();
+  const int row = blockIdx.x / a.CS;
+  const int req = row / a.b;
+  const Slice s = slice_at<ES>(a, row, (int)rank);
 
+  sc.hist1[tid] = 0u;
   if (tid == 0) {
     mbar_init(bar, 1);
     fence_mbar_init();
-    sc.n_surv = 0;
+    sc.n_surv = 0u;
   }
   griddep_wait();
   griddep_launch_dependents();
   __syncthreads();
-  if (tid == 0 && m.body) {
-    mbar_arrive_expect_tx(bar, (uint32_t)m.body);
-    bulk_g2s(body, reinterpret_cast<const void *>(m.ga0), (uint32_t)m.body, bar);
+  if (tid == 0 && s.body) {
+    mbar_arrive_expect_tx(bar, (uint32_t)s.body);
+    bulk_g2s(body, reinterpret_cast<const void *>(s.ga0), (uint32_t)s.body, bar);
   }
-  // unaligned head and tail elements: plain loads (read before the wait)
-  const int nscal = m.nh + (m.n - m.t0);
-  float tmax = -INFINITY;
-  for (int j = tid; j < nscal; j += kT) {
-    const int e = j < m.nh ? j : m.t0 + (j - m.nh);
-    tmax = fmaxf(tmax, load_elem<ES>(m.g0 + (size_t)e * ES));
+  cluster_arrive();  // phase 0: this CTA runs and its counter is set
+  // the unaligned head and tail of the slice (at most 2 * (NE - 1) elements):
+  // one per thread, read while the copy is in flight
+  const int nscal = s.nh + (s.n - s.t0);
+  const bool has_x = tid < nscal;
+  float xs = -INFINITY;
+  uint32_t xtok = 0;
+  if (has_x) {
+    const int e = tid < s.nh ? tid : s.t0 + (tid - s.nh);
+    xs = load_elem<ES>(s.g0 + (size_t)e * ES);
+    xtok = (uint32_t)(s.e0 + e);
   }
-  // one thread waits for the bulk copy; the barrier below releases the rest
-  // (spinning in every thread would take issue slots from the other CTAs)
-  if (tid == 0 && m.body && !mbar_wait_bounded(bar, 0)) atomicOr(&a.status[req], BASTION_STATUS_TIMEOUT);
+  // one thread waits for the copy; the barrier releases the rest
+  if (tid == 0 && s.body && !mbar_wait_bounded(bar, 0)) atomicOr(&a.status[req], BASTION_STATUS_TIMEOUT);
   __syncthreads();
 
-  // ---- sweep 1: vector maxima (kept), thread maxima, chunk max, T0
-  float vm[kVPT];
+  // ---- pass A: vector maxima and the thread max into the leader's table
+  float vm[NV];
+  float tmax = xs;
 #pragma unroll
-  for (int u = 0; u < kVPT; ++u) {
+  for (int u = 0; u < NV; ++u) {
     const int v = tid + u * kT;
-    vm[u] = v < m.nvec ? vmax<ES>(ld_shared_v4(body + v * 16)) : -INFINITY;
+    vm[u] = v < s.nvec ? vmax<ES>(ld_shared_v4(body + v * 16)) : -INFINITY;
     tmax = fmaxf(tmax, vm[u]);
   }
   {
     const float wm = warp_max_f(tmax);
     if (lane == 0) sc.red_f[warp] = wm;
   }
-  float T0 = -INFINITY;
-  if (a.K <= kT) T0 = kth_prefix_threshold(tmax, a.K, sc);  // has barriers
-  else __syncthreads();                                     // the maxima above
-  float M = -INFINITY;
-#pragma unroll
-  for (int w = 0; w < kT / 32; ++w) M = fmaxf(M, sc.red_f[w]);
-  const bool have_mass = M != -INFINITY;
-
-  // ---- sweep 2: sum of exp(l - M) and survivors >= T0
+  cluster_wait();
+  dsmem_st_u16(dsmem_addr(&keys[rank * kT + tid], 0), (uint16_t)(ord_f32(tmax) >> 16));
+  cluster_arrive();  // phase 1: this CTA's prefixes are in the table
+  // sum of exp(l - m_t) while the other CTAs of the row catch up
   float sum = 0.f;
-  const uint32_t tok_vec0 = (uint32_t)(m.e0 + m.nh);
+  if (tmax != -INFINITY) {
 #pragma unroll
-  for (int u = 0; u < kVPT; ++u) {
-    const int v = tid + u * kT;
-    if (v < m.nvec) {
-      const uint4 x = ld_shared_v4(body + v * 16);
-      float f[NE];
-      unpack<ES>(x, f);
-      if constexpr (ES == 2) {
-        float p0, p1, q0, q1;
-        exp4(f[0], f[1], f[2], f[3], M, p0, p1);
-        exp4(f[4], f[5], f[6], f[7], M, q0, q1);
-        sum += (p0 + p1) + (q0 + q1);
-      } else {
-        float p0, p1;
-        exp4(f[0], f[1], f[2], f[3], M, p0, p1);
-        sum += p0 + p1;
-      }
-      if (vm[u] >= T0) append_lane<NE>(f, T0, tok_vec0 + (uint32_t)(v * NE), surv, &sc.n_surv, a.cap);
+    for (int u = 0; u < NV; ++u) {
+      const int v = tid + u * kT;
+      if (v < s.nvec) sum += vexp_sum<ES>(ld_shared_v4(body + v * 16), tmax);
     }
+    if (has_x) sum += exp_shifted(xs - tmax);
   }
-  for (int j = tid; j < nscal; j += kT) {  // head and tail
-    const int e = j < m.nh ? j : m.t0 + (j - m.nh);
-    const float f[1] = {load_elem<ES>(m.g0 + (size_t)e * ES)};
-    sum += exp_shifted(f[0] - M);
-    if (f[0] >= T0) append_lane<1>(f, T0, (uint32_t)(m.e0 + e), surv, &sc.n_surv, a.cap);
-  }
+  cluster_wait();
+
+  // ---- the row threshold: the K-th largest prefix of the table, counted by
+  // its distance below the largest one (256 bins: 0..254 steps, then "more")
+  const int nw = a.CS * (kT / 2);  // 32-bit words of the table, two prefixes each
+  uint32_t w[kMaxCS / 2];
+  uint32_t m16 = 0;
   {
-    const float2 ws = ff_warp_sum(make_float2(sum, 0.f));
+    const uint32_t tab = dsmem_addr(keys, 0);
+#pragma unroll
+    for (int j = 0; j < kMaxCS / 2; ++j)
+      if (tid + j * kT < nw) w[j] = dsmem_ld_u32(tab + (uint32_t)(tid + j * kT) * 4u);
+#pragma unroll
+    for (int j = 0; j < kMaxCS / 2; ++j)
+      if (tid + j * kT < nw) m16 = max(m16, max(w[j] & 0xffffu, w[j] >> 16));
+  }
+  m16 = __reduce_max_sync(kFull, m16);
+  if (lane == 0) sc.red_u[warp] = m16;
+  float Mc = -INFINITY;
+#pragma unroll
+  for (int q = 0; q < kT / 32; ++q) Mc = fmaxf(Mc, sc.red_f[q]);
+  {
+    const float st = tmax == -INFINITY ? 0.f : sum * exp_shifted(tmax - Mc);
+    const float2 ws = ff_warp_sum(make_float2(st, 0.f));
     if (lane == 0) sc.red_s[warp] = ws;
   }
-  __syncthreads();  // B
-
-  int n_s = sc.n_surv;
-  if (n_s > a.cap) {
-    chunk_topk_exact<ES>(m, body, a.K, surv, sc);
-    n_s = sc.n_surv;
-  }
-  // ---- the chunk's sorted top list
-  const size_t part = (size_t)m.row * a.C + m.c;
-  sort_top(surv, n_s, a.K, a.part_keys + part * a.K);
-  if (tid == 0) {
-    float2 st = make_float2(0.f, 0.f);
-    for (int w = 0; w < kT / 32; ++w) st = ff_add(st, sc.red_s[w]);
-    a.part_m[part] = M;
-    a.part_s[part] = have_mass ? st : make_float2(0.f, 0.f);
-    a.part_n[part] = min(n_s, a.K);
-  }
-  __threadfence();
-  __syncthreads();  // C
-  if (tid == 0) sc.last = atomicAdd(&a.row_cnt[m.row], 1u) == (uint32_t)(a.C - 1);
-  __syncthreads();  // D
-  if (!sc.last) return;
-  __threadfence();
-
-  // ---- merge of the row's chunk partials (last arriving CTA)
-  const size_t part0 = (size_t)m.row * a.C;
-  float *pm = sc.lanemax;  // [C] chunk maxima (C <= 256)
-  int *offs = sc.scan;     // [C + 1] list starts
-  if (tid < a.C) {
-    pm[tid] = __ldcg(&a.part_m[part0 + tid]);
-    offs[tid + 1] = __ldcg(&a.part_n[part0 + tid]);
-  }
-  if (tid == 0) { sc.kth = 0ull; sc.n_cand = 0; }
   __syncthreads();
-  // the best chunk K-th key: every chunk holding K keys has K keys >= its K-th
-  if (tid < a.C && offs[tid + 1] == a.K) {
-    const uint64_t kth = __ldcg(&a.part_keys[(part0 + tid) * a.K + a.K - 1]);
-    atomicMax(reinterpret_cast<unsigned long long *>(&sc.kth), (unsigned long long)kth);
-  }
-  if (tid == 0) {
-    offs[0] = 0;
-    for (int q = 0; q < a.C; ++q) offs[q + 1] += offs[q];
-  }
-  float Mrow = -INFINITY;
-  for (int q = 0; q < a.C; ++q) Mrow = fmaxf(Mrow, pm[q]);
-  if (warp == 0) {
-    float2 acc = make_float2(0.f, 0.f);
-    for (int q = lane; q < a.C; q += 32) {
-      const float mq = pm[q];
-      if (mq != -INFINITY) {
-        const float2 sq = __ldcg(&a.part_s[part0 + q]);
-        const float e = expf(mq - Mrow);
-        const float ph = sq.x * e;
-        const float pl = fmaf(sq.x, e, -ph) + sq.y * e;
-        acc = ff_add(acc, make_float2(ph, pl));
+  uint32_t M16 = 0;
+#pragma unroll
+  for (int q = 0; q < kT / 32; ++q) M16 = max(M16, sc.red_u[q]);
+  {
+    uint32_t more = 0;
+#pragma unroll
+    for (int j = 0; j < kMaxCS / 2; ++j) {
+      if (tid + j * kT < nw) {
+        const uint32_t d0 = M16 - (w[j] & 0xffffu), d1 = M16 - (w[j] >> 16);
+        if (d0 < 255u) atomicAdd(&sc.hist1[255u - d0], 1u); else ++more;
+        if (d1 < 255u) atomicAdd(&sc.hist1[255u - d1], 1u); else ++more;
       }
     }
+    more = __reduce_add_sync(kFull, more);
+    if (lane == 0 && more) atomicAdd(&sc.hist1[0], more);
+  }
+  if (warp == 0) {  // this CTA's (max, sum) into the leader's slots
+    float2 acc = lane < kT / 32 ? sc.red_s[lane] : make_float2(0.f, 0.f);
     acc = ff_warp_sum(acc);
-    if (lane == 0) sc.s_row = acc;
+    if (lane == 0) {
+      dsmem_st_f32(dsmem_addr(&sc.part_m[rank], 0), Mc);
+      dsmem_st_f32(dsmem_addr(&sc.part_s[rank].x, 0), acc.x);
+      dsmem_st_f32(dsmem_addr(&sc.part_s[rank].y, 0), acc.y);
+    }
   }
   __syncthreads();
-  // candidates: list entries at or above the bound (at least K of them)
-  const int total = offs[a.C];
-  const uint64_t bound = sc.kth;
-  for (int i = tid; i < total; i += kT) {
-    int q = 0;
-    while (offs[q + 1] <= i) ++q;
-    const uint64_t key = __ldcg(&a.part_keys[(part0 + q) * a.K + (i - offs[q])]);
-    if (key >= bound) lists[atomicAdd(&sc.n_cand, 1)] = key;
-  }
+  if (warp == 0) find_digit(sc.hist1, (uint32_t)a.K, sc.digit_info, lane);
   __syncthreads();
-  sort_top(lists, sc.n_cand, a.K, surv);
-  __shared__ double s_lse;
-  if (tid == 0) {
-    const float2 sr = sc.s_row;
-    const double acc = (double)sr.x + (double)sr.y;
-    const double lse = (double)Mrow + log(acc);
-    s_lse = lse;
-    int st = 0;
-    if (Mrow == INFINITY || !(acc == acc) || acc == INFINITY) st |= BASTION_STATUS_NONFINITE;
-    if (Mrow == -INFINITY) st |= BASTION_STATUS_EMPTY_ROW;
-    if (st) atomicOr(&a.status[req], st);
-    a.lse[m.row] = lse;
-    a.row_cnt[m.row] = 0u;
+  // a K-th prefix 255 or more steps below the largest: every element survives
+  // (and the leader falls back to the exact selection if they do not fit)
+  const uint32_t dK = 255u - sc.digit_info[0];
+  float T = dK < 255u ? unord_f32((M16 - dK) << 16) : -INFINITY;
+  if (!(T == T)) T = -INFINITY;  // the prefix of -inf maps to a NaN pattern
+
+  // ---- pass B: this thread's elements >= T into the leader's list
+  uint32_t hmask = 0, cnt = 0;
+#pragma unroll
+  for (int u = 0; u < NV; ++u) hmask |= (tid + u * kT < s.nvec && vm[u] >= T ? 1u : 0u) << u;
+  const bool hx = has_x && xs >= T;
+  for (uint32_t hm = hmask; hm; hm &= hm - 1u) {
+    float f[NE];
+    unpack<ES>(ld_shared_v4(body + (tid + (__ffs(hm) - 1) * kT) * 16), f);
+#pragma unroll
+    for (int i = 0; i < NE; ++i) cnt += f[i] >= T ? 1u : 0u;
   }
+  cnt += hx ? 1u : 0u;
+  if (cnt) {
+    uint32_t idx = dsmem_atom_add(dsmem_addr(&sc.n_surv, 0), cnt);
+    const uint32_t lst = dsmem_addr(list, 0);
+    const uint32_t cap = (uint32_t)a.cap;
+    if (hx) {
+      if (idx < cap) dsmem_st_u64(lst + idx * 8u, make_key(xs, xtok));
+      ++idx;
+    }
+    for (uint32_t hm = hmask; hm; hm &= hm - 1u) {
+      const int v = tid + (__ffs(hm) - 1) * kT;
+      float f[NE];
+      unpack<ES>(ld_shared_v4(body + v * 16), f);
+      const uint32_t tok0 = (uint32_t)(s.e0 + s.nh + v * NE);
+#pragma unroll
+      for (int i = 0; i < NE; ++i) {
+        if (f[i] >= T) {
+          if (idx < cap) dsmem_st_u64(lst + idx * 8u, make_key(f[i], tok0 + (uint32_t)i));
+          ++idx;
+        }
+      }
+    }
+  }
+  cluster_arrive();  // phase 2: this CTA's part of the row is in the leader
+  if (rank != 0) return;  // nothing reads a non-leader's shared memory after phase 1
+  cluster_wait();
+
+  // ---- leader: the ranked top K, and lse (last warp) meanwhile
+  int n = (int)sc.n_surv;
+  if (n > a.cap || n < a.K) {
+    const unsigned char *g = a.logits + (size_t)row * (size_t)a.ld * ES;
+    n = row_topk_exact<ES>(g, a.V, a.K, list, sc);
+  }
+  if (tid == 0 && (n & 1)) list[n] = 0ull;
   __syncthreads();
-  const double lse = s_lse;
-  for (int j = tid; j < a.K; j += kT) {
-    const uint64_t key = surv[j];
-    const float v = key_value(key);
-    const size_t o = (size_t)m.row * a.K + j;
-    a.topk_logit[o] = v;
-    a.topk_tok[o] = (int32_t)key_token(key);
-    if (a.topk_logq) a.topk_logq[o] = (float)((double)v - lse);
-  }
+  if (tid == kT - 32) sc.lse = row_lse(a, row, sc.part_m, sc.part_s, a.CS);
+  int *rk = reinterpret_cast<int *>(keys);  // the table is no longer read
+  rank_keys(a, row, list, n, rk);
+  __syncthreads();
+  write_logq(a, row, list, n, rk, sc.lse);
 }
 
-size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+// Rows too wide for the cluster path: one CTA per row, exact selection over
+// global memory.
+template <int ES>
+__global__ void __launch_bounds__(kT) topk_exact_kernel(TopkArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  Scratch &sc = *reinterpret_cast<Scratch *>(smem + 128);
+  uint64_t *list = reinterpret_cast<uint64_t *>(smem + 128 + kScratchBytes);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int row = blockIdx.x;
+  const unsigned char *g = a.logits + (size_t)row * (size_t)a.ld * ES;
+  griddep_wait();
+  griddep_launch_dependents();
+  float m = -INFINITY;
+  for (int e = tid; e < a.V; e += kT) m = fmaxf(m, load_elem<ES>(g + (size_t)e * ES));
+  m = warp_max_f(m);
+  if (lane == 0) sc.red_f[warp] = m;
+  __syncthreads();
+  float M = -INFINITY;
+  for (int w = 0; w < kT / 32; ++w) M = fmaxf(M, sc.red_f[w]);
+  float2 sum = make_float2(0.f, 0.f);  // long per-thread runs: compensated
+  if (M != -INFINITY)
+    for (int e = tid; e < a.V; e += kT) {
+      const float2 t = two_sum(sum.x, exp_shifted(load_elem<ES>(g + (size_t)e * ES) - M));
+      sum = make_float2(t.x, sum.y + t.y);
+    }
+  const float2 ws = ff_warp_sum(sum);
+  if (lane == 0) sc.red_s[warp] = ws;
+  __syncthreads();
+  if (tid == 0) {
+    float2 acc = make_float2(0.f, 0.f);
+    for (int w = 0; w < kT / 32; ++w) acc = ff_add(acc, sc.red_s[w]);
+    sc.part_m[0] = M;
+    sc.part_s[0] = acc;
+    sc.lse = row_lse(a, row, sc.part_m, sc.part_s, 1);
+  }
+  const int n = row_topk_exact<ES>(g, a.V, a.K, list, sc);
+  if (tid == 0 && (n & 1)) list[n] = 0ull;
+  __syncthreads();
+  int *rk = reinterpret_cast<int *>(list + a.cap);
+  rank_keys(a, row, list, n, rk);
+  __syncthreads();
+  write_logq(a, row, list, n, rk, sc.lse);
+}
 
 struct TopkPlan {
-  int CL, C, cap, chunk_bytes, lists_bytes;
+  int CS, SL, NV, cap, tab_bytes;
   size_t smem;
+  bool exact;
 };
 
 TopkPlan plan_topk(int V, int K, int es) {
-  // chunks of at most 32 KB (2048 vectors of 16 bytes, 8 per thread); the
-  // merge buffer holds C lists of K keys
   TopkPlan p;
-  const int cl_max = es == 2 ? 16384 : 8192;
-  p.C = (V + cl_max - 1) / cl_max;
-  p.CL = (V + p.C - 1) / p.C;
-  p.CL = (p.CL + 7) & ~7;
-  p.cap = ((K > 512 ? K : 512) + 15) & ~15;  // keeps every later section 16-byte aligned
-  p.chunk_bytes = (int)(((size_t)kPad + (size_t)p.CL * es + 32 + 127) / 128 * 128);
-  p.lists_bytes = (int)(((size_t)p.C * K * 8 + 127) / 128 * 128);
-  p.smem = 128 + (size_t)p.cap * 8 + ((sizeof(Scratch) + 127) / 128) * 128 + p.lists_bytes +
-           p.chunk_bytes;
+  p.cap = ((K * 2 > 128 ? K * 2 : 128) + 31) & ~31;
+  p.exact = K > kT;  // the row threshold uses one key per thread of a CTA at least
+  const int max_vec = kT * 16;  // 16 vectors per thread at most
+  int cs = (V + 8191) / 8192;
+  cs = cs < 1 ? 1 : (cs > 8 ? 8 : cs);
+  auto slice = [&](int c) { return (((V + c - 1) / c) + 7) & ~7; };
+  p.SL = slice(cs);
+  if ((size_t)p.SL * es / 16 + 1 > (size_t)max_vec) {
+    cs = kMaxCS;
+    p.SL = slice(cs);
+  }
+  p.CS = cs;
+  const int nvec = (int)((size_t)p.SL * es / 16 + 1);
+  const int per = (nvec + kT - 1) / kT;
+  p.NV = per <= 2 ? 2 : per <= 4 ? 4 : per <= 8 ? 8 : per <= 12 ? 12 : 16;
+  // the table of thread-max prefixes, later the leader's ranks of its list
+  const int tab = cs * kT * 2 > p.cap * 4 ? cs * kT * 2 : p.cap * 4;
+  p.tab_bytes = (tab + 127) & ~127;
+  p.smem = 128 + kScratchBytes + (size_t)p.tab_bytes + (size_t)p.cap * 8 +
+           (((size_t)p.SL * es + 127) / 128) * 128;
+  if (per > 16 || p.smem > 227 * 1024) p.exact = true;
+  if (p.exact) {
+    p.CS = 1;
+    p.smem = 128 + kScratchBytes + (size_t)p.cap * 12;
+  }
   return p;
+}
+
+template <int ES>
+cudaError_t launch_cluster(const TopkPlan &p, const TopkArgs &a, cudaStream_t stream) {
+  void (*kern)(TopkArgs) = nullptr;
+  switch (p.NV) {
+    case 2: kern = topk_cluster_kernel<ES, 2>; break;
+    case 4: kern = topk_cluster_kernel<ES, 4>; break;
+    case 8: kern = topk_cluster_kernel<ES, 8>; break;
+    case 12: kern = topk_cluster_kernel<ES, 12>; break;
+    default: kern = topk_cluster_kernel<ES, 16>; break;
+  }
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
+  if (e == cudaSuccess && p.CS > 8)
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e != cudaSuccess) return e;
+  return launch_cluster_pdl(kern, dim3((unsigned)(a.rows * p.CS)), dim3(kT), p.smem, stream, p.CS, a);
 }
 
 }  // namespace
 
-size_t topk_workspace_bytes(int B, int b, int V, int K, int es) {
-  TopkPlan p = plan_topk(V, K, es);
-  size_t R = (size_t)B * b, P = R * p.C;
-  return align256(P * 4) + align256(P * 8) + align256(P * 4) + align256(P * K * 8) + align256(R * 4);
-}
+// The kernels keep all their state on chip; the workspace is reserved.
+size_t topk_workspace_bytes(int, int, int, int, int) { return 256; }
 
-int topk_max_smem_ok(int V, int K, int es) {
-  TopkPlan p = plan_topk(V, K, es);
-  return p.C <= 256 && p.smem <= 227 * 1024;
-}
+int topk_max_smem_ok(int, int, int) { return 1; }
 
 int launch_topk(const void *logits, int dtype, int B, int b, int V, int64_t ld, int K,
                 float *topk_logq, float *topk_logit, int32_t *topk_tok, double *lse,
-                void *ws, int32_t *status, cudaStream_t stream) {
+                void *, int32_t *status, cudaStream_t stream) {
   const int es = dtype == BASTION_F32 ? 4 : 2;
-  TopkPlan p = plan_topk(V, K, es);
+  const TopkPlan p = plan_topk(V, K, es);
   TopkArgs a;
   a.logits = static_cast<const unsigned char *>(logits);
   a.rows = B * b;
   a.b = b;
   a.V = V;
   a.K = K;
-  a.CL = p.CL;
-  a.C = p.C;
+  a.CS = p.CS;
+  a.SL = p.SL;
   a.cap = p.cap;
-  a.chunk_bytes = p.chunk_bytes;
-  a.lists_bytes = p.lists_bytes;
+  a.tab_bytes = p.tab_bytes;
   a.ld = ld;
   a.topk_logq = topk_logq;
   a.topk_logit = topk_logit;
   a.topk_tok = topk_tok;
   a.lse = lse;
   a.status = status;
-  size_t R = (size_t)B * b, P = R * p.C;
-  unsigned char *w = static_cast<unsigned char *>(ws);
-  a.part_m = reinterpret_cast<float *>(w);
-  w += align256(P * 4);
-  a.part_s = reinterpret_cast<float2 *>(w);
-  w += align256(P * 8);
-  a.part_n = reinterpret_cast<int32_t *>(w);
-  w += align256(P * 4);
-  a.part_keys = reinterpret_cast<uint64_t *>(w);
-  w += align256(P * K * 8);
-  a.row_cnt = reinterpret_cast<uint32_t *>(w);
-  auto kern = es == 4 ? topk_kernel<4> : topk_kernel<2>;
-  if (p.smem > 48 * 1024)
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
-  const cudaError_t e = launch_pdl(kern, dim3((unsigned)P), dim3(kT), p.smem, stream, a);
+  cudaError_t e;
+  if (p.exact) {
+    auto kern = es == 4 ? topk_exact_kernel<4> : topk_exact_kernel<2>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
+    if (e == cudaSuccess) e = launch_pdl(kern, dim3((unsigned)a.rows), dim3(kT), p.smem, stream, a);
+  } else {
+    e = es == 4 ? launch_cluster<4>(p, a, stream) : launch_cluster<2>(p, a, stream);
+  }
   return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? BASTION_OK : BASTION_ERR_LAUNCH;
 }
 

@@ -92,3 +92,41 @@ def test_topk_deterministic(cuda_lib):
     b, _ = gpu_topk(None, w.K, x_dev=xd)
     for f in ("logq", "logit", "tok", "lse"):
         assert np.array_equal(host(getattr(a, f)), host(getattr(b, f)))
+
+
+@pytest.mark.parametrize("V,dtype", [(151936, "f32"), (262144, "bf16"), (600000, "bf16"), (300000, "f32")])
+def test_topk_wide_rows(cuda_lib, V, dtype):
+    """Rows that need 16 slices per row, 16 vectors per thread, or the
+    one-CTA-per-row exact path."""
+    w = synth.Workload(92, "wide", B=1, b=3, V=V, K=64, n_max=8, dtype=dtype, l_ar_ms=1.0,
+                       cost="flat", drafter="spike-geometric", p_agree="uniform", seed=4321 + V)
+    x = synth.drafter_logits(w)
+    g, st = gpu_topk(x, w.K)
+    assert int(st.abs().sum()) == 0
+    compare_topk(g, oracle.topk_marginals(x, w.K))
+
+
+def test_topk_ascending_row_overflows_list(cuda_lib):
+    """Logits increasing with the token id: the row threshold leaves more than
+    the list holds, so the exact selection over the row takes over."""
+    V = 151936
+    x = np.empty((1, 2, V), np.float32)
+    x[0, 0] = np.linspace(-8.0, 8.0, V, dtype=np.float32)
+    x[0, 1] = x[0, 0][::-1]
+    g, st = gpu_topk(x, 64)
+    assert int(st[0]) == 0
+    ref = oracle.topk_marginals(x, 64)
+    compare_topk(g, ref)
+    assert np.array_equal(host(g.tok)[0, 0], np.arange(V - 1, V - 65, -1))
+
+
+def test_topk_ties_at_threshold(cuda_lib):
+    """Many elements equal to the K-th value: lowest token ids win."""
+    V = 65536
+    x = np.full((1, 2, V), synth.f64_to_bf16_bits(-3.0), np.uint16)
+    x[0, 0, ::97] = synth.f64_to_bf16_bits(1.0)   # 676 ties for 64 places
+    x[0, 1, 5::1000] = synth.f64_to_bf16_bits(2.0)  # 66 distinct-position leaders
+    x[0, 1, 7::1000] = synth.f64_to_bf16_bits(1.5)
+    g, _ = gpu_topk(x, 64)
+    compare_topk(g, oracle.topk_marginals(x, 64))
+    assert np.array_equal(host(g.tok)[0, 0], np.arange(0, 97 * 64, 97))
