@@ -113,13 +113,20 @@ def barrier(ws):
 
 
 def max_over_ranks(x: float, ws: int) -> float:
+    """The largest x over the ranks (the slowest replica's time)."""
     if ws == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate_rate(units_per_rank: float, elapsed_ms: float, ws: int) -> float:
+    """Whole-job throughput: the units all ranks processed / the slowest rank's time."""
+    return ws * units_per_rank / (elapsed_ms * 1e-3)
 
 
 def pinned_from(arr: np.ndarray):
@@ -167,6 +174,26 @@ def run_ours(args, ws, rank, local):
     bytes_k1 = w.B * w.b * w.V * es
     bytes_k4 = int(n_nodes.sum()) * w.V * es
     bytes_step = bytes_k1 + bytes_k4
+
+    if args.profile_kernel:  # a few direct launches of one kernel, for a profiler
+        t, tr, v = step.topk, step.tree, step.ver
+        for i in range(args.launches):
+            xd, td = xs[i & 1], ts[i & 1]
+            if args.profile_kernel in ("topk", "step"):
+                bastion.bastion_topk_marginals(xd, w.K, t.logq, t.logit, t.tok, t.lse, step.ws_topk,
+                                               step.status)
+            if args.profile_kernel in ("tree", "step"):
+                bastion.bastion_build_tree(t.logit, t.tok, t.lse, w.n_max, step.root_token, step.ctx_len,
+                                           step.cost_ms, step.l_ar, tr.n_nodes, tr.parent, tr.depth,
+                                           tr.pos_id, tr.token, tr.rank, tr.log_rho, tr.a_hat,
+                                           tr.speedup, tr.anc_mask, step.status)
+            if args.profile_kernel in ("verify", "step"):
+                bastion.bastion_verify_greedy(td, w.b, tr.n_nodes, tr.parent, tr.token, v.argmax,
+                                              v.accept_len, v.accept_nodes, v.out_tokens, step.ws_verify,
+                                              step.status)
+        torch.cuda.synchronize()
+        assert int(step.status.abs().sum()) == 0, "device status bits set"
+        return None
 
     graphs = [step.capture(xs[i], ts[i]) for i in range(2)]
     stream = torch.cuda.current_stream()
@@ -260,7 +287,7 @@ def run_ours(args, ws, rank, local):
     dom = max(("topk_marginals", "verify_greedy"), key=lambda k: kern[k]["ms"])
     ach = kern[dom]["gbs"]
     res = {
-        "metric": METRIC, "value": ws * args.steps / (elapsed_ms * 1e-3), "unit": UNIT,
+        "metric": METRIC, "value": aggregate_rate(args.steps, elapsed_ms, ws), "unit": UNIT,
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
@@ -275,7 +302,7 @@ def run_ours(args, ws, rank, local):
                      "bytes_per_step": bytes_step},
         "kernels": kern,
         "clocks": clk,
-        "e2e": {"value": ws / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": aggregate_rate(1, e2e_ms, ws), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": 3 * args.steps,
     }
@@ -355,6 +382,11 @@ def run_with_attention(args, ws, rank, local):
     body = attn if args.workload == 4 else full
     body()
     torch.cuda.synchronize()
+    if args.profile_kernel:  # a few direct launches, for a profiler
+        for _ in range(args.launches):
+            attn() if args.profile_kernel == "attn" else full()
+        torch.cuda.synchronize()
+        return None
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         body()
@@ -423,7 +455,7 @@ def run_with_attention(args, ws, rank, local):
     metric = ("tree-attention calls/s (B=8, 32/8 heads, d=128, ctx 4096, N=64)" if args.workload == 4
               else "full tree steps/s (top-K+best-first+attention+verify) B=64 V=128256 ctx 16384 N=256")
     return {
-        "metric": metric, "value": ws * args.steps / (elapsed_ms * 1e-3),
+        "metric": metric, "value": aggregate_rate(args.steps, elapsed_ms, ws),
         "unit": "calls/s" if args.workload == 4 else "steps/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16-in/f32-acc", "data": "synthetic",
@@ -521,6 +553,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", type=int, default=3, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-kernel", choices=["topk", "tree", "verify", "step", "attn"],
+                    help="launch one kernel (or the step) --launches times and exit, for ncu")
+    ap.add_argument("--launches", type=int, default=3)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -539,7 +574,9 @@ def main():
         res = run_with_attention(args, ws, rank, local)
     else:
         res = run_ours(args, ws, rank, local)
-    if rank == 0:
+    if res is None:
+        print("profile launches done", flush=True)
+    elif rank == 0:
         if ws == 1 and not args.no_cpu_baseline and args.workload not in (4, 5):
             res["cpu_baseline"] = cpu_baseline(args)
         print(json.dumps(res), flush=True)

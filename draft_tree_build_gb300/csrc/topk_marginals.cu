@@ -9,14 +9,15 @@
 //    rows).  CTA r stages slice r of the row in shared memory with one TMA
 //    bulk copy (cp.async.bulk);
 //  * pass A, per thread: the max of each of its 16-byte vectors (kept in
-//    registers) and the thread max m_t.  Each thread stores the 16-bit prefix
-//    of m_t's order key into the cluster leader's table (distributed shared
-//    memory) and the CTA arrives on a cluster barrier; while the other CTAs
-//    catch up it sums exp(l - m_t) over its elements with packed f32x2
-//    arithmetic and ex2 (the log2(e) factor split in two parts so its
-//    rounding does not bias all terms alike);
-//  * the row threshold T: every CTA copies the row's CS*256 prefixes back and
-//    runs a two-round radix select over them.  T is the smallest float with
+//    registers) and the thread max m_t.  Every CTA sends the 16-bit prefixes
+//    of its 256 thread maxima' order keys to every CTA of the cluster with
+//    asynchronous distributed-shared-memory stores (st.async), counted on the
+//    receiver's mbarrier; while they travel it sums exp(l - m_t) over its
+//    elements with packed f32x2 arithmetic and ex2 (the log2(e) factor split
+//    in two parts so its rounding does not bias all terms alike);
+//  * the row threshold T: from its copy of the row's CS*256 prefixes, every
+//    CTA finds the K-th largest with one histogram of distances below the
+//    largest.  T is the smallest float with
 //    the K-th largest prefix, so at least K elements of the row reach it and
 //    the row's top K lies among the elements >= T (on logit rows, K plus a
 //    few);
@@ -357,9 +358,10 @@ __device__ __forceinline__ double row_lse(const TopkArgs &a, int row, const floa
 template <int ES, int NV>
 __global__ void __launch_bounds__(kT, 5) topk_cluster_kernel(TopkArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
-  uint64_t *bar = reinterpret_cast<uint64_t *>(smem);
+  uint64_t *bar = reinterpret_cast<uint64_t *>(smem);      // the slice's bulk copy
+  uint64_t *tab_bar = bar + 1;                              // the table's arrival
   Scratch &sc = *reinterpret_cast<Scratch *>(smem + 128);
-  // the row's thread-max prefixes [CS * 256] (the leader's copy is the table)
+  // the row's thread-max prefixes [CS * 256], one copy in every CTA
   uint16_t *keys = reinterpret_cast<uint16_t *>(smem + 128 + kScratchBytes);
   uint64_t *list = reinterpret_cast<uint64_t *>(smem + 128 + kScratchBytes + a.tab_bytes);  // [cap], leader
   unsigned char *body = reinterpret_cast<unsigned char *>(list + a.cap);
@@ -374,17 +376,22 @@ __global__ void __launch_bounds__(kT, 5) topk_cluster_kernel(TopkArgs a) {
   sc.hist1[tid] = 0u;
   if (tid == 0) {
     mbar_init(bar, 1);
+    mbar_init(tab_bar, 1);
     fence_mbar_init();
     sc.n_surv = 0u;
   }
   griddep_wait();
   griddep_launch_dependents();
   __syncthreads();
-  if (tid == 0 && s.body) {
-    mbar_arrive_expect_tx(bar, (uint32_t)s.body);
-    bulk_g2s(body, reinterpret_cast<const void *>(s.ga0), (uint32_t)s.body, bar);
+  if (tid == 0) {
+    if (s.body) {
+      mbar_arrive_expect_tx(bar, (uint32_t)s.body);
+      bulk_g2s(body, reinterpret_cast<const void *>(s.ga0), (uint32_t)s.body, bar);
+    }
+    mbar_arrive_expect_tx(tab_bar, (uint32_t)a.CS * kT * 2);  // every CTA's prefixes
+    fence_acq_rel_cluster();                                   // the counter above
   }
-  cluster_arrive();  // phase 0: this CTA runs and its counter is set
+  cluster_arrive_relaxed();  // phase 0: this CTA runs; its barriers and counter are set
   // the unaligned head and tail of the slice (at most 2 * (NE - 1) elements):
   // one per thread, read while the copy is in flight
   const int nscal = s.nh + (s.n - s.t0);
@@ -414,9 +421,23 @@ __global__ void __launch_bounds__(kT, 5) topk_cluster_kernel(TopkArgs a) {
     if (lane == 0) sc.red_f[warp] = wm;
   }
   cluster_wait();
-  dsmem_st_u16(dsmem_addr(&keys[rank * kT + tid], 0), (uint16_t)(ord_f32(tmax) >> 16));
-  cluster_arrive();  // phase 1: this CTA's prefixes are in the table
-  // sum of exp(l - m_t) while the other CTAs of the row catch up
+  {
+    // this warp's 32 prefixes as four 16-byte chunks; lane k sends chunk k % 4
+    // to CTA k / 4 (asynchronous stores counted on the receiver's barrier)
+    const uint32_t k16 = ord_f32(tmax) >> 16;
+    const int chunk = lane & 3;
+    uint32_t wv[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      wv[q] = __shfl_sync(kFull, k16, chunk * 8 + 2 * q) |
+              (__shfl_sync(kFull, k16, chunk * 8 + 2 * q + 1) << 16);
+    const uint32_t off = (uint32_t)((rank * kT + warp * 32 + chunk * 8) * 2);
+    for (int k = lane; k < 4 * a.CS; k += 32) {
+      const uint32_t dst = (uint32_t)(k >> 2);
+      st_async_v4(dsmem_addr(keys, dst) + off, wv[0], wv[1], wv[2], wv[3], dsmem_addr(tab_bar, dst));
+    }
+  }
+  // sum of exp(l - m_t) while the other CTAs' prefixes arrive
   float sum = 0.f;
   if (tmax != -INFINITY) {
 #pragma unroll
@@ -426,7 +447,7 @@ __global__ void __launch_bounds__(kT, 5) topk_cluster_kernel(TopkArgs a) {
     }
     if (has_x) sum += exp_shifted(xs - tmax);
   }
-  cluster_wait();
+  if (!mbar_wait_bounded(tab_bar, 0) && lane == 0) atomicOr(&a.status[req], BASTION_STATUS_TIMEOUT);
 
   // ---- the row threshold: the K-th largest prefix of the table, counted by
   // its distance below the largest one (256 bins: 0..254 steps, then "more")
@@ -434,10 +455,10 @@ __global__ void __launch_bounds__(kT, 5) topk_cluster_kernel(TopkArgs a) {
   uint32_t w[kMaxCS / 2];
   uint32_t m16 = 0;
   {
-    const uint32_t tab = dsmem_addr(keys, 0);
+    const uint32_t *tab = reinterpret_cast<const uint32_t *>(keys);
 #pragma unroll
     for (int j = 0; j < kMaxCS / 2; ++j)
-      if (tid + j * kT < nw) w[j] = dsmem_ld_u32(tab + (uint32_t)(tid + j * kT) * 4u);
+      if (tid + j * kT < nw) w[j] = tab[tid + j * kT];
 #pragma unroll
     for (int j = 0; j < kMaxCS / 2; ++j)
       if (tid + j * kT < nw) m16 = max(m16, max(w[j] & 0xffffu, w[j] >> 16));
@@ -521,8 +542,8 @@ __global__ void __launch_bounds__(kT, 5) topk_cluster_kernel(TopkArgs a) {
       }
     }
   }
-  cluster_arrive();  // phase 2: this CTA's part of the row is in the leader
-  if (rank != 0) return;  // nothing reads a non-leader's shared memory after phase 1
+  cluster_arrive();  // phase 1: this CTA's part of the row is in the leader
+  if (rank != 0) return;  // nothing reads a non-leader's shared memory
   cluster_wait();
 
   // ---- leader: the ranked top K, and lse (last warp) meanwhile
