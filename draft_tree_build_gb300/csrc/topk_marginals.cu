@@ -17,18 +17,18 @@
 //    in two parts so its rounding does not bias all terms alike);
 //  * the row threshold T: from its copy of the row's CS*256 prefixes, every
 //    CTA finds the K-th largest with one histogram of distances below the
-//    largest.  T is the smallest float with
-//    the K-th largest prefix, so at least K elements of the row reach it and
-//    the row's top K lies among the elements >= T (on logit rows, K plus a
-//    few);
-//  * pass B: each thread counts its elements >= T, reserves room in the
-//    leader's list with one remote atomic and stores them there as 64-bit
-//    keys (value desc, token asc); the CTA hands the leader its max and its
-//    two-float sum of exp(l - max), arrives on the cluster barrier and exits;
-//  * the leader waits, ranks the list by counting (the keys are unique),
-//    writes the top K and lse = M + log(sum) in fp64.  If the list overflows
-//    (long runs of equal values), it selects the row's top K exactly with a
-//    radix select over the row in global memory.
+//    largest.  T is the smallest float with the K-th largest prefix, so at
+//    least K elements of the row reach it and the row's top K lies among the
+//    elements >= T (on logit rows, K plus a few);
+//  * pass B: the slice's elements >= T go to a list in shared memory as
+//    64-bit keys (value desc, token asc); the CTA then sends the list
+//    (zero-padded to a fixed length) and its (max, two-float sum of
+//    exp(l - max), count) to the cluster's leader with asynchronous stores
+//    counted on the leader's mbarrier, and exits;
+//  * the leader waits for the row, ranks its keys by counting (the keys are
+//    unique), writes the top K and lse = M + log(sum).  If a CTA's list
+//    overflows (long runs of equal values), it selects the row's top K
+//    exactly with a radix select over the row in global memory.
 // Rows too wide for 16 slices, and K > 256, take the exact path in a kernel
 // of their own.
 #include <cuda_bf16.h>
@@ -47,7 +47,7 @@ constexpr double kLn2 = 0.6931471805599453;       // ln 2
 
 struct TopkArgs {
   const unsigned char *logits;
-  int rows, b, V, K, CS, SL, cap, tab_bytes;
+  int rows, b, V, K, CS, SL, seg, tab_bytes, body_bytes;
   int64_t ld;  // elements
   float *topk_logq, *topk_logit;
   int32_t *topk_tok;
@@ -55,14 +55,21 @@ struct TopkArgs {
   int32_t *status;
 };
 
+// One CTA's share of a row: its max, its two-float sum of exp(l - max) and
+// the number of its keys >= T (16 bytes: one asynchronous store).
+struct __align__(16) Part {
+  float m, sx, sy;
+  uint32_t n;
+};
+
 struct Scratch {
   uint32_t hist1[256];
   uint32_t red_u[8];
   float red_f[8];
   float2 red_s[8];
-  float part_m[kMaxCS];   // leader: each CTA's max
-  float2 part_s[kMaxCS];  // leader: each CTA's two-float sum of exp(l - max)
-  uint32_t n_surv;        // leader: keys pushed by the cluster
+  Part part[kMaxCS];      // leader: each CTA's (max, sum, key count)
+  int off[kMaxCS + 1];    // leader: where each CTA's keys go in the row list
+  uint32_t n_loc;         // keys in this CTA's list (may pass seg: overflow)
   uint32_t n_exact;
   uint32_t digit_info[2];
   int warp_tot[8];
@@ -327,16 +334,15 @@ __device__ __forceinline__ Slice slice_at(const TopkArgs &a, int row, int r) {
 }
 
 // lse of the row from per-CTA (max, two-float sum) pairs; sets status bits.
-__device__ __forceinline__ double row_lse(const TopkArgs &a, int row, const float *pm,
-                                          const float2 *ps, int n) {
+__device__ __forceinline__ double row_lse(const TopkArgs &a, int row, const Part *pt, int n) {
   float M = -INFINITY;
-  for (int q = 0; q < n; ++q) M = fmaxf(M, pm[q]);
+  for (int q = 0; q < n; ++q) M = fmaxf(M, pt[q].m);
   float2 acc = make_float2(0.f, 0.f);
   for (int q = 0; q < n; ++q) {
-    if (pm[q] == -INFINITY) continue;
-    const float e = expf(pm[q] - M);
-    const float ph = ps[q].x * e;
-    const float pl = fmaf(ps[q].x, e, -ph) + ps[q].y * e;
+    if (pt[q].m == -INFINITY) continue;
+    const float e = expf(pt[q].m - M);
+    const float ph = pt[q].sx * e;
+    const float pl = fmaf(pt[q].sx, e, -ph) + pt[q].sy * e;
     acc = ff_add(acc, make_float2(ph, pl));
   }
   const double s = (double)acc.x + (double)acc.y;
@@ -360,11 +366,15 @@ __global__ void __launch_bounds__(kT, 5) topk_cluster_kernel(TopkArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem);      // the slice's bulk copy
   uint64_t *tab_bar = bar + 1;                              // the table's arrival
+  uint64_t *row_bar = bar + 2;                              // leader: the row's keys' arrival
   Scratch &sc = *reinterpret_cast<Scratch *>(smem + 128);
-  // the row's thread-max prefixes [CS * 256], one copy in every CTA
+  // the row's thread-max prefixes [CS * 256], one copy in every CTA (the
+  // leader's ranks later)
   uint16_t *keys = reinterpret_cast<uint16_t *>(smem + 128 + kScratchBytes);
-  uint64_t *list = reinterpret_cast<uint64_t *>(smem + 128 + kScratchBytes + a.tab_bytes);  // [cap], leader
-  unsigned char *body = reinterpret_cast<unsigned char *>(list + a.cap);
+  uint64_t *loc = reinterpret_cast<uint64_t *>(smem + 128 + kScratchBytes + a.tab_bytes);  // [seg]
+  uint64_t *rlist = loc + a.seg;  // leader: [CS][seg], each CTA's keys, zero-padded
+  // the slice (the leader's row list once its own pass is done)
+  unsigned char *body = reinterpret_cast<unsigned char *>(rlist + (size_t)a.CS * a.seg);
 
   constexpr int NE = 16 / ES;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -377,8 +387,9 @@ __global__ void __launch_bounds__(kT, 5) topk_cluster_kernel(TopkArgs a) {
   if (tid == 0) {
     mbar_init(bar, 1);
     mbar_init(tab_bar, 1);
+    mbar_init(row_bar, 1);
     fence_mbar_init();
-    sc.n_surv = 0u;
+    sc.n_loc = 0u;
   }
   griddep_wait();
   griddep_launch_dependents();
@@ -389,9 +400,10 @@ __global__ void __launch_bounds__(kT, 5) topk_cluster_kernel(TopkArgs a) {
       bulk_g2s(body, reinterpret_cast<const void *>(s.ga0), (uint32_t)s.body, bar);
     }
     mbar_arrive_expect_tx(tab_bar, (uint32_t)a.CS * kT * 2);  // every CTA's prefixes
-    fence_acq_rel_cluster();                                   // the counter above
+    if (rank == 0)  // every CTA's keys and share
+      mbar_arrive_expect_tx(row_bar, (uint32_t)a.CS * ((uint32_t)a.seg * 8u + 16u));
   }
-  cluster_arrive_relaxed();  // phase 0: this CTA runs; its barriers and counter are set
+  cluster_arrive_relaxed();  // this CTA runs and its barriers are set
   // the unaligned head and tail of the slice (at most 2 * (NE - 1) elements):
   // one per thread, read while the copy is in flight
   const int nscal = s.nh + (s.n - s.t0);
@@ -490,15 +502,6 @@ __global__ void __launch_bounds__(kT, 5) topk_cluster_kernel(TopkArgs a) {
     more = __reduce_add_sync(kFull, more);
     if (lane == 0 && more) atomicAdd(&sc.hist1[0], more);
   }
-  if (warp == 0) {  // this CTA's (max, sum) into the leader's slots
-    float2 acc = lane < kT / 32 ? sc.red_s[lane] : make_float2(0.f, 0.f);
-    acc = ff_warp_sum(acc);
-    if (lane == 0) {
-      dsmem_st_f32(dsmem_addr(&sc.part_m[rank], 0), Mc);
-      dsmem_st_f32(dsmem_addr(&sc.part_s[rank].x, 0), acc.x);
-      dsmem_st_f32(dsmem_addr(&sc.part_s[rank].y, 0), acc.y);
-    }
-  }
   __syncthreads();
   if (warp == 0) find_digit(sc.hist1, (uint32_t)a.K, sc.digit_info, lane);
   __syncthreads();
@@ -508,7 +511,7 @@ __global__ void __launch_bounds__(kT, 5) topk_cluster_kernel(TopkArgs a) {
   float T = dK < 255u ? unord_f32((M16 - dK) << 16) : -INFINITY;
   if (!(T == T)) T = -INFINITY;  // the prefix of -inf maps to a NaN pattern
 
-  // ---- pass B: this thread's elements >= T into the leader's list
+  // ---- pass B: this thread's elements >= T into the CTA's list
   uint32_t hmask = 0, cnt = 0;
 #pragma unroll
   for (int u = 0; u < NV; ++u) hmask |= (tid + u * kT < s.nvec && vm[u] >= T ? 1u : 0u) << u;
@@ -521,11 +524,10 @@ __global__ void __launch_bounds__(kT, 5) topk_cluster_kernel(TopkArgs a) {
   }
   cnt += hx ? 1u : 0u;
   if (cnt) {
-    uint32_t idx = dsmem_atom_add(dsmem_addr(&sc.n_surv, 0), cnt);
-    const uint32_t lst = dsmem_addr(list, 0);
-    const uint32_t cap = (uint32_t)a.cap;
+    uint32_t idx = atomicAdd(&sc.n_loc, cnt);
+    const uint32_t seg = (uint32_t)a.seg;
     if (hx) {
-      if (idx < cap) dsmem_st_u64(lst + idx * 8u, make_key(xs, xtok));
+      if (idx < seg) loc[idx] = make_key(xs, xtok);
       ++idx;
     }
     for (uint32_t hm = hmask; hm; hm &= hm - 1u) {
@@ -536,25 +538,57 @@ __global__ void __launch_bounds__(kT, 5) topk_cluster_kernel(TopkArgs a) {
 #pragma unroll
       for (int i = 0; i < NE; ++i) {
         if (f[i] >= T) {
-          if (idx < cap) dsmem_st_u64(lst + idx * 8u, make_key(f[i], tok0 + (uint32_t)i));
+          if (idx < seg) loc[idx] = make_key(f[i], tok0 + (uint32_t)i);
           ++idx;
         }
       }
     }
   }
-  cluster_arrive();  // phase 1: this CTA's part of the row is in the leader
-  if (rank != 0) return;  // nothing reads a non-leader's shared memory
-  cluster_wait();
+  __syncthreads();
+  if (warp == 0) {
+    // the CTA's keys (zero-padded to seg) and its share, by asynchronous
+    // stores into the leader, counted on the leader's row barrier
+    float2 acc = lane < kT / 32 ? sc.red_s[lane] : make_float2(0.f, 0.f);
+    acc = ff_warp_sum(acc);
+    const uint32_t nl = sc.n_loc, seg = (uint32_t)a.seg;
+    const uint32_t rl = dsmem_addr(rlist, 0) + rank * seg * 8u, rb = dsmem_addr(row_bar, 0);
+    for (uint32_t c = lane; c < seg / 2; c += 32) {
+      const uint64_t k0 = 2 * c < nl ? loc[2 * c] : 0ull, k1 = 2 * c + 1 < nl ? loc[2 * c + 1] : 0ull;
+      st_async_v4(rl + c * 16u, (uint32_t)k0, (uint32_t)(k0 >> 32), (uint32_t)k1,
+                  (uint32_t)(k1 >> 32), rb);
+    }
+    if (lane == 0)
+      st_async_v4(dsmem_addr(&sc.part[rank], 0), __float_as_uint(Mc), __float_as_uint(acc.x),
+                  __float_as_uint(acc.y), nl, rb);
+  }
+  if (rank != 0) return;  // nothing reads or writes a non-leader's shared memory now
 
-  // ---- leader: the ranked top K, and lse (last warp) meanwhile
-  int n = (int)sc.n_surv;
-  if (n > a.cap || n < a.K) {
+  // ---- leader: the row's keys, their ranks, and lse (last warp) meanwhile
+  if (!mbar_wait_bounded(row_bar, 0) && lane == 0) atomicOr(&a.status[req], BASTION_STATUS_TIMEOUT);
+  uint64_t *list = reinterpret_cast<uint64_t *>(body);  // this CTA's slice is spent
+  if (tid == 0) {
+    int o = 0, over = 0;
+    for (int r = 0; r < a.CS; ++r) {
+      sc.off[r] = o;
+      o += (int)min(sc.part[r].n, (uint32_t)a.seg);
+      over |= sc.part[r].n > (uint32_t)a.seg;
+    }
+    sc.off[a.CS] = over ? -1 : o;
+  }
+  if (tid == kT - 32) sc.lse = row_lse(a, row, sc.part, a.CS);
+  __syncthreads();
+  int n = sc.off[a.CS];
+  if (n >= a.K) {
+    for (int i = tid; i < a.CS * a.seg; i += kT) {
+      const int r = i / a.seg, j = i - r * a.seg;
+      if (j < sc.off[r + 1] - sc.off[r]) list[sc.off[r] + j] = rlist[i];
+    }
+  } else {  // a list overflowed (or too few keys): exact selection
     const unsigned char *g = a.logits + (size_t)row * (size_t)a.ld * ES;
     n = row_topk_exact<ES>(g, a.V, a.K, list, sc);
   }
   if (tid == 0 && (n & 1)) list[n] = 0ull;
   __syncthreads();
-  if (tid == kT - 32) sc.lse = row_lse(a, row, sc.part_m, sc.part_s, a.CS);
   int *rk = reinterpret_cast<int *>(keys);  // the table is no longer read
   rank_keys(a, row, list, n, rk);
   __syncthreads();
@@ -592,28 +626,27 @@ __global__ void __launch_bounds__(kT) topk_exact_kernel(TopkArgs a) {
   if (tid == 0) {
     float2 acc = make_float2(0.f, 0.f);
     for (int w = 0; w < kT / 32; ++w) acc = ff_add(acc, sc.red_s[w]);
-    sc.part_m[0] = M;
-    sc.part_s[0] = acc;
-    sc.lse = row_lse(a, row, sc.part_m, sc.part_s, 1);
+    sc.part[0] = Part{M, acc.x, acc.y, 0u};
+    sc.lse = row_lse(a, row, sc.part, 1);
   }
   const int n = row_topk_exact<ES>(g, a.V, a.K, list, sc);
   if (tid == 0 && (n & 1)) list[n] = 0ull;
   __syncthreads();
-  int *rk = reinterpret_cast<int *>(list + a.cap);
+  int *rk = reinterpret_cast<int *>(list + 2 * a.K + 2);
   rank_keys(a, row, list, n, rk);
   __syncthreads();
   write_logq(a, row, list, n, rk, sc.lse);
 }
 
 struct TopkPlan {
-  int CS, SL, NV, cap, tab_bytes;
+  int CS, SL, NV, seg, tab_bytes, body_bytes;
   size_t smem;
   bool exact;
 };
 
 TopkPlan plan_topk(int V, int K, int es) {
   TopkPlan p;
-  p.cap = ((K * 2 > 128 ? K * 2 : 128) + 31) & ~31;
+
   p.exact = K > kT;  // the row threshold uses one key per thread of a CTA at least
   const int max_vec = kT * 16;  // 16 vectors per thread at most
   int cs = (V + 8191) / 8192;
@@ -628,15 +661,22 @@ TopkPlan plan_topk(int V, int K, int es) {
   const int nvec = (int)((size_t)p.SL * es / 16 + 1);
   const int per = (nvec + kT - 1) / kT;
   p.NV = per <= 2 ? 2 : per <= 4 ? 4 : per <= 8 ? 8 : per <= 12 ? 12 : 16;
-  // the table of thread-max prefixes, later the leader's ranks of its list
-  const int tab = cs * kT * 2 > p.cap * 4 ? cs * kT * 2 : p.cap * 4;
+  // keys per CTA in the leader's row list: twice the fair share, >= 32, even
+  p.seg = (2 * K + cs - 1) / cs;
+  p.seg = ((p.seg > 32 ? p.seg : 32) + 1) & ~1;
+  const int nrow = cs * p.seg;  // the row list: its keys (and a pad) and their ranks
+  // the table of thread-max prefixes, later the leader's ranks
+  const int tab = cs * kT * 2 > (nrow + 2) * 4 ? cs * kT * 2 : (nrow + 2) * 4;
   p.tab_bytes = (tab + 127) & ~127;
-  p.smem = 128 + kScratchBytes + (size_t)p.tab_bytes + (size_t)p.cap * 8 +
-           (((size_t)p.SL * es + 127) / 128) * 128;
+  // the slice, later the leader's compacted row list
+  const size_t body = (size_t)p.SL * es > (size_t)(nrow + 2) * 8 ? (size_t)p.SL * es : (size_t)(nrow + 2) * 8;
+  p.body_bytes = (int)((body + 127) / 128 * 128);
+  p.smem = 128 + kScratchBytes + (size_t)p.tab_bytes + (size_t)(p.seg + nrow) * 8 +
+           (size_t)p.body_bytes;
   if (per > 16 || p.smem > 227 * 1024) p.exact = true;
   if (p.exact) {
     p.CS = 1;
-    p.smem = 128 + kScratchBytes + (size_t)p.cap * 12;
+    p.smem = 128 + kScratchBytes + (size_t)(2 * K + 2) * 12;
   }
   return p;
 }
@@ -678,8 +718,9 @@ int launch_topk(const void *logits, int dtype, int B, int b, int V, int64_t ld, 
   a.K = K;
   a.CS = p.CS;
   a.SL = p.SL;
-  a.cap = p.cap;
+  a.seg = p.seg;
   a.tab_bytes = p.tab_bytes;
+  a.body_bytes = p.body_bytes;
   a.ld = ld;
   a.topk_logq = topk_logq;
   a.topk_logit = topk_logit;
