@@ -7,29 +7,27 @@
 // ("Adaptief Stoppen": grow until S(N) = A_hat(T_N) L_AR / C(N) starts to fall).
 //
 // One warp builds one request's tree; requests are independent CTAs.
-//  * Scores: log rho of a depth-d node = L - Lam[d], L = the sum of its path's
-//    logits and Lam[d] = lse_1 + ... + lse_d.  L is carried as an unevaluated
-//    float pair (hi + lo), in which sums of bf16/fp32 logits are exact, so two
-//    paths of equal depth and equal logit sum get identical scores and the tie
-//    rule decides between them; log rho itself is a float pair (~2^-44
-//    relative), far inside the 1e-6 band where floating point may decide.
+//  * Scores: log rho of a depth-d node = sum over its path of (logit - lse),
+//    kept as a 64-bit fixed-point integer with 2^-40 resolution.  A bf16
+//    logit (and an fp32 logit of magnitude >= 2^-17) converts exactly, and
+//    every path of depth d subtracts the same rounded lse terms, so two paths
+//    of equal depth and equal logit sum get identical scores and the tie rule
+//    decides between them; across depths the score is within ~2^-36 of the
+//    exact value, far inside the 1e-6 band where floating point may decide.
+//    A child's score is its parent's plus one table entry
+//    lq[d][j] = fix(logit) - fix(lse_{d+1}), so a pop does integer adds only.
 //  * Frontier: node p has one pending candidate, its next-ranked child (p, j);
 //    with sorted ranks, the best of these is the best candidate overall.  The
 //    pending candidate of node p is held in lane p % 32, register slot p / 32,
-//    as a 96-bit key: order-preserving images of the hi and lo floats of log
-//    rho, then tie bits 0xFFFFFF - (depth<<18 | rank<<8 | parent) so equal
-//    scores prefer lower depth, rank and parent.  A pop is three redux.sync
-//    reductions over the lanes' cached best keys.
-//  * Each slot keeps, in a shared-memory record, its current and next-ranked
-//    candidates (logit sum, rho, first-child key; the next one's key too).  A
-//    pop reads the winner's record: the winner's slot moves to its next
-//    candidate and the new node's slot starts at the precomputed first child,
-//    so the pop itself does only integer work and selects.  The three records
-//    the pop invalidates are recomputed one per lane in the same straight-line
-//    block as the next pop's reductions, so the two overlap.
+//    as a 96-bit key: the order-preserving image of the score (two words),
+//    then tie bits 0xFFFFFF - (depth<<18 | rank<<8 | parent) so equal scores
+//    prefer lower depth, rank and parent; the slot also keeps node p's score.
+//    A pop is three redux.sync reductions, two broadcast table loads, two
+//    64-bit adds and selects; no lane waits for another.
 //  * Stop test before adding candidate c to a tree of N nodes (C > 0):
 //    S(N+1) < S(N)  <=>  rho_c C(N) < A_hat (C(N+1) - C(N)), in fp32 with
-//    A_hat summed with Kahan compensation.
+//    A_hat summed with Kahan compensation; rho_c = exp(hi) (1 + lo) from the
+//    float pair nearest the score.
 //  * Per-node results and ancestor masks are kept in shared memory during the
 //    build and written out, coalesced, after it.
 #include "common.cuh"
@@ -55,33 +53,23 @@ struct TreeArgs {
   int32_t *status;
 };
 
-struct F2 {  // unevaluated sum hi + lo, |lo| <= ulp(hi)/2
-  float h, l;
-};
+constexpr float kFix = 1099511627776.f;         // 2^40
+constexpr float kUnfix = 9.094947017729282e-13f;  // 2^-40
+constexpr int64_t kNegFix = -(1ll << 58);         // the score of a -inf logit
+constexpr int64_t kInfCut = -(1ll << 57);         // scores below count as -inf
+constexpr float kMaxLogit = 131072.f;             // finite logits clamped to 2^17
 
-// a + b (float) with the rounding error of the leading sum kept (TwoSum);
-// a non-finite leading sum is returned as (sum, 0).
-__device__ __forceinline__ F2 f2_add(F2 a, float b) {
-  const float s = a.h + b;
-  const float bb = s - a.h;
-  float e = (a.h - (s - bb)) + (b - bb);
-  e += a.l;
-  const float h = s + e;
-  const float l = e - (h - s);
-  const bool fin = isfinite(s);
-  return {fin ? h : s, fin ? l : 0.f};
+// Fixed-point images (2^-40 units) of a logit and of an lse value.
+__device__ __forceinline__ int64_t fix_logit(float x) {
+  if (!(x > -INFINITY)) return kNegFix;  // -inf (and NaN, which K1 flags)
+  return __float2ll_rn(fminf(fmaxf(x, -kMaxLogit), kMaxLogit) * kFix);
+}
+__device__ __forceinline__ int64_t fix_lse(double x) {
+  return __double2ll_rn(fmin(fmax(x, -131072.0), 131072.0) * 1099511627776.0);
 }
 
-// a - b for two pairs.
-__device__ __forceinline__ F2 f2_sub(F2 a, F2 b) {
-  const float s = a.h - b.h;
-  const float bb = s - a.h;
-  float e = (a.h - (s - bb)) + (-b.h - bb);
-  e += a.l - b.l;
-  const float h = s + e;
-  const float l = e - (h - s);
-  const bool fin = isfinite(s);
-  return {fin ? h : s, fin ? l : 0.f};
+__device__ __forceinline__ uint64_t key_of(int64_t score) {
+  return (uint64_t)score ^ 0x8000000000000000ull;
 }
 
 // 96-bit key comparison a > b without branches.
@@ -90,70 +78,35 @@ __device__ __forceinline__ bool key_gt(uint32_t ah, uint32_t al, uint32_t at, ui
   return (ah > bh) | ((ah == bh) & ((al > bl) | ((al == bl) & (at > bt))));
 }
 
-// rho of a candidate from its log rho pair (0 below the float range).
-__device__ __forceinline__ float rho_of(F2 lr) {
-  const float e = lr.h < -104.f ? 0.f : expf(lr.h);
-  return fmaf(e, lr.l, e);
+// rho = exp(score) from the float pair nearest the fixed-point score.
+__device__ __forceinline__ float rho_of(int64_t score) {
+  const float hi = __ll2float_rn(score) * kUnfix;
+  const float lo = __ll2float_rn(score - __float2ll_rn(hi * kFix)) * kUnfix;
+  const float e = hi < -104.f ? 0.f : expf(hi);
+  return fmaf(e, lo, e);
 }
 
-// A candidate (parent P, rank j, depth d): its key, logit sum, rho and the
-// key of its first child (whose parent index is filled in at pop time).
-struct Cand {
-  uint32_t h, l, t;    // key (0, 0, 0 = none)
-  F2 L;                // path logit sum
-  float rho;
-  uint32_t ch, cl, ct; // first child key; ct lacks the child's parent index
-};
-
-// Branch-free: invalid (or out of range) candidates come back as key 0.
-__device__ __forceinline__ Cand cand_of(F2 Lp, int P, int d, int j, bool valid, int b, int R,
-                                        const float *lg, const F2 *Lam) {
-  valid = valid && j < R && d >= 1 && d <= b;
-  const int jj = valid ? j : 0, dd = valid ? d : 1;
-  Cand c;
-  c.L = f2_add(Lp, lg[(dd - 1) * R + jj]);
-  const F2 lr = f2_sub(c.L, Lam[dd]);
-  c.h = valid ? ord_f32(lr.h) : 0u;
-  c.l = valid ? ord_f32(lr.l) : 0u;
-  c.t = valid ? 0xFFFFFFu - (((uint32_t)dd << 18) | ((uint32_t)jj << 8) | (uint32_t)P) : 0u;
-  c.rho = rho_of(lr);
-  const bool kid = valid && dd < b;
-  const int dc = dd < b ? dd : b - 1;  // a valid row to read either way
-  const F2 lg2 = f2_sub(f2_add(c.L, lg[dc * R]), Lam[dc + 1]);
-  c.ch = kid ? ord_f32(lg2.h) : 0u;
-  c.cl = kid ? ord_f32(lg2.l) : 0u;
-  c.ct = kid ? 0xFFFFFFu - ((uint32_t)(dd + 1) << 18) : 0u;
-  return c;
+// The largest 96-bit key over the warp.
+__device__ __forceinline__ void warp_best(uint32_t bh, uint32_t bl, uint32_t bt, uint32_t &mh,
+                                          uint32_t &ml, uint32_t &mt) {
+  mh = __reduce_max_sync(kFull, bh);
+  ml = __reduce_max_sync(kFull, bh == mh ? bl : 0u);
+  mt = __reduce_max_sync(kFull, (bh == mh && bl == ml) ? bt : 0u);
 }
-
-// Shared-memory record of slot s: its current candidate (logit sum, rho,
-// first child key) and its next candidate (key, rho, logit sum, first child
-// key).
-struct __align__(16) Rec {
-  F2 cL;
-  uint32_t ch, cl, ct;
-  float crho;
-  uint32_t nh, nl, nt;
-  float nrho;
-  F2 nL;
-  uint32_t nch, ncl, nct;
-  uint32_t pad;
-};
 
 template <int S>  // register slots per lane: S * 32 >= n_max
 __global__ void __launch_bounds__(32) build_tree_kernel(TreeArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
-  Rec *rec = reinterpret_cast<Rec *>(smem);                         // [n_max]
-  float *lg = reinterpret_cast<float *>(rec + a.n_max);              // [b * R] (16-byte aligned)
-  int *tk = reinterpret_cast<int *>(lg + a.b * a.R);                 // [b * R]
-  F2 *Lam = reinterpret_cast<F2 *>(tk + a.b * a.R);                  // [33]
-  F2 *Lnode = Lam + 33;                                              // [n_max] node logit sums
-  float *C = reinterpret_cast<float *>(Lnode + a.n_max);             // [n_max + 1]
+  // [n_max] node scores (padded to an even count, so every later array stays
+  // 16-byte aligned), then [b * R] the scores' steps
+  int64_t *lq = reinterpret_cast<int64_t *>(smem) + ((a.n_max + 1) & ~1);
+  int *tk = reinterpret_cast<int *>(lq + a.b * a.R);                 // [b * R] tokens
+  float *C = reinterpret_cast<float *>(tk + a.b * a.R);              // [n_max + 1]
   uint32_t *mask = reinterpret_cast<uint32_t *>(C + a.n_max + 1);   // [n_max * W]
   int *nd_par = reinterpret_cast<int *>(mask + a.n_max * a.W);       // [n_max] per node:
   int *nd_dj = nd_par + a.n_max;                                     //   depth << 16 | rank
-  float *nd_lr = reinterpret_cast<float *>(nd_dj + a.n_max);         //   log rho (hi)
-  float *nd_A = nd_lr + a.n_max;                                     //   A_hat after it
+  float *nd_A = reinterpret_cast<float *>(nd_dj + a.n_max);          //   A_hat after it
+  int64_t *nd_sc = reinterpret_cast<int64_t *>(smem);               //   score (first array)
 
   const int r = blockIdx.x, lane = threadIdx.x;
   const int R = a.R, W = a.W, b = a.b;
@@ -163,7 +116,7 @@ __global__ void __launch_bounds__(32) build_tree_kernel(TreeArgs a) {
   const int ctx = a.ctx_len[r];
   const float L_ar = a.l_ar[r];
   const int root_tok = a.root_token[r];
-  const double lse_v = lane < b ? a.lse[(size_t)r * b + lane] : 0.0;
+  const int64_t lse_fix = fix_lse(lane < b ? a.lse[(size_t)r * b + lane] : 0.0);
   const float *cr = a.cost + (a.cost_per_request ? (size_t)r * (a.n_max + 1) : 0);
   float cv[9];  // n_max + 1 <= 257 <= 9 * 32
 #pragma unroll
@@ -175,10 +128,10 @@ __global__ void __launch_bounds__(32) build_tree_kernel(TreeArgs a) {
     const int nlg = b * R;
     const float *gl = a.topk_logit + (size_t)r * b * a.K;
     const int32_t *gt = a.topk_tok + (size_t)r * b * a.K;
-    const bool vec = R == a.K && (nlg & 3) == 0 && ((uintptr_t)gl & 15) == 0 &&
+    const bool vec = R == a.K && (R & 3) == 0 && ((uintptr_t)gl & 15) == 0 &&
                      ((uintptr_t)gt & 15) == 0;
-    if (vec) {  // the [b][K] block is contiguous: 16-byte loads
-      const int n4 = nlg >> 2;
+    if (vec) {  // the [b][K] block is contiguous and each 16 bytes lie in one row
+      const int n4 = nlg >> 2, r4 = R >> 2;
       for (int base = 0; base < n4; base += 32 * kBatch / 2) {
         float4 v[kBatch / 2];
         int4 t[kBatch / 2];
@@ -193,8 +146,14 @@ __global__ void __launch_bounds__(32) build_tree_kernel(TreeArgs a) {
 #pragma unroll
         for (int u = 0; u < kBatch / 2; ++u) {
           const int i = base + u * 32 + lane;
+          const int64_t ls = __shfl_sync(kFull, lse_fix, min(i, n4 - 1) / r4);
           if (i < n4) {
-            reinterpret_cast<float4 *>(lg)[i] = v[u];
+            const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int64_t f = fix_logit(e[q]);
+              lq[4 * i + q] = f == kNegFix ? kNegFix : f - ls;
+            }
             reinterpret_cast<int4 *>(tk)[i] = t[u];
           }
         }
@@ -215,8 +174,10 @@ __global__ void __launch_bounds__(32) build_tree_kernel(TreeArgs a) {
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
           const int idx = base + u * 32 + lane;
+          const int64_t ls = __shfl_sync(kFull, lse_fix, min(idx, nlg - 1) / R);
           if (idx < nlg) {
-            lg[idx] = v[u];
+            const int64_t f = fix_logit(v[u]);
+            lq[idx] = f == kNegFix ? kNegFix : f - ls;
             tk[idx] = t[u];
           }
         }
@@ -233,81 +194,60 @@ __global__ void __launch_bounds__(32) build_tree_kernel(TreeArgs a) {
     }
   }
   if (__any_sync(kFull, bad) && lane == 0) atomicOr(&a.status[r], BASTION_STATUS_BAD_COST);
-  {
-    // Lam[d] = lse_1 + ... + lse_d: each lse as a float pair, then a prefix scan
-    F2 v = {0.f, 0.f};
-    if (lane < b) {
-      const float h = (float)lse_v;
-      v = {h, (float)(lse_v - (double)h)};
-    }
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const F2 u = {__shfl_up_sync(kFull, v.h, o), __shfl_up_sync(kFull, v.l, o)};
-      if (lane >= o) v = f2_sub(v, F2{-u.h, -u.l});
-    }
-    if (lane < b) Lam[lane + 1] = v;
-    if (lane == 0) Lam[0] = {0.f, 0.f};
-  }
-  if (lane == 0) Lnode[0] = {0.f, 0.f};
   for (int w = lane; w < W; w += 32) mask[w] = w == 0 ? 1u : 0u;
   __syncwarp();
 
-  // the root's slot: current candidate (0, 0), next (0, 1)
+  // ---- the build; slot s of this lane holds node s * 32 + lane: the key of
+  // its pending candidate and the node's own score
   uint32_t kh[S], kl[S], kt[S];
+  int64_t sc[S];
 #pragma unroll
-  for (int s = 0; s < S; ++s) kh[s] = kl[s] = kt[s] = 0u;
-  {
-    const Cand c = cand_of({0.f, 0.f}, 0, 1, lane, lane < 2, b, R, lg, Lam);  // lanes 0, 1
-    const float c0rho = __shfl_sync(kFull, c.rho, 0);
-    const F2 c0L = {__shfl_sync(kFull, c.L.h, 0), __shfl_sync(kFull, c.L.l, 0)};
-    const uint32_t c0ch = __shfl_sync(kFull, c.ch, 0), c0cl = __shfl_sync(kFull, c.cl, 0),
-                   c0ct = __shfl_sync(kFull, c.ct, 0);
-    if (lane == 1) {
-      Rec q;
-      q.cL = c0L; q.ch = c0ch; q.cl = c0cl; q.ct = c0ct; q.crho = c0rho;
-      q.nh = c.h; q.nl = c.l; q.nt = c.t; q.nrho = c.rho; q.nL = c.L;
-      q.nch = c.ch; q.ncl = c.cl; q.nct = c.ct; q.pad = 0u;
-      rec[0] = q;
-    }
-    if (lane == 0) { kh[0] = c.h; kl[0] = c.l; kt[0] = c.t; }
+  for (int s = 0; s < S; ++s) { kh[s] = kl[s] = kt[s] = 0u; sc[s] = 0; }
+  if (lane == 0) {  // the root: score 0, pending candidate (0, 0) at depth 1
+    const uint64_t k = key_of(lq[0]);
+    kh[0] = (uint32_t)(k >> 32);
+    kl[0] = (uint32_t)k;
+    kt[0] = 0xFFFFFFu - (1u << 18);
   }
-  __syncwarp();
   uint32_t bh = kh[0], bl = kl[0], bt = kt[0];
-  uint32_t mh = __reduce_max_sync(kFull, bh);
-  uint32_t ml = __reduce_max_sync(kFull, bh == mh ? bl : 0u);
-  uint32_t mt = __reduce_max_sync(kFull, (bh == mh && bl == ml) ? bt : 0u);
+  uint32_t mh, ml, mt;
+  warp_best(bh, bl, bt, mh, ml, mt);
 
   float A_hi = 1.f, A_lo = 0.f;  // A_hat with Kahan compensation
   int N = 1;
   while (N < a.n_max) {
     if ((mh | ml | mt) == 0u) break;  // no candidate left
-    const float lr_h = unord_f32(mh);
-    if (lr_h == -INFINITY) break;
+    const int64_t lr = (int64_t)((((uint64_t)mh << 32) | ml) ^ 0x8000000000000000ull);
+    if (lr < kInfCut) break;  // the best candidate has log rho = -inf
     const uint32_t sec = 0xFFFFFFu - mt;
     const int d = (int)(sec >> 18), j = (int)((sec >> 8) & 1023u), p = (int)(sec & 255u);
-    const Rec w = rec[p];
-    const float Cp = C[N], Cn = C[N + 1];
-    if (w.crho * Cp < (A_hi + A_lo) * (Cn - Cp)) break;  // S would decrease: keep T_N
-
     const int n = N;
-    N = n + 1;
-    {
-      const float y = w.crho - A_lo;
-      const float t = A_hi + y;
-      A_lo = (t - A_hi) - y;
-      A_hi = t;
-    }
-    // the two slots that change: p moves to its next candidate, n starts at its
-    // first child; then every lane rescans its slots
-    const bool kid = d < b;
     const int lp = p & 31, sp = p >> 5, ln = n & 31, sn = n >> 5;
+    // the winner's rho, the two candidates this pop creates ((p, j + 1) and
+    // (n, 0)) and the parent's mask row, all independent of one another
+    const float rho = rho_of(lr);
+    int64_t sp_score = 0;
+#pragma unroll
+    for (int s = 0; s < S; ++s) sp_score = s == sp ? sc[s] : sp_score;
+    const int jn = j + 1;
+    const bool vs = jn < R, vc = d < b;
+    const int64_t qs = lq[(d - 1) * R + (vs ? jn : j)];
+    const int64_t qc = lq[(vc ? d : d - 1) * R];
+    const uint32_t mrow = lane < W ? mask[p * W + lane] : 0u;
+    const float Cp = C[N], Cn = C[N + 1];
+    const uint64_t ks = key_of(sp_score + qs), kc = key_of(lr + qc);
+    const uint32_t ts = 0xFFFFFFu - (((uint32_t)d << 18) | ((uint32_t)jn << 8) | (uint32_t)p);
+    const uint32_t tc = 0xFFFFFFu - (((uint32_t)(d + 1) << 18) | (uint32_t)n);
+    // the slots change before the stop test: if the build stops they are
+    // dropped with it
 #pragma unroll
     for (int s = 0; s < S; ++s) {
       const bool up = lane == lp && s == sp;
-      const bool un = kid && lane == ln && s == sn;
-      kh[s] = up ? w.nh : (un ? w.ch : kh[s]);
-      kl[s] = up ? w.nl : (un ? w.cl : kl[s]);
-      kt[s] = up ? w.nt : (un ? w.ct - (uint32_t)n : kt[s]);
+      const bool un = lane == ln && s == sn;
+      kh[s] = up ? (vs ? (uint32_t)(ks >> 32) : 0u) : (un ? (vc ? (uint32_t)(kc >> 32) : 0u) : kh[s]);
+      kl[s] = up ? (vs ? (uint32_t)ks : 0u) : (un ? (vc ? (uint32_t)kc : 0u) : kl[s]);
+      kt[s] = up ? (vs ? ts : 0u) : (un ? (vc ? tc : 0u) : kt[s]);
+      sc[s] = un ? lr : sc[s];
     }
     bh = kh[0]; bl = kl[0]; bt = kt[0];
 #pragma unroll
@@ -315,42 +255,25 @@ __global__ void __launch_bounds__(32) build_tree_kernel(TreeArgs a) {
       const bool g = key_gt(kh[s], kl[s], kt[s], bh, bl, bt);
       bh = g ? kh[s] : bh; bl = g ? kl[s] : bl; bt = g ? kt[s] : bt;
     }
-    // the records this pop invalidates, one per lane, and the next pop's
-    // reductions (independent of them):
-    //   lane 0: slot p's new next candidate (p, j + 2)
-    //   lane 1: the new node's current candidate (n, 0)
-    //   lane 2: the new node's next candidate (n, 1)
-    const bool l0 = lane == 0;
-    const F2 Lpar = l0 ? Lnode[p] : w.cL;
-    const Cand c = cand_of(Lpar, l0 ? p : n, l0 ? d : d + 1, l0 ? j + 2 : lane - 1,
-                           l0 || (kid && lane < 3), b, R, lg, Lam);
-    mh = __reduce_max_sync(kFull, bh);
-    ml = __reduce_max_sync(kFull, bh == mh ? bl : 0u);
-    mt = __reduce_max_sync(kFull, (bh == mh && bl == ml) ? bt : 0u);
-    if (l0) {  // slot p advances: current <- next, next <- (p, j + 2)
-      Rec q;
-      q.cL = w.nL; q.ch = w.nch; q.cl = w.ncl; q.ct = w.nct; q.crho = w.nrho;
-      q.nh = c.h; q.nl = c.l; q.nt = c.t; q.nrho = c.rho; q.nL = c.L;
-      q.nch = c.ch; q.ncl = c.cl; q.nct = c.ct; q.pad = 0u;
-      rec[p] = q;
+    if (rho * Cp < (A_hi + A_lo) * (Cn - Cp)) break;  // S would decrease: keep T_N
+
+    N = n + 1;
+    {
+      const float y = rho - A_lo;
+      const float t = A_hi + y;
+      A_lo = (t - A_hi) - y;
+      A_hi = t;
     }
-    if (kid && lane == 1) {
-      rec[n].cL = c.L; rec[n].ch = c.ch; rec[n].cl = c.cl; rec[n].ct = c.ct; rec[n].crho = c.rho;
-    }
-    if (kid && lane == 2) {
-      rec[n].nh = c.h; rec[n].nl = c.l; rec[n].nt = c.t; rec[n].nrho = c.rho; rec[n].nL = c.L;
-      rec[n].nch = c.ch; rec[n].ncl = c.cl; rec[n].nct = c.ct;
-    }
-    if (lane == 3) Lnode[n] = w.cL;
-    if (lane == 4) {
+    if (lane == 0) {
       nd_par[n] = p;
       nd_dj[n] = (d << 16) | j;
-      nd_lr[n] = lr_h;
+      nd_sc[n] = lr;
       nd_A[n] = A_hi + A_lo;
     }
-    if (lane < W) mask[n * W + lane] = mask[p * W + lane] | (lane == (n >> 5) ? (1u << (n & 31)) : 0u);
-    __syncwarp();
+    if (lane < W) mask[n * W + lane] = mrow | (lane == (n >> 5) ? (1u << (n & 31)) : 0u);
+    warp_best(bh, bl, bt, mh, ml, mt);
   }
+  __syncwarp();
 
   // ---- outputs, coalesced
   const size_t nb = (size_t)r * a.n_max;
@@ -374,7 +297,7 @@ __global__ void __launch_bounds__(32) build_tree_kernel(TreeArgs a) {
       a.pos_id[o] = ctx + d;
       a.token[o] = tk[(d - 1) * R + j];
       a.rank[o] = j;
-      a.log_rho[o] = nd_lr[i];
+      a.log_rho[o] = __ll2float_rn(nd_sc[i]) * kUnfix;
       a.a_hat[o] = Ah;
       a.speedup[o] = Ah * L_ar / C[i + 1];
     }
@@ -423,9 +346,8 @@ int launch_build_tree(const float *topk_logit, const int32_t *topk_tok, const do
   a.speedup = speedup;
   a.anc_mask = anc_mask;
   a.status = status;
-  const size_t smem = (size_t)n_max * sizeof(Rec) + 33 * 8 + (size_t)n_max * 8 +
-                      (size_t)(n_max + 1) * 4 + (size_t)n_max * a.W * 4 + (size_t)b * a.R * 8 +
-                      (size_t)n_max * 16;
+  const size_t smem = (size_t)((n_max + 1) & ~1) * 8 + (size_t)b * a.R * 12 + (size_t)(n_max + 1) * 4 +
+                      (size_t)n_max * a.W * 4 + (size_t)n_max * 12;
   if (n_max <= 32) launch_s<1>(a, smem, stream);
   else if (n_max <= 64) launch_s<2>(a, smem, stream);
   else if (n_max <= 128) launch_s<4>(a, smem, stream);
