@@ -8,15 +8,19 @@
 // sm_103a design, one CTA per (request, KV head, 128 query rows):
 //  * the 128 rows are (tree node, query head of the KV group) pairs, so the G
 //    heads that share a KV head share every K/V tile read;
-//  * warp 0 streams Q once and K/V tiles of 128 keys through a 2-stage ring
-//    with TMA (cp.async.bulk.tensor, 128-byte swizzle, no multicast);
+//  * warp 0 streams Q once and the K tiles of 128 keys, warp 3 the V tiles,
+//    each through its own 2-slot ring with TMA (cp.async.bulk.tensor, 128-byte
+//    swizzle, no multicast); a K slot frees as soon as S has read it;
 //  * warp 1 (one thread) issues tcgen05.mma kind::f16 (bf16 in, fp32 out):
 //    S_t = Q K_t^T into one of two TMEM buffers, then O += P_{t-1} V_{t-1};
-//  * warps 4-7 (one TMEM lane = one query row per thread) read S_t with
-//    tcgen05.ld, apply the tree mask and the online softmax in base 2, and write
-//    P_t as bf16 into shared memory in the MMA operand layout; O stays in TMEM
-//    and is rescaled only when a row's running max grows by more than 2^8
-//    (the final normalisation uses the same reference max, so this is exact);
+//  * warps 4-11 run the softmax, two warps per TMEM lane quadrant (one query
+//    row per lane), each on half of the tile's 128 keys: they read S_t with
+//    tcgen05.ld, apply the tree mask, exchange their half-row maxima through
+//    shared memory (one named barrier per warp pair and tile), and write P_t
+//    as bf16 into shared memory in the MMA operand layout; O stays in TMEM and
+//    is rescaled (each warp its half of the columns) only when a row's running
+//    max grows by more than 2^8 (the final normalisation uses the same
+//    reference max, so this is exact);
 //  * epilogue: O / l as bf16 (round to nearest even) to global memory.
 // Every wait is bounded (~1 s); on a timeout the CTA flags the request, waits
 // for its own copies and MMAs (bounded), frees its TMEM and returns.
@@ -29,7 +33,7 @@ namespace bastion {
 
 namespace {
 
-constexpr int kAT = 256;
+constexpr int kAT = 384;  // warp 0 TMA (Q, K), 1 MMA, 2 TMEM, 3 TMA (V), 4-11 softmax
 constexpr int kBM = 128;
 constexpr int kBN = 128;
 constexpr uint32_t kAtom = 128 * 128;          // 128 rows x 128 bytes
@@ -38,7 +42,8 @@ constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffKV = kTile;             // stage s: K at +0, V at +kTile
 constexpr uint32_t kOffP = kOffKV + 2 * 2 * kTile;
 constexpr uint32_t kOffBar = kOffP + 2 * kTile;
-constexpr uint32_t kSmem = kOffBar + 256 + 1024;  // + alignment slack
+constexpr uint32_t kOffX = kOffBar + 256;     // [2][128] floats: half-row exchange
+constexpr uint32_t kSmem = kOffX + 1024 + 1024;  // + alignment slack
 constexpr float kRescale = 8.0f;               // lazy rescale threshold (log2 units)
 
 struct AttnArgs {
@@ -52,7 +57,7 @@ struct AttnArgs {
 };
 
 struct Bars {
-  uint64_t q_full, kv_full[2], kv_empty[2], s_full[2], p_full[2], pv_done[2];
+  uint64_t q_full, k_full[2], v_full[2], k_empty[2], v_empty[2], s_full[2], p_full[2], pv_done[2];
   uint32_t tmem;
   int abort;
 };
@@ -209,10 +214,12 @@ __global__ void __launch_bounds__(kAT, 1)
   if (tid == 0) {
     mbar_init(&bs.q_full, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&bs.kv_full[s], 1);
-      mbar_init(&bs.kv_empty[s], 1);
+      mbar_init(&bs.k_full[s], 1);
+      mbar_init(&bs.v_full[s], 1);
+      mbar_init(&bs.k_empty[s], 1);
+      mbar_init(&bs.v_empty[s], 1);
       mbar_init(&bs.s_full[s], 1);
-      mbar_init(&bs.p_full[s], 128);
+      mbar_init(&bs.p_full[s], 256);
       mbar_init(&bs.pv_done[s], 1);
     }
     bs.abort = 0;
@@ -228,28 +235,33 @@ __global__ void __launch_bounds__(kAT, 1)
   tc_fence_after();
   const uint32_t tmem = bs.tmem;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+  if (warp == 0 || warp == 3) {
+    // ------------------------------------------------------------ TMA producers
+    // warp 0: Q and the K tiles (a K slot frees once S = QK^T has read it);
+    // warp 3: the V tiles (a V slot frees once O += PV has read it)
     if (lane == 0) {
-      mbar_arrive_expect_tx(&bs.q_full, kTile);
-      tma_load_4d(smem + kOffQ, &tm_q, 0, g * a.G, i0, r, &bs.q_full);
-      tma_load_4d(smem + kOffQ + kAtom, &tm_q, 64, g * a.G, i0, r, &bs.q_full);
+      const bool is_k = warp == 0;
+      if (is_k) {
+        mbar_arrive_expect_tx(&bs.q_full, kTile);
+        tma_load_4d(smem + kOffQ, &tm_q, 0, g * a.G, i0, r, &bs.q_full);
+        tma_load_4d(smem + kOffQ + kAtom, &tm_q, 64, g * a.G, i0, r, &bs.q_full);
+      }
+      uint64_t *full = is_k ? bs.k_full : bs.v_full, *empty = is_k ? bs.k_empty : bs.v_empty;
+      const CUtensorMap *map = is_k ? &tm_k : &tm_v;
       int issued = 0;
       for (int t = 0; t < n_tiles; ++t) {
         const int s = t & 1;
-        if (t >= 2 && !wait_bar(&bs.kv_empty[s], ((t - 2) >> 1) & 1, abort, &a.status[r])) break;
-        unsigned char *kb = smem + kOffKV + s * 2 * kTile;
-        mbar_arrive_expect_tx(&bs.kv_full[s], 2 * kTile);
-        tma_load_4d(kb, &tm_k, 0, g, t * kBN, r, &bs.kv_full[s]);
-        tma_load_4d(kb + kAtom, &tm_k, 64, g, t * kBN, r, &bs.kv_full[s]);
-        tma_load_4d(kb + kTile, &tm_v, 0, g, t * kBN, r, &bs.kv_full[s]);
-        tma_load_4d(kb + kTile + kAtom, &tm_v, 64, g, t * kBN, r, &bs.kv_full[s]);
+        if (t >= 2 && !wait_bar(&empty[s], ((t - 2) >> 1) & 1, abort, &a.status[r])) break;
+        unsigned char *dst = smem + kOffKV + s * 2 * kTile + (is_k ? 0 : kTile);
+        mbar_arrive_expect_tx(&full[s], kTile);
+        tma_load_4d(dst, map, 0, g, t * kBN, r, &full[s]);
+        tma_load_4d(dst + kAtom, map, 64, g, t * kBN, r, &full[s]);
         issued = t + 1;
       }
       // drain: our last copies have landed (bounded) before the CTA may exit
       for (int t = issued > 2 ? issued - 2 : 0; t < issued; ++t)
-        mbar_wait_bounded(&bs.kv_full[t & 1], (t >> 1) & 1);
-      mbar_wait_bounded(&bs.q_full, 0);
+        mbar_wait_bounded(&full[t & 1], (t >> 1) & 1);
+      if (is_k) mbar_wait_bounded(&bs.q_full, 0);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -262,7 +274,7 @@ __global__ void __launch_bounds__(kAT, 1)
       for (int t = 0; ok && t <= n_tiles; ++t) {
         if (t < n_tiles) {
           const int s = t & 1;
-          if (!wait_bar(&bs.kv_full[s], (t >> 1) & 1, abort, &a.status[r])) break;
+          if (!wait_bar(&bs.k_full[s], (t >> 1) & 1, abort, &a.status[r])) break;
           tc_fence_after();
           const uint32_t sk = smem_u32(smem + kOffKV + s * 2 * kTile);
           const uint32_t d = tmem + 128u * (1u + (uint32_t)s);
@@ -273,10 +285,12 @@ __global__ void __launch_bounds__(kAT, 1)
                      ks > 0);
           }
           mma_commit(&bs.s_full[s]);
+          mma_commit(&bs.k_empty[s]);
         }
         if (t >= 1) {
           const int u = t - 1, s = u & 1;
           if (!wait_bar(&bs.p_full[s], (u >> 1) & 1, abort, &a.status[r])) break;
+          if (!wait_bar(&bs.v_full[s], (u >> 1) & 1, abort, &a.status[r])) break;
           tc_fence_after();
           const uint32_t sp = smem_u32(smem + kOffP + s * kTile);
           const uint32_t sv = smem_u32(smem + kOffKV + s * 2 * kTile + kTile);
@@ -287,7 +301,7 @@ __global__ void __launch_bounds__(kAT, 1)
                      sw128_desc(sv + (uint32_t)ks * 2048u, kAtom, 1024), id_pv, (u > 0 || ks > 0));
           }
           mma_commit(&bs.pv_done[s]);
-          mma_commit(&bs.kv_empty[s]);
+          mma_commit(&bs.v_empty[s]);
           last_pv = u;
         }
       }
@@ -295,27 +309,35 @@ __global__ void __launch_bounds__(kAT, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax + epilogue
-    const int m = (warp - 4) * 32 + lane;  // query row = TMEM lane
+    // warps w and w + 4 (w = 4..7) share TMEM lane quadrant w - 4: the same 32
+    // query rows, keys [64 h, 64 h + 64) of each tile for half h
+    const int quad = (warp - 4) & 3, half = (warp - 4) >> 2;
+    const int m = quad * 32 + lane;  // query row = TMEM lane
     const int node = i0 + m / a.G;
     const int hh = m % a.G;
     const bool row_live = node < nn;
+    float *xm = reinterpret_cast<float *>(smem + kOffX);  // [2][128]
     uint32_t anc[8];
 #pragma unroll
     for (int w = 0; w < 8; ++w)
       anc[w] = (row_live && w < a.W) ? a.anc_mask[((size_t)r * a.n_max + node) * a.W + w] : 0u;
-    const uint32_t lane_base = tmem + ((uint32_t)((warp - 4) * 32) << 16);
+    const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+    const uint32_t col0 = 64u * (uint32_t)half;
     float m_ref = -INFINITY, l_sum = 0.f;
     bool ok = true;
     for (int t = 0; t < n_tiles && ok; ++t) {
       const int s = t & 1;
-      ok = __all_sync(kFull, wait_bar(&bs.s_full[s], (t >> 1) & 1, abort, &a.status[r]));
-      if (!ok) break;
+      // every wait of the tile comes before the pair's exchange, and a failed
+      // one still reaches it, so both warps of the pair leave together
+      bool okw = __all_sync(kFull, wait_bar(&bs.s_full[s], (t >> 1) & 1, abort, &a.status[r]));
+      if (okw && t >= 2)  // P buffer s free: PV of tile t-2 done
+        okw = __all_sync(kFull, wait_bar(&bs.pv_done[s], ((t - 2) >> 1) & 1, abort, &a.status[r]));
       tc_fence_after();
-      const int kb = t * kBN;
-      // visibility of the 128 keys of this tile, 32 per word
-      uint32_t vis[4];
+      const int kb = t * kBN + 64 * half;
+      // visibility of this half's 64 keys, 32 per word
+      uint32_t vis[2];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < 2; ++q) {
         const int j0 = kb + 32 * q;           // first key of the group
         uint32_t ctxbits;
         if (j0 + 32 <= ctx_c) ctxbits = 0xffffffffu;
@@ -338,62 +360,75 @@ __global__ void __launch_bounds__(kAT, 1)
         else if (left < 32) lim = (1u << left) - 1u;
         vis[q] = (ctxbits | tb) & lim;
       }
-      // pass 1: tile max of the visible scaled scores
-      float mt = -INFINITY;
+      // this half's scaled scores and their max
+      float v[64];
+      float mh = -INFINITY;
+      if (okw) {
+        float u0[32], u1[32];
+        tmem_ld32(lane_base + 128u * (1u + (uint32_t)s) + col0, u0);
+        tmem_ld32(lane_base + 128u * (1u + (uint32_t)s) + col0 + 32u, u1);
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        float v[32];
-        tmem_ld32(lane_base + 128u * (1u + (uint32_t)s) + 32u * cc, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if ((vis[cc] >> i) & 1u) mt = fmaxf(mt, v[i] * a.scale_log2);
+        for (int i = 0; i < 32; ++i) {
+          v[i] = u0[i] * a.scale_log2;
+          v[32 + i] = u1[i] * a.scale_log2;
+          if ((vis[0] >> i) & 1u) mh = fmaxf(mh, v[i]);
+          if ((vis[1] >> i) & 1u) mh = fmaxf(mh, v[32 + i]);
+        }
       }
+      // exchange with the partner warp: its half max, and whether it is ok
+      xm[half * 128 + m] = okw ? mh : __int_as_float(0x7fc00001);  // NaN: failed
+      asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");
+      const float mp = xm[(half ^ 1) * 128 + m];
+      ok = __all_sync(kFull, okw && !(mp != mp));
+      asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");  // xm reusable
+      if (!ok) break;
+      const float mt = fmaxf(mh, mp);
       // lazy rescale: a row moves its reference max only when the tile max
       // exceeds it by more than 2^8; O in TMEM is rescaled by the whole warp
       // (tcgen05.ld/st are warp-collective), with alpha = 1 for other rows.
       const bool grow = mt > m_ref + kRescale || (m_ref == -INFINITY && mt != -INFINITY);
       const bool rescale = grow && t > 0 && m_ref != -INFINITY;
       const float alpha = rescale ? ex2f(m_ref - mt) : 1.0f;
-      if (__any_sync(kFull, rescale)) {
-        ok = __all_sync(kFull, wait_bar(&bs.pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, abort,
-                                        &a.status[r]));
-        if (!ok) break;
+      if (__any_sync(kFull, rescale)) {  // the partner takes the same branch
+        bool okr = __all_sync(kFull, wait_bar(&bs.pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, abort,
+                                              &a.status[r]));
         tc_fence_after();
+        if (okr) {
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          float o[32];
-          tmem_ld32(lane_base + 32u * cc, o);
+          for (int cc = 0; cc < 2; ++cc) {
+            float o[32];
+            tmem_ld32(lane_base + col0 + 32u * cc, o);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= alpha;
-          tmem_st32(lane_base + 32u * cc, o);
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            tmem_st32(lane_base + col0 + 32u * cc, o);
+          }
         }
+        xm[half * 128 + m] = okr ? 0.f : __int_as_float(0x7fc00001);
+        asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");
+        const float fp = xm[(half ^ 1) * 128 + m];
+        ok = __all_sync(kFull, okr && !(fp != fp));
+        asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");
+        if (!ok) break;
       }
       if (rescale) l_sum *= alpha;
       if (grow) m_ref = mt;
-      // P buffer s must be free: PV of tile t-2 done
-      if (t >= 2) {
-        ok = __all_sync(kFull, wait_bar(&bs.pv_done[s], ((t - 2) >> 1) & 1, abort, &a.status[r]));
-        if (!ok) break;
-      }
       unsigned char *pb = smem + kOffP + s * kTile;
       float part = 0.f;
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        float v[32];
-        tmem_ld32(lane_base + 128u * (1u + (uint32_t)s) + 32u * cc, v);
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          float p0 = ((vis[cc] >> i) & 1u) && m_ref != -INFINITY ? ex2f(v[i] * a.scale_log2 - m_ref) : 0.f;
-          float p1 = ((vis[cc] >> (i + 1)) & 1u) && m_ref != -INFINITY ? ex2f(v[i + 1] * a.scale_log2 - m_ref) : 0.f;
+          const float p0 = ((vis[cc] >> i) & 1u) && m_ref != -INFINITY ? ex2f(v[32 * cc + i] - m_ref) : 0.f;
+          const float p1 = ((vis[cc] >> (i + 1)) & 1u) && m_ref != -INFINITY ? ex2f(v[32 * cc + i + 1] - m_ref) : 0.f;
           part += p0 + p1;
           pk[i >> 1] = pack_bf16(p0, p1);
         }
-        // columns 32cc .. 32cc+31: atom cc/2, 16-byte chunks (4cc+q) % 8
-        unsigned char *rowp = pb + (cc >> 1) * kAtom + (m >> 3) * 1024 + (m & 7) * 128;
+        // columns 64 h + 32 cc ..: atom h, 16-byte chunks (4 cc + q) ^ (m % 8)
+        unsigned char *rowp = pb + half * kAtom + (m >> 3) * 1024 + (m & 7) * 128;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const int ch = ((cc & 1) * 4 + q) ^ (m & 7);
+          const int ch = (cc * 4 + q) ^ (m & 7);
           *reinterpret_cast<uint4 *>(rowp + ch * 16) =
               make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
         }
@@ -403,19 +438,24 @@ __global__ void __launch_bounds__(kAT, 1)
       tc_fence_before();
       mbar_arrive(&bs.p_full[s]);
     }
-    // epilogue: the whole warp reads O from TMEM; live rows store O / l
+    // epilogue: the whole warp reads its half of O from TMEM; the pair adds
+    // its two halves of l; live rows store O / l
     if (ok && n_tiles > 0) {
       const int u = n_tiles - 1;
-      ok = __all_sync(kFull, wait_bar(&bs.pv_done[u & 1], (u >> 1) & 1, abort, &a.status[r]));
+      const bool okw = __all_sync(kFull, wait_bar(&bs.pv_done[u & 1], (u >> 1) & 1, abort, &a.status[r]));
       tc_fence_after();
+      xm[half * 128 + m] = okw ? l_sum : __int_as_float(0x7fc00001);
+      asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");
+      const float lp = xm[(half ^ 1) * 128 + m];
+      ok = __all_sync(kFull, okw && !(lp != lp));
       if (ok) {
-        const float inv = row_live ? 1.0f / l_sum : 0.0f;
+        const float inv = row_live ? 1.0f / (l_sum + lp) : 0.0f;
         uint16_t *dst = a.out + (((size_t)r * a.n_max + (row_live ? node : 0)) * a.Hq +
-                                 (size_t)g * a.G + hh) * 128;
+                                 (size_t)g * a.G + hh) * 128 + col0;
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < 2; ++cc) {
           float o[32];
-          tmem_ld32(lane_base + 32u * cc, o);
+          tmem_ld32(lane_base + col0 + 32u * cc, o);
           if (row_live) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
