@@ -114,6 +114,28 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 64 consecutive columns of the warp's 32 lanes: two loads, one wait.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+  uint32_t r[64];
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+        "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[32 * h + 0]), "=r"(r[32 * h + 1]), "=r"(r[32 * h + 2]), "=r"(r[32 * h + 3]),
+          "=r"(r[32 * h + 4]), "=r"(r[32 * h + 5]), "=r"(r[32 * h + 6]), "=r"(r[32 * h + 7]),
+          "=r"(r[32 * h + 8]), "=r"(r[32 * h + 9]), "=r"(r[32 * h + 10]), "=r"(r[32 * h + 11]),
+          "=r"(r[32 * h + 12]), "=r"(r[32 * h + 13]), "=r"(r[32 * h + 14]), "=r"(r[32 * h + 15]),
+          "=r"(r[32 * h + 16]), "=r"(r[32 * h + 17]), "=r"(r[32 * h + 18]), "=r"(r[32 * h + 19]),
+          "=r"(r[32 * h + 20]), "=r"(r[32 * h + 21]), "=r"(r[32 * h + 22]), "=r"(r[32 * h + 23]),
+          "=r"(r[32 * h + 24]), "=r"(r[32 * h + 25]), "=r"(r[32 * h + 26]), "=r"(r[32 * h + 27]),
+          "=r"(r[32 * h + 28]), "=r"(r[32 * h + 29]), "=r"(r[32 * h + 30]), "=r"(r[32 * h + 31])
+        : "r"(taddr + 32u * (uint32_t)h));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
@@ -360,20 +382,25 @@ __global__ void __launch_bounds__(kAT, 1)
         else if (left < 32) lim = (1u << left) - 1u;
         vis[q] = (ctxbits | tb) & lim;
       }
-      // this half's scaled scores and their max
+      // this half's raw scores and the max of the visible ones, scaled (the
+      // scale is positive); context tiles are fully visible to every row
+      const bool full = __all_sync(kFull, (vis[0] & vis[1]) == 0xffffffffu);
       float v[64];
       float mh = -INFINITY;
       if (okw) {
-        float u0[32], u1[32];
-        tmem_ld32(lane_base + 128u * (1u + (uint32_t)s) + col0, u0);
-        tmem_ld32(lane_base + 128u * (1u + (uint32_t)s) + col0 + 32u, u1);
+        tmem_ld64(lane_base + 128u * (1u + (uint32_t)s) + col0, v);
+        float mr = -INFINITY;
+        if (full) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          v[i] = u0[i] * a.scale_log2;
-          v[32 + i] = u1[i] * a.scale_log2;
-          if ((vis[0] >> i) & 1u) mh = fmaxf(mh, v[i]);
-          if ((vis[1] >> i) & 1u) mh = fmaxf(mh, v[32 + i]);
+          for (int i = 0; i < 64; i += 2) mr = fmaxf(mr, fmaxf(v[i], v[i + 1]));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            if ((vis[0] >> i) & 1u) mr = fmaxf(mr, v[i]);
+            if ((vis[1] >> i) & 1u) mr = fmaxf(mr, v[32 + i]);
+          }
         }
+        mh = mr * a.scale_log2;
       }
       // exchange with the partner warp: its half max, and whether it is ok
       xm[half * 128 + m] = okw ? mh : __int_as_float(0x7fc00001);  // NaN: failed
@@ -414,15 +441,28 @@ __global__ void __launch_bounds__(kAT, 1)
       if (grow) m_ref = mt;
       unsigned char *pb = smem + kOffP + s * kTile;
       float part = 0.f;
+      const float nm = m_ref == -INFINITY ? 0.f : -m_ref;  // no visible key yet: all p = 0
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         uint32_t pk[16];
+        if (full && m_ref != -INFINITY) {
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float p0 = ((vis[cc] >> i) & 1u) && m_ref != -INFINITY ? ex2f(v[32 * cc + i] - m_ref) : 0.f;
-          const float p1 = ((vis[cc] >> (i + 1)) & 1u) && m_ref != -INFINITY ? ex2f(v[32 * cc + i + 1] - m_ref) : 0.f;
-          part += p0 + p1;
-          pk[i >> 1] = pack_bf16(p0, p1);
+          for (int i = 0; i < 32; i += 2) {
+            const float p0 = ex2f(fmaf(v[32 * cc + i], a.scale_log2, nm));
+            const float p1 = ex2f(fmaf(v[32 * cc + i + 1], a.scale_log2, nm));
+            part += p0 + p1;
+            pk[i >> 1] = pack_bf16(p0, p1);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const bool s0 = ((vis[cc] >> i) & 1u) && m_ref != -INFINITY;
+            const bool s1 = ((vis[cc] >> (i + 1)) & 1u) && m_ref != -INFINITY;
+            const float p0 = s0 ? ex2f(fmaf(v[32 * cc + i], a.scale_log2, nm)) : 0.f;
+            const float p1 = s1 ? ex2f(fmaf(v[32 * cc + i + 1], a.scale_log2, nm)) : 0.f;
+            part += p0 + p1;
+            pk[i >> 1] = pack_bf16(p0, p1);
+          }
         }
         // columns 64 h + 32 cc ..: atom h, 16-byte chunks (4 cc + q) ^ (m % 8)
         unsigned char *rowp = pb + half * kAtom + (m >> 3) * 1024 + (m & 7) * 128;
