@@ -171,6 +171,27 @@ __device__ __forceinline__ float ex2f(float x) {
   return y;
 }
 
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// (x0, x1) * s + c, both lanes of a packed f32x2 FMA.
+__device__ __forceinline__ void fma2(float x0, float x1, float sc, float c, float &d0, float &d1) {
+  asm("{\n .reg .b64 x, m, a, d;\n mov.b64 x, {%2, %3};\n mov.b64 m, {%4, %4};\n"
+      " mov.b64 a, {%5, %5};\n fma.rn.f32x2 d, x, m, a;\n mov.b64 {%0, %1}, d;\n}\n"
+      : "=f"(d0), "=f"(d1)
+      : "f"(x0), "f"(x1), "f"(sc), "f"(c));
+}
+
+__device__ __forceinline__ void add2(float &a0, float &a1, float b0, float b1) {
+  asm("{\n .reg .b64 a, b;\n mov.b64 a, {%0, %1};\n mov.b64 b, {%2, %3};\n"
+      " add.rn.f32x2 a, a, b;\n mov.b64 {%0, %1}, a;\n}\n"
+      : "+f"(a0), "+f"(a1)
+      : "f"(b0), "f"(b1));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
@@ -391,8 +412,15 @@ __global__ void __launch_bounds__(kAT, 1)
         tmem_ld64(lane_base + 128u * (1u + (uint32_t)s) + col0, v);
         float mr = -INFINITY;
         if (full) {
+          float q0 = v[0], q1 = v[1], q2 = v[2], q3 = v[3];
 #pragma unroll
-          for (int i = 0; i < 64; i += 2) mr = fmaxf(mr, fmaxf(v[i], v[i + 1]));
+          for (int i = 4; i < 64; i += 8) {
+            q0 = max3f(q0, v[i], v[i + 1]);
+            q1 = max3f(q1, v[i + 2], v[i + 3]);
+            q2 = max3f(q2, v[i + 4], v[i + 5]);
+            q3 = max3f(q3, v[i + 6], v[i + 7]);
+          }
+          mr = max3f(fmaxf(q0, q1), q2, q3);
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
@@ -446,13 +474,16 @@ __global__ void __launch_bounds__(kAT, 1)
       for (int cc = 0; cc < 2; ++cc) {
         uint32_t pk[16];
         if (full && m_ref != -INFINITY) {
+          float s0 = 0.f, s1 = 0.f;
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
-            const float p0 = ex2f(fmaf(v[32 * cc + i], a.scale_log2, nm));
-            const float p1 = ex2f(fmaf(v[32 * cc + i + 1], a.scale_log2, nm));
-            part += p0 + p1;
+            float t0, t1;
+            fma2(v[32 * cc + i], v[32 * cc + i + 1], a.scale_log2, nm, t0, t1);
+            const float p0 = ex2f(t0), p1 = ex2f(t1);
+            add2(s0, s1, p0, p1);
             pk[i >> 1] = pack_bf16(p0, p1);
           }
+          part += s0 + s1;
         } else {
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
