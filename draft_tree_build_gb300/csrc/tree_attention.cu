@@ -378,9 +378,10 @@ __global__ void __launch_bounds__(kAT, 1)
       tc_fence_after();
       const int kb = t * kBN + 64 * half;
       // visibility of this half's 64 keys, 32 per word
-      uint32_t vis[2];
+      uint32_t vis[2] = {0xffffffffu, 0xffffffffu};
+      const bool ctx_tile = kb + 64 <= ctx_c;  // the context: visible to every row
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
+      for (int q = 0; q < 2 && !ctx_tile; ++q) {
         const int j0 = kb + 32 * q;           // first key of the group
         uint32_t ctxbits;
         if (j0 + 32 <= ctx_c) ctxbits = 0xffffffffu;
