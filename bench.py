@@ -253,21 +253,31 @@ def run_ours(args, ws, rank, local):
     assert int(step.status.abs().sum()) == 0, "device status bits set"
 
     # end to end through the public API with host buffers (pinned), per step:
-    # H2D of the drafter and target logits, the step, D2H of the results
+    # H2D of the drafter logits; the tree; D2H of its sizes; H2D of the target
+    # logits of the tree's nodes (the only target rows a step has: one copy per
+    # request); verification; D2H of the results
     E = max(3, min(args.steps, 20))
     out_host = torch.empty((w.B, w.b + 1), dtype=torch.int32, pin_memory=True)
     acc_host = torch.empty((w.B,), dtype=torch.int32, pin_memory=True)
+    nn_host = torch.empty((w.B,), dtype=torch.int32, pin_memory=True)
     xin, tin = torch.empty_like(xs[0]), torch.empty_like(ts[0])
 
     def e2e_step():
         xin.copy_(x_pin, non_blocking=True)
-        tin.copy_(t_pin, non_blocking=True)
-        step.run(xin, tin)
+        step.draft(xin)
+        nn_host.copy_(step.tree.n_nodes, non_blocking=True)
+        stream.synchronize()
+        for r in range(w.B):
+            n = int(nn_host[r])
+            tin[r, :n].copy_(t_pin[r, :n], non_blocking=True)
+        step.verify(tin)
         out_host.copy_(step.ver.out_tokens, non_blocking=True)
         acc_host.copy_(step.ver.accept_len, non_blocking=True)
 
+    acc_graph = step.ver.accept_len.cpu()  # from the graph replays above
     e2e_step()
     torch.cuda.synchronize()
+    assert torch.equal(acc_host, acc_graph), "end-to-end result differs from the device-resident one"
     barrier(ws)
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     f0.record(stream)
@@ -276,8 +286,8 @@ def run_ours(args, ws, rank, local):
     f1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(f0.elapsed_time(f1), ws) / E
-    h2d = x_pin.numel() * x_pin.element_size() + t_pin.numel() * t_pin.element_size()
-    d2h = out_host.numel() * 4 + acc_host.numel() * 4
+    h2d = x_pin.numel() * x_pin.element_size() + int(n_nodes.sum()) * w.V * es
+    d2h = out_host.numel() * 4 + acc_host.numel() * 4 + nn_host.numel() * 4
 
     hbm, peak_kind = peaks()
     ms_step = elapsed_ms / args.steps

@@ -289,17 +289,26 @@ class TreeStep:
         self.l_ar = l_ar.to(device=device, dtype=torch.float32)
         self.graph = None
 
-    def run(self, drafter_logits, target_logits, stream=None):
-        t, tr, v = self.topk, self.tree, self.ver
+    def draft(self, drafter_logits, stream=None):
+        """Steps 1-3: marginals, then the tree (its size decides which target rows exist)."""
+        t, tr = self.topk, self.tree
         bastion_topk_marginals(drafter_logits, self.K, t.logq, t.logit, t.tok, t.lse, self.ws_topk,
                                self.status, stream)
         bastion_build_tree(t.logit, t.tok, t.lse, self.n_max, self.root_token, self.ctx_len,
                            self.cost_ms, self.l_ar, tr.n_nodes, tr.parent, tr.depth, tr.pos_id,
                            tr.token, tr.rank, tr.log_rho, tr.a_hat, tr.speedup, tr.anc_mask,
                            self.status, stream)
+
+    def verify(self, target_logits, stream=None):
+        """Step 4: greedy verification of the tree against the target's logits."""
+        tr, v = self.tree, self.ver
         bastion_verify_greedy(target_logits, self.b, tr.n_nodes, tr.parent, tr.token, v.argmax,
                               v.accept_len, v.accept_nodes, v.out_tokens, self.ws_verify,
                               self.status, stream)
+
+    def run(self, drafter_logits, target_logits, stream=None):
+        self.draft(drafter_logits, stream)
+        self.verify(target_logits, stream)
 
     def capture(self, drafter_logits, target_logits):
         s = torch.cuda.Stream(device=self.device)
