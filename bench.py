@@ -92,6 +92,24 @@ class Clocks:
                 "power_w_max": max(power) if power else None, "reasons": sorted(reasons)}
 
 
+def profiled_traffic(summary: str, source: str):
+    """DRAM bytes per launch from a committed ncu summary, or None when the
+    kernel source has changed since the counters were taken."""
+    import hashlib
+    try:
+        text = open(os.path.join(ROOT, "profiles", summary)).read()
+        digest = hashlib.sha256(open(os.path.join(ROOT, "draft_tree_build_gb300", "csrc", source), "rb").read()).hexdigest()
+    except OSError:
+        return None
+    fields = dict(line.split(": ", 1) for line in text.splitlines() if ": " in line and line[:1].isalpha())
+    if fields.get("kernel_source_sha256_16", "").strip() != digest[:16]:
+        return None
+    try:
+        return int(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
 def dist_setup():
     import torch
     ws = int(os.environ.get("WORLD_SIZE", "1"))
@@ -307,7 +325,8 @@ def run_ours(args, ws, rank, local):
                    "parallelism": f"replicas x{ws}"},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": hbm, "unit": "GB/s",
                      "frac": ach / hbm, "peak_source": f"{peak_kind} copy bandwidth",
-                     "traffic": None,
+                     "traffic": (profiled_traffic("topk_marginals_b32_v151936.md", "topk_marginals.cu")
+                                 if dom == "topk_marginals" and w.cid == 3 else None),
                      "step_frac": bytes_step / (ms_step * 1e-3) / 1e9 / hbm,
                      "bytes_per_step": bytes_step},
         "kernels": kern,
@@ -458,7 +477,8 @@ def run_with_attention(args, ws, rank, local):
         roof = {"bound": "tensor", "kernel": "tree_attention", "achieved": flops / (t_attn * 1e-3) / 1e12,
                 "peak": tf_peak, "unit": "TFLOP/s", "peak_source": f"{peak_kind} bf16 (burst)"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
+    roof["traffic"] = (profiled_traffic("tree_attention_b8_ctx4096_n64.md", "tree_attention.cu")
+                       if args.workload == 4 else None)
     roof["roofline_us"] = max(t_mem, t_tc) * 1e6
     roof["attn_bytes"] = bytes_attn
     roof["attn_flops"] = flops
