@@ -109,8 +109,11 @@ int bastion_topk_marginals(const void *logits, int dtype, int B, int b, int V, i
  * rho = 1, counted in N and A_hat.  The children of a depth-d node are the K
  * ranked tokens of q_{d+1}; a node's next candidate child is its next-ranked
  * token.  Candidates are ordered by log rho (descending), then depth, rank and
- * parent index (ascending).  log rho of a depth-d node is evaluated in fp64 as
- * (sum of its path's logits) - (lse_1 + ... + lse_d).  From N = 1 (root only),
+ * parent index (ascending).  log rho of a depth-d node is the sum over its
+ * path of (logit - lse_k), formed in 64-bit fixed point with 2^-40 resolution:
+ * exact for bf16 logits (and fp32 logits of magnitude >= 2^-17), so paths of
+ * equal depth and equal logit sum tie exactly and the tie rule decides; finite
+ * logits are clamped to +-2^17.  From N = 1 (root only),
  * the best candidate is added as node N while S(N+1) >= S(N); the build stops
  * at the first strict decrease, when no candidate is left, or at n_max nodes.
  * One warp builds one request's tree.
