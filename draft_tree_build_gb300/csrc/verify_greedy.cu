@@ -9,7 +9,8 @@
 // Design (HBM-bound sweep over sum_r n_nodes[r] rows of V logits), two kernels
 // chained with programmatic dependent launch:
 //  * sweep: persistent grid sized from the occupancy; every warp works on its
-//    own items with no barrier and no waiting on other warps.  An item is one
+//    own contiguous run of items with no barrier and no waiting on other
+//    warps.  An item is one
 //    4 KB segment of one tree row (row counts are read on the device, so only
 //    rows < n_nodes[r] are read).  A lane issues its 8 x 16-byte non-allocating
 //    loads at once, keeps the running max (NaN-propagating packed bf16x2 max)
@@ -164,16 +165,30 @@ __global__ void __launch_bounds__(kVT) verify_kernel(VerifyArgs a) {
   }
   const int total = prefix[a.B];
   const int gw = blockIdx.x * kWarps + warp, nw = gridDim.x * kWarps;
-
-  for (int item = gw; item < total; item += nw) {
+  // each warp takes a contiguous run of items; its position (request r, row
+  // i, segment sg) is found once and then stepped
+  const int per = (total + nw - 1) / nw;
+  const int it0 = min(total, gw * per), it1 = min(total, it0 + per);
+  int r = 0, i = 0, sg = 0;
+  if (it0 < it1) {
     int lo = 0, hi = a.B;
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
-      if (prefix[mid] <= item) lo = mid; else hi = mid;
+      if (prefix[mid] <= it0) lo = mid; else hi = mid;
     }
-    const int r = lo;
-    const int off = item - prefix[r];
-    const int i = off / a.nseg, sg = off - i * a.nseg;
+    r = lo;
+    const int off = it0 - prefix[r];
+    i = off / a.nseg;
+    sg = off - i * a.nseg;
+  }
+  for (int item = it0; item < it1; ++item) {
+    if (item > it0 && ++sg == a.nseg) {
+      sg = 0;
+      if (++i * a.nseg >= prefix[r + 1] - prefix[r]) {  // next request with items
+        i = 0;
+        do { ++r; } while (prefix[r + 1] == prefix[r]);
+      }
+    }
     const int e0 = sg * a.SEG;
     const int n = min(a.V - e0, a.SEG);
     const unsigned char *g0 = a.logits + (((size_t)r * a.n_max + i) * (size_t)a.ld + e0) * ES;
