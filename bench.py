@@ -333,7 +333,7 @@ def run_ours(args, ws, rank, local):
         "clocks": clk,
         "e2e": {"value": aggregate_rate(1, e2e_ms, ws), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 4 * args.steps,  # top-K, tree, verify sweep, verify finish
     }
     return res
 
@@ -493,7 +493,7 @@ def run_with_attention(args, ws, rank, local):
                    "D": w.D, "mean_tree_nodes": float(n_nodes.mean()),
                    "l2": "inputs larger than L2", "parallelism": f"replicas x{ws}"},
         "roofline": roof, "kernels": {"tree_attention": {"ms": t_attn}}, "clocks": clk,
-        "gpu_launches": (1 if args.workload == 4 else 4) * args.steps,
+        "gpu_launches": (1 if args.workload == 4 else 5) * args.steps,  # + attention
     }
 
 
