@@ -13,8 +13,8 @@
 //    of its 256 thread maxima' order keys to every CTA of the cluster with
 //    asynchronous distributed-shared-memory stores (st.async), counted on the
 //    receiver's mbarrier; while they travel it sums exp(l - m_t) over its
-//    elements with packed f32x2 arithmetic and ex2 (the log2(e) factor split
-//    in two parts so its rounding does not bias all terms alike);
+//    elements, one packed f32x2 FMA per two exponents and ex2 (the rounding
+//    of m_t log2(e) is a common factor of the thread's terms, removed once);
 //  * the row threshold T: from its copy of the row's CS*256 prefixes, every
 //    CTA finds the K-th largest with one histogram of distances below the
 //    largest.  T is the smallest float with the K-th largest prefix, so at
@@ -41,8 +41,8 @@ namespace {
 
 constexpr int kT = 256;      // threads per CTA (8 warps)
 constexpr int kMaxCS = 16;   // CTAs per row at most
-constexpr float kL2eHi = 1.4426950216293335f;     // log2(e) rounded to float
-constexpr float kL2eLo = 1.925963033500011e-08f;  // log2(e) - kL2eHi
+constexpr float kL2e = 1.4426950216293335f;       // log2(e) rounded to float
+constexpr float kL2eLo = 1.925963033500011e-08f;  // log2(e) - kL2e
 constexpr double kLn2 = 0.6931471805599453;       // ln 2
 
 struct TopkArgs {
@@ -84,20 +84,20 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// exp(x0 - m) + exp(x1 - m), exp(x2 - m) + exp(x3 - m) as a pair, with the
-// subtraction and the split log2(e) product in packed f32x2 arithmetic.
-__device__ __forceinline__ void exp4(float x0, float x1, float x2, float x3, float m, float &s0,
+// 2^(x_i log2(e) - c) for four elements, summed in pairs: one packed f32x2
+// FMA per two elements, then ex2.  With c = the float nearest m log2(e), the
+// exponent is (x_i - m) log2(e) + (m log2(e) - c): every term of one thread
+// carries the same factor 2^(m log2(e) - c), removed from the thread's sum
+// once (see the callers).
+__device__ __forceinline__ void exp4(float x0, float x1, float x2, float x3, float nc, float &s0,
                                      float &s1) {
   float t0, t1, t2, t3;
-  asm("{\n .reg .b64 d, e, mm, hh, ll, p, q;\n"
-      " mov.b64 d, {%4, %5};\n mov.b64 e, {%6, %7};\n mov.b64 mm, {%8, %8};\n"
-      " mov.b64 hh, {%9, %9};\n mov.b64 ll, {%10, %10};\n"
-      " sub.rn.f32x2 d, d, mm;\n sub.rn.f32x2 e, e, mm;\n"
-      " mul.rn.f32x2 p, d, ll;\n mul.rn.f32x2 q, e, ll;\n"
-      " fma.rn.f32x2 d, d, hh, p;\n fma.rn.f32x2 e, e, hh, q;\n"
+  asm("{\n .reg .b64 d, e, k, c;\n"
+      " mov.b64 d, {%4, %5};\n mov.b64 e, {%6, %7};\n mov.b64 k, {%9, %9};\n"
+      " mov.b64 c, {%8, %8};\n fma.rn.f32x2 d, d, k, c;\n fma.rn.f32x2 e, e, k, c;\n"
       " mov.b64 {%0, %1}, d;\n mov.b64 {%2, %3}, e;\n}\n"
       : "=f"(t0), "=f"(t1), "=f"(t2), "=f"(t3)
-      : "f"(x0), "f"(x1), "f"(x2), "f"(x3), "f"(m), "f"(kL2eHi), "f"(kL2eLo));
+      : "f"(x0), "f"(x1), "f"(x2), "f"(x3), "f"(nc), "f"(kL2e));
   const float e0 = ex2(t0), e1 = ex2(t1), e2 = ex2(t2), e3 = ex2(t3);
   asm("{\n .reg .b64 a, c;\n mov.b64 a, {%2, %3};\n mov.b64 c, {%4, %5};\n"
       " add.rn.f32x2 a, a, c;\n mov.b64 {%0, %1}, a;\n}\n"
@@ -105,7 +105,7 @@ __device__ __forceinline__ void exp4(float x0, float x1, float x2, float x3, flo
       : "f"(e0), "f"(e1), "f"(e2), "f"(e3));
 }
 
-__device__ __forceinline__ float exp_shifted(float d) { return ex2(fmaf(d, kL2eHi, d * kL2eLo)); }
+__device__ __forceinline__ float exp_shifted(float d) { return ex2(fmaf(d, kL2e, d * kL2eLo)); }
 
 // Two-float sums: value = hi + lo.
 __device__ __forceinline__ float2 two_sum(float a, float b) {
@@ -161,19 +161,19 @@ __device__ __forceinline__ float vmax(const uint4 &x) {
   }
 }
 
-// Sum of exp(x - m) over one 16-byte vector.
+// Sum of 2^(x log2(e) + nc) over one 16-byte vector.
 template <int ES>
-__device__ __forceinline__ float vexp_sum(const uint4 &x, float m) {
+__device__ __forceinline__ float vexp_sum(const uint4 &x, float nc) {
   float f[16 / ES];
   unpack<ES>(x, f);
   if constexpr (ES == 2) {
     float p0, p1, q0, q1;
-    exp4(f[0], f[1], f[2], f[3], m, p0, p1);
-    exp4(f[4], f[5], f[6], f[7], m, q0, q1);
+    exp4(f[0], f[1], f[2], f[3], nc, p0, p1);
+    exp4(f[4], f[5], f[6], f[7], nc, q0, q1);
     return (p0 + p1) + (q0 + q1);
   } else {
     float p0, p1;
-    exp4(f[0], f[1], f[2], f[3], m, p0, p1);
+    exp4(f[0], f[1], f[2], f[3], nc, p0, p1);
     return p0 + p1;
   }
 }
@@ -452,11 +452,16 @@ __global__ void __launch_bounds__(kT, 5) topk_cluster_kernel(TopkArgs a) {
   // sum of exp(l - m_t) while the other CTAs' prefixes arrive
   float sum = 0.f;
   if (tmax != -INFINITY) {
+    // c = the float nearest tmax log2(e); every term below is off by the
+    // factor 2^(tmax log2(e) - c), taken out of the sum at the end
+    const float c = tmax * kL2e;
+    const float c_err = fmaf(tmax, kL2e, -c);
 #pragma unroll
     for (int u = 0; u < NV; ++u) {
       const int v = tid + u * kT;
-      if (v < s.nvec) sum += vexp_sum<ES>(ld_shared_v4(body + v * 16), tmax);
+      if (v < s.nvec) sum += vexp_sum<ES>(ld_shared_v4(body + v * 16), -c);
     }
+    sum *= ex2(-c_err);
     if (has_x) sum += exp_shifted(xs - tmax);
   }
   if (!mbar_wait_bounded(tab_bar, 0) && lane == 0) atomicOr(&a.status[req], BASTION_STATUS_TIMEOUT);
