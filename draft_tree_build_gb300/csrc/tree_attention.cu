@@ -14,14 +14,16 @@
 //  * warp 1 (one thread) issues tcgen05.mma kind::f16 (bf16 in, fp32 out):
 //    S_t = Q K_t^T into one of two TMEM buffers, then O += P_{t-1} V_{t-1};
 //  * warps 4-11 run the softmax, two warps per TMEM lane quadrant (one query
-//    row per lane), each on half of the tile's 128 keys: they read S_t with
-//    tcgen05.ld, apply the tree mask, exchange their half-row maxima through
-//    shared memory (one named barrier per warp pair and tile), and write P_t
-//    as bf16 into shared memory in the MMA operand layout; O stays in TMEM and
-//    is rescaled (each warp its half of the columns) only when a row's running
-//    max grows by more than 2^8 (the final normalisation uses the same
-//    reference max, so this is exact);
-//  * epilogue: O / l as bf16 (round to nearest even) to global memory.
+//    row per lane), each on half of the tile's 128 keys with its own online
+//    softmax: PV is issued as two K=64 MMAs into two accumulators O_A, O_B
+//    (TMEM columns 0 and 384), so the halves never wait for each other.  Each
+//    warp reads S_t with tcgen05.ld, applies the tree mask (context tiles are
+//    visible to every row and skip it), and writes its half of P_t as bf16
+//    into shared memory in the MMA operand layout; its O_h is rescaled only
+//    when a row's running max grows by more than 2^8 (the final
+//    normalisation uses the same reference max, so this is exact);
+//  * epilogue: the pair exchanges its (max, sum) once and writes
+//    (O_A 2^(m_A - M) + O_B 2^(m_B - M)) / l as bf16 (round to nearest even).
 // Every wait is bounded (~1 s); on a timeout the CTA flags the request, waits
 // for its own copies and MMAs (bounded), frees its TMEM and returns.
 #include <cuda.h>
@@ -42,9 +44,9 @@ constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffKV = kTile;             // stage s: K at +0, V at +kTile
 constexpr uint32_t kOffP = kOffKV + 2 * 2 * kTile;
 constexpr uint32_t kOffBar = kOffP + 2 * kTile;
-constexpr uint32_t kOffX = kOffBar + 256;     // [2][128] floats: half-row exchange
-constexpr uint32_t kSmem = kOffX + 1024 + 1024;  // + alignment slack
+constexpr uint32_t kSmem = kOffBar + 256 + 1024;  // + alignment slack
 constexpr float kRescale = 8.0f;               // lazy rescale threshold (log2 units)
+constexpr uint32_t kColOB = 384;               // TMEM columns of O_B (O_A at 0, S at 128, 256)
 
 struct AttnArgs {
   int B, n_max, Hq, Hkv, G, W, qt_max;
@@ -337,11 +339,14 @@ __global__ void __launch_bounds__(kAT, 1)
           tc_fence_after();
           const uint32_t sp = smem_u32(smem + kOffP + s * kTile);
           const uint32_t sv = smem_u32(smem + kOffKV + s * 2 * kTile + kTile);
+          // keys 0-63 of the tile into O_A (TMEM columns 0-127), keys 64-127
+          // into O_B (columns 384-511): each half has its own softmax state
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             const uint32_t offp = (uint32_t)(ks >> 2) * kAtom + (uint32_t)(ks & 3) * 32u;
-            mma_bf16(tmem, sw128_desc(sp + offp, 16, 1024),
-                     sw128_desc(sv + (uint32_t)ks * 2048u, kAtom, 1024), id_pv, (u > 0 || ks > 0));
+            mma_bf16(ks < 4 ? tmem : tmem + kColOB, sw128_desc(sp + offp, 16, 1024),
+                     sw128_desc(sv + (uint32_t)ks * 2048u, kAtom, 1024), id_pv,
+                     (u > 0 || (ks & 3) > 0));
           }
           mma_commit(&bs.pv_done[s]);
           mma_commit(&bs.v_empty[s]);
@@ -353,28 +358,29 @@ __global__ void __launch_bounds__(kAT, 1)
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax + epilogue
     // warps w and w + 4 (w = 4..7) share TMEM lane quadrant w - 4: the same 32
-    // query rows, keys [64 h, 64 h + 64) of each tile for half h
+    // query rows.  Half h takes keys [64 h, 64 h + 64) of every tile with its
+    // own online softmax (reference max, sum) and its own accumulator O_h;
+    // the two halves are combined once, at the end.
     const int quad = (warp - 4) & 3, half = (warp - 4) >> 2;
     const int m = quad * 32 + lane;  // query row = TMEM lane
     const int node = i0 + m / a.G;
     const int hh = m % a.G;
     const bool row_live = node < nn;
-    float *xm = reinterpret_cast<float *>(smem + kOffX);  // [2][128]
     uint32_t anc[8];
 #pragma unroll
     for (int w = 0; w < 8; ++w)
       anc[w] = (row_live && w < a.W) ? a.anc_mask[((size_t)r * a.n_max + node) * a.W + w] : 0u;
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
     const uint32_t col0 = 64u * (uint32_t)half;
+    const uint32_t o_base = lane_base + (half ? kColOB : 0u);
     float m_ref = -INFINITY, l_sum = 0.f;
     bool ok = true;
     for (int t = 0; t < n_tiles && ok; ++t) {
       const int s = t & 1;
-      // every wait of the tile comes before the pair's exchange, and a failed
-      // one still reaches it, so both warps of the pair leave together
-      bool okw = __all_sync(kFull, wait_bar(&bs.s_full[s], (t >> 1) & 1, abort, &a.status[r]));
-      if (okw && t >= 2)  // P buffer s free: PV of tile t-2 done
-        okw = __all_sync(kFull, wait_bar(&bs.pv_done[s], ((t - 2) >> 1) & 1, abort, &a.status[r]));
+      ok = __all_sync(kFull, wait_bar(&bs.s_full[s], (t >> 1) & 1, abort, &a.status[r]));
+      if (ok && t >= 2)  // P buffer s free: PV of tile t-2 done
+        ok = __all_sync(kFull, wait_bar(&bs.pv_done[s], ((t - 2) >> 1) & 1, abort, &a.status[r]));
+      if (!ok) break;
       tc_fence_after();
       const int kb = t * kBN + 64 * half;
       // visibility of this half's 64 keys, 32 per word
@@ -408,63 +414,45 @@ __global__ void __launch_bounds__(kAT, 1)
       // scale is positive); context tiles are fully visible to every row
       const bool full = __all_sync(kFull, (vis[0] & vis[1]) == 0xffffffffu);
       float v[64];
-      float mh = -INFINITY;
-      if (okw) {
-        tmem_ld64(lane_base + 128u * (1u + (uint32_t)s) + col0, v);
-        float mr = -INFINITY;
-        if (full) {
-          float q0 = v[0], q1 = v[1], q2 = v[2], q3 = v[3];
+      tmem_ld64(lane_base + 128u * (1u + (uint32_t)s) + col0, v);
+      float mr = -INFINITY;
+      if (full) {
+        float q0 = v[0], q1 = v[1], q2 = v[2], q3 = v[3];
 #pragma unroll
-          for (int i = 4; i < 64; i += 8) {
-            q0 = max3f(q0, v[i], v[i + 1]);
-            q1 = max3f(q1, v[i + 2], v[i + 3]);
-            q2 = max3f(q2, v[i + 4], v[i + 5]);
-            q3 = max3f(q3, v[i + 6], v[i + 7]);
-          }
-          mr = max3f(fmaxf(q0, q1), q2, q3);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            if ((vis[0] >> i) & 1u) mr = fmaxf(mr, v[i]);
-            if ((vis[1] >> i) & 1u) mr = fmaxf(mr, v[32 + i]);
-          }
+        for (int i = 4; i < 64; i += 8) {
+          q0 = max3f(q0, v[i], v[i + 1]);
+          q1 = max3f(q1, v[i + 2], v[i + 3]);
+          q2 = max3f(q2, v[i + 4], v[i + 5]);
+          q3 = max3f(q3, v[i + 6], v[i + 7]);
         }
-        mh = mr * a.scale_log2;
+        mr = max3f(fmaxf(q0, q1), q2, q3);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          if ((vis[0] >> i) & 1u) mr = fmaxf(mr, v[i]);
+          if ((vis[1] >> i) & 1u) mr = fmaxf(mr, v[32 + i]);
+        }
       }
-      // exchange with the partner warp: its half max, and whether it is ok
-      xm[half * 128 + m] = okw ? mh : __int_as_float(0x7fc00001);  // NaN: failed
-      asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");
-      const float mp = xm[(half ^ 1) * 128 + m];
-      ok = __all_sync(kFull, okw && !(mp != mp));
-      asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");  // xm reusable
-      if (!ok) break;
-      const float mt = fmaxf(mh, mp);
+      const float mt = mr * a.scale_log2;
       // lazy rescale: a row moves its reference max only when the tile max
-      // exceeds it by more than 2^8; O in TMEM is rescaled by the whole warp
+      // exceeds it by more than 2^8; O_h in TMEM is rescaled by the whole warp
       // (tcgen05.ld/st are warp-collective), with alpha = 1 for other rows.
       const bool grow = mt > m_ref + kRescale || (m_ref == -INFINITY && mt != -INFINITY);
       const bool rescale = grow && t > 0 && m_ref != -INFINITY;
       const float alpha = rescale ? ex2f(m_ref - mt) : 1.0f;
-      if (__any_sync(kFull, rescale)) {  // the partner takes the same branch
-        bool okr = __all_sync(kFull, wait_bar(&bs.pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, abort,
-                                              &a.status[r]));
-        tc_fence_after();
-        if (okr) {
-#pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            float o[32];
-            tmem_ld32(lane_base + col0 + 32u * cc, o);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= alpha;
-            tmem_st32(lane_base + col0 + 32u * cc, o);
-          }
-        }
-        xm[half * 128 + m] = okr ? 0.f : __int_as_float(0x7fc00001);
-        asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");
-        const float fp = xm[(half ^ 1) * 128 + m];
-        ok = __all_sync(kFull, okr && !(fp != fp));
-        asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");
+      if (__any_sync(kFull, rescale)) {
+        ok = __all_sync(kFull, wait_bar(&bs.pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, abort,
+                                        &a.status[r]));
         if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          float o[32];
+          tmem_ld32(o_base + 32u * cc, o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= alpha;
+          tmem_st32(o_base + 32u * cc, o);
+        }
       }
       if (rescale) l_sum *= alpha;
       if (grow) m_ref = mt;
@@ -510,32 +498,48 @@ __global__ void __launch_bounds__(kAT, 1)
       tc_fence_before();
       mbar_arrive(&bs.p_full[s]);
     }
-    // epilogue: the whole warp reads its half of O from TMEM; the pair adds
-    // its two halves of l; live rows store O / l
-    if (ok && n_tiles > 0) {
-      const int u = n_tiles - 1;
-      const bool okw = __all_sync(kFull, wait_bar(&bs.pv_done[u & 1], (u >> 1) & 1, abort, &a.status[r]));
+    // epilogue: the pair exchanges (reference max, sum) once -- both warps
+    // always reach this barrier, a failed one with a NaN -- and each warp
+    // writes its half of the columns: O = (O_A 2^(m_A - M) + O_B 2^(m_B - M)) /
+    // (l_A 2^(m_A - M) + l_B 2^(m_B - M)), M = max(m_A, m_B).
+    if (n_tiles > 0) {
+      bool okw = ok;
+      if (okw) {
+        const int u = n_tiles - 1;
+        okw = __all_sync(kFull, wait_bar(&bs.pv_done[u & 1], (u >> 1) & 1, abort, &a.status[r]));
+      }
       tc_fence_after();
-      xm[half * 128 + m] = okw ? l_sum : __int_as_float(0x7fc00001);
+      // the exchange uses P buffer 0: the last PV has read it (a warp that
+      // failed only writes its NaN flag)
+      float *xm = reinterpret_cast<float *>(smem + kOffP);  // [2][128] maxima
+      float *xl = xm + 256;                                  // [2][128] sums
+      xm[half * 128 + m] = okw ? m_ref : __int_as_float(0x7fc00001);
+      xl[half * 128 + m] = l_sum;
       asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");
-      const float lp = xm[(half ^ 1) * 128 + m];
-      ok = __all_sync(kFull, okw && !(lp != lp));
+      const float mA = xm[m], mB = xm[128 + m], lA = xl[m], lB = xl[128 + m];
+      ok = __all_sync(kFull, !(mA != mA) && !(mB != mB));
       if (ok) {
-        const float inv = row_live ? 1.0f / (l_sum + lp) : 0.0f;
+        const float M = fmaxf(mA, mB);
+        const float fA = mA == -INFINITY ? 0.f : ex2f(mA - M);
+        const float fB = mB == -INFINITY ? 0.f : ex2f(mB - M);
+        const float l = lA * fA + lB * fB;
+        const float inv = row_live && l > 0.f ? 1.0f / l : 0.0f;
+        const float gA = fA * inv, gB = fB * inv;
         uint16_t *dst = a.out + (((size_t)r * a.n_max + (row_live ? node : 0)) * a.Hq +
                                  (size_t)g * a.G + hh) * 128 + col0;
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
-          float o[32];
-          tmem_ld32(lane_base + col0 + 32u * cc, o);
+          float oa[32], ob[32];
+          tmem_ld32(lane_base + col0 + 32u * cc, oa);
+          tmem_ld32(lane_base + kColOB + col0 + 32u * cc, ob);
           if (row_live) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               uint4 pkt;
-              pkt.x = pack_bf16(o[8 * q + 0] * inv, o[8 * q + 1] * inv);
-              pkt.y = pack_bf16(o[8 * q + 2] * inv, o[8 * q + 3] * inv);
-              pkt.z = pack_bf16(o[8 * q + 4] * inv, o[8 * q + 5] * inv);
-              pkt.w = pack_bf16(o[8 * q + 6] * inv, o[8 * q + 7] * inv);
+              pkt.x = pack_bf16(oa[8 * q + 0] * gA + ob[8 * q + 0] * gB, oa[8 * q + 1] * gA + ob[8 * q + 1] * gB);
+              pkt.y = pack_bf16(oa[8 * q + 2] * gA + ob[8 * q + 2] * gB, oa[8 * q + 3] * gA + ob[8 * q + 3] * gB);
+              pkt.z = pack_bf16(oa[8 * q + 4] * gA + ob[8 * q + 4] * gB, oa[8 * q + 5] * gA + ob[8 * q + 5] * gB);
+              pkt.w = pack_bf16(oa[8 * q + 6] * gA + ob[8 * q + 6] * gB, oa[8 * q + 7] * gA + ob[8 * q + 7] * gB);
               *reinterpret_cast<uint4 *>(dst + 32 * cc + 8 * q) = pkt;
             }
           }
