@@ -130,3 +130,26 @@ def test_attention_kv_overflow_flag(cuda_lib):
     q, k, v = _attn_inputs(B, n_max, Hq, Hkv, ctx, 9)
     _, st = _run(q, k, v, [ctx + 5], tr.n_nodes, tr.anc_mask)   # ctx + n > L_cap
     assert st[0] & bastion.STATUS_KV_OVERFLOW
+
+
+def test_attention_serving_size_sampled_rows(cuda_lib):
+    """The serving step's attention shape: 64 requests, 256-node trees, 32/8
+    heads, d=128, a 16,384-token context; sampled rows against the oracle.
+    The trees come from the oracle (a small-vocabulary drafter, flat cost)."""
+    B, n_max, Hq, Hkv, ctx = 64, 256, 32, 8, 16384
+    w = synth.Workload(94, "trees", B=B, b=16, V=1024, K=64, n_max=n_max, dtype="bf16", l_ar_ms=15.0,
+                       cost="flat", drafter="spike-geometric", p_agree="uniform", seed=777)
+    x = synth.drafter_logits(w)
+    tk = oracle.topk_marginals(x, w.K)
+    cost = np.full((1, n_max + 1), 6.0, np.float32)
+    tr = oracle.build_tree(tk.logit, tk.tok, tk.lse, n_max, np.zeros(B, np.int32),
+                           np.full(B, ctx, np.int32), cost, np.full(B, 15.0, np.float32))
+    assert np.all(tr.n_nodes == n_max)
+    q, k, v = _attn_inputs(B, n_max, Hq, Hkv, ctx, 31)
+    out, st = _run(q, k, v, np.full(B, ctx, np.int32), tr.n_nodes, tr.anc_mask)
+    assert np.all(st == 0)
+    rng = np.random.default_rng(5)
+    sel = [(int(r), int(i), int(h)) for r, i, h in zip(rng.integers(0, B, 160),
+                                                       rng.integers(0, n_max, 160), rng.integers(0, Hq, 160))]
+    sel += [(0, 0, h) for h in range(0, 32, 4)] + [(B - 1, n_max - 1, h) for h in range(0, 32, 4)]
+    _check_rows(out, q, k, v, np.full(B, ctx, np.int32), tr, sel)
