@@ -213,7 +213,7 @@ def run_ours(args, ws, rank, local):
         assert int(step.status.abs().sum()) == 0, "device status bits set"
         return None
 
-    graphs = [step.capture(xs[i], ts[i]) for i in range(2)]
+    graphs = [step.capture(xs[i], ts[i], chunks=args.chunks) for i in range(2)]
     stream = torch.cuda.current_stream()
 
     # warm-up (W steps, then, for long runs, ~1 s more so the clocks settle)
@@ -586,6 +586,8 @@ def main():
     ap.add_argument("--profile-kernel", choices=["topk", "tree", "verify", "step", "attn"],
                     help="launch one kernel (or the step) --launches times and exit, for ncu")
     ap.add_argument("--launches", type=int, default=3)
+    ap.add_argument("--chunks", type=int, default=1,
+                    help="request chunks of the step on forked streams inside the graph")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 

@@ -310,15 +310,65 @@ class TreeStep:
         self.draft(drafter_logits, stream)
         self.verify(target_logits, stream)
 
-    def capture(self, drafter_logits, target_logits):
+    def run_chunked(self, drafter_logits, target_logits, chunks):
+        """The same step with the batch split into request chunks on their own
+        streams (forked from and joined to the current stream).  A chunk's
+        top-K starts after the previous chunk's top-K, so one chunk's tree build
+        (a serial chain per request) overlaps the other chunks' sweeps.
+        Requests are independent, so the results equal run()'s."""
+        B = self.B
+        chunks = max(1, min(chunks, B))
+        bounds = [B * c // chunks for c in range(chunks + 1)]
+        if getattr(self, "_chunk_state", None) is None or len(self._chunk_state) != chunks:
+            self._chunk_state = []
+            for c in range(chunks):
+                nb = bounds[c + 1] - bounds[c]
+                self._chunk_state.append((torch.cuda.Stream(device=self.device),
+                                          workspace(bastion_verify_greedy_workspace_bytes(nb, self.n_max, self.V),
+                                                    self.device)))
+        main = torch.cuda.current_stream(self.device)
+        t, tr, v = self.topk, self.tree, self.ver
+        per_req_cost = self.cost_ms.dim() == 2 and self.cost_ms.shape[0] == B and B > 1
+        prev = None
+        for c in range(chunks):
+            c0, c1 = bounds[c], bounds[c + 1]
+            st, ws_v = self._chunk_state[c]
+            st.wait_stream(main)
+            if prev is not None:
+                st.wait_event(prev)
+            with torch.cuda.stream(st):
+                bastion_topk_marginals(drafter_logits[c0:c1], self.K, t.logq[c0:c1], t.logit[c0:c1],
+                                       t.tok[c0:c1], t.lse[c0:c1], self.ws_topk, self.status[c0:c1], st)
+                prev = torch.cuda.Event()
+                prev.record(st)
+                cost = self.cost_ms[c0:c1] if per_req_cost else self.cost_ms
+                bastion_build_tree(t.logit[c0:c1], t.tok[c0:c1], t.lse[c0:c1], self.n_max,
+                                   self.root_token[c0:c1], self.ctx_len[c0:c1], cost, self.l_ar[c0:c1],
+                                   tr.n_nodes[c0:c1], tr.parent[c0:c1], tr.depth[c0:c1], tr.pos_id[c0:c1],
+                                   tr.token[c0:c1], tr.rank[c0:c1], tr.log_rho[c0:c1], tr.a_hat[c0:c1],
+                                   tr.speedup[c0:c1], tr.anc_mask[c0:c1], self.status[c0:c1], st)
+                bastion_verify_greedy(target_logits[c0:c1], self.b, tr.n_nodes[c0:c1], tr.parent[c0:c1],
+                                      tr.token[c0:c1], v.argmax[c0:c1], v.accept_len[c0:c1],
+                                      v.accept_nodes[c0:c1], v.out_tokens[c0:c1], ws_v,
+                                      self.status[c0:c1], st)
+        for c in range(chunks):
+            main.wait_stream(self._chunk_state[c][0])
+
+    def capture(self, drafter_logits, target_logits, chunks=1):
+        """Records one step in a CUDA graph (chunks > 1: run_chunked)."""
+        def step():
+            if chunks > 1:
+                self.run_chunked(drafter_logits, target_logits, chunks)
+            else:
+                self.run(drafter_logits, target_logits)
         s = torch.cuda.Stream(device=self.device)
         s.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(s):
-            self.run(drafter_logits, target_logits, s)  # warm (sets kernel attributes)
+            step()  # warm (sets kernel attributes, creates the chunk streams)
         torch.cuda.current_stream().wait_stream(s)
         torch.cuda.synchronize(self.device)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            self.run(drafter_logits, target_logits)
+            step()
         self.graph = g
         return g

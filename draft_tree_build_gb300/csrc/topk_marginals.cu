@@ -33,6 +33,9 @@
 // of their own.
 #include <cuda_bf16.h>
 
+#include <cstdlib>
+#include <cstring>
+
 #include "common.cuh"
 
 namespace bastion {
@@ -48,6 +51,7 @@ constexpr double kLn2 = 0.6931471805599453;       // ln 2
 struct TopkArgs {
   const unsigned char *logits;
   int rows, b, V, K, CS, SL, seg, tab_bytes, body_bytes;
+  int ring_off;  // stream path: the ring's offset in shared memory
   int64_t ld;  // elements
   float *topk_logq, *topk_logit;
   int32_t *topk_tok;
@@ -643,14 +647,313 @@ __global__ void __launch_bounds__(kT) topk_exact_kernel(TopkArgs a) {
   write_logq(a, row, list, n, rk, sc.lse);
 }
 
+
+// --------------------------------------------------------------------------- stream path
+// Many rows (at least two per SM): one CTA per row, all resident at once.  The
+// row streams through a ring of kRing shared-memory stages filled by bulk
+// copies; the warp that frees a stage last refills it.  Per stage a thread
+// reads its kSV vectors into registers, frees the stage, and then
+//  * keeps the stage's max (a 16-bit order-key prefix) in shared memory;
+//  * adds 2^(l log2(e) - c) over its elements, where c is an integer kept at
+//    floor(m log2(e)) of its running max m: when m grows, the running sum is
+//    rescaled by the exact power of two 2^(c_old - c_new), so every exponent
+//    stays below ~1 and the sum is exact up to the terms' own rounding.
+// At the end the threads' sums are scaled to the CTA's largest c (exact
+// powers of two again) and summed in two-float arithmetic: lse = c ln 2 +
+// log(sum), corrected for log2(e) having been rounded to float.  T, the
+// K-th largest thread max (prefix), leaves at least K elements >= T (each of
+// the K largest thread maxima is one).  The stages whose max reaches T are
+// read again from global memory, a thread's loads issued together (a load
+// takes microseconds while the other rows stream), and their elements >= T
+// form the row's list, ranked by counting.  A list longer than the spent
+// ring holds (long runs of equal values) hands the row to the exact
+// selection over global memory.
+constexpr int kSV = 4;                         // vectors per thread per stage
+constexpr int kRing = 2;                       // stages in flight
+constexpr int kStageBytes = kT * kSV * 16;     // 16 KB
+constexpr float kCNone = -1.0e30f;             // c before the first finite element
+
+// 2^d for an integer-valued d <= 0 (0 below the normal range).
+__device__ __forceinline__ float pow2_int(float d) {
+  return d < -126.f ? 0.f : __int_as_float(((int)d + 127) << 23);
+}
+
+// The K-th largest of the kT 16-bit keys at keys (16-byte aligned), bit by
+// bit: the largest p with #{keys >= p} >= K.  Every lane of the calling warp
+// gets it.
+__device__ __forceinline__ uint32_t kth_largest_key16(const uint16_t *keys, uint32_t K, int lane) {
+  const uint4 kw = ld_shared_v4(keys + lane * 8);
+  const uint32_t k8[8] = {kw.x & 0xffffu, kw.x >> 16, kw.y & 0xffffu, kw.y >> 16,
+                          kw.z & 0xffffu, kw.z >> 16, kw.w & 0xffffu, kw.w >> 16};
+  uint32_t p = 0;
+#pragma unroll 1
+  for (int bit = 15; bit >= 0; --bit) {
+    const uint32_t cand = p | (1u << bit);
+    uint32_t cnt = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) cnt += k8[q] >= cand ? 1u : 0u;
+    if (__reduce_add_sync(kFull, cnt) >= K) p = cand;
+  }
+  return p;
+}
+
+// The smallest float whose order-key prefix is p (-inf for the prefix of -inf).
+__device__ __forceinline__ float prefix_floor(uint32_t p) {
+  const float T = unord_f32(p << 16);
+  return T == T ? T : -INFINITY;
+}
+
+// Elements >= T of the vectors tid + u kT (u < kSV, below lim) of stage q,
+// appended to the list (count n, capacity cap).
+template <int ES>
+__device__ __forceinline__ void append_stage(const uint4 (&x)[kSV], int q, int lim, int tid, int nh,
+                                             float T, uint64_t *list, uint32_t *n, int cap) {
+  constexpr int NE = 16 / ES;
+#pragma unroll
+  for (int u = 0; u < kSV; ++u) {
+    const int v = tid + u * kT;
+    if (v >= lim) continue;
+    float f[NE];
+    unpack<ES>(x[u], f);
+    const uint32_t tok0 = (uint32_t)(nh + (q * kStageBytes + v * 16) / ES);
+#pragma unroll
+    for (int i = 0; i < NE; ++i)
+      if (f[i] >= T) {
+        const uint32_t j = atomicAdd(n, 1u);
+        if (j < (uint32_t)cap) list[j] = make_key(f[i], tok0 + (uint32_t)i);
+      }
+  }
+}
+
+template <int ES>
+__global__ void __launch_bounds__(kT, 4) topk_stream_kernel(TopkArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem);            // [kRing] stage landed
+  uint32_t *freed = reinterpret_cast<uint32_t *>(smem + 64);      // [kRing] warp releases
+  Scratch &sc = *reinterpret_cast<Scratch *>(smem + 128);
+  uint16_t *tkey = reinterpret_cast<uint16_t *>(smem + 128 + kScratchBytes);  // [kT] thread maxima
+  uint16_t *smax = tkey + kT;                                                   // [nst][kT]
+  unsigned char *ring = smem + a.ring_off;  // [kRing][kStageBytes]; later the row list
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int row = blockIdx.x;
+  const int req = row / a.b;
+  const Slice s = slice_at<ES>(a, row, 0);
+  const int nst = (s.body + kStageBytes - 1) / kStageBytes;
+  const unsigned char *gbody = reinterpret_cast<const unsigned char *>(s.ga0);
+
+  if (tid == 0) {
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(&full[i], 1);
+      freed[i] = 0u;
+    }
+    fence_mbar_init();
+    sc.n_loc = 0u;
+  }
+  griddep_wait();
+  griddep_launch_dependents();
+  __syncthreads();
+  if (tid == 0)
+    for (int st = 0; st < nst && st < kRing; ++st) {
+      const uint32_t bytes = (uint32_t)min(kStageBytes, s.body - st * kStageBytes);
+      mbar_arrive_expect_tx(&full[st], bytes);
+      bulk_g2s(ring + st * kStageBytes, gbody + (size_t)st * kStageBytes, bytes, &full[st]);
+    }
+  // the unaligned head and tail of the row, one element per thread
+  const int nscal = s.nh + (s.n - s.t0);
+  const bool has_x = tid < nscal;
+  float xs = -INFINITY;
+  uint32_t xtok = 0;
+  if (has_x) {
+    const int e = tid < s.nh ? tid : s.t0 + (tid - s.nh);
+    xs = load_elem<ES>(s.g0 + (size_t)e * ES);
+    xtok = (uint32_t)e;
+  }
+  float m = xs;
+  float c = (xs > -INFINITY && xs < INFINITY) ? floorf(xs * kL2e) : kCNone;
+  float hi = has_x ? ex2(fmaf(xs, kL2e, -c)) : 0.f, lo = 0.f;
+
+  bool ok = true;
+  for (int st = 0; st < nst; ++st) {
+    const int slot = st % kRing;
+    // after a wait that ran out, the thread goes on without data and waits
+    // no more (every thread still reaches each barrier below)
+    ok = ok && mbar_wait_bounded(&full[slot], (uint32_t)(st / kRing) & 1u);
+    const unsigned char *buf = ring + slot * kStageBytes;
+    const int lim = ok ? min(kStageBytes, s.body - st * kStageBytes) / 16 : 0;
+    uint4 x[kSV];
+#pragma unroll
+    for (int u = 0; u < kSV; ++u) {
+      const int v = tid + u * kT;
+      x[u] = v < lim ? ld_shared_v4(buf + v * 16)
+                     : (ES == 2 ? make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u)
+                                : make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u));
+    }
+    // the stage is free once every warp holds its vectors; the last warp
+    // to let go refills it with stage st + kRing
+    __syncwarp();
+    if (lane == 0 && ok) {
+      __threadfence_block();
+      // the count only grows: every eighth arrival is a stage's last
+      if (((atomicAdd(&freed[slot], 1u) + 1u) & (kT / 32 - 1)) == 0u) {
+        __threadfence_block();
+        const int nx = st + kRing;
+        if (nx < nst) {
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          const uint32_t bytes = (uint32_t)min(kStageBytes, s.body - nx * kStageBytes);
+          mbar_arrive_expect_tx(&full[slot], bytes);
+          bulk_g2s(ring + slot * kStageBytes, gbody + (size_t)nx * kStageBytes, bytes, &full[slot]);
+        }
+      }
+    }
+    float smx = vmax<ES>(x[0]);
+#pragma unroll
+    for (int u = 1; u < kSV; ++u) smx = fmaxf(smx, vmax<ES>(x[u]));
+    smax[st * kT + tid] = (uint16_t)(ord_f32(smx) >> 16);
+    m = fmaxf(m, smx);
+    const float cn = floorf(m * kL2e);
+    if (cn > c) {  // exact rescale of the running sum by 2^(c - cn)
+      const float f = pow2_int(c - cn);
+      hi *= f;
+      lo *= f;
+      c = cn;
+    }
+    float ssum = 0.f;
+#pragma unroll
+    for (int u = 0; u < kSV; ++u) ssum += vexp_sum<ES>(x[u], -c);
+    const float2 t = two_sum(hi, ssum);
+    hi = t.x;
+    lo += t.y;
+  }
+  if (!ok) {
+    atomicOr(&a.status[req], BASTION_STATUS_TIMEOUT);
+    // let the copies that may still be in flight into this CTA end
+    if (tid == 0)
+      for (int j = 0; j < kRing; ++j) {
+        const int q = nst - kRing + j;
+        if (q >= 0) mbar_wait_bounded(&full[q % kRing], (uint32_t)(q / kRing) & 1u);
+      }
+  }
+
+  // ---- the row's max, c and sum; T
+  tkey[tid] = (uint16_t)(ord_f32(m) >> 16);
+  {
+    const float wm = warp_max_f(m), wc = warp_max_f(c);
+    if (lane == 0) {
+      sc.red_f[warp] = wm;
+      sc.red_u[warp] = __float_as_uint(wc);
+    }
+  }
+  __syncthreads();
+  float M = -INFINITY, cM = kCNone;
+#pragma unroll
+  for (int q = 0; q < kT / 32; ++q) {
+    M = fmaxf(M, sc.red_f[q]);
+    cM = fmaxf(cM, __uint_as_float(sc.red_u[q]));
+  }
+  {
+    const float f = c > kCNone ? pow2_int(c - cM) : 0.f;
+    const float2 ws = ff_warp_sum(make_float2(hi * f, lo * f));
+    if (lane == 0) sc.red_s[warp] = ws;
+  }
+  const uint32_t T16 = kth_largest_key16(tkey, (uint32_t)a.K, lane);
+  const float T = prefix_floor(T16);
+
+  // ---- the row list: elements >= T of the stages whose max reaches T, read
+  // again two stages at a time
+  uint64_t *list = reinterpret_cast<uint64_t *>(ring);  // the ring is spent
+  const int cap = (kRing * kStageBytes - 16) / 12;      // keys, then their ranks
+  if (has_x && xs >= T) {
+    const uint32_t i = atomicAdd(&sc.n_loc, 1u);
+    if (i < (uint32_t)cap) list[i] = make_key(xs, xtok);
+  }
+  uint64_t hm = 0;  // stages (nst <= 64) whose max reaches T
+  for (int q = 0; q < nst; ++q) hm |= (uint64_t)((uint32_t)smax[q * kT + tid] >= T16) << q;
+  while (hm) {
+    const int q0 = __ffsll((long long)hm) - 1;
+    hm &= hm - 1;
+    const int q1 = hm ? __ffsll((long long)hm) - 1 : -1;
+    if (q1 >= 0) hm &= hm - 1;
+    const int lim0 = min(kStageBytes, s.body - q0 * kStageBytes) / 16;
+    const int lim1 = q1 >= 0 ? min(kStageBytes, s.body - q1 * kStageBytes) / 16 : 0;
+    uint4 x0[kSV], x1[kSV];
+#pragma unroll
+    for (int u = 0; u < kSV; ++u) {
+      const int v = tid + u * kT;
+      if (v < lim0) x0[u] = ld_stream_v4(gbody + (size_t)q0 * kStageBytes + (size_t)v * 16);
+      if (v < lim1) x1[u] = ld_stream_v4(gbody + (size_t)q1 * kStageBytes + (size_t)v * 16);
+    }
+    append_stage<ES>(x0, q0, lim0, tid, s.nh, T, list, &sc.n_loc, cap);
+    if (q1 >= 0) append_stage<ES>(x1, q1, lim1, tid, s.nh, T, list, &sc.n_loc, cap);
+  }
+  __syncthreads();
+  int n = (int)sc.n_loc;
+  if (tid == kT - 32) {
+    float2 acc = make_float2(0.f, 0.f);
+    for (int q = 0; q < kT / 32; ++q) acc = ff_add(acc, sc.red_s[q]);
+    int e2 = 0;
+    const float mant = frexpf(acc.x, &e2);
+    const double corr = (acc.x > 0.f && acc.x < INFINITY) ? (double)(acc.y / acc.x) : 0.0;
+    // acc = sum_i 2^(l_i kL2e - cM) with log2(e) = kL2e + kL2eLo; the terms
+    // that matter have l_i within a few units of M
+    const double lse = (double)cM * kLn2 + ((double)e2 * kLn2 + (double)logf(mant) + corr) +
+                       (double)M * (double)kL2eLo * kLn2;
+    int stt = 0;
+    const double sd = (double)acc.x + (double)acc.y;
+    if (M == INFINITY || !(sd == sd) || sd == INFINITY || !(cM < INFINITY)) stt |= BASTION_STATUS_NONFINITE;
+    if (M == -INFINITY) stt |= BASTION_STATUS_EMPTY_ROW;
+    if (stt) atomicOr(&a.status[req], stt);
+    a.lse[row] = lse;
+    sc.lse = lse;
+  }
+  const int want = min(a.K, a.V);
+  if (n < want || n > cap) {  // too few keys (non-finite rows) or too many: exact selection
+    __syncthreads();
+    const unsigned char *g = a.logits + (size_t)row * (size_t)a.ld * ES;
+    n = row_topk_exact<ES>(g, a.V, a.K, list, sc);
+  }
+  if (tid == 0 && (n & 1)) list[n] = 0ull;
+  __syncthreads();
+  int *rk = reinterpret_cast<int *>(list + cap + 2);
+  rank_keys(a, row, list, n, rk);
+  __syncthreads();
+  write_logq(a, row, list, n, rk, sc.lse);
+}
+
 struct TopkPlan {
-  int CS, SL, NV, seg, tab_bytes, body_bytes;
+  int CS, SL, NV, seg, tab_bytes, body_bytes, ring_off;
   size_t smem;
-  bool exact;
+  bool exact, stream;
 };
 
-TopkPlan plan_topk(int V, int K, int es) {
+// Which kernel takes the rows: BASTION_TOPK_PATH=stream|cluster forces one
+// (where it applies), otherwise the stream kernel once there are two rows
+// per SM and four of its CTAs fit on an SM.
+TopkPlan plan_topk(int V, int K, int es, int rows, int sms) {
   TopkPlan p;
+  p.stream = false;
+  p.ring_off = 0;
+  {
+    const int nst = (int)(((size_t)V * es + kStageBytes - 1) / kStageBytes);
+    const size_t off = ((size_t)128 + kScratchBytes + (size_t)kT * 2 + (size_t)nst * kT * 2 + 127) / 128 * 128;
+    const size_t smem = off + (size_t)kRing * kStageBytes;
+    const char *force = getenv("BASTION_TOPK_PATH");
+    const bool fs = force && strcmp(force, "stream") == 0, fc = force && strcmp(force, "cluster") == 0;
+    const bool fits = K <= kT && nst <= 64 && smem <= 227 * 1024;
+    if (fits && !fc && (fs || (rows >= 2 * sms && smem <= 55 * 1024))) {
+      p.stream = true;
+      p.exact = false;
+      p.CS = 1;
+      p.SL = V;
+      p.NV = 0;
+      p.seg = 0;
+      p.tab_bytes = 0;
+      p.body_bytes = 0;
+      p.ring_off = (int)off;
+      p.smem = smem;
+      return p;
+    }
+  }
 
   p.exact = K > kT;  // the row threshold uses one key per thread of a CTA at least
   const int max_vec = kT * 16;  // 16 vectors per thread at most
@@ -714,7 +1017,10 @@ int launch_topk(const void *logits, int dtype, int B, int b, int V, int64_t ld, 
                 float *topk_logq, float *topk_logit, int32_t *topk_tok, double *lse,
                 void *, int32_t *status, cudaStream_t stream) {
   const int es = dtype == BASTION_F32 ? 4 : 2;
-  const TopkPlan p = plan_topk(V, K, es);
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const TopkPlan p = plan_topk(V, K, es, B * b, sms);
   TopkArgs a;
   a.logits = static_cast<const unsigned char *>(logits);
   a.rows = B * b;
@@ -726,6 +1032,7 @@ int launch_topk(const void *logits, int dtype, int B, int b, int V, int64_t ld, 
   a.seg = p.seg;
   a.tab_bytes = p.tab_bytes;
   a.body_bytes = p.body_bytes;
+  a.ring_off = p.ring_off;
   a.ld = ld;
   a.topk_logq = topk_logq;
   a.topk_logit = topk_logit;
@@ -733,7 +1040,11 @@ int launch_topk(const void *logits, int dtype, int B, int b, int V, int64_t ld, 
   a.lse = lse;
   a.status = status;
   cudaError_t e;
-  if (p.exact) {
+  if (p.stream) {
+    auto kern = es == 4 ? topk_stream_kernel<4> : topk_stream_kernel<2>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
+    if (e == cudaSuccess) e = launch_pdl(kern, dim3((unsigned)a.rows), dim3(kT), p.smem, stream, a);
+  } else if (p.exact) {
     auto kern = es == 4 ? topk_exact_kernel<4> : topk_exact_kernel<2>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
     if (e == cudaSuccess) e = launch_pdl(kern, dim3((unsigned)a.rows), dim3(kT), p.smem, stream, a);

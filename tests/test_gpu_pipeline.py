@@ -13,11 +13,13 @@ from gpuhelp import compare_topk, compare_verify, compare_tree, dev, host, oracl
 pytestmark = pytest.mark.gpu
 
 
-def _step(w, graph=False):
+def _step(w, graph=False, chunks=1, cost_per_request=False):
     from draft_tree_build_gb300 import bastion
     x = synth.drafter_logits(w)
     tk = oracle.topk_marginals(x, w.K)
     roots, ctx, cost, lar = workload_inputs(w)
+    if cost_per_request:  # request r's costs scaled by 1 + r/4: trees differ across requests
+        cost = (cost * (1.0 + np.arange(w.B, dtype=np.float32)[:, None] / 4)).astype(np.float32)
     step = bastion.TreeStep(w.B, w.b, w.V, w.K, w.n_max, dev(), torch.from_numpy(roots),
                             torch.from_numpy(ctx), torch.from_numpy(cost), torch.from_numpy(lar))
     xd = to_dev(x)
@@ -26,9 +28,11 @@ def _step(w, graph=False):
     tgt, _ = synth.target_logits(w, ref_tree.n_nodes, ref_tree.depth, tk.tok)
     td = to_dev(tgt)
     if graph:
-        g = step.capture(xd, td)
+        g = step.capture(xd, td, chunks=chunks)
         step.status.zero_()
         g.replay()
+    elif chunks > 1:
+        step.run_chunked(xd, td, chunks)
     else:
         step.run(xd, td)
     torch.cuda.synchronize()
@@ -57,3 +61,17 @@ def test_pipeline_serving_llama_vocab(cuda_lib):
     """B=64, b=16, V=128256, K=64, N_max=256 (every tree fills the budget)."""
     step, vf = _step(synth.workload(5))
     assert np.all(host(step.tree.n_nodes) == 256)
+
+
+@pytest.mark.parametrize("chunks", [2, 3, 4])
+def test_pipeline_chunked_graph(cuda_lib, chunks):
+    """The batch split into request chunks on forked streams inside the graph
+    (three chunks leave unequal slices of 32 requests)."""
+    _step(synth.workload(3), graph=True, chunks=chunks)
+
+
+@pytest.mark.parametrize("cost_per_request", [False, True])
+def test_pipeline_chunked_eager(cuda_lib, cost_per_request):
+    """Chunks on streams without a graph; B=5 in four chunks (1, 1, 1, 2
+    requests), with a shared and a per-request cost table."""
+    _step(synth.workload(3, B=5), chunks=4, cost_per_request=cost_per_request)

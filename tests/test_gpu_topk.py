@@ -1,7 +1,7 @@
 """GPU parity: softmax + top-K marginals (C ABI) against the CPU oracle.
 
 Bit-exact: kept tokens and logits.  lse and log q: within 2e-6 absolute (the
-kernel sums exp in fp32 per thread, Kahan-compensated, and merges in fp64).
+kernels sum exp in fp32 per thread, compensated, and take the log in fp64).
 """
 import numpy as np
 import pytest
@@ -11,6 +11,14 @@ import synth
 from gpuhelp import compare_topk, gpu_topk, host, to_dev
 
 pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True, params=["stream", "cluster"])
+def topk_path(request, monkeypatch):
+    """Every case runs on both kernels: one CTA per row streaming the row
+    (the default from two rows per SM) and a cluster of CTAs per row."""
+    monkeypatch.setenv("BASTION_TOPK_PATH", request.param)
+    return request.param
 
 
 @pytest.mark.parametrize("cid", [1, 2, 3])
