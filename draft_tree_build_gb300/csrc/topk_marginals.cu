@@ -51,7 +51,7 @@ constexpr double kLn2 = 0.6931471805599453;       // ln 2
 struct TopkArgs {
   const unsigned char *logits;
   int rows, b, V, K, CS, SL, seg, tab_bytes, body_bytes;
-  int ring_off;  // stream path: the ring's offset in shared memory
+  int nst;  // stream path: stages of the widest row (its shared-memory layout)
   int64_t ld;  // elements
   float *topk_logq, *topk_logit;
   int32_t *topk_tok;
@@ -75,6 +75,7 @@ struct Scratch {
   int off[kMaxCS + 1];    // leader: where each CTA's keys go in the row list
   uint32_t n_loc;         // keys in this CTA's list (may pass seg: overflow)
   uint32_t n_exact;
+  uint32_t n_hit;         // stream path: stages to read again
   uint32_t digit_info[2];
   int warp_tot[8];
   double lse;
@@ -281,25 +282,31 @@ __device__ int row_topk_exact(const unsigned char *g, int V, int K, uint64_t *ds
 
 // Ranks n unique keys of list by counting, writes the top K's logits and
 // tokens and keeps each key's rank in rk (all threads call it; list[n] must be
-// readable and zero when n is odd).
+// readable and zero when n is odd).  Four lanes count for one key, each over
+// a quarter of the list.
 __device__ __forceinline__ void rank_keys(const TopkArgs &a, int row, const uint64_t *list, int n,
                                           int *rk) {
-  const int K = a.K;
+  const int K = a.K, sub = threadIdx.x & 3;
   const ulonglong2 *l2 = reinterpret_cast<const ulonglong2 *>(list);
   const int n2 = (n + 1) >> 1;
-  for (int i = threadIdx.x; i < n; i += kT) {
-    const uint64_t key = list[i];
+  const int end = (n + kT / 4 - 1) / (kT / 4) * (kT / 4);  // the same trip count for a warp's lanes
+  for (int i = threadIdx.x >> 2; i < end; i += kT / 4) {
+    const uint64_t key = i < n ? list[i] : ~0ull;
     int r = 0;
 #pragma unroll 4
-    for (int j = 0; j < n2; ++j) {
+    for (int j = sub; j < n2; j += 4) {
       const ulonglong2 p = l2[j];
       r += (p.x > key) + (p.y > key);
     }
-    rk[i] = r;
-    if (r < K) {
-      const size_t o = (size_t)row * K + r;
-      a.topk_logit[o] = key_value(key);
-      a.topk_tok[o] = (int32_t)key_token(key);
+    r += __shfl_xor_sync(kFull, r, 1);
+    r += __shfl_xor_sync(kFull, r, 2);
+    if (sub == 0 && i < n) {
+      rk[i] = r;
+      if (r < K) {
+        const size_t o = (size_t)row * K + r;
+        a.topk_logit[o] = key_value(key);
+        a.topk_tok[o] = (int32_t)key_token(key);
+      }
     }
   }
 }
@@ -662,37 +669,112 @@ __global__ void __launch_bounds__(kT) topk_exact_kernel(TopkArgs a) {
 // powers of two again) and summed in two-float arithmetic: lse = c ln 2 +
 // log(sum), corrected for log2(e) having been rounded to float.  T, the
 // K-th largest thread max (prefix), leaves at least K elements >= T (each of
-// the K largest thread maxima is one).  The stages whose max reaches T are
-// read again from global memory, a thread's loads issued together (a load
-// takes microseconds while the other rows stream), and their elements >= T
-// form the row's list, ranked by counting.  A list longer than the spent
-// ring holds (long runs of equal values) hands the row to the exact
-// selection over global memory.
+// the K largest thread maxima is one).  The (stage, thread) pairs whose max
+// reaches T are listed and read again from global memory, one pair per
+// thread, so that a single round of loads (microseconds while the other rows
+// stream) covers them all; their elements >= T form the row's list, ranked by
+// counting.  A list longer than the spent ring holds (long runs of equal
+// values) hands the row to the exact selection over global memory.
 constexpr int kSV = 4;                         // vectors per thread per stage
 constexpr int kRing = 2;                       // stages in flight
 constexpr int kStageBytes = kT * kSV * 16;     // 16 KB
 constexpr float kCNone = -1.0e30f;             // c before the first finite element
+constexpr int kListCap = 2048;                 // the row list's keys (the spent ring)
+constexpr int kHitCap = 1024;                  // stages to read again, after the list
+static_assert((kListCap + 2) * 8 + kListCap * 4 + kHitCap * 4 <= kRing * kStageBytes, "ring reuse");
+
+// Max over a thread's kSV vectors of a stage: one chain of packed maxima.
+template <int ES>
+__device__ __forceinline__ float stage_max(const uint4 (&x)[kSV]) {
+  if constexpr (ES == 2) {
+    uint32_t m = x[0].x;
+#pragma unroll
+    for (int u = 0; u < kSV; ++u) {
+      if (u) asm("max.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(x[u].x));
+      asm("max.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(x[u].y));
+      asm("max.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(x[u].z));
+      asm("max.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(x[u].w));
+    }
+    return fmaxf(bf16lo(m), bf16hi(m));
+  } else {
+    float m = vmax<ES>(x[0]);
+#pragma unroll
+    for (int u = 1; u < kSV; ++u) m = fmaxf(m, vmax<ES>(x[u]));
+    return m;
+  }
+}
+
+// Sum of 2^(x log2(e) + nc) over a thread's kSV vectors of a stage: packed
+// FMAs and adds, four partial sums.
+template <int ES>
+__device__ __forceinline__ float stage_exp_sum(const uint4 (&x)[kSV], float nc) {
+  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+  for (int u = 0; u < kSV; ++u) {
+    float f[16 / ES];
+    unpack<ES>(x[u], f);
+#pragma unroll
+    for (int i = 0; i < 16 / ES; i += 4) {
+      float t0, t1, t2, t3;
+      asm("{\n .reg .b64 d, e, k, c;\n"
+          " mov.b64 d, {%4, %5};\n mov.b64 e, {%6, %7};\n mov.b64 k, {%9, %9};\n"
+          " mov.b64 c, {%8, %8};\n fma.rn.f32x2 d, d, k, c;\n fma.rn.f32x2 e, e, k, c;\n"
+          " mov.b64 {%0, %1}, d;\n mov.b64 {%2, %3}, e;\n}\n"
+          : "=f"(t0), "=f"(t1), "=f"(t2), "=f"(t3)
+          : "f"(f[i]), "f"(f[i + 1]), "f"(f[i + 2]), "f"(f[i + 3]), "f"(nc), "f"(kL2e));
+      const float e0 = ex2(t0), e1 = ex2(t1), e2 = ex2(t2), e3 = ex2(t3);
+      asm("{\n .reg .b64 a, b, p, q;\n mov.b64 a, {%0, %1};\n mov.b64 b, {%2, %3};\n"
+          " mov.b64 p, {%4, %5};\n mov.b64 q, {%6, %7};\n"
+          " add.rn.f32x2 a, a, p;\n add.rn.f32x2 b, b, q;\n"
+          " mov.b64 {%0, %1}, a;\n mov.b64 {%2, %3}, b;\n}\n"
+          : "+f"(s0), "+f"(s1), "+f"(s2), "+f"(s3)
+          : "f"(e0), "f"(e1), "f"(e2), "f"(e3));
+    }
+  }
+  return (s0 + s1) + (s2 + s3);
+}
+
 
 // 2^d for an integer-valued d <= 0 (0 below the normal range).
 __device__ __forceinline__ float pow2_int(float d) {
   return d < -126.f ? 0.f : __int_as_float(((int)d + 127) << 23);
 }
 
-// The K-th largest of the kT 16-bit keys at keys (16-byte aligned), bit by
-// bit: the largest p with #{keys >= p} >= K.  Every lane of the calling warp
-// gets it.
+// Shared-memory layout of the stream kernel for rows of nst stages.
+struct StreamLayout {
+  int tkey, smax, ring, bytes;
+};
+__host__ __device__ inline StreamLayout stream_layout(int nst) {
+  StreamLayout l;
+  l.tkey = 128 + kScratchBytes;
+  l.smax = l.tkey + kT * 2;
+  l.ring = (l.smax + nst * kT * 2 + 127) / 128 * 128;
+  l.bytes = l.ring + kRing * kStageBytes;
+  return l;
+}
+
+// The K-th largest of the kT 16-bit keys at keys (16-byte aligned), two bits
+// a round: the largest p with #{keys >= p} >= K.  Every lane of the calling
+// warp gets it.
 __device__ __forceinline__ uint32_t kth_largest_key16(const uint16_t *keys, uint32_t K, int lane) {
   const uint4 kw = ld_shared_v4(keys + lane * 8);
   const uint32_t k8[8] = {kw.x & 0xffffu, kw.x >> 16, kw.y & 0xffffu, kw.y >> 16,
                           kw.z & 0xffffu, kw.z >> 16, kw.w & 0xffffu, kw.w >> 16};
   uint32_t p = 0;
 #pragma unroll 1
-  for (int bit = 15; bit >= 0; --bit) {
-    const uint32_t cand = p | (1u << bit);
-    uint32_t cnt = 0;
+  for (int bit = 14; bit >= 0; bit -= 2) {
+    const uint32_t c1 = p | (1u << bit), c2 = p | (2u << bit), c3 = p | (3u << bit);
+    uint32_t n1 = 0, n2 = 0, n3 = 0;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) cnt += k8[q] >= cand ? 1u : 0u;
-    if (__reduce_add_sync(kFull, cnt) >= K) p = cand;
+    for (int q = 0; q < 8; ++q) {
+      n1 += k8[q] >= c1 ? 1u : 0u;
+      n2 += k8[q] >= c2 ? 1u : 0u;
+      n3 += k8[q] >= c3 ? 1u : 0u;
+    }
+    n1 = __reduce_add_sync(kFull, n1);
+    n2 = __reduce_add_sync(kFull, n2);
+    n3 = __reduce_add_sync(kFull, n3);
+    p = n3 >= K ? c3 : n2 >= K ? c2 : n1 >= K ? c1 : p;
   }
   return p;
 }
@@ -731,15 +813,15 @@ __global__ void __launch_bounds__(kT, 4) topk_stream_kernel(TopkArgs a) {
   uint64_t *full = reinterpret_cast<uint64_t *>(smem);            // [kRing] stage landed
   uint32_t *freed = reinterpret_cast<uint32_t *>(smem + 64);      // [kRing] warp releases
   Scratch &sc = *reinterpret_cast<Scratch *>(smem + 128);
-  uint16_t *tkey = reinterpret_cast<uint16_t *>(smem + 128 + kScratchBytes);  // [kT] thread maxima
-  uint16_t *smax = tkey + kT;                                                   // [nst][kT]
-  unsigned char *ring = smem + a.ring_off;  // [kRing][kStageBytes]; later the row list
-
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int row = blockIdx.x;
   const int req = row / a.b;
   const Slice s = slice_at<ES>(a, row, 0);
   const int nst = (s.body + kStageBytes - 1) / kStageBytes;
+  const StreamLayout L = stream_layout(a.nst);  // the row's stages, at most a.nst
+  uint16_t *tkey = reinterpret_cast<uint16_t *>(smem + L.tkey);    // [kT] thread maxima
+  uint16_t *smax = reinterpret_cast<uint16_t *>(smem + L.smax);    // [nst][kT] stage maxima
+  unsigned char *ring = smem + L.ring;  // [kRing][kStageBytes]; later the row list
   const unsigned char *gbody = reinterpret_cast<const unsigned char *>(s.ga0);
 
   if (tid == 0) {
@@ -749,6 +831,7 @@ __global__ void __launch_bounds__(kT, 4) topk_stream_kernel(TopkArgs a) {
     }
     fence_mbar_init();
     sc.n_loc = 0u;
+    sc.n_hit = 0u;
   }
   griddep_wait();
   griddep_launch_dependents();
@@ -806,9 +889,7 @@ __global__ void __launch_bounds__(kT, 4) topk_stream_kernel(TopkArgs a) {
         }
       }
     }
-    float smx = vmax<ES>(x[0]);
-#pragma unroll
-    for (int u = 1; u < kSV; ++u) smx = fmaxf(smx, vmax<ES>(x[u]));
+    const float smx = stage_max<ES>(x);
     smax[st * kT + tid] = (uint16_t)(ord_f32(smx) >> 16);
     m = fmaxf(m, smx);
     const float cn = floorf(m * kL2e);
@@ -818,9 +899,7 @@ __global__ void __launch_bounds__(kT, 4) topk_stream_kernel(TopkArgs a) {
       lo *= f;
       c = cn;
     }
-    float ssum = 0.f;
-#pragma unroll
-    for (int u = 0; u < kSV; ++u) ssum += vexp_sum<ES>(x[u], -c);
+    const float ssum = stage_exp_sum<ES>(x, -c);
     const float2 t = two_sum(hi, ssum);
     hi = t.x;
     lo += t.y;
@@ -859,33 +938,34 @@ __global__ void __launch_bounds__(kT, 4) topk_stream_kernel(TopkArgs a) {
   const uint32_t T16 = kth_largest_key16(tkey, (uint32_t)a.K, lane);
   const float T = prefix_floor(T16);
 
-  // ---- the row list: elements >= T of the stages whose max reaches T, read
-  // again two stages at a time
+  // ---- the row list: elements >= T of the stages whose max reaches T.  The
+  // (stage, thread) pairs of those stages go to a list first, so that one
+  // round of loads, a pair per thread, reads them all again.
   uint64_t *list = reinterpret_cast<uint64_t *>(ring);  // the ring is spent
-  const int cap = (kRing * kStageBytes - 16) / 12;      // keys, then their ranks
+  uint32_t *hits = reinterpret_cast<uint32_t *>(ring + kRing * kStageBytes - 4 * kHitCap);
   if (has_x && xs >= T) {
     const uint32_t i = atomicAdd(&sc.n_loc, 1u);
-    if (i < (uint32_t)cap) list[i] = make_key(xs, xtok);
+    if (i < (uint32_t)kListCap) list[i] = make_key(xs, xtok);
   }
-  uint64_t hm = 0;  // stages (nst <= 64) whose max reaches T
-  for (int q = 0; q < nst; ++q) hm |= (uint64_t)((uint32_t)smax[q * kT + tid] >= T16) << q;
-  while (hm) {
-    const int q0 = __ffsll((long long)hm) - 1;
-    hm &= hm - 1;
-    const int q1 = hm ? __ffsll((long long)hm) - 1 : -1;
-    if (q1 >= 0) hm &= hm - 1;
-    const int lim0 = min(kStageBytes, s.body - q0 * kStageBytes) / 16;
-    const int lim1 = q1 >= 0 ? min(kStageBytes, s.body - q1 * kStageBytes) / 16 : 0;
-    uint4 x0[kSV], x1[kSV];
-#pragma unroll
-    for (int u = 0; u < kSV; ++u) {
-      const int v = tid + u * kT;
-      if (v < lim0) x0[u] = ld_stream_v4(gbody + (size_t)q0 * kStageBytes + (size_t)v * 16);
-      if (v < lim1) x1[u] = ld_stream_v4(gbody + (size_t)q1 * kStageBytes + (size_t)v * 16);
+  for (int q = 0; q < nst; ++q)
+    if ((uint32_t)smax[q * kT + tid] >= T16) {
+      const uint32_t h = atomicAdd(&sc.n_hit, 1u);
+      if (h < (uint32_t)kHitCap) hits[h] = (uint32_t)(q * kT + tid);
     }
-    append_stage<ES>(x0, q0, lim0, tid, s.nh, T, list, &sc.n_loc, cap);
-    if (q1 >= 0) append_stage<ES>(x1, q1, lim1, tid, s.nh, T, list, &sc.n_loc, cap);
-  }
+  __syncthreads();
+  const int nhit = (int)min(sc.n_hit, (uint32_t)kHitCap + 1u);
+  if (nhit <= kHitCap)
+    for (int h = tid; h < nhit; h += kT) {
+      const int q = (int)(hits[h] / kT), t = (int)(hits[h] % kT);
+      const int lim = min(kStageBytes, s.body - q * kStageBytes) / 16;
+      uint4 x[kSV];
+#pragma unroll
+      for (int u = 0; u < kSV; ++u) {
+        const int v = t + u * kT;
+        if (v < lim) x[u] = ld_stream_v4(gbody + (size_t)q * kStageBytes + (size_t)v * 16);
+      }
+      append_stage<ES>(x, q, lim, t, s.nh, T, list, &sc.n_loc, kListCap);
+    }
   __syncthreads();
   int n = (int)sc.n_loc;
   if (tid == kT - 32) {
@@ -907,21 +987,21 @@ __global__ void __launch_bounds__(kT, 4) topk_stream_kernel(TopkArgs a) {
     sc.lse = lse;
   }
   const int want = min(a.K, a.V);
-  if (n < want || n > cap) {  // too few keys (non-finite rows) or too many: exact selection
+  if (n < want || n > kListCap || nhit > kHitCap) {  // too few keys (non-finite rows) or too many: exact selection
     __syncthreads();
     const unsigned char *g = a.logits + (size_t)row * (size_t)a.ld * ES;
     n = row_topk_exact<ES>(g, a.V, a.K, list, sc);
   }
   if (tid == 0 && (n & 1)) list[n] = 0ull;
   __syncthreads();
-  int *rk = reinterpret_cast<int *>(list + cap + 2);
+  int *rk = reinterpret_cast<int *>(list + kListCap + 2);
   rank_keys(a, row, list, n, rk);
   __syncthreads();
   write_logq(a, row, list, n, rk, sc.lse);
 }
 
 struct TopkPlan {
-  int CS, SL, NV, seg, tab_bytes, body_bytes, ring_off;
+  int CS, SL, NV, seg, tab_bytes, body_bytes, nst;
   size_t smem;
   bool exact, stream;
 };
@@ -932,15 +1012,14 @@ struct TopkPlan {
 TopkPlan plan_topk(int V, int K, int es, int rows, int sms) {
   TopkPlan p;
   p.stream = false;
-  p.ring_off = 0;
+  p.nst = 0;
   {
     const int nst = (int)(((size_t)V * es + kStageBytes - 1) / kStageBytes);
-    const size_t off = ((size_t)128 + kScratchBytes + (size_t)kT * 2 + (size_t)nst * kT * 2 + 127) / 128 * 128;
-    const size_t smem = off + (size_t)kRing * kStageBytes;
+    const size_t smem = nst <= 64 ? (size_t)stream_layout(nst).bytes : ~(size_t)0;
     const char *force = getenv("BASTION_TOPK_PATH");
     const bool fs = force && strcmp(force, "stream") == 0, fc = force && strcmp(force, "cluster") == 0;
     const bool fits = K <= kT && nst <= 64 && smem <= 227 * 1024;
-    if (fits && !fc && (fs || (rows >= 2 * sms && smem <= 55 * 1024))) {
+    if (fits && !fc && (fs || (rows >= 2 * sms && smem <= 56 * 1024 - 256))) {
       p.stream = true;
       p.exact = false;
       p.CS = 1;
@@ -949,7 +1028,7 @@ TopkPlan plan_topk(int V, int K, int es, int rows, int sms) {
       p.seg = 0;
       p.tab_bytes = 0;
       p.body_bytes = 0;
-      p.ring_off = (int)off;
+      p.nst = nst;
       p.smem = smem;
       return p;
     }
@@ -1032,7 +1111,7 @@ int launch_topk(const void *logits, int dtype, int B, int b, int V, int64_t ld, 
   a.seg = p.seg;
   a.tab_bytes = p.tab_bytes;
   a.body_bytes = p.body_bytes;
-  a.ring_off = p.ring_off;
+  a.nst = p.nst;
   a.ld = ld;
   a.topk_logq = topk_logq;
   a.topk_logit = topk_logit;
