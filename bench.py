@@ -325,8 +325,11 @@ def run_ours(args, ws, rank, local):
                    "parallelism": f"replicas x{ws}"},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": hbm, "unit": "GB/s",
                      "frac": ach / hbm, "peak_source": f"{peak_kind} copy bandwidth",
-                     "traffic": (profiled_traffic("topk_marginals_b32_v151936.md", "topk_marginals.cu")
-                                 if dom == "topk_marginals" and w.cid == 3 else None),
+                     "traffic": (profiled_traffic(*{"topk_marginals": ("topk_marginals_b32_v151936.md",
+                                                                       "topk_marginals.cu"),
+                                                    "verify_greedy": ("verify_greedy_b32_v151936.md",
+                                                                      "verify_greedy.cu")}[dom])
+                                 if w.cid == 3 else None),
                      "step_frac": bytes_step / (ms_step * 1e-3) / 1e9 / hbm,
                      "bytes_per_step": bytes_step},
         "kernels": kern,
