@@ -86,10 +86,16 @@ const char *bastion_status_string(int code);
  *            May be NULL.
  * topk_logit [B, b, K] float  the kept logits exactly as given (fp32 value).
  * topk_tok   [B, b, K] int32  token ids, rank order.
- * lse        [B, b] double    log sum_v exp(l_v).
+ * lse        [B, b] double    log sum_v exp(l_v), within ~2e-6 absolute
+ *                             (fp32 exponentials, compensated sums, fp64 log).
  * status     [B] int32        OR-ed BASTION_STATUS_* bits.
  * Limits: B >= 1, 1 <= b <= 32, 1 <= K <= min(V, 1024), V < 2^30.
  * Workspace: bastion_topk_marginals_workspace_bytes(B, b, V, K) bytes.
+ * One kernel launch.  From two rows per SM on, one CTA streams each row; with
+ * fewer rows a cluster of CTAs shares each row.  Tokens and logits do not
+ * depend on which kernel ran, lse only within its stated bound;
+ * BASTION_TOPK_PATH=stream|cluster in the environment forces one of them where
+ * it applies (for tests).
  */
 size_t bastion_topk_marginals_workspace_bytes(int B, int b, int V, int K);
 int bastion_topk_marginals(const void *logits, int dtype, int B, int b, int V, int64_t ld_row,
