@@ -330,6 +330,100 @@ int oracle_verify_greedy(const void* target, int dtype, int B, int n_max, int V,
 }
 
 // ---------------------------------------------------------------------------
+// Stochastic verification at temperature T > 0.  The pages evaluate greedy
+// decoding only ("Experimentele Resultaten"); for sampled decoding of a tree of
+// deterministic candidates the plainest lossless reading is taken: at every
+// node i the target's token y_i is a draw from softmax(l_i / T), by inverse
+// transform with the caller's uniform u[r][i] in [0, 1):
+//   y_i = the smallest v whose cumulative weight C_v = sum_{w <= v} w_w, with
+//         w_w = exp((l_w - M) / T) and M the row's largest finite logit,
+//         exceeds u * C_{V-1};
+// the walk is the greedy walk with y in place of the argmax (accept the child
+// of the current node whose token is y while one exists, at most b), and the
+// bonus is y at the last accepted node.  Each emitted token is then a draw
+// from the target's conditional distribution at its prefix.
+//
+// margin[r][i] = min(u S - C_{y-1}, C_y - u S) / S with S = C_{V-1}: how close
+// the draw lies to a neighbouring token's interval (the tests use it where
+// floating point may decide).  A row without a finite logit has S = 0: y = 0,
+// margin 0 and the OR_EMPTY_ROW bit; NaN or +inf set OR_NONFINITE.
+int oracle_verify_sample(const void* target, int dtype, int B, int n_max, int V, int64_t ld,
+                         int b, double T, const double* u, const int32_t* n_nodes,
+                         const int32_t* parent, const int32_t* token, int32_t* sampled,
+                         double* margin, int32_t* accept_len, int32_t* accept_nodes,
+                         int32_t* out_tokens, int32_t* status) {
+  if (B < 0 || n_max < 1 || V < 1 || ld < V || b < 1 || !(T > 0.0)) return -1;
+  std::vector<double> w((size_t)V);
+  for (int r = 0; r < B; ++r) {
+    int st = 0;
+    const int nn = n_nodes[r];
+    for (int i = 0; i < nn; ++i) {
+      const int64_t row = ((int64_t)r * n_max + i) * ld;
+      const int64_t o = (int64_t)r * n_max + i;
+      double M = -kInf;
+      for (int v = 0; v < V; ++v) {
+        const double x = load_logit(target, dtype, row + v);
+        if (std::isnan(x) || x == kInf) st |= OR_NONFINITE;
+        else if (x > M) M = x;
+      }
+      double S = 0.0;
+      for (int v = 0; v < V; ++v) {
+        const double x = load_logit(target, dtype, row + v);
+        w[(size_t)v] = (M == -kInf || std::isnan(x) || x == -kInf) ? 0.0 : std::exp((x - M) / T);
+        S += w[(size_t)v];
+      }
+      if (!(S > 0.0)) {
+        st |= OR_EMPTY_ROW;
+        sampled[o] = 0;
+        margin[o] = 0.0;
+        continue;
+      }
+      const double t = u[o] * S;
+      double C = 0.0;
+      int y = V - 1;
+      double lo = 0.0, hi = S;
+      for (int v = 0; v < V; ++v) {
+        const double Cn = C + w[(size_t)v];
+        if (Cn > t) {
+          y = v;
+          lo = C;
+          hi = Cn;
+          break;
+        }
+        C = Cn;
+      }
+      sampled[o] = y;
+      margin[o] = std::min(t - lo, hi - t) / S;
+    }
+    int32_t* an = accept_nodes + (int64_t)r * (b + 1);
+    int32_t* ot = out_tokens + (int64_t)r * (b + 1);
+    for (int k = 0; k <= b; ++k) { an[k] = -1; ot[k] = -1; }
+    int cur = 0, len = 0;
+    an[0] = 0;
+    if (nn >= 1) {
+      while (true) {
+        const int y = sampled[(int64_t)r * n_max + cur];
+        int next = -1;
+        for (int c = 1; c < nn; ++c)
+          if (parent[(int64_t)r * n_max + c] == cur && token[(int64_t)r * n_max + c] == y) {
+            next = c;
+            break;
+          }
+        if (next < 0 || len >= b) break;
+        ot[len] = y;
+        ++len;
+        an[len] = next;
+        cur = next;
+      }
+      ot[len] = sampled[(int64_t)r * n_max + cur];
+    }
+    accept_len[r] = len;
+    if (status) status[r] = st;
+  }
+  return 0;
+}
+
+// ---------------------------------------------------------------------------
 // Tree-masked GQA attention of the tree's query tokens against the KV cache
 // (the target verifies the whole tree in one parallel forward: "Probleemstelling"
 // and "Methodologie" §2 of the pages; the mask is what makes that forward

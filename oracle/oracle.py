@@ -55,6 +55,9 @@ def lib():
         L.oracle_verify_greedy.argtypes = [vp, i32, i32, i32, i32, i64, i32, vp, vp, vp,
                                            vp, vp, vp, vp, vp]
         L.oracle_verify_greedy.restype = i32
+        L.oracle_verify_sample.argtypes = [vp, i32, i32, i32, i32, i64, i32, dbl, vp, vp, vp, vp,
+                                           vp, vp, vp, vp, vp, vp]
+        L.oracle_verify_sample.restype = i32
         L.oracle_tree_attention.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i64, vp, vp, vp,
                                             dbl, vp, i64, vp]
         L.oracle_tree_attention.restype = i64
@@ -179,6 +182,39 @@ def verify_greedy(target: np.ndarray, b: int, n_nodes, parent, token) -> Verify:
     if rc != 0:
         raise ValueError("oracle_verify_greedy: bad arguments")
     return Verify(am, al, an, ot, st)
+
+
+@dataclass
+class VerifySample:
+    sampled: np.ndarray       # int32 [B, n_max] the token drawn at each node (-1 past n_nodes)
+    margin: np.ndarray        # float64 [B, n_max] distance of the draw to a neighbouring interval / S
+    accept_len: np.ndarray    # int32 [B]
+    accept_nodes: np.ndarray  # int32 [B, b+1]
+    out_tokens: np.ndarray    # int32 [B, b+1]
+    status: np.ndarray
+
+
+def verify_sample(target: np.ndarray, b: int, T: float, u, n_nodes, parent, token) -> VerifySample:
+    """Stochastic verification at temperature T with the uniforms u [B, n_max]
+    (float64 in [0, 1)); target [B, n_max, V] (float32 or bf16 bits)."""
+    target = np.ascontiguousarray(target)
+    B, n_max, V = target.shape
+    u = np.ascontiguousarray(u, dtype=np.float64).reshape(B, n_max)
+    n_nodes = np.ascontiguousarray(n_nodes, dtype=np.int32)
+    parent = np.ascontiguousarray(parent, dtype=np.int32)
+    token = np.ascontiguousarray(token, dtype=np.int32)
+    sm = np.full((B, n_max), -1, np.int32)
+    mg = np.zeros((B, n_max), np.float64)
+    al = np.zeros(B, np.int32)
+    an = np.zeros((B, b + 1), np.int32)
+    ot = np.zeros((B, b + 1), np.int32)
+    st = np.zeros(B, np.int32)
+    rc = lib().oracle_verify_sample(_p(target), _dtype_code(target), B, n_max, V, V, b, float(T),
+                                    _p(u), _p(n_nodes), _p(parent), _p(token), _p(sm), _p(mg), _p(al),
+                                    _p(an), _p(ot), _p(st))
+    if rc != 0:
+        raise ValueError("oracle_verify_sample: bad arguments")
+    return VerifySample(sm, mg, al, an, ot, st)
 
 
 def tree_attention(q, k, v, ctx_len, n_nodes, anc_mask, scale: float, sel=None) -> np.ndarray:
