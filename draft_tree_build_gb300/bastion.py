@@ -31,6 +31,7 @@ SYMBOLS = (
     "bastion_build_tree",
     "bastion_tree_attention_workspace_bytes", "bastion_tree_attention",
     "bastion_verify_greedy_workspace_bytes", "bastion_verify_greedy",
+    "bastion_verify_sample_workspace_bytes", "bastion_verify_sample",
     "bastion_verify_greedy_noalloc",
 )
 
@@ -77,6 +78,11 @@ def lib(build_if_missing: bool = True):
     L.bastion_verify_greedy.restype = i32
     L.bastion_verify_greedy.argtypes = [vp, i32, i32, i32, i32, i64, i32, vp, vp, vp, vp, vp, vp, vp,
                                         vp, sz, vp, vp]
+    L.bastion_verify_sample_workspace_bytes.restype = sz
+    L.bastion_verify_sample_workspace_bytes.argtypes = [i32, i32, i32]
+    L.bastion_verify_sample.restype = i32
+    L.bastion_verify_sample.argtypes = [vp, i32, i32, i32, i32, i64, i32, f32, vp, vp, vp, vp, vp, vp,
+                                        vp, vp, vp, sz, vp, vp]
     L.bastion_verify_greedy_noalloc.restype = i32
     L.bastion_verify_greedy_noalloc.argtypes = [vp, i32, i32, i32, i32, i64, i32, vp, vp, vp, vp, vp,
                                                 vp, vp, vp, vp]
@@ -193,6 +199,25 @@ def bastion_verify_greedy(target_logits, b, n_nodes, parent, token, argmax, acce
                                      _p(accept_nodes), _p(out_tokens), _p(workspace),
                                      workspace.numel() * workspace.element_size(), _p(status), _s(stream))
     _check(rc, "bastion_verify_greedy")
+
+
+def bastion_verify_sample_workspace_bytes(B: int, n_max: int, V: int) -> int:
+    return int(lib().bastion_verify_sample_workspace_bytes(B, n_max, V))
+
+
+def bastion_verify_sample(target_logits, b, temperature, uniforms, n_nodes, parent, token, sampled,
+                          accept_len, accept_nodes, out_tokens, workspace, status, stream=None):
+    """target_logits [B, n_max, V] (fp32/bf16, last dim contiguous); uniforms [B, n_max] float64."""
+    B, n_max, V = target_logits.shape
+    ld = _rows_view(target_logits, 3)
+    if uniforms.dtype != torch.float64 or not uniforms.is_contiguous():
+        raise BastionError("uniforms must be a contiguous float64 tensor")
+    rc = lib().bastion_verify_sample(_p(target_logits), _dtype(target_logits), B, n_max, V, ld, int(b),
+                                     float(temperature), _p(uniforms), _p(n_nodes), _p(parent), _p(token),
+                                     _p(sampled), _p(accept_len), _p(accept_nodes), _p(out_tokens),
+                                     _p(workspace), workspace.numel() * workspace.element_size(),
+                                     _p(status), _s(stream))
+    _check(rc, "bastion_verify_sample")
 
 
 def bastion_verify_greedy_noalloc(target_logits, b, n_nodes, parent, token, argmax, accept_len,

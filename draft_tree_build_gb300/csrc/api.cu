@@ -23,6 +23,12 @@ int launch_verify(const void *target, int dtype, int B, int n_max, int V, int64_
                   const int32_t *n_nodes, const int32_t *parent, const int32_t *token,
                   int32_t *argmax, int32_t *accept_len, int32_t *accept_nodes,
                   int32_t *out_tokens, void *ws, int32_t *status, cudaStream_t stream);
+size_t verify_sample_workspace_bytes(int B, int n_max, int V);
+int launch_verify_sample(const void *target, int dtype, int B, int n_max, int V, int64_t ld, int b,
+                         float temperature, const double *uniforms, const int32_t *n_nodes,
+                         const int32_t *parent, const int32_t *token, int32_t *sampled,
+                         int32_t *accept_len, int32_t *accept_nodes, int32_t *out_tokens, void *ws,
+                         int32_t *status, cudaStream_t stream);
 size_t attention_workspace_bytes(int B, int n_max, int Hq, int Hkv, int D, int64_t L_cap);
 int launch_attention(const void *q, const void *k, const void *v, int B, int n_max, int Hq,
                      int Hkv, int D, int64_t L_cap, const int32_t *ctx_len,
@@ -128,6 +134,34 @@ int bastion_verify_greedy(const void *target_logits, int dtype, int B, int n_max
   return bastion::launch_verify(target_logits, dtype, B, n_max, V, ld_row, b, n_nodes, parent,
                                 token, argmax, accept_len, accept_nodes, out_tokens, workspace,
                                 status, (cudaStream_t)stream);
+}
+
+size_t bastion_verify_sample_workspace_bytes(int B, int n_max, int V) {
+  if (B < 1 || B > 4096 || n_max < 1 || n_max > 256 || V < 1 || V >= (1 << 30)) return 0;
+  return bastion::verify_sample_workspace_bytes(B, n_max, V);
+}
+
+int bastion_verify_sample(const void *target_logits, int dtype, int B, int n_max, int V,
+                          int64_t ld_row, int b, float temperature, const double *uniforms,
+                          const int32_t *n_nodes, const int32_t *parent, const int32_t *token,
+                          int32_t *sampled, int32_t *accept_len, int32_t *accept_nodes,
+                          int32_t *out_tokens, void *workspace, size_t workspace_bytes,
+                          int32_t *status, bastion_stream_t stream) {
+  if (!target_logits || !uniforms || !n_nodes || !parent || !token || !sampled || !accept_len ||
+      !accept_nodes || !out_tokens || !workspace || !status)
+    return BASTION_ERR_NULL;
+  if (dtype != BASTION_F32 && dtype != BASTION_BF16) return BASTION_ERR_DTYPE;
+  if (B < 1 || B > 4096 || n_max < 1 || n_max > 256 || V < 1 || V >= (1 << 30) || ld_row < V ||
+      b < 1 || b > 32 || !(temperature > 0.f) || !(temperature < 1e30f))
+    return BASTION_ERR_SIZE;
+  const int es = dtype == BASTION_F32 ? 4 : 2;
+  if (!aligned(target_logits, es) || !aligned(uniforms, 8) || !aligned(workspace, 256))
+    return BASTION_ERR_ALIGN;
+  if (workspace_bytes < bastion::verify_sample_workspace_bytes(B, n_max, V)) return BASTION_ERR_WORKSPACE;
+  return bastion::launch_verify_sample(target_logits, dtype, B, n_max, V, ld_row, b, temperature,
+                                       uniforms, n_nodes, parent, token, sampled, accept_len,
+                                       accept_nodes, out_tokens, workspace, status,
+                                       (cudaStream_t)stream);
 }
 
 size_t bastion_tree_attention_workspace_bytes(int B, int n_max, int Hq, int Hkv, int D,

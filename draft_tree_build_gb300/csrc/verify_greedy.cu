@@ -294,6 +294,28 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 size_t verify_workspace_bytes(int B, int n_max) { return align256((size_t)B * n_max * 8); }
 
+// The decode + walk + reset of row keys alone (the stochastic verification
+// writes its drawn tokens as row keys and finishes here).
+int launch_verify_finish(const int32_t *n_nodes, const int32_t *parent, const int32_t *token, int B,
+                         int n_max, int b, int32_t *argmax, int32_t *accept_len, int32_t *accept_nodes,
+                         int32_t *out_tokens, uint64_t *row_key, int32_t *status, cudaStream_t stream) {
+  VerifyArgs a = {};
+  a.B = B;
+  a.n_max = n_max;
+  a.b = b;
+  a.n_nodes = n_nodes;
+  a.parent = parent;
+  a.token = token;
+  a.argmax = argmax;
+  a.accept_len = accept_len;
+  a.accept_nodes = accept_nodes;
+  a.out_tokens = out_tokens;
+  a.row_key = row_key;
+  a.status = status;
+  const cudaError_t e = launch_pdl(verify_finish_kernel, dim3((unsigned)((B + 7) / 8)), dim3(256), 0, stream, a);
+  return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? BASTION_OK : BASTION_ERR_LAUNCH;
+}
+
 int launch_verify(const void *target, int dtype, int B, int n_max, int V, int64_t ld, int b,
                   const int32_t *n_nodes, const int32_t *parent, const int32_t *token,
                   int32_t *argmax, int32_t *accept_len, int32_t *accept_nodes,

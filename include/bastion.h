@@ -196,6 +196,36 @@ int bastion_verify_greedy(const void *target_logits, int dtype, int B, int n_max
                           size_t workspace_bytes, int32_t *status, bastion_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Step 4 at temperature T > 0 -- stochastic verification.  The pages evaluate
+ * greedy decoding only ("Experimentele Resultaten"; DBlast, introduction:
+ * sampled decoding is the regime that matters).  For a tree of deterministic
+ * candidates the lossless reading is taken: the target's token at node i is a
+ * draw from softmax(target[r,i,:] / T) by inverse transform with the caller's
+ * uniform u = uniforms[r,i] in [0, 1) -- the smallest v whose cumulative
+ * weight sum_{w <= v} exp(l_w / T) exceeds u times the row's total -- and the
+ * greedy walk runs over the draws (the bonus is the draw at the last accepted
+ * node).  Every emitted token is then a draw from the target's conditional.
+ *
+ * The cumulative weights are formed in fp32 (compensated across 4 KB items)
+ * with fp32 exponentials: a draw within ~1e-6 of the row's total from a
+ * neighbouring token's interval may land on that neighbour.
+ * uniforms [B, n_max] double (8-byte aligned), caller-generated.
+ * Other arguments, outputs and limits as bastion_verify_greedy; sampled
+ * [B, n_max] holds the draws (rows >= n_nodes untouched).  temperature in
+ * (0, 1e30).  NaN / +inf logits set BASTION_STATUS_NONFINITE, a row without a
+ * finite logit BASTION_STATUS_EMPTY_ROW (its draw is token 0).
+ * Workspace: bastion_verify_sample_workspace_bytes(B, n_max, V) bytes.
+ * Three kernel launches (a sweep of the live rows, the draws, the walk).
+ */
+size_t bastion_verify_sample_workspace_bytes(int B, int n_max, int V);
+int bastion_verify_sample(const void *target_logits, int dtype, int B, int n_max, int V,
+                          int64_t ld_row, int b, float temperature, const double *uniforms,
+                          const int32_t *n_nodes, const int32_t *parent, const int32_t *token,
+                          int32_t *sampled, int32_t *accept_len, int32_t *accept_nodes,
+                          int32_t *out_tokens, void *workspace, size_t workspace_bytes,
+                          int32_t *status, bastion_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Greedy verification without a workspace, for callers that cannot allocate.
  * The pages have no counterpart: this is a deployment variant of the call
  * above, not a step of the method.

@@ -42,6 +42,7 @@ S_PAGREE = 8
 S_Q = 9
 S_K = 10
 S_V = 11
+S_VERIFY_U = 12
 
 PLANT_VALUE = 12.0  # above any Box-Muller draw (|z| < 8.7 since u1 >= 2^-54)
 
@@ -108,6 +109,11 @@ def uniforms(seed: int, stream: int, n: int, offset: int = 0) -> np.ndarray:
 
 def normals(seed: int, stream: int, n: int, offset: int = 0) -> np.ndarray:
     return np.array([lib().synth_normal(seed, stream, offset + i) for i in range(n)])
+
+
+def verify_uniforms(w: "Workload") -> np.ndarray:
+    """float64 [B, n_max] in [0, 1): the draws of stochastic verification."""
+    return uniforms(w.seed, S_VERIFY_U, w.B * w.n_max).reshape(w.B, w.n_max)
 
 
 def f64_to_bf16_bits(x: float) -> int:

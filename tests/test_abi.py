@@ -42,7 +42,7 @@ def _header_arg_counts():
 
 def test_binding_argtypes_match_header(L):
     counts = _header_arg_counts()
-    assert len(counts) == 10
+    assert len(counts) == 12
     for name, n in counts.items():
         assert len(getattr(L, name).argtypes) == n, name
 
@@ -80,10 +80,24 @@ def test_host_checks_reject_before_launch(L):
     assert L.bastion_tree_attention(*base) == -2
     # verify: B > 4096
     assert L.bastion_verify_greedy(fake, 1, 5000, 4, 8, 8, 4, fake, fake, fake, fake, fake, fake, fake, ws, 1 << 20, fake, None) == -2
+    # stochastic verify: temperature <= 0 or NaN; misaligned uniforms; null uniforms
+    sv = [fake, 1, 2, 4, 8, 8, 4, ctypes.c_float(0.0), fake] + [fake] * 7 + [ws, 1 << 20, fake, None]
+    assert L.bastion_verify_sample(*sv) == -2
+    sv[7] = ctypes.c_float(float("nan"))
+    assert L.bastion_verify_sample(*sv) == -2
+    sv[7], sv[8] = ctypes.c_float(1.0), vp(0x10004)
+    assert L.bastion_verify_sample(*sv) == -4
+    sv[8] = None
+    assert L.bastion_verify_sample(*sv) == -1
+    sv[8] = fake
+    sv[17] = 16
+    assert L.bastion_verify_sample(*sv) == -5
 
 
 def test_workspace_queries(L):
     assert L.bastion_topk_marginals_workspace_bytes(32, 16, 151936, 64) > 0
     assert L.bastion_topk_marginals_workspace_bytes(1, 1, 8, 9) == 0
     assert L.bastion_verify_greedy_workspace_bytes(32, 128, 151936) >= 32 * 128 * 8
+    assert L.bastion_verify_sample_workspace_bytes(32, 128, 151936) >= 32 * 128 * (8 + 75 * 16)
+    assert L.bastion_verify_sample_workspace_bytes(1, 257, 8) == 0
     assert L.bastion_tree_attention_workspace_bytes(8, 64, 32, 8, 128, 4160) > 0
