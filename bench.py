@@ -175,6 +175,9 @@ def run_ours(args, ws, rank, local):
     xs = [x_pin.to(dev, non_blocking=False) for _ in range(2)]
     step = bastion.TreeStep(w.B, w.b, w.V, w.K, w.n_max, dev, torch.from_numpy(roots),
                             torch.from_numpy(ctx), torch.from_numpy(cost), torch.from_numpy(lar))
+    sampled = args.temperature > 0
+    if sampled:  # stochastic verification with seeded uniforms
+        step.set_sampling(args.temperature, torch.from_numpy(synth.verify_uniforms(w)))
     # the target rows are planted at the nodes of the tree this device builds
     tgt_tmp = torch.zeros((w.B, w.n_max, w.V), dtype=xs[0].dtype, device=dev)
     step.run(xs[0], tgt_tmp)
@@ -206,9 +209,7 @@ def run_ours(args, ws, rank, local):
                                            tr.pos_id, tr.token, tr.rank, tr.log_rho, tr.a_hat,
                                            tr.speedup, tr.anc_mask, step.status)
             if args.profile_kernel in ("verify", "step"):
-                bastion.bastion_verify_greedy(td, w.b, tr.n_nodes, tr.parent, tr.token, v.argmax,
-                                              v.accept_len, v.accept_nodes, v.out_tokens, step.ws_verify,
-                                              step.status)
+                step.verify(td)
         torch.cuda.synchronize()
         assert int(step.status.abs().sum()) == 0, "device status bits set"
         return None
@@ -261,8 +262,7 @@ def run_ours(args, ws, rank, local):
                                    tr.token, tr.rank, tr.log_rho, tr.a_hat, tr.speedup, tr.anc_mask,
                                    step.status)
         evs[p][2].record(stream)
-        bastion.bastion_verify_greedy(td, w.b, tr.n_nodes, tr.parent, tr.token, v.argmax, v.accept_len,
-                                      v.accept_nodes, v.out_tokens, step.ws_verify, step.status)
+        step.verify(td)
         evs[p][3].record(stream)
     torch.cuda.synchronize()
     k1 = statistics.mean(evs[p][0].elapsed_time(evs[p][1]) for p in range(P))
@@ -309,13 +309,16 @@ def run_ours(args, ws, rank, local):
 
     hbm, peak_kind = peaks()
     ms_step = elapsed_ms / args.steps
+    vname = "verify_sample" if sampled else "verify_greedy"
     kern = {"topk_marginals": {"ms": k1, "bytes": bytes_k1, "gbs": bytes_k1 / (k1 * 1e-3) / 1e9},
             "build_tree": {"ms": k2, "bytes": w.B * w.b * w.K * 16},
-            "verify_greedy": {"ms": k4, "bytes": bytes_k4, "gbs": bytes_k4 / (k4 * 1e-3) / 1e9}}
-    dom = max(("topk_marginals", "verify_greedy"), key=lambda k: kern[k]["ms"])
+            vname: {"ms": k4, "bytes": bytes_k4, "gbs": bytes_k4 / (k4 * 1e-3) / 1e9}}
+    dom = max(("topk_marginals", vname), key=lambda k: kern[k]["ms"])
     ach = kern[dom]["gbs"]
     res = {
-        "metric": METRIC, "value": aggregate_rate(args.steps, elapsed_ms, ws), "unit": UNIT,
+        "metric": (METRIC if not sampled else
+                   METRIC.replace("+verify)", f"+sampled verify, T={args.temperature:g})")),
+        "value": aggregate_rate(args.steps, elapsed_ms, ws), "unit": UNIT,
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
@@ -328,7 +331,9 @@ def run_ours(args, ws, rank, local):
                      "traffic": (profiled_traffic(*{"topk_marginals": ("topk_marginals_b32_v151936.md",
                                                                        "topk_marginals.cu"),
                                                     "verify_greedy": ("verify_greedy_b32_v151936.md",
-                                                                      "verify_greedy.cu")}[dom])
+                                                                      "verify_greedy.cu"),
+                                                    "verify_sample": ("verify_sample_b32_v151936.md",
+                                                                      "verify_sample.cu")}[dom])
                                  if w.cid == 3 else None),
                      "step_frac": bytes_step / (ms_step * 1e-3) / 1e9 / hbm,
                      "bytes_per_step": bytes_step},
@@ -336,7 +341,8 @@ def run_ours(args, ws, rank, local):
         "clocks": clk,
         "e2e": {"value": aggregate_rate(1, e2e_ms, ws), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": 4 * args.steps,  # top-K, tree, verify sweep, verify finish
+        # top-K, tree, verify sweep, (sampled: the draws,) verify finish
+        "gpu_launches": (5 if sampled else 4) * args.steps,
     }
     return res
 
@@ -514,6 +520,15 @@ def oracle_step(w, req, x, lse_rows=None, pre=None):
     return tk, tr
 
 
+def oracle_verify(args, w, tgt, u, r, tr):
+    """The oracle's verification of request r (greedy, or sampled at T > 0)."""
+    import oracle
+    if args.temperature > 0:
+        oracle.verify_sample(tgt[r:r + 1], w.b, args.temperature, u[r:r + 1], tr.n_nodes, tr.parent, tr.token)
+    else:
+        oracle.verify_greedy(tgt[r:r + 1], w.b, tr.n_nodes, tr.parent, tr.token)
+
+
 def cpu_baseline(args, budget_s=12.0):
     """Times the oracle as it stands on the host (single thread) on a bounded
     sample: whole requests of the bench workload, cycled until ~budget_s."""
@@ -526,12 +541,13 @@ def cpu_baseline(args, budget_s=12.0):
     tk_all = oracle.topk_marginals(x, w.K)
     tr_all = oracle.build_tree(tk_all.logit, tk_all.tok, tk_all.lse, w.n_max, *pre)
     tgt, _ = synth.target_logits(w, tr_all.n_nodes, tr_all.depth, tk_all.tok)
+    u = synth.verify_uniforms(w)
     t0 = time.perf_counter()
     done = 0
     while True:
         r = done % w.B
         tk, tr = oracle_step(w, r, x, pre=pre)
-        oracle.verify_greedy(tgt[r:r + 1], w.b, tr.n_nodes, tr.parent, tr.token)
+        oracle_verify(args, w, tgt, u, r, tr)
         done += 1
         if time.perf_counter() - t0 > budget_s and done >= 1:
             break
@@ -554,9 +570,11 @@ def run_reference(args, ws, rank):
     tr_all = oracle.build_tree(tk_all.logit, tk_all.tok, tk_all.lse, w.n_max, *pre)
     tgt, _ = synth.target_logits(w, tr_all.n_nodes, tr_all.depth, tk_all.tok)
 
+    u = synth.verify_uniforms(w)
+
     def one(r):
         tk, tr = oracle_step(w, r, x, pre=pre)
-        oracle.verify_greedy(tgt[r:r + 1], w.b, tr.n_nodes, tr.parent, tr.token)
+        oracle_verify(args, w, tgt, u, r, tr)
 
     for i in range(args.warmup):
         one(i % w.B)
@@ -566,7 +584,9 @@ def run_reference(args, ws, rank):
     dt = time.perf_counter() - t0
     per_full_step = dt / args.steps * w.B
     val = 1.0 / per_full_step
-    return {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": ws,
+    metric = METRIC if args.temperature <= 0 else METRIC.replace(
+        "+verify)", f"+sampled verify, T={args.temperature:g})")
+    return {"impl": "reference", "metric": metric, "value": val, "unit": UNIT, "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_full_step * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
@@ -589,6 +609,8 @@ def main():
     ap.add_argument("--profile-kernel", choices=["topk", "tree", "verify", "step", "attn"],
                     help="launch one kernel (or the step) --launches times and exit, for ncu")
     ap.add_argument("--launches", type=int, default=3)
+    ap.add_argument("--temperature", type=float, default=0.0,
+                    help="verify by sampling at this temperature (0: greedy, the headline)")
     ap.add_argument("--chunks", type=int, default=1,
                     help="request chunks of the step on forked streams inside the graph")
     args = ap.parse_args()

@@ -324,9 +324,24 @@ class TreeStep:
                            tr.token, tr.rank, tr.log_rho, tr.a_hat, tr.speedup, tr.anc_mask,
                            self.status, stream)
 
+    def set_sampling(self, temperature, uniforms):
+        """Verify at temperature T > 0 with the uniforms [B, n_max] (float64 in
+        [0, 1), refreshed by the caller between steps); T = 0 returns to greedy."""
+        self.temperature = float(temperature)
+        if self.temperature > 0:
+            self.uniforms = uniforms.to(device=self.device, dtype=torch.float64).contiguous()
+            self.ws_sample = workspace(bastion_verify_sample_workspace_bytes(self.B, self.n_max, self.V),
+                                       self.device)
+
     def verify(self, target_logits, stream=None):
-        """Step 4: greedy verification of the tree against the target's logits."""
+        """Step 4: verification of the tree against the target's logits (greedy,
+        or sampled at the temperature set by set_sampling)."""
         tr, v = self.tree, self.ver
+        if getattr(self, "temperature", 0.0) > 0:
+            bastion_verify_sample(target_logits, self.b, self.temperature, self.uniforms, tr.n_nodes,
+                                  tr.parent, tr.token, v.argmax, v.accept_len, v.accept_nodes,
+                                  v.out_tokens, self.ws_sample, self.status, stream)
+            return
         bastion_verify_greedy(target_logits, self.b, tr.n_nodes, tr.parent, tr.token, v.argmax,
                               v.accept_len, v.accept_nodes, v.out_tokens, self.ws_verify,
                               self.status, stream)

@@ -16,11 +16,15 @@
 //    is below ~1; the warp scales the lanes' sums to the item's largest c by
 //    exact powers of two and adds them in two-float arithmetic.  The item's
 //    (max, c, sum) goes to the workspace;
-//  * find: one warp per live row scales the items' sums to the row's largest c
-//    (exact), scans them in item order, takes the item holding u times the
-//    total, reads that item again and scans its elements in token order (head
-//    elements, then 8 blocks of 32 lanes x 8 elements, then tail elements).
-//    The drawn token goes to the row's key in the workspace;
+//  * draw: persistent warps take the live rows in turn.  A warp scales the
+//    row's item sums to its largest c (exact), scans them in item order in
+//    two-float arithmetic (no fp64: GB300's fp64 rate is a small fraction of
+//    its fp32 rate), takes the item holding u times the total, and reads that
+//    item again with all of its loads in flight at once.  In token order (head
+//    elements, 8 blocks of 32 lanes x 8 elements, tail elements) it forms every
+//    vector's weight first, the 8 block totals by independent reductions,
+//    then scans only the block that holds the draw.  The drawn token goes to
+//    the row's key in the workspace;
 //  * the greedy finish kernel decodes the keys, walks the tree and resets them.
 #include <cuda_bf16.h>
 
@@ -266,6 +270,20 @@ __global__ void __launch_bounds__(kST, 4) sample_sweep_kernel(SampleArgs a) {
   }
 }
 
+constexpr int kCacheP = 4;  // item results a lane of the draw kernel keeps in registers
+
+// Item q (the lane's k-th): from the registers when cached, else from L2.
+__device__ __forceinline__ float4 part_at(const float4 (&pc)[kCacheP], const float4 *pp, int q, int k) {
+  float4 p = pc[0];
+#pragma unroll
+  for (int j = 1; j < kCacheP; ++j)
+    if (k == j) p = pc[j];
+  return k < kCacheP ? p : __ldcg(pp + q);
+}
+
+// a > b for normalised two-float values.
+__device__ __forceinline__ bool ff_gt(float2 a, float2 b) { return a.x > b.x || (a.x == b.x && a.y > b.y); }
+
 // Inclusive scan of a float over the warp's lanes.
 __device__ __forceinline__ float warp_incl_scan(float v, int lane) {
 #pragma unroll
@@ -278,23 +296,23 @@ __device__ __forceinline__ float warp_incl_scan(float v, int lane) {
 
 // One warp per live row: the draw by inverse transform.
 template <int ES>
-__global__ void __launch_bounds__(kST) sample_find_kernel(SampleArgs a) {
+__device__ __forceinline__ void draw_row(const SampleArgs &a, int r, int i, int lane) {
   constexpr int NE = 16 / ES;
-  const int lane = threadIdx.x & 31;
-  const int w = blockIdx.x * kSW + (threadIdx.x >> 5);
-  griddep_wait();
-  griddep_launch_dependents();
-  if (w >= a.B * a.n_max) return;
-  const int r = w / a.n_max, i = w - r * a.n_max;
-  const int nn = a.n_nodes[r];
-  if (nn < 1 || nn > a.n_max || i >= nn) return;
+  const int w = r * a.n_max + i;
+  const double ud = a.u[w];  // loaded with the items' results
   const float4 *pp = a.part + (size_t)w * a.nseg;
   const int P = (a.nseg + 31) / 32;  // items per lane, contiguous
+  float4 pc[kCacheP];                // the first kCacheP of them, loaded once
+#pragma unroll
+  for (int k = 0; k < kCacheP; ++k) {
+    const int q = lane * P + k;
+    pc[k] = k < P && q < a.nseg ? __ldcg(pp + q) : make_float4(-INFINITY, kCNone, 0.f, 0.f);
+  }
   float M = -INFINITY, cR = kCNone;
   for (int k = 0; k < P; ++k) {
     const int q = lane * P + k;
     if (q < a.nseg) {
-      const float4 p = __ldcg(pp + q);
+      const float4 p = part_at(pc, pp, q, k);
       M = fmaxf(M, p.x);
       cR = fmaxf(cR, p.y);
     }
@@ -306,7 +324,7 @@ __global__ void __launch_bounds__(kST) sample_find_kernel(SampleArgs a) {
   for (int k = 0; k < P; ++k) {
     const int q = lane * P + k;
     if (q < a.nseg) {
-      const float4 p = __ldcg(pp + q);
+      const float4 p = part_at(pc, pp, q, k);
       const float f = p.y > kCNone ? pow2_int(p.y - cR) : 0.f;
       ls = ff_add(ls, make_float2(p.z * f, p.w * f));
     }
@@ -317,11 +335,11 @@ __global__ void __launch_bounds__(kST) sample_find_kernel(SampleArgs a) {
     const float2 y = make_float2(__shfl_up_sync(kFull, inc.x, o), __shfl_up_sync(kFull, inc.y, o));
     if (lane >= o) inc = ff_add(y, inc);
   }
-  const double total = (double)__shfl_sync(kFull, inc.x, 31) + (double)__shfl_sync(kFull, inc.y, 31);
+  const float2 total = make_float2(__shfl_sync(kFull, inc.x, 31), __shfl_sync(kFull, inc.y, 31));
   int st = 0;
-  if (M == INFINITY || !(total == total) || total == (double)INFINITY || !(cR < INFINITY))
+  if (M == INFINITY || !(total.x == total.x) || total.x == INFINITY || !(cR < INFINITY))
     st |= BASTION_STATUS_NONFINITE;
-  if (!(total > 0.0)) st |= BASTION_STATUS_EMPTY_ROW;
+  if (!(total.x > 0.f)) st |= BASTION_STATUS_EMPTY_ROW;
   if (st) {
     if (lane == 0) {
       atomicOr(&a.status[r], st);
@@ -329,90 +347,168 @@ __global__ void __launch_bounds__(kST) sample_find_kernel(SampleArgs a) {
     }
     return;
   }
-  const double t = a.u[w] * total;
+  // t = u * total in two-float arithmetic (the only double is the uniform)
+  float2 t;
+  {
+    const float uh = (float)ud, ul = (float)(ud - (double)uh);
+    const float th = uh * total.x;
+    t = two_sum(th, fmaf(uh, total.x, -th) + (uh * total.y + ul * total.x));
+  }
   // the lane, then the item, holding t
-  const double lin = (double)inc.x + (double)inc.y, lex = lin - ((double)ls.x + (double)ls.y);
-  const unsigned over = __ballot_sync(kFull, lin > t);
-  const int L = over ? __ffs(over) - 1 : 31;
+  float2 ex = make_float2(__shfl_up_sync(kFull, inc.x, 1), __shfl_up_sync(kFull, inc.y, 1));
+  if (lane == 0) ex = make_float2(0.f, 0.f);
+  const unsigned over = __ballot_sync(kFull, ff_gt(inc, t));
+  // rounding may leave t at the total: then the last lane with weight
+  const int L = over ? __ffs(over) - 1 : 31 - __clz(__ballot_sync(kFull, ls.x > 0.f) | 1u);
   int q = -1;
-  double res = 0.0;
+  float cq = kCNone;
+  float2 res = make_float2(0.f, 0.f);
   if (lane == L) {
-    double cum = lex;
+    float2 cum = ex;
     for (int k = 0; k < P; ++k) {
       const int qq = lane * P + k;
       if (qq >= a.nseg) break;
-      const float4 p = __ldcg(pp + qq);
+      const float4 p = part_at(pc, pp, qq, k);
       const float f = p.y > kCNone ? pow2_int(p.y - cR) : 0.f;
-      const double wq = (double)(p.z * f) + (double)(p.w * f);
-      if (wq > 0.0) {  // the last item with weight, should rounding pass the end
+      const float2 wq = make_float2(p.z * f, p.w * f);
+      if (wq.x > 0.f) {  // the last item with weight, should rounding pass the end
         q = qq;
-        res = t - cum;
+        cq = p.y;
+        res = ff_add(t, make_float2(-cum.x, -cum.y));
       }
-      if (cum + wq > t) break;
-      cum += wq;
+      const float2 nc = ff_add(cum, wq);
+      if (ff_gt(nc, t)) break;
+      cum = nc;
     }
   }
   q = __shfl_sync(kFull, q, L);
-  res = __shfl_sync(kFull, res, L);
+  cq = __shfl_sync(kFull, cq, L);
+  const float resf = __shfl_sync(kFull, res.x + res.y, L);
   if (q < 0) q = 0;
-  // the item again, in token order, in units of its own c
-  const float cq = __ldcg(pp + q).y;
-  const float fq = pow2_int(cq - cR);
-  float rem = fq > 0.f ? (float)(res / (double)fq) : 0.f;
+  // the item again, in token order, in units of its own c (an exact power of
+  // two away); all of its loads (head, middle, tail) are issued before any is
+  // used
+  const float dq = cR - cq;  // >= 0, <= 126 for an item with weight
+  float rem = dq <= 126.f ? resf * __int_as_float(((int)dq + 127) << 23) : 0.f;
   const Item it = item_of<ES>(a, r, i, q);
+  const int eh = lane < it.nh ? lane : -1;
+  const int et = lane < it.n - it.t0 ? it.t0 + lane : -1;
+  uint4 xv[kSV];
+#pragma unroll
+  for (int u = 0; u < kSV; ++u) {
+    const int v = lane + 32 * u;
+    xv[u] = v < it.nvec ? ld_stream_v4(it.vp + v) : neg_inf_vec<ES>();
+  }
+  const float xh = eh >= 0 ? elem_at<ES>(it.g0 + (size_t)eh * ES) : -INFINITY;
+  const float xt = et >= 0 ? elem_at<ES>(it.g0 + (size_t)et * ES) : -INFINITY;
   int y = -1, last = -1;
   {  // head elements
-    const int e = lane < it.nh ? lane : -1;
-    const float wv = e >= 0 ? weight(elem_at<ES>(it.g0 + (size_t)e * ES), a.l2et, cq) : 0.f;
+    const float wv = eh >= 0 ? weight(xh, a.l2et, cq) : 0.f;
     const float incl = warp_incl_scan(wv, lane);
-    if (wv > 0.f) last = max(last, e);
+    if (wv > 0.f) last = max(last, eh);
     const unsigned hit = __ballot_sync(kFull, incl > rem && wv > 0.f);
     if (hit) y = __ffs(hit) - 1;
     rem -= __shfl_sync(kFull, incl, 31);
   }
-  for (int u = 0; u < kSV && y < 0; ++u) {  // the middle, 32 vectors at a time
-    const int v = lane + 32 * u;
-    float f[NE];
-    float vs = 0.f;
-    if (v < it.nvec) {
-      unpack<ES>(ld_stream_v4(it.vp + v), f);
+  if (y < 0) {
+    // the middle: every vector's weight first (independent), then the block
+    // of 32 vectors holding rem, then the lane, then the element
+    float vsu[kSV], bt[kSV];
+#pragma unroll
+    for (int u = 0; u < kSV; ++u) {
+      float f[NE];
+      unpack<ES>(xv[u], f);
+      float vs = 0.f;
 #pragma unroll
       for (int k = 0; k < NE; ++k) {
-        f[k] = weight(f[k], a.l2et, cq);
-        vs += f[k];
-        if (f[k] > 0.f) last = max(last, it.nh + v * NE + k);
+        const float wk = weight(f[k], a.l2et, cq);
+        vs += wk;
+        if (wk > 0.f) last = max(last, it.nh + (lane + 32 * u) * NE + k);
+      }
+      vsu[u] = vs;
+    }
+#pragma unroll
+    for (int u = 0; u < kSV; ++u) {
+      float t2 = vsu[u];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) t2 += __shfl_xor_sync(kFull, t2, o);
+      bt[u] = t2;
+    }
+    int ub = -1;
+    float before = 0.f;
+#pragma unroll
+    for (int u = 0; u < kSV; ++u) {
+      if (ub < 0) {
+        if (bt[u] > 0.f && before + bt[u] > rem) ub = u;
+        else before += bt[u];
       }
     }
-    const float incl = warp_incl_scan(vs, lane);
-    const unsigned hit = __ballot_sync(kFull, incl > rem && vs > 0.f);
-    if (hit) {
+    if (ub >= 0) {
+      float vs = vsu[0];
+      uint4 xb = xv[0];
+#pragma unroll
+      for (int u = 1; u < kSV; ++u)
+        if (u == ub) {
+          vs = vsu[u];
+          xb = xv[u];
+        }
+      const float r2 = rem - before;
+      const float incl = warp_incl_scan(vs, lane);
+      unsigned hit = __ballot_sync(kFull, incl > r2 && vs > 0.f);
+      if (!hit) hit = 1u << (31 - __clz(__ballot_sync(kFull, vs > 0.f)));  // rounding: the last lane with weight
       const int hl = __ffs(hit) - 1;
       if (lane == hl) {
+        // the first element whose cumulative weight passes r2, else (rounding)
+        // the last element with weight; static indices only
+        float f[NE];
+        unpack<ES>(xb, f);
         float cum = incl - vs;
-        int k = 0;
-        for (; k < NE - 1; ++k) {
-          if (f[k] > 0.f && cum + f[k] > rem) break;
-          cum += f[k];
+        int kf = -1, kl = 0;
+#pragma unroll
+        for (int k = 0; k < NE; ++k) {
+          const float wk = weight(f[k], a.l2et, cq);
+          if (kf < 0 && wk > 0.f && cum + wk > r2) kf = k;
+          if (wk > 0.f) kl = k;
+          cum += wk;
         }
-        while (k > 0 && !(f[k] > 0.f)) --k;  // rounding: the last element with weight
-        y = it.nh + v * NE + k;
+        y = it.nh + (lane + 32 * ub) * NE + (kf >= 0 ? kf : kl);
       }
       y = __shfl_sync(kFull, y, hl);
+    } else {
+      rem -= before;
     }
-    rem -= __shfl_sync(kFull, incl, 31);
   }
   if (y < 0) {  // tail elements
-    const int j = lane;
-    const int e = j < it.n - it.t0 ? it.t0 + j : -1;
-    const float wv = e >= 0 ? weight(elem_at<ES>(it.g0 + (size_t)e * ES), a.l2et, cq) : 0.f;
+    const float wv = et >= 0 ? weight(xt, a.l2et, cq) : 0.f;
     const float incl = warp_incl_scan(wv, lane);
-    if (wv > 0.f) last = max(last, e);
+    if (wv > 0.f) last = max(last, et);
     const unsigned hit = __ballot_sync(kFull, incl > rem && wv > 0.f);
-    if (hit) y = __shfl_sync(kFull, e, __ffs(hit) - 1);
+    if (hit) y = __shfl_sync(kFull, et, __ffs(hit) - 1);
   }
   last = __reduce_max_sync(kFull, (unsigned)(last + 1)) - 1;
   if (y < 0) y = last >= 0 ? last : 0;
   if (lane == 0) a.row_key[w] = make_key(0.f, (uint32_t)(it.e0 + y));
+}
+
+// A persistent grid whose warps take the live rows in turn.
+template <int ES>
+__global__ void __launch_bounds__(kST, 2) sample_find_kernel(SampleArgs a) {
+  extern __shared__ int prefix[];  // [B + 1] live rows before each request
+  __shared__ int s_tot[kSW];
+  const int lane = threadIdx.x & 31;
+  griddep_wait();
+  griddep_launch_dependents();
+  request_prefix(a.n_nodes, a.B, a.n_max, 1, prefix, s_tot);
+  const int total = prefix[a.B];
+  const int nw = gridDim.x * kSW;
+  for (int g = blockIdx.x * kSW + (threadIdx.x >> 5); g < total; g += nw) {
+    int lo = 0, hi = a.B;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (prefix[mid] <= g) lo = mid; else hi = mid;
+    }
+    draw_row<ES>(a, lo, g - prefix[lo], lane);
+  }
 }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -459,8 +555,14 @@ int launch_verify_sample(const void *target, int dtype, int B, int n_max, int V,
   if (grid > max_ctas) grid = max_ctas;
   if (grid < 1) grid = 1;
   cudaError_t e = launch_pdl(sweep, dim3((unsigned)grid), dim3(kST), smem, stream, a);
-  if (e == cudaSuccess)
-    e = launch_pdl(find, dim3((unsigned)(((long long)B * n_max + kSW - 1) / kSW)), dim3(kST), 0, stream, a);
+  if (e == cudaSuccess) {
+    int fsm = 1;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fsm, find, kST, smem);
+    long long fgrid = (long long)sms * (fsm < 1 ? 1 : fsm);
+    const long long fmax = ((long long)B * n_max + kSW - 1) / kSW;
+    if (fgrid > fmax) fgrid = fmax;
+    e = launch_pdl(find, dim3((unsigned)fgrid), dim3(kST), smem, stream, a);
+  }
   if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return BASTION_ERR_LAUNCH;
   return launch_verify_finish(n_nodes, parent, token, B, n_max, b, sampled, accept_len, accept_nodes,
                               out_tokens, a.row_key, status, stream);
