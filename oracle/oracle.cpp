@@ -424,6 +424,50 @@ int oracle_verify_sample(const void* target, int dtype, int B, int n_max, int V,
 }
 
 // ---------------------------------------------------------------------------
+// Calibration of the verification cost model ("Methodologie" §3,
+// "Latentiemodellering": T_verify(N) comes from a hardware-aware roofline model
+// of memory bandwidth and compute, calibrated with observed runtimes to correct
+// for kernel fusion and scheduling overhead).
+//
+// Reading: the roofline of a target forward over N tree tokens is
+//   roof(N) = max((bytes0 + bytes1 N) / bw, (flops0 + flops1 N) / peak)   [ms]
+// and the calibration is the least-squares line T_verify = alpha roof + beta
+// through the observed samples (N_i, t_i ms).  When the samples' roofline
+// values have no spread, alpha = 1 and beta = mean(t - roof).  The table the
+// tree controller reads is C(N) = t_draft + alpha roof(N) + beta for
+// N = 0 .. n_max.
+//
+// out_params = {alpha, beta}.  Returns -1 on bad arguments.
+int oracle_calibrate_cost(const double* sample_n, const double* sample_ms, int n_samples,
+                          double bytes0, double bytes1, double flops0, double flops1, double bw,
+                          double peak, double t_draft, int n_max, double* cost_out,
+                          double* out_params) {
+  if (n_samples < 1 || n_max < 1 || !(bw > 0.0) || !(peak > 0.0)) return -1;
+  auto roof = [&](double N) { return std::max((bytes0 + bytes1 * N) / bw, (flops0 + flops1 * N) / peak); };
+  double sr = 0.0, st = 0.0;
+  for (int k = 0; k < n_samples; ++k) {
+    sr += roof(sample_n[k]);
+    st += sample_ms[k];
+  }
+  const double mr = sr / n_samples, mt = st / n_samples;
+  double srr = 0.0, srt = 0.0;
+  for (int k = 0; k < n_samples; ++k) {
+    const double dr = roof(sample_n[k]) - mr;
+    srr += dr * dr;
+    srt += dr * (sample_ms[k] - mt);
+  }
+  double alpha = 1.0, beta = mt - mr;
+  if (srr > 1e-12 * std::max(1.0, mr * mr) * n_samples) {
+    alpha = srt / srr;
+    beta = mt - alpha * mr;
+  }
+  for (int N = 0; N <= n_max; ++N) cost_out[N] = t_draft + alpha * roof((double)N) + beta;
+  out_params[0] = alpha;
+  out_params[1] = beta;
+  return 0;
+}
+
+// ---------------------------------------------------------------------------
 // Tree-masked GQA attention of the tree's query tokens against the KV cache
 // (the target verifies the whole tree in one parallel forward: "Probleemstelling"
 // and "Methodologie" §2 of the pages; the mask is what makes that forward

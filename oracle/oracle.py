@@ -58,6 +58,8 @@ def lib():
         L.oracle_verify_sample.argtypes = [vp, i32, i32, i32, i32, i64, i32, dbl, vp, vp, vp, vp,
                                            vp, vp, vp, vp, vp, vp]
         L.oracle_verify_sample.restype = i32
+        L.oracle_calibrate_cost.argtypes = [vp, vp, i32] + [dbl] * 7 + [i32, vp, vp]
+        L.oracle_calibrate_cost.restype = i32
         L.oracle_tree_attention.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i64, vp, vp, vp,
                                             dbl, vp, i64, vp]
         L.oracle_tree_attention.restype = i64
@@ -215,6 +217,23 @@ def verify_sample(target: np.ndarray, b: int, T: float, u, n_nodes, parent, toke
     if rc != 0:
         raise ValueError("oracle_verify_sample: bad arguments")
     return VerifySample(sm, mg, al, an, ot, st)
+
+
+def calibrate_cost(sample_n, sample_ms, roofline: dict, t_draft: float, n_max: int):
+    """Least-squares calibration of T_verify = alpha roof(N) + beta; returns
+    (cost table C(0..n_max) float64, alpha, beta).  roofline holds bytes0,
+    bytes1, flops0, flops1, bw, peak (any consistent units giving ms)."""
+    n = np.ascontiguousarray(sample_n, dtype=np.float64)
+    t = np.ascontiguousarray(sample_ms, dtype=np.float64)
+    cost = np.zeros(n_max + 1, np.float64)
+    par = np.zeros(2, np.float64)
+    r = roofline
+    rc = lib().oracle_calibrate_cost(_p(n), _p(t), len(n), r["bytes0"], r["bytes1"], r["flops0"],
+                                     r["flops1"], r["bw"], r["peak"], float(t_draft), n_max, _p(cost),
+                                     _p(par))
+    if rc != 0:
+        raise ValueError("oracle_calibrate_cost: bad arguments")
+    return cost, float(par[0]), float(par[1])
 
 
 def tree_attention(q, k, v, ctx_len, n_nodes, anc_mask, scale: float, sel=None) -> np.ndarray:
