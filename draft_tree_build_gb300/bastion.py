@@ -29,6 +29,7 @@ SYMBOLS = (
     "bastion_version", "bastion_status_string",
     "bastion_topk_marginals_workspace_bytes", "bastion_topk_marginals",
     "bastion_build_tree",
+    "bastion_calibrate_cost",
     "bastion_tree_attention_workspace_bytes", "bastion_tree_attention",
     "bastion_verify_greedy_workspace_bytes", "bastion_verify_greedy",
     "bastion_verify_sample_workspace_bytes", "bastion_verify_sample",
@@ -68,6 +69,8 @@ def lib(build_if_missing: bool = True):
     L.bastion_topk_marginals.argtypes = [vp, i32, i32, i32, i32, i64, i32, vp, vp, vp, vp, vp, sz, vp, vp]
     L.bastion_build_tree.restype = i32
     L.bastion_build_tree.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, i32, vp] + [vp] * 11 + [vp]
+    L.bastion_calibrate_cost.restype = i32
+    L.bastion_calibrate_cost.argtypes = [vp, vp, i32] + [ctypes.c_double] * 7 + [i32, vp, vp, vp, vp]
     L.bastion_tree_attention_workspace_bytes.restype = sz
     L.bastion_tree_attention_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i64]
     L.bastion_tree_attention.restype = i32
@@ -164,6 +167,18 @@ def bastion_build_tree(topk_logit, topk_tok, lse, n_max, root_token, ctx_len, co
                                   _p(n_nodes), _p(parent), _p(depth), _p(pos_id), _p(token), _p(rank),
                                   _p(log_rho), _p(a_hat), _p(speedup), _p(anc_mask), _p(status), _s(stream))
     _check(rc, "bastion_build_tree")
+
+
+def bastion_calibrate_cost(sample_n, sample_ms, roofline: dict, t_draft, n_max, cost_ms, params, status,
+                           stream=None):
+    """sample_n / sample_ms [n] float32 on the device; cost_ms [n_max + 1], params [2] float32.
+    roofline: bytes0, bytes1, flops0, flops1, bw, peak (roof(N) in ms)."""
+    r = roofline
+    rc = lib().bastion_calibrate_cost(_p(sample_n), _p(sample_ms), int(sample_n.numel()), r["bytes0"],
+                                      r["bytes1"], r["flops0"], r["flops1"], r["bw"], r["peak"],
+                                      float(t_draft), int(n_max), _p(cost_ms), _p(params), _p(status),
+                                      _s(stream))
+    _check(rc, "bastion_calibrate_cost")
 
 
 def bastion_tree_attention_workspace_bytes(B, n_max, Hq, Hkv, D, L_cap) -> int:

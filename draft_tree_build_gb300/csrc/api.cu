@@ -29,6 +29,10 @@ int launch_verify_sample(const void *target, int dtype, int B, int n_max, int V,
                          const int32_t *parent, const int32_t *token, int32_t *sampled,
                          int32_t *accept_len, int32_t *accept_nodes, int32_t *out_tokens, void *ws,
                          int32_t *status, cudaStream_t stream);
+int launch_calibrate(const float *sample_n, const float *sample_ms, int n_samples, double bytes0,
+                     double bytes1, double flops0, double flops1, double bw, double peak,
+                     double t_draft, int n_max, float *cost_ms, float *params, int32_t *status,
+                     cudaStream_t stream);
 size_t attention_workspace_bytes(int B, int n_max, int Hq, int Hkv, int D, int64_t L_cap);
 int launch_attention(const void *q, const void *k, const void *v, int B, int n_max, int Hq,
                      int Hkv, int D, int64_t L_cap, const int32_t *ctx_len,
@@ -162,6 +166,23 @@ int bastion_verify_sample(const void *target_logits, int dtype, int B, int n_max
                                        uniforms, n_nodes, parent, token, sampled, accept_len,
                                        accept_nodes, out_tokens, workspace, status,
                                        (cudaStream_t)stream);
+}
+
+int bastion_calibrate_cost(const float *sample_n, const float *sample_ms, int n_samples,
+                           double bytes0, double bytes1, double flops0, double flops1, double bw,
+                           double peak, double t_draft, int n_max, float *cost_ms, float *params,
+                           int32_t *status, bastion_stream_t stream) {
+  if (!sample_n || !sample_ms || !cost_ms || !params || !status) return BASTION_ERR_NULL;
+  if (n_samples < 1 || n_samples > (1 << 24) || n_max < 1 || n_max > 256) return BASTION_ERR_SIZE;
+  const double v[7] = {bytes0, bytes1, flops0, flops1, bw, peak, t_draft};
+  for (double x : v)
+    if (!(x == x) || x < 0.0 || x > 1e300) return BASTION_ERR_SIZE;
+  if (!(bw > 0.0) || !(peak > 0.0)) return BASTION_ERR_SIZE;
+  if (!aligned(sample_n, 4) || !aligned(sample_ms, 4) || !aligned(cost_ms, 4) || !aligned(params, 4))
+    return BASTION_ERR_ALIGN;
+  return bastion::launch_calibrate(sample_n, sample_ms, n_samples, bytes0, bytes1, flops0, flops1,
+                                   bw, peak, t_draft, n_max, cost_ms, params, status,
+                                   (cudaStream_t)stream);
 }
 
 size_t bastion_tree_attention_workspace_bytes(int B, int n_max, int Hq, int Hkv, int D,

@@ -173,6 +173,28 @@ int bastion_tree_attention(const void *q, const void *k_cache, const void *v_cac
                            size_t workspace_bytes, int32_t *status, bastion_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * The cost model of step 2, calibrated on the device.  "Methodologie" §3,
+ * "Latentiemodellering": T_verify(N) comes from a hardware-aware roofline model
+ * of memory bandwidth and compute, calibrated with observed runtimes.  Here
+ *   roof(N)   = max((bytes0 + bytes1 N) / bw, (flops0 + flops1 N) / peak)
+ * (units chosen so that roof is in ms, e.g. bytes per ms and flop per ms), and
+ * the calibration is the least-squares line T_verify = alpha roof(N) + beta
+ * through the observed samples (sample_n[k] tree nodes, sample_ms[k] ms); with
+ * no spread in the samples' roofline values alpha = 1 and beta is the mean
+ * residual.  Output: cost_ms [n_max + 1] float, C(N) = t_draft + alpha roof(N)
+ * + beta, the single-row table bastion_build_tree reads (cost_per_request = 0);
+ * params [2] float = {alpha, beta}.  Sums in fp64, one CTA.
+ * status [1] int32: BASTION_STATUS_BAD_COST if a sample is non-finite or a
+ * C(N), N >= 1, is not positive and finite.
+ * Limits: 1 <= n_samples <= 2^24, 1 <= n_max <= 256; the six roofline
+ * constants and t_draft finite and >= 0, bw and peak > 0.  One kernel launch.
+ */
+int bastion_calibrate_cost(const float *sample_n, const float *sample_ms, int n_samples,
+                           double bytes0, double bytes1, double flops0, double flops1, double bw,
+                           double peak, double t_draft, int n_max, float *cost_ms, float *params,
+                           int32_t *status, bastion_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Step 4 -- greedy (temperature 0) verification ("Experimentele Resultaten":
  * greedy decoding).  For every tree node i < n_nodes[r] the target's greedy
  * token is argmax_v target[r,i,v] (ties: lowest v).  From the root, the child

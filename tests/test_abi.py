@@ -42,7 +42,7 @@ def _header_arg_counts():
 
 def test_binding_argtypes_match_header(L):
     counts = _header_arg_counts()
-    assert len(counts) == 12
+    assert len(counts) == 13
     for name, n in counts.items():
         assert len(getattr(L, name).argtypes) == n, name
 
@@ -92,6 +92,15 @@ def test_host_checks_reject_before_launch(L):
     sv[8] = fake
     sv[17] = 16
     assert L.bastion_verify_sample(*sv) == -5
+    # calibration: no samples, n_max > 256, bw = 0, a NaN constant, misaligned table
+    d = ctypes.c_double
+    cal = [fake, fake, 8] + [d(1.0)] * 7 + [16, fake, fake, fake, None]
+    assert L.bastion_calibrate_cost(*(cal[:2] + [0] + cal[3:])) == -2
+    assert L.bastion_calibrate_cost(*(cal[:10] + [257] + cal[11:])) == -2
+    assert L.bastion_calibrate_cost(*(cal[:7] + [d(0.0)] + cal[8:])) == -2
+    assert L.bastion_calibrate_cost(*(cal[:3] + [d(float("nan"))] + cal[4:])) == -2
+    assert L.bastion_calibrate_cost(*(cal[:11] + [vp(0x10002)] + cal[12:])) == -4
+    assert L.bastion_calibrate_cost(*(cal[:12] + [None] + cal[13:])) == -1
 
 
 def test_workspace_queries(L):
