@@ -11,17 +11,22 @@
 //  * warp 0 streams Q once and the K tiles of 128 keys, warp 3 the V tiles,
 //    each through its own 2-slot ring with TMA (cp.async.bulk.tensor, 128-byte
 //    swizzle, no multicast); a K slot frees as soon as S has read it;
-//  * warp 1 (one thread) issues tcgen05.mma kind::f16 (bf16 in, fp32 out):
-//    S_t = Q K_t^T into one of two TMEM buffers, then O += P_{t-1} V_{t-1};
+//  * the tile's keys are split into two halves of 64 that run as independent
+//    pipelines, each with its own online softmax, TMEM buffers and MMA
+//    issuer, so that one half's latency-bound phases (waiting for S, the TMEM
+//    load, the max, handing P over) overlap the other half's exponentials;
+//  * lane 0 of warp 1 + h issues half h's tcgen05.mma kind::f16 (bf16 in,
+//    fp32 out): S_h = Q K_t[64 h : 64 h + 64]^T into one of its two TMEM
+//    buffers (N = 64), issued as soon as the half's softmax has read the
+//    buffer's previous tile, then O_h += P_h V_t[64 h : 64 h + 64] into its
+//    accumulator (O_A at TMEM column 0, O_B at 384);
 //  * warps 4-11 run the softmax, two warps per TMEM lane quadrant (one query
-//    row per lane), each on half of the tile's 128 keys with its own online
-//    softmax: PV is issued as two K=64 MMAs into two accumulators O_A, O_B
-//    (TMEM columns 0 and 384), so the halves never wait for each other.  Each
-//    warp reads S_t with tcgen05.ld, applies the tree mask (context tiles are
-//    visible to every row and skip it), and writes its half of P_t as bf16
-//    into shared memory in the MMA operand layout; its O_h is rescaled only
-//    when a row's running max grows by more than 2^8 (the final
-//    normalisation uses the same reference max, so this is exact);
+//    row per lane), warp 4 + 4 h for half h.  Each warp reads its S with
+//    tcgen05.ld, applies the tree mask (context tiles are visible to every
+//    row and skip it), and writes P_h as bf16 into shared memory in the MMA
+//    operand layout; O_h is rescaled only when a row's running max grows by
+//    more than 2^8 (the final normalisation uses the same reference max, so
+//    this is exact);
 //  * epilogue: the pair exchanges its (max, sum) once and writes
 //    (O_A 2^(m_A - M) + O_B 2^(m_B - M)) / l as bf16 (round to nearest even).
 // Every wait is bounded (~1 s); on a timeout the CTA flags the request, waits
@@ -35,7 +40,7 @@ namespace bastion {
 
 namespace {
 
-constexpr int kAT = 384;  // warp 0 TMA (Q, K), 1 MMA, 2 TMEM, 3 TMA (V), 4-11 softmax
+constexpr int kAT = 384;  // warp 0 TMA (Q, K), 1-2 MMA (2 also TMEM), 3 TMA (V), 4-11 softmax
 constexpr int kBM = 128;
 constexpr int kBN = 128;
 constexpr uint32_t kAtom = 128 * 128;          // 128 rows x 128 bytes
@@ -46,7 +51,7 @@ constexpr uint32_t kOffP = kOffKV + 2 * 2 * kTile;
 constexpr uint32_t kOffBar = kOffP + 2 * kTile;
 constexpr uint32_t kSmem = kOffBar + 256 + 1024;  // + alignment slack
 constexpr float kRescale = 8.0f;               // lazy rescale threshold (log2 units)
-constexpr uint32_t kColOB = 384;               // TMEM columns of O_B (O_A at 0, S at 128, 256)
+constexpr uint32_t kColOB = 384;  // TMEM columns: O_A 0, S_A 128 and 192, S_B 256 and 320, O_B 384
 
 struct AttnArgs {
   int B, n_max, Hq, Hkv, G, W, qt_max;
@@ -59,7 +64,9 @@ struct AttnArgs {
 };
 
 struct Bars {
-  uint64_t q_full, k_full[2], v_full[2], k_empty[2], v_empty[2], s_full[2], p_full[2], pv_done[2];
+  // [h][s]: half h of the keys, buffer s
+  uint64_t q_full, k_full[2], v_full[2], k_empty[2], v_empty[2], s_full[2][2], s_free[2][2],
+      p_full[2][2], pv_done[2][2], mma_done[2];
   uint32_t tmem;
   int abort;
 };
@@ -73,10 +80,10 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
   return d;
 }
 
-// kind::f16 instruction descriptor: fp32 accumulate, bf16 A and B, M = N = 128.
-__device__ __forceinline__ uint32_t idesc_bf16(bool b_mn_major) {
+// kind::f16 instruction descriptor: fp32 accumulate, bf16 A and B, M = 128, N = n.
+__device__ __forceinline__ uint32_t idesc_bf16(bool b_mn_major, int n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
-         ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+         ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
 }
 
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
@@ -91,6 +98,17 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    smem_u32(bar))
                : "memory");
+}
+
+// S = Q K^T for the keys whose rows start at sk (64 or 128 of them, as the
+// instruction descriptor says): eight K = 16 steps over the two 64-column
+// atoms of Q and K.
+__device__ __forceinline__ void mma_qk(uint32_t d, uint32_t sq, uint32_t sk, uint32_t idesc) {
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    const uint32_t off = (uint32_t)(ks >> 2) * kAtom + (uint32_t)(ks & 3) * 32u;
+    mma_bf16(d, sw128_desc(sq + off, 16, 1024), sw128_desc(sk + off, 16, 1024), idesc, ks > 0);
+  }
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -237,6 +255,11 @@ __global__ void __launch_bounds__(kAT, 1)
   volatile int *abort = &bs.abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {  // the descriptors are parameters: fetch them while the producer kernel ends
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_k)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_v)) : "memory");
+  }
   griddep_wait();
   griddep_launch_dependents();
   const int qt = blockIdx.x % a.qt_max;
@@ -261,14 +284,33 @@ __global__ void __launch_bounds__(kAT, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bs.k_full[s], 1);
       mbar_init(&bs.v_full[s], 1);
-      mbar_init(&bs.k_empty[s], 1);
-      mbar_init(&bs.v_empty[s], 1);
-      mbar_init(&bs.s_full[s], 1);
-      mbar_init(&bs.p_full[s], 256);
-      mbar_init(&bs.pv_done[s], 1);
+      mbar_init(&bs.k_empty[s], 2);  // both halves' S MMAs have read the K slot
+      mbar_init(&bs.v_empty[s], 2);  // both halves' PV MMAs have read the V slot
+      for (int h = 0; h < 2; ++h) {
+        mbar_init(&bs.s_full[h][s], 1);
+        mbar_init(&bs.s_free[h][s], 4);
+        mbar_init(&bs.p_full[h][s], 128);
+        mbar_init(&bs.pv_done[h][s], 1);
+      }
     }
+    mbar_init(&bs.mma_done[0], 1);
+    mbar_init(&bs.mma_done[1], 1);
     bs.abort = 0;
     fence_mbar_init();
+    // Q and the first two K and V tiles start loading before the TMEM
+    // allocation and the CTA barrier; the producers continue from tile 2
+    mbar_arrive_expect_tx(&bs.q_full, kTile);
+    tma_load_4d(smem + kOffQ, &tm_q, 0, g * a.G, i0, r, &bs.q_full);
+    tma_load_4d(smem + kOffQ + kAtom, &tm_q, 64, g * a.G, i0, r, &bs.q_full);
+    for (int t = 0; t < n_tiles && t < 2; ++t) {
+      unsigned char *dk = smem + kOffKV + t * 2 * kTile;
+      mbar_arrive_expect_tx(&bs.k_full[t], kTile);
+      tma_load_4d(dk, &tm_k, 0, g, t * kBN, r, &bs.k_full[t]);
+      tma_load_4d(dk + kAtom, &tm_k, 64, g, t * kBN, r, &bs.k_full[t]);
+      mbar_arrive_expect_tx(&bs.v_full[t], kTile);
+      tma_load_4d(dk + kTile, &tm_v, 0, g, t * kBN, r, &bs.v_full[t]);
+      tma_load_4d(dk + kTile + kAtom, &tm_v, 64, g, t * kBN, r, &bs.v_full[t]);
+    }
   }
   if (warp == 2) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
@@ -282,21 +324,17 @@ __global__ void __launch_bounds__(kAT, 1)
 
   if (warp == 0 || warp == 3) {
     // ------------------------------------------------------------ TMA producers
-    // warp 0: Q and the K tiles (a K slot frees once S = QK^T has read it);
-    // warp 3: the V tiles (a V slot frees once O += PV has read it)
+    // warp 0: the K tiles from tile 2 on (a K slot frees once both halves'
+    // S MMAs have read it); warp 3: the V tiles (a V slot frees once both
+    // halves' PV MMAs have read it)
     if (lane == 0) {
       const bool is_k = warp == 0;
-      if (is_k) {
-        mbar_arrive_expect_tx(&bs.q_full, kTile);
-        tma_load_4d(smem + kOffQ, &tm_q, 0, g * a.G, i0, r, &bs.q_full);
-        tma_load_4d(smem + kOffQ + kAtom, &tm_q, 64, g * a.G, i0, r, &bs.q_full);
-      }
       uint64_t *full = is_k ? bs.k_full : bs.v_full, *empty = is_k ? bs.k_empty : bs.v_empty;
       const CUtensorMap *map = is_k ? &tm_k : &tm_v;
-      int issued = 0;
-      for (int t = 0; t < n_tiles; ++t) {
+      int issued = n_tiles < 2 ? n_tiles : 2;
+      for (int t = 2; t < n_tiles; ++t) {
         const int s = t & 1;
-        if (t >= 2 && !wait_bar(&empty[s], ((t - 2) >> 1) & 1, abort, &a.status[r])) break;
+        if (!wait_bar(&empty[s], ((t - 2) >> 1) & 1, abort, &a.status[r])) break;
         unsigned char *dst = smem + kOffKV + s * 2 * kTile + (is_k ? 0 : kTile);
         mbar_arrive_expect_tx(&full[s], kTile);
         tma_load_4d(dst, map, 0, g, t * kBN, r, &full[s]);
@@ -308,52 +346,61 @@ __global__ void __launch_bounds__(kAT, 1)
         mbar_wait_bounded(&full[t & 1], (t >> 1) & 1);
       if (is_k) mbar_wait_bounded(&bs.q_full, 0);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issuers
+    // lane 0 of warp 1 + h issues half h's MMAs: S_h = Q K^T over keys
+    // [64 h, 64 h + 64) of each tile into its own two TMEM buffers, and
+    // O_h += P_h V over the same keys.  The halves are independent pipelines:
+    // neither waits for the other's softmax, so one half's latency-bound
+    // phases overlap the other's exponentials.
+    const int h = warp - 1;
     if (lane == 0) {
-      const uint32_t id_qk = idesc_bf16(false), id_pv = idesc_bf16(true);
+      const uint32_t id_qk = idesc_bf16(false, 64), id_pv = idesc_bf16(true, 128);
       const uint32_t sq = smem_u32(smem + kOffQ);
+      const uint32_t s_col = tmem + 128u + 128u * (uint32_t)h;  // S_h buffer s at + 64 s
+      const uint32_t o_col = tmem + (h ? kColOB : 0u);
       bool ok = wait_bar(&bs.q_full, 0, abort, &a.status[r]);
       tc_fence_after();
-      int last_pv = -1;
-      for (int t = 0; ok && t <= n_tiles; ++t) {
-        if (t < n_tiles) {
-          const int s = t & 1;
-          if (!wait_bar(&bs.k_full[s], (t >> 1) & 1, abort, &a.status[r])) break;
+      // S_0 and S_1 first; then, per tile u, S_{u+2} goes into buffer u % 2
+      // as soon as the half's softmax warps have read S_u, ahead of
+      // O_h += P_u V_u, so the softmax never finds its S queued behind a PV
+      for (int t = 0; ok && t < n_tiles && t < 2; ++t) {
+        if (!wait_bar(&bs.k_full[t], 0, abort, &a.status[r])) ok = false;
+        if (!ok) break;
+        tc_fence_after();
+        mma_qk(s_col + 64u * (uint32_t)t, sq, smem_u32(smem + kOffKV + t * 2 * kTile) + 8192u * (uint32_t)h,
+               id_qk);
+        mma_commit(&bs.s_full[h][t]);
+        mma_commit(&bs.k_empty[t]);
+      }
+      for (int u = 0; ok && u < n_tiles; ++u) {
+        const int s = u & 1;
+        if (u + 2 < n_tiles) {
+          if (!wait_bar(&bs.s_free[h][s], (u >> 1) & 1, abort, &a.status[r])) break;
+          if (!wait_bar(&bs.k_full[s], ((u + 2) >> 1) & 1, abort, &a.status[r])) break;
           tc_fence_after();
-          const uint32_t sk = smem_u32(smem + kOffKV + s * 2 * kTile);
-          const uint32_t d = tmem + 128u * (1u + (uint32_t)s);
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t off = (uint32_t)(ks >> 2) * kAtom + (uint32_t)(ks & 3) * 32u;
-            mma_bf16(d, sw128_desc(sq + off, 16, 1024), sw128_desc(sk + off, 16, 1024), id_qk,
-                     ks > 0);
-          }
-          mma_commit(&bs.s_full[s]);
+          mma_qk(s_col + 64u * (uint32_t)s, sq, smem_u32(smem + kOffKV + s * 2 * kTile) + 8192u * (uint32_t)h,
+                 id_qk);
+          mma_commit(&bs.s_full[h][s]);
           mma_commit(&bs.k_empty[s]);
         }
-        if (t >= 1) {
-          const int u = t - 1, s = u & 1;
-          if (!wait_bar(&bs.p_full[s], (u >> 1) & 1, abort, &a.status[r])) break;
-          if (!wait_bar(&bs.v_full[s], (u >> 1) & 1, abort, &a.status[r])) break;
-          tc_fence_after();
-          const uint32_t sp = smem_u32(smem + kOffP + s * kTile);
-          const uint32_t sv = smem_u32(smem + kOffKV + s * 2 * kTile + kTile);
-          // keys 0-63 of the tile into O_A (TMEM columns 0-127), keys 64-127
-          // into O_B (columns 384-511): each half has its own softmax state
+        if (!wait_bar(&bs.p_full[h][s], (u >> 1) & 1, abort, &a.status[r])) break;
+        if (!wait_bar(&bs.v_full[s], (u >> 1) & 1, abort, &a.status[r])) break;
+        tc_fence_after();
+        // P_h is atom h of P buffer s; V rows 64 h .. 64 h + 63 of slot s
+        const uint32_t sp = smem_u32(smem + kOffP + s * kTile) + (uint32_t)h * kAtom;
+        const uint32_t sv = smem_u32(smem + kOffKV + s * 2 * kTile + kTile) + 8192u * (uint32_t)h;
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t offp = (uint32_t)(ks >> 2) * kAtom + (uint32_t)(ks & 3) * 32u;
-            mma_bf16(ks < 4 ? tmem : tmem + kColOB, sw128_desc(sp + offp, 16, 1024),
-                     sw128_desc(sv + (uint32_t)ks * 2048u, kAtom, 1024), id_pv,
-                     (u > 0 || (ks & 3) > 0));
-          }
-          mma_commit(&bs.pv_done[s]);
-          mma_commit(&bs.v_empty[s]);
-          last_pv = u;
-        }
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16(o_col, sw128_desc(sp + (uint32_t)ks * 32u, 16, 1024),
+                   sw128_desc(sv + (uint32_t)ks * 2048u, kAtom, 1024), id_pv, (u > 0 || ks > 0));
+        mma_commit(&bs.pv_done[h][s]);
+        mma_commit(&bs.v_empty[s]);
       }
-      if (last_pv >= 0) mbar_wait_bounded(&bs.pv_done[last_pv & 1], (last_pv >> 1) & 1);
+      // every MMA this thread issued has completed (bounded) before the CTA
+      // may free its TMEM
+      mma_commit(&bs.mma_done[h]);
+      mbar_wait_bounded(&bs.mma_done[h], 0);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax + epilogue
@@ -374,12 +421,11 @@ __global__ void __launch_bounds__(kAT, 1)
     const uint32_t col0 = 64u * (uint32_t)half;
     const uint32_t o_base = lane_base + (half ? kColOB : 0u);
     float m_ref = -INFINITY, l_sum = 0.f;
+    bool all_ref = false;  // every row of the warp has a reference max
     bool ok = true;
     for (int t = 0; t < n_tiles && ok; ++t) {
       const int s = t & 1;
-      ok = __all_sync(kFull, wait_bar(&bs.s_full[s], (t >> 1) & 1, abort, &a.status[r]));
-      if (ok && t >= 2)  // P buffer s free: PV of tile t-2 done
-        ok = __all_sync(kFull, wait_bar(&bs.pv_done[s], ((t - 2) >> 1) & 1, abort, &a.status[r]));
+      ok = __all_sync(kFull, wait_bar(&bs.s_full[half][s], (t >> 1) & 1, abort, &a.status[r]));
       if (!ok) break;
       tc_fence_after();
       const int kb = t * kBN + 64 * half;
@@ -414,89 +460,125 @@ __global__ void __launch_bounds__(kAT, 1)
       // scale is positive); context tiles are fully visible to every row
       const bool full = __all_sync(kFull, (vis[0] & vis[1]) == 0xffffffffu);
       float v[64];
-      tmem_ld64(lane_base + 128u * (1u + (uint32_t)s) + col0, v);
-      float mr = -INFINITY;
-      if (full) {
-        float q0 = v[0], q1 = v[1], q2 = v[2], q3 = v[3];
-#pragma unroll
-        for (int i = 4; i < 64; i += 8) {
-          q0 = max3f(q0, v[i], v[i + 1]);
-          q1 = max3f(q1, v[i + 2], v[i + 3]);
-          q2 = max3f(q2, v[i + 4], v[i + 5]);
-          q3 = max3f(q3, v[i + 6], v[i + 7]);
-        }
-        mr = max3f(fmaxf(q0, q1), q2, q3);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          if ((vis[0] >> i) & 1u) mr = fmaxf(mr, v[i]);
-          if ((vis[1] >> i) & 1u) mr = fmaxf(mr, v[32 + i]);
-        }
-      }
-      const float mt = mr * a.scale_log2;
-      // lazy rescale: a row moves its reference max only when the tile max
-      // exceeds it by more than 2^8; O_h in TMEM is rescaled by the whole warp
-      // (tcgen05.ld/st are warp-collective), with alpha = 1 for other rows.
-      const bool grow = mt > m_ref + kRescale || (m_ref == -INFINITY && mt != -INFINITY);
-      const bool rescale = grow && t > 0 && m_ref != -INFINITY;
-      const float alpha = rescale ? ex2f(m_ref - mt) : 1.0f;
-      if (__any_sync(kFull, rescale)) {
-        ok = __all_sync(kFull, wait_bar(&bs.pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, abort,
-                                        &a.status[r]));
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          float o[32];
-          tmem_ld32(o_base + 32u * cc, o);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= alpha;
-          tmem_st32(o_base + 32u * cc, o);
-        }
-      }
-      if (rescale) l_sum *= alpha;
-      if (grow) m_ref = mt;
-      unsigned char *pb = smem + kOffP + s * kTile;
+      const uint32_t s_addr = lane_base + 128u + 128u * (uint32_t)half + 64u * (uint32_t)s;
+      tmem_ld64(s_addr, v);
+      // At most two passes.  Once every row has a reference max, a fully
+      // visible tile is first exponentiated against the current references,
+      // its max taken alongside; only if some row's tile max exceeds its
+      // reference by more than 2^8 is the tile redone the exact way (max
+      // first, then the lazy rescale), which gives the same values whenever
+      // no row grows, so the max leaves the critical path of the common tile.
+      bool spec = full && all_ref, redo = false;
+      bool p_free = t < 2;
       float part = 0.f;
-      const float nm = m_ref == -INFINITY ? 0.f : -m_ref;  // no visible key yet: all p = 0
+      for (;;) {
+        if (!spec) {
+          if (redo) tmem_ld64(s_addr, v);  // the speculative pass consumed v
+          float mr = -INFINITY;
+          if (full) {
+            float q0 = v[0], q1 = v[1], q2 = v[2], q3 = v[3];
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        uint32_t pk[16];
-        if (full && m_ref != -INFINITY) {
-          float s0 = 0.f, s1 = 0.f;
+            for (int i = 4; i < 64; i += 8) {
+              q0 = max3f(q0, v[i], v[i + 1]);
+              q1 = max3f(q1, v[i + 2], v[i + 3]);
+              q2 = max3f(q2, v[i + 4], v[i + 5]);
+              q3 = max3f(q3, v[i + 6], v[i + 7]);
+            }
+            mr = max3f(fmaxf(q0, q1), q2, q3);
+          } else {
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            float t0, t1;
-            fma2(v[32 * cc + i], v[32 * cc + i + 1], a.scale_log2, nm, t0, t1);
-            const float p0 = ex2f(t0), p1 = ex2f(t1);
-            add2(s0, s1, p0, p1);
-            pk[i >> 1] = pack_bf16(p0, p1);
+            for (int i = 0; i < 32; ++i) {
+              if ((vis[0] >> i) & 1u) mr = fmaxf(mr, v[i]);
+              if ((vis[1] >> i) & 1u) mr = fmaxf(mr, v[32 + i]);
+            }
           }
-          part += s0 + s1;
-        } else {
+          const float mt = mr * a.scale_log2;
+          // lazy rescale: a row moves its reference max only when the tile
+          // max exceeds it by more than 2^8; O_h in TMEM is rescaled by the
+          // whole warp (tcgen05.ld/st are warp-collective), with alpha = 1 for
+          // other rows.
+          const bool grow = mt > m_ref + kRescale || (m_ref == -INFINITY && mt != -INFINITY);
+          const bool rescale = grow && t > 0 && m_ref != -INFINITY;
+          const float alpha = rescale ? ex2f(m_ref - mt) : 1.0f;
+          if (__any_sync(kFull, rescale)) {
+            ok = __all_sync(kFull, wait_bar(&bs.pv_done[half][(t - 1) & 1], ((t - 1) >> 1) & 1, abort,
+                                            &a.status[r]));
+            if (!ok) break;
+            tc_fence_after();
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            const bool s0 = ((vis[cc] >> i) & 1u) && m_ref != -INFINITY;
-            const bool s1 = ((vis[cc] >> (i + 1)) & 1u) && m_ref != -INFINITY;
-            const float p0 = s0 ? ex2f(fmaf(v[32 * cc + i], a.scale_log2, nm)) : 0.f;
-            const float p1 = s1 ? ex2f(fmaf(v[32 * cc + i + 1], a.scale_log2, nm)) : 0.f;
-            part += p0 + p1;
-            pk[i >> 1] = pack_bf16(p0, p1);
+            for (int cc = 0; cc < 4; ++cc) {
+              float o[32];
+              tmem_ld32(o_base + 32u * cc, o);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] *= alpha;
+              tmem_st32(o_base + 32u * cc, o);
+            }
+          }
+          if (rescale) l_sum *= alpha;
+          if (grow) m_ref = mt;
+          all_ref = __all_sync(kFull, m_ref != -INFINITY);
+        }
+        if (!p_free) {  // P buffer s free: PV of tile t-2 done
+          ok = __all_sync(kFull, wait_bar(&bs.pv_done[half][s], ((t - 2) >> 1) & 1, abort, &a.status[r]));
+          if (!ok) break;
+          p_free = true;
+        }
+        unsigned char *pb = smem + kOffP + s * kTile;
+        part = 0.f;
+        float mx[2] = {-INFINITY, -INFINITY};
+        const float nm = m_ref == -INFINITY ? 0.f : -m_ref;  // no visible key yet: all p = 0
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t pk[16];
+          if (full && m_ref != -INFINITY) {
+            float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              float t0, t1;
+              fma2(v[32 * cc + i], v[32 * cc + i + 1], a.scale_log2, nm, t0, t1);
+              const float p0 = ex2f(t0), p1 = ex2f(t1);
+              mx[cc] = max3f(mx[cc], v[32 * cc + i], v[32 * cc + i + 1]);
+              add2(s0, s1, p0, p1);
+              pk[i >> 1] = pack_bf16(p0, p1);
+            }
+            part += s0 + s1;
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              const bool s0 = ((vis[cc] >> i) & 1u) && m_ref != -INFINITY;
+              const bool s1 = ((vis[cc] >> (i + 1)) & 1u) && m_ref != -INFINITY;
+              const float p0 = s0 ? ex2f(fmaf(v[32 * cc + i], a.scale_log2, nm)) : 0.f;
+              const float p1 = s1 ? ex2f(fmaf(v[32 * cc + i + 1], a.scale_log2, nm)) : 0.f;
+              part += p0 + p1;
+              pk[i >> 1] = pack_bf16(p0, p1);
+            }
+          }
+          // columns 64 h + 32 cc ..: atom h, 16-byte chunks (4 cc + q) ^ (m % 8)
+          unsigned char *rowp = pb + half * kAtom + (m >> 3) * 1024 + (m & 7) * 128;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int ch = (cc * 4 + q) ^ (m & 7);
+            *reinterpret_cast<uint4 *>(rowp + ch * 16) =
+                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
           }
         }
-        // columns 64 h + 32 cc ..: atom h, 16-byte chunks (4 cc + q) ^ (m % 8)
-        unsigned char *rowp = pb + half * kAtom + (m >> 3) * 1024 + (m & 7) * 128;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int ch = (cc * 4 + q) ^ (m & 7);
-          *reinterpret_cast<uint4 *>(rowp + ch * 16) =
-              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        if (spec && __any_sync(kFull, fmaxf(mx[0], mx[1]) * a.scale_log2 > m_ref + kRescale)) {
+          spec = false;  // some row grows: redo the tile exactly
+          redo = true;
+          continue;
         }
+        break;
       }
+      // S_t is no longer needed: its TMEM buffer may take S_{t+2} (a failed
+      // warp releases it too, so the issuer is never left waiting on it)
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bs.s_free[half][s]);
+      if (!ok) break;
       l_sum += part;
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tc_fence_before();
-      mbar_arrive(&bs.p_full[s]);
+      mbar_arrive(&bs.p_full[half][s]);
     }
     // epilogue: the pair exchanges (reference max, sum) once -- both warps
     // always reach this barrier, a failed one with a NaN -- and each warp
@@ -506,8 +588,13 @@ __global__ void __launch_bounds__(kAT, 1)
       bool okw = ok;
       if (okw) {
         const int u = n_tiles - 1;
-        okw = __all_sync(kFull, wait_bar(&bs.pv_done[u & 1], (u >> 1) & 1, abort, &a.status[r]));
+        okw = __all_sync(kFull, wait_bar(&bs.pv_done[half][u & 1], (u >> 1) & 1, abort, &a.status[r]));
       }
+      // both halves' last PV has completed (every softmax warp passes its own
+      // wait, or fails it, before this barrier): P buffer 0 is free and O_A,
+      // O_B are final
+      tc_fence_before();
+      asm volatile("bar.sync 5, 256;" ::: "memory");
       tc_fence_after();
       // the exchange uses P buffer 0: the last PV has read it (a warp that
       // failed only writes its NaN flag)
