@@ -255,6 +255,9 @@ __global__ void __launch_bounds__(32) build_tree_kernel(TreeArgs a) {
       const bool g = key_gt(kh[s], kl[s], kt[s], bh, bl, bt);
       bh = g ? kh[s] : bh; bl = g ? kl[s] : bl; bt = g ? kt[s] : bt;
     }
+    // the next winner does not depend on the stop test: its reductions
+    // overlap the winner's rho (discarded if the build stops here)
+    warp_best(bh, bl, bt, mh, ml, mt);
     if (rho * Cp < (A_hi + A_lo) * (Cn - Cp)) break;  // S would decrease: keep T_N
 
     N = n + 1;
@@ -271,7 +274,6 @@ __global__ void __launch_bounds__(32) build_tree_kernel(TreeArgs a) {
       nd_A[n] = A_hi + A_lo;
     }
     if (lane < W) mask[n * W + lane] = mrow | (lane == (n >> 5) ? (1u << (n & 31)) : 0u);
-    warp_best(bh, bl, bt, mh, ml, mt);
   }
   __syncwarp();
 
