@@ -153,3 +153,44 @@ def test_attention_serving_size_sampled_rows(cuda_lib):
                                                        rng.integers(0, n_max, 160), rng.integers(0, Hq, 160))]
     sel += [(0, 0, h) for h in range(0, 32, 4)] + [(B - 1, n_max - 1, h) for h in range(0, 32, 4)]
     _check_rows(out, q, k, v, np.full(B, ctx, np.int32), tr, sel)
+
+
+def _to_bf16(x):
+    """float -> bf16 bits, round to nearest even (test input construction)."""
+    b = np.ascontiguousarray(x, np.float32).view(np.uint32).astype(np.uint64)
+    return ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def test_attention_late_max_jump_rescales(cuda_lib):
+    """Context keys far into the context whose scores exceed every earlier one
+    by more than 2^8 in log2 units for every row (keys 700 and 900, tiles 5 and
+    7): the tile taken against the old reference max must be redone with the
+    new one and the accumulator rescaled, twice."""
+    B, n_max, Hq, Hkv, ctx = 1, 24, 4, 1, 1000
+    tr = _trees(B, n_max, 15)
+    q, k, v = _attn_inputs(B, n_max, Hq, Hkv, ctx, 10)
+    D = q.shape[-1]
+    rng = np.random.default_rng(3)
+    u = rng.normal(size=D)
+    u /= np.linalg.norm(u)
+    qf = synth.bf16_bits_to_f32(q).astype(np.float64) + 3.0 * u   # every row shares a component on u
+    kf = synth.bf16_bits_to_f32(k).astype(np.float64)
+    kf[0, 700, 0] = 40.0 * u    # ~15 log2 units above the earlier scores
+    kf[0, 900, 0] = 80.0 * u    # ~15 more
+    q2, k2 = _to_bf16(qf), _to_bf16(kf)
+    out, st = _run(q2, k2, v, [ctx], tr.n_nodes, tr.anc_mask)
+    assert st[0] == 0
+    _check_rows(out, q2, k2, v, [ctx], tr, [(0, i, h) for i in range(int(tr.n_nodes[0])) for h in range(Hq)])
+
+
+def test_attention_context_tile_boundaries(cuda_lib):
+    """Context lengths 0, 1, 127, 128, 129 and 255 in one batch: the tree's
+    keys start inside, at and just past a 128-key tile boundary."""
+    ctxs = np.array([0, 1, 127, 128, 129, 255], np.int32)
+    B, n_max, Hq, Hkv = len(ctxs), 20, 8, 2
+    tr = _trees(B, n_max, 16)
+    q, k, v = _attn_inputs(B, n_max, Hq, Hkv, int(ctxs.max()), 11)
+    out, st = _run(q, k, v, ctxs, tr.n_nodes, tr.anc_mask)
+    assert np.all(st == 0)
+    sel = [(r, i, h) for r in range(B) for i in range(int(tr.n_nodes[r])) for h in range(Hq)]
+    _check_rows(out, q, k, v, ctxs, tr, sel)
