@@ -265,20 +265,8 @@ __global__ void __launch_bounds__(kAT, 1)
   const int qt = blockIdx.x % a.qt_max;
   const int g = (blockIdx.x / a.qt_max) % a.Hkv;
   const int r = blockIdx.x / (a.qt_max * a.Hkv);
-  const int nn = a.n_nodes[r];
-  const int ctx = a.ctx_len[r];
-  const int rows = nn * a.G;
-  if (nn < 1 || nn > a.n_max || qt * kBM >= rows) return;
   const int nodes_per_tile = kBM / a.G;
   const int i0 = qt * nodes_per_tile;
-  int64_t keys = (int64_t)ctx + nn;
-  if (ctx < 0 || keys > a.L_cap) {
-    if (tid == 0 && qt == 0 && g == 0) atomicOr(&a.status[r], BASTION_STATUS_KV_OVERFLOW);
-    keys = keys > a.L_cap ? a.L_cap : keys;
-  }
-  const int ctx_c = ctx < 0 ? 0 : ctx;
-  const int n_tiles = (int)((keys + kBN - 1) / kBN);
-
   if (tid == 0) {
     mbar_init(&bs.q_full, 1);
     for (int s = 0; s < 2; ++s) {
@@ -297,12 +285,14 @@ __global__ void __launch_bounds__(kAT, 1)
     mbar_init(&bs.mma_done[1], 1);
     bs.abort = 0;
     fence_mbar_init();
-    // Q and the first two K and V tiles start loading before the TMEM
-    // allocation and the CTA barrier; the producers continue from tile 2
+    // Q and the first two K and V tiles start loading before anything else:
+    // their coordinates depend on neither the tree's size nor the context
+    // length (a tile past the cache reads the fill value); the producers
+    // continue from tile 2
     mbar_arrive_expect_tx(&bs.q_full, kTile);
     tma_load_4d(smem + kOffQ, &tm_q, 0, g * a.G, i0, r, &bs.q_full);
     tma_load_4d(smem + kOffQ + kAtom, &tm_q, 64, g * a.G, i0, r, &bs.q_full);
-    for (int t = 0; t < n_tiles && t < 2; ++t) {
+    for (int t = 0; t < 2; ++t) {
       unsigned char *dk = smem + kOffKV + t * 2 * kTile;
       mbar_arrive_expect_tx(&bs.k_full[t], kTile);
       tma_load_4d(dk, &tm_k, 0, g, t * kBN, r, &bs.k_full[t]);
@@ -312,6 +302,27 @@ __global__ void __launch_bounds__(kAT, 1)
       tma_load_4d(dk + kTile + kAtom, &tm_v, 64, g, t * kBN, r, &bs.v_full[t]);
     }
   }
+  const int nn = a.n_nodes[r];
+  const int ctx = a.ctx_len[r];
+  const int rows = nn * a.G;
+  if (nn < 1 || nn > a.n_max || qt * kBM >= rows) {
+    if (tid == 0) {  // no rows here: the copies issued above land before the CTA leaves
+      mbar_wait_bounded(&bs.q_full, 0);
+      for (int t = 0; t < 2; ++t) {
+        mbar_wait_bounded(&bs.k_full[t], 0);
+        mbar_wait_bounded(&bs.v_full[t], 0);
+      }
+    }
+    return;
+  }
+  int64_t keys = (int64_t)ctx + nn;
+  if (ctx < 0 || keys > a.L_cap) {
+    if (tid == 0 && qt == 0 && g == 0) atomicOr(&a.status[r], BASTION_STATUS_KV_OVERFLOW);
+    keys = keys > a.L_cap ? a.L_cap : keys;
+  }
+  const int ctx_c = ctx < 0 ? 0 : ctx;
+  const int n_tiles = (int)((keys + kBN - 1) / kBN);
+
   if (warp == 2) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
                      smem_u32(&bs.tmem)));
@@ -331,7 +342,7 @@ __global__ void __launch_bounds__(kAT, 1)
       const bool is_k = warp == 0;
       uint64_t *full = is_k ? bs.k_full : bs.v_full, *empty = is_k ? bs.k_empty : bs.v_empty;
       const CUtensorMap *map = is_k ? &tm_k : &tm_v;
-      int issued = n_tiles < 2 ? n_tiles : 2;
+      int issued = 2;  // tiles 0 and 1 were issued at the start
       for (int t = 2; t < n_tiles; ++t) {
         const int s = t & 1;
         if (!wait_bar(&empty[s], ((t - 2) >> 1) & 1, abort, &a.status[r])) break;
