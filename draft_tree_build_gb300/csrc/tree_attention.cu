@@ -8,9 +8,11 @@
 // sm_103a design, one CTA per (request, KV head, 128 query rows):
 //  * the 128 rows are (tree node, query head of the KV group) pairs, so the G
 //    heads that share a KV head share every K/V tile read;
-//  * warp 0 streams Q once and the K tiles of 128 keys, warp 3 the V tiles,
-//    each through its own 2-slot ring with TMA (cp.async.bulk.tensor, 128-byte
-//    swizzle, no multicast); a K slot frees as soon as S has read it;
+//  * thread 0 issues Q and the first two K and V tiles right after the
+//    barrier initialisation, before the tree size and context length are read;
+//    then warp 0 streams the K tiles of 128 keys and warp 3 the V tiles, each
+//    through its own 2-slot ring with TMA (cp.async.bulk.tensor, 128-byte
+//    swizzle, no multicast); a slot frees once both halves' MMAs have read it;
 //  * the tile's keys are split into two halves of 64 that run as independent
 //    pipelines, each with its own online softmax, TMEM buffers and MMA
 //    issuer, so that one half's latency-bound phases (waiting for S, the TMEM
@@ -26,9 +28,12 @@
 //    row and skip it), and writes P_h as bf16 into shared memory in the MMA
 //    operand layout; O_h is rescaled only when a row's running max grows by
 //    more than 2^8 (the final normalisation uses the same reference max, so
-//    this is exact);
-//  * epilogue: the pair exchanges its (max, sum) once and writes
-//    (O_A 2^(m_A - M) + O_B 2^(m_B - M)) / l as bf16 (round to nearest even).
+//    this is exact).  Once every row has a reference, a fully visible tile is
+//    exponentiated against it directly, its max taken alongside, and redone
+//    the exact way only if some row grows;
+//  * epilogue, after both halves' last PV: the pair exchanges its (max, sum)
+//    once and writes (O_A 2^(m_A - M) + O_B 2^(m_B - M)) / l as bf16 (round to
+//    nearest even).
 // Every wait is bounded (~1 s); on a timeout the CTA flags the request, waits
 // for its own copies and MMAs (bounded), frees its TMEM and returns.
 #include <cuda.h>
