@@ -58,7 +58,7 @@ const char *bastion_status_string(int code) {
     case BASTION_ERR_DTYPE: return "unknown dtype";
     case BASTION_ERR_ALIGN: return "a pointer misses its documented alignment";
     case BASTION_ERR_WORKSPACE: return "workspace missing or too small";
-    case BASTION_ERR_UNSUPPORTED: return "valid arguments that this build does not implement";
+    case BASTION_ERR_UNSUPPORTED: return "valid arguments that the library does not support";
     case BASTION_ERR_LAUNCH: return "the CUDA launch reported an error";
     case BASTION_STATUS_NONFINITE: return "a NaN or +inf logit";
     case BASTION_STATUS_EMPTY_ROW: return "a drafter row with no finite logit";
