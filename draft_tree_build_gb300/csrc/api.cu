@@ -204,7 +204,8 @@ int bastion_tree_attention(const void *q, const void *k_cache, const void *v_cac
   if (B < 1 || n_max < 1 || n_max > 256 || Hq < 1 || Hkv < 1 || L_cap < 1 || L_cap >= (1LL << 31))
     return BASTION_ERR_SIZE;
   if (Hq % Hkv) return BASTION_ERR_SIZE;
-  if (D != 128 || Hq / Hkv > 8) return BASTION_ERR_UNSUPPORTED;
+  if (!(scale > 0.f) || !(scale < 1e30f)) return BASTION_ERR_SIZE;  // the kernel takes maxima of raw scores
+  if (D != 128 || Hq / Hkv > 8 || 128 % (Hq / Hkv)) return BASTION_ERR_UNSUPPORTED;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
       !aligned(workspace, 256))
     return BASTION_ERR_ALIGN;

@@ -161,7 +161,9 @@ int bastion_build_tree(const float *topk_logit, const int32_t *topk_tok, const d
  *          with the tree's keys/values at slots ctx_len .. ctx_len+n_nodes-1;
  *          all 16-byte aligned.
  * out      [B, n_max, Hq, D] bf16.
- * Limits: D = 128, Hq % Hkv == 0, Hq/Hkv <= 8, 1 <= n_max <= 256.
+ * scale    the softmax scale (1/sqrt(D) for standard attention): finite and
+ *          > 0, else BASTION_ERR_SIZE.
+ * Limits: D = 128, Hq % Hkv == 0, Hq/Hkv in {1, 2, 4, 8}, 1 <= n_max <= 256.
  * Workspace: bastion_tree_attention_workspace_bytes(...) bytes.
  */
 size_t bastion_tree_attention_workspace_bytes(int B, int n_max, int Hq, int Hkv, int D,

@@ -78,6 +78,13 @@ def test_host_checks_reject_before_launch(L):
     assert L.bastion_tree_attention(*base) == -6
     base[6], base[7] = 5, 128
     assert L.bastion_tree_attention(*base) == -2
+    # attention: a scale that is not finite and positive -> size; G = 3 -> unsupported
+    base[6] = 8
+    for bad in (0.0, -0.1, float("nan"), float("inf")):
+        base[12] = ctypes.c_float(bad)
+        assert L.bastion_tree_attention(*base) == -2
+    base[12], base[5], base[6] = ctypes.c_float(0.1), 24, 8
+    assert L.bastion_tree_attention(*base) == -6
     # verify: B > 4096
     assert L.bastion_verify_greedy(fake, 1, 5000, 4, 8, 8, 4, fake, fake, fake, fake, fake, fake, fake, ws, 1 << 20, fake, None) == -2
     # stochastic verify: temperature <= 0 or NaN; misaligned uniforms; null uniforms
