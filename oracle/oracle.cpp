@@ -36,6 +36,7 @@ const double kInf = std::numeric_limits<double>::infinity();
 
 double load_logit(const void* base, int dtype, int64_t idx) {
   if (dtype == 0) return (double)((const float*)base)[idx];
+  if (dtype == 2) return ((const double*)base)[idx];
   uint32_t bits = (uint32_t)((const uint16_t*)base)[idx] << 16;
   float f;
   std::memcpy(&f, &bits, 4);
@@ -65,7 +66,8 @@ enum { OR_NONFINITE = 1, OR_EMPTY_ROW = 2, OR_BAD_COST = 4 };
 // Outputs per row: the K best logits as given (topk_logit, exact), their
 // tokens, log q = l - lse rounded to float (topk_logq), and lse in fp64.
 //
-// logits: rows x V values (dtype 0 = float32, 1 = bfloat16 bits), row stride ld.
+// logits: rows x V values (dtype 0 = float32, 1 = bfloat16 bits, 2 = double),
+// row stride ld.
 int oracle_topk_marginals(const void* logits, int dtype, int rows, int V, int64_t ld, int K,
                           float* topk_logq, float* topk_logit, int32_t* topk_tok,
                           double* lse_f64, int32_t* row_status) {
@@ -537,6 +539,39 @@ int64_t oracle_tree_attention(const uint16_t* q, const uint16_t* k, const uint16
         }
   }
   return cnt;
+}
+
+// ---------------------------------------------------------------------------
+// Fused drafter LM-head + top-K.  The drafter's final hidden state h_k of block
+// position k times its output embedding W gives that position's logits,
+// l_k[v] = W[v] . h_k ("Methodologie" §1: one drafter forward pass yields the
+// position-wise marginals q_k = softmax(l_k)); the outputs are those of step 1
+// applied to l_k, without the logits ever being an input.
+//
+// hidden: rows x H, weight: V x H (dtype 0 = float32, 1 = bfloat16 bits).  The
+// logits are formed in double: each product of two bf16 or fp32 values is
+// exact, and the sum runs over i = 0 .. H-1 in order.  logits_out (optional)
+// receives them, rows x V.
+int oracle_lm_head_topk(const void* hidden, const void* weight, int dtype, int rows, int H, int V,
+                        int K, float* topk_logq, float* topk_logit, int32_t* topk_tok,
+                        double* lse_f64, double* logits_out, int32_t* row_status) {
+  if (rows < 0 || H < 1 || V < 1 || K < 1 || K > V || (dtype != 0 && dtype != 1)) return -1;
+  std::vector<double> h(H), w((size_t)V * H), l(V);
+  for (int64_t e = 0; e < (int64_t)V * H; ++e) w[e] = load_logit(weight, dtype, e);
+  for (int r = 0; r < rows; ++r) {
+    for (int i = 0; i < H; ++i) h[i] = load_logit(hidden, dtype, (int64_t)r * H + i);
+    for (int v = 0; v < V; ++v) {
+      double s = 0.0;
+      for (int i = 0; i < H; ++i) s += w[(size_t)v * H + i] * h[i];
+      l[v] = s;
+    }
+    if (logits_out) std::copy(l.begin(), l.end(), logits_out + (int64_t)r * V);
+    const int rc = oracle_topk_marginals(l.data(), 2, 1, V, V, K, topk_logq + (int64_t)r * K,
+                                         topk_logit + (int64_t)r * K, topk_tok + (int64_t)r * K,
+                                         lse_f64 + r, row_status ? row_status + r : nullptr);
+    if (rc != 0) return rc;
+  }
+  return 0;
 }
 
 }  // extern "C"

@@ -49,6 +49,8 @@ def lib():
         vp, i32, i64, dbl = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
         L.oracle_topk_marginals.argtypes = [vp, i32, i32, i32, i64, i32, vp, vp, vp, vp, vp]
         L.oracle_topk_marginals.restype = i32
+        L.oracle_lm_head_topk.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
+        L.oracle_lm_head_topk.restype = i32
         L.oracle_build_tree.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, i32, vp, i32,
                                         vp, vp, vp] + [vp] * 11 + [vp, vp, vp]
         L.oracle_build_tree.restype = i32
@@ -99,6 +101,32 @@ def topk_marginals(logits: np.ndarray, K: int) -> TopK:
     if rc != 0:
         raise ValueError("oracle_topk_marginals: bad arguments")
     return TopK(logq, logit, tok, lse, st)
+
+
+def lm_head_topk(hidden: np.ndarray, weight: np.ndarray, K: int):
+    """Fused drafter LM-head + top-K: hidden [..., H] and weight [V, H], both
+    float32 or bf16 bits (uint16).  Returns (TopK of the logits hidden . weight^T
+    formed in fp64, the logits [..., V] in fp64)."""
+    hidden = np.ascontiguousarray(hidden)
+    weight = np.ascontiguousarray(weight)
+    if hidden.dtype != weight.dtype:
+        raise TypeError("hidden and weight must share a dtype")
+    lead, H = hidden.shape[:-1], hidden.shape[-1]
+    V = weight.shape[0]
+    if weight.shape != (V, H):
+        raise ValueError("weight must be [V, H]")
+    rows = int(np.prod(lead)) if lead else 1
+    logq = np.empty(lead + (K,), np.float32)
+    logit = np.empty(lead + (K,), np.float32)
+    tok = np.empty(lead + (K,), np.int32)
+    lse = np.empty(lead, np.float64)
+    st = np.empty(lead, np.int32)
+    logits = np.empty(lead + (V,), np.float64)
+    rc = lib().oracle_lm_head_topk(_p(hidden), _p(weight), _dtype_code(hidden), rows, H, V, K,
+                                   _p(logq), _p(logit), _p(tok), _p(lse), _p(logits), _p(st))
+    if rc != 0:
+        raise ValueError("oracle_lm_head_topk: bad arguments")
+    return TopK(logq, logit, tok, lse, st), logits
 
 
 @dataclass
