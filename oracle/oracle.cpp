@@ -542,6 +542,143 @@ int64_t oracle_tree_attention(const uint16_t* q, const uint16_t* k, const uint16
 }
 
 // ---------------------------------------------------------------------------
+// Latent-mixture trees.  DBlast (the third page on this subject, "Methodologie"
+// 1, "Afhankelijke Blok-sampling via Latente Mix") replaces the factorised
+// block proposal by a mixture over a latent branch z:
+//   q_dep(x_1..b | y) = sum_z q(z|y) prod_i q_i(x_i | y, z).
+// The tree of Bastion's §1-§3 is grown on the path score this induces: the
+// mixture probability of a prefix,
+//   rho(x_1..d) = sum_z pi_z prod_{k<=d} q_k^z(x_k),   pi_z = q(z|y),
+// which is non-increasing along a path (every term is), so best-first on it
+// still yields, for every N, the prefix-closed tree of N nodes with the largest
+// sum of rho (the nodes with the N largest scores).
+//
+// Readings:
+//  * Each branch keeps its K ranked tokens per position (step 1 applied per
+//    branch); a token outside branch z's list at position k has q_k^z = 0.
+//  * The children of a depth-d node are the union over z of the branches'
+//    tokens at position d+1; depth is at most b.
+//  * Per branch, log of the path product = (sum of the path's logits in that
+//    branch) - (that branch's lse_1 + ... + lse_d), both sums in fp64 (-inf when
+//    a token is missing from the branch); log rho = log sum_z exp(log pi_z +
+//    that), taken with the largest term factored out.
+//  * Candidate order: log rho descending, then depth, token id and parent node
+//    index ascending.  The root is node 0 with rho = 1 (sum_z pi_z, the caller
+//    passes pi summing to 1) and is counted in N and A_hat; the stop rule is
+//    step 2's.
+//
+// Inputs: topk_logit/topk_tok [B, Z, b, K]; lse [B, Z, b]; pi [B, Z];
+// root_token, ctx_len [B]; cost_ms [Bc, n_max+1]; l_ar [B].  Outputs as step 2
+// without rank: n_nodes; parent, depth, pos_id, token, log_rho, a_hat,
+// speedup [B, n_max]; anc_mask [B, n_max, W]; status [B].
+int oracle_build_tree_mixture(const float* topk_logit, const int32_t* topk_tok, const double* lse,
+                              const double* pi, int B, int Z, int b, int K, int n_max,
+                              const int32_t* root_token, const int32_t* ctx_len,
+                              const float* cost_ms, int cost_per_request, const float* l_ar,
+                              int32_t* n_nodes, int32_t* parent, int32_t* depth, int32_t* pos_id,
+                              int32_t* token, double* log_rho, double* a_hat, double* speedup,
+                              uint32_t* anc_mask, int32_t* status) {
+  if (B < 0 || Z < 1 || b < 1 || K < 1 || n_max < 1) return -1;
+  const int W = (n_max + 31) / 32;
+  for (int r = 0; r < B; ++r) {
+    // branch z, position k (0-based), rank j
+    auto lg = [&](int z, int k, int j) {
+      return (double)topk_logit[(((int64_t)r * Z + z) * b + k) * K + j];
+    };
+    auto tk = [&](int z, int k, int j) { return topk_tok[(((int64_t)r * Z + z) * b + k) * K + j]; };
+    std::vector<std::vector<double>> Lam(Z, std::vector<double>(b + 1, 0.0));
+    for (int z = 0; z < Z; ++z)
+      for (int d = 1; d <= b; ++d) Lam[z][d] = Lam[z][d - 1] + lse[((int64_t)r * Z + z) * b + d - 1];
+    std::vector<double> lpi(Z);
+    for (int z = 0; z < Z; ++z) lpi[z] = std::log(pi[(int64_t)r * Z + z]);
+    // per node and branch: sum of the path's logits in that branch (-inf if absent)
+    std::vector<std::vector<double>> Ls(n_max, std::vector<double>(Z, 0.0));
+    auto log_rho_of = [&](const std::vector<double>& ls, int d) {
+      double m = -kInf;
+      std::vector<double> t(Z);
+      for (int z = 0; z < Z; ++z) {
+        t[z] = ls[z] == -kInf ? -kInf : lpi[z] + (ls[z] - Lam[z][d]);
+        if (t[z] > m) m = t[z];
+      }
+      if (m == -kInf) return -kInf;
+      double s = 0.0;
+      for (int z = 0; z < Z; ++z) s += std::exp(t[z] - m);
+      return m + std::log(s);
+    };
+    const float* C = cost_ms + (cost_per_request ? (int64_t)r * (n_max + 1) : 0);
+    const double L = (double)l_ar[r];
+    int32_t* par = parent + (int64_t)r * n_max;
+    int32_t* dep = depth + (int64_t)r * n_max;
+    int32_t* pos = pos_id + (int64_t)r * n_max;
+    int32_t* tok = token + (int64_t)r * n_max;
+    double* lr = log_rho + (int64_t)r * n_max;
+    double* ah = a_hat + (int64_t)r * n_max;
+    double* sp = speedup + (int64_t)r * n_max;
+    uint32_t* mk = anc_mask + (int64_t)r * n_max * W;
+    int st = 0;
+    for (int N = 1; N <= n_max; ++N)
+      if (!(C[N] > 0.0f) || std::isinf(C[N])) st |= OR_BAD_COST;
+    int n = 1;
+    par[0] = -1; dep[0] = 0; pos[0] = ctx_len[r]; tok[0] = root_token[r]; lr[0] = 0.0;
+    for (int w = 0; w < W; ++w) mk[w] = 0;
+    mk[0] = 1u;
+    std::vector<std::vector<int32_t>> kids(n_max);  // tokens already added under each node
+    double A = 1.0;
+    auto S_of = [&](double a, int size) { return a * L / (double)C[size]; };
+    ah[0] = A;
+    sp[0] = S_of(A, 1);
+    while (n < n_max) {
+      struct Cand { double lr; std::vector<double> ls; int d, t, p; };
+      auto better = [](const Cand& x, const Cand& y) {
+        if (x.lr != y.lr) return x.lr > y.lr;
+        if (x.d != y.d) return x.d < y.d;
+        if (x.t != y.t) return x.t < y.t;
+        return x.p < y.p;
+      };
+      std::vector<Cand> cands;
+      for (int p = 0; p < n; ++p) {
+        if (dep[p] >= b) continue;
+        const int d = dep[p] + 1;
+        std::vector<int32_t> seen;
+        for (int z = 0; z < Z; ++z)
+          for (int j = 0; j < K; ++j) {
+            const int32_t t = tk(z, d - 1, j);
+            if (std::find(seen.begin(), seen.end(), t) != seen.end()) continue;
+            seen.push_back(t);
+            if (std::find(kids[p].begin(), kids[p].end(), t) != kids[p].end()) continue;
+            std::vector<double> ls(Z);
+            for (int y = 0; y < Z; ++y) {
+              double lv = -kInf;
+              for (int i = 0; i < K; ++i)
+                if (tk(y, d - 1, i) == t) { lv = lg(y, d - 1, i); break; }
+              ls[y] = (Ls[p][y] == -kInf || lv == -kInf) ? -kInf : Ls[p][y] + lv;
+            }
+            cands.push_back({log_rho_of(ls, d), ls, d, t, p});
+          }
+      }
+      if (cands.empty()) break;
+      int best = 0;
+      for (int c = 1; c < (int)cands.size(); ++c)
+        if (better(cands[c], cands[best])) best = c;
+      const Cand& c = cands[best];
+      if (c.lr == -kInf) break;
+      const double rho = std::exp(c.lr);
+      if (S_of(A + rho, n + 1) < S_of(A, n)) break;  // S would decrease: keep T_n
+      const int i = n++;
+      kids[c.p].push_back(c.t);
+      A += rho;
+      par[i] = c.p; dep[i] = c.d; pos[i] = ctx_len[r] + c.d; tok[i] = c.t;
+      lr[i] = c.lr; Ls[i] = c.ls; ah[i] = A; sp[i] = S_of(A, n);
+      for (int w = 0; w < W; ++w) mk[(int64_t)i * W + w] = mk[(int64_t)c.p * W + w];
+      mk[(int64_t)i * W + i / 32] |= 1u << (i % 32);
+    }
+    n_nodes[r] = n;
+    if (status) status[r] = st;
+  }
+  return 0;
+}
+
+// ---------------------------------------------------------------------------
 // Fused drafter LM-head + top-K.  The drafter's final hidden state h_k of block
 // position k times its output embedding W gives that position's logits,
 // l_k[v] = W[v] . h_k ("Methodologie" §1: one drafter forward pass yields the

@@ -51,6 +51,9 @@ def lib():
         L.oracle_topk_marginals.restype = i32
         L.oracle_lm_head_topk.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
         L.oracle_lm_head_topk.restype = i32
+        L.oracle_build_tree_mixture.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp,
+                                                i32, vp] + [vp] * 10
+        L.oracle_build_tree_mixture.restype = i32
         L.oracle_build_tree.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, i32, vp, i32,
                                         vp, vp, vp] + [vp] * 11 + [vp, vp, vp]
         L.oracle_build_tree.restype = i32
@@ -101,6 +104,48 @@ def topk_marginals(logits: np.ndarray, K: int) -> TopK:
     if rc != 0:
         raise ValueError("oracle_topk_marginals: bad arguments")
     return TopK(logq, logit, tok, lse, st)
+
+
+@dataclass
+class MixTree:
+    n_nodes: np.ndarray   # int32 [B]
+    parent: np.ndarray    # int32 [B, n_max]
+    depth: np.ndarray
+    pos_id: np.ndarray
+    token: np.ndarray
+    log_rho: np.ndarray   # float64 [B, n_max]
+    a_hat: np.ndarray
+    speedup: np.ndarray
+    anc_mask: np.ndarray  # uint32 [B, n_max, W]
+    status: np.ndarray
+
+
+def build_tree_mixture(topk_logit, topk_tok, lse, pi, n_max: int, root_token, ctx_len, cost_ms,
+                       l_ar) -> MixTree:
+    """Best-first tree on the latent-mixture path score.  topk_logit/tok
+    [B, Z, b, K]; lse [B, Z, b] fp64; pi [B, Z] (rows summing to 1); cost_ms
+    [Bc, n_max+1] (Bc = 1 or B)."""
+    lg = np.ascontiguousarray(topk_logit, dtype=np.float32)
+    tk = np.ascontiguousarray(topk_tok, dtype=np.int32)
+    ls = np.ascontiguousarray(lse, dtype=np.float64)
+    pz = np.ascontiguousarray(pi, dtype=np.float64)
+    B, Z, b, K = lg.shape
+    cost = np.ascontiguousarray(cost_ms, dtype=np.float32).reshape(-1, n_max + 1)
+    W = (n_max + 31) // 32
+    out = MixTree(np.zeros(B, np.int32), np.full((B, n_max), -1, np.int32),
+                  np.zeros((B, n_max), np.int32), np.zeros((B, n_max), np.int32),
+                  np.zeros((B, n_max), np.int32), np.zeros((B, n_max)), np.zeros((B, n_max)),
+                  np.zeros((B, n_max)), np.zeros((B, n_max, W), np.uint32), np.zeros(B, np.int32))
+    rc = lib().oracle_build_tree_mixture(
+        _p(lg), _p(tk), _p(ls), _p(pz), B, Z, b, K, n_max,
+        _p(np.ascontiguousarray(root_token, dtype=np.int32)),
+        _p(np.ascontiguousarray(ctx_len, dtype=np.int32)), _p(cost), int(cost.shape[0] == B and B > 1),
+        _p(np.ascontiguousarray(l_ar, dtype=np.float32)), _p(out.n_nodes), _p(out.parent),
+        _p(out.depth), _p(out.pos_id), _p(out.token), _p(out.log_rho), _p(out.a_hat),
+        _p(out.speedup), _p(out.anc_mask), _p(out.status))
+    if rc != 0:
+        raise ValueError("oracle_build_tree_mixture: bad arguments")
+    return out
 
 
 def lm_head_topk(hidden: np.ndarray, weight: np.ndarray, K: int):
