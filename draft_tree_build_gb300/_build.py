@@ -17,7 +17,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libbastion.so")
 SOURCES = ["api.cu", "topk_marginals.cu", "build_tree.cu", "verify_greedy.cu", "tree_attention.cu",
-           "verify_noalloc.cu", "verify_sample.cu", "calibrate.cu"]
+           "verify_noalloc.cu", "verify_sample.cu", "calibrate.cu",
+           "build_tree_mixture.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

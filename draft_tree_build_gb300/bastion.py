@@ -28,7 +28,7 @@ STATUS_TIMEOUT = 1 << 30
 SYMBOLS = (
     "bastion_version", "bastion_status_string",
     "bastion_topk_marginals_workspace_bytes", "bastion_topk_marginals",
-    "bastion_build_tree",
+    "bastion_build_tree", "bastion_build_tree_mixture",
     "bastion_calibrate_cost",
     "bastion_tree_attention_workspace_bytes", "bastion_tree_attention",
     "bastion_verify_greedy_workspace_bytes", "bastion_verify_greedy",
@@ -69,6 +69,9 @@ def lib(build_if_missing: bool = True):
     L.bastion_topk_marginals.argtypes = [vp, i32, i32, i32, i32, i64, i32, vp, vp, vp, vp, vp, sz, vp, vp]
     L.bastion_build_tree.restype = i32
     L.bastion_build_tree.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, i32, vp] + [vp] * 11 + [vp]
+    L.bastion_build_tree_mixture.restype = i32
+    L.bastion_build_tree_mixture.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, i32,
+                                             vp] + [vp] * 10 + [vp]
     L.bastion_calibrate_cost.restype = i32
     L.bastion_calibrate_cost.argtypes = [vp, vp, i32] + [ctypes.c_double] * 7 + [i32, vp, vp, vp, vp]
     L.bastion_tree_attention_workspace_bytes.restype = sz
@@ -167,6 +170,23 @@ def bastion_build_tree(topk_logit, topk_tok, lse, n_max, root_token, ctx_len, co
                                   _p(n_nodes), _p(parent), _p(depth), _p(pos_id), _p(token), _p(rank),
                                   _p(log_rho), _p(a_hat), _p(speedup), _p(anc_mask), _p(status), _s(stream))
     _check(rc, "bastion_build_tree")
+
+
+def bastion_build_tree_mixture(topk_logit, topk_tok, lse, pi, n_max, root_token, ctx_len, cost_ms, l_ar,
+                               n_nodes, parent, depth, pos_id, token, log_rho, a_hat, speedup, anc_mask,
+                               status, stream=None):
+    """topk_logit/tok [B, Z, b, K], lse [B, Z, b] float64, pi [B, Z] float64 (contiguous)."""
+    B, Z, b, K = topk_logit.shape
+    for t in (topk_logit, topk_tok, lse, pi):
+        if not t.is_contiguous():
+            raise BastionError("mixture tree inputs must be contiguous")
+    per_req = 1 if (cost_ms.dim() == 2 and cost_ms.shape[0] == B and B > 1) else 0
+    rc = lib().bastion_build_tree_mixture(_p(topk_logit), _p(topk_tok), _p(lse), _p(pi), B, Z, b, K,
+                                          int(n_max), _p(root_token), _p(ctx_len), _p(cost_ms), per_req,
+                                          _p(l_ar), _p(n_nodes), _p(parent), _p(depth), _p(pos_id),
+                                          _p(token), _p(log_rho), _p(a_hat), _p(speedup), _p(anc_mask),
+                                          _p(status), _s(stream))
+    _check(rc, "bastion_build_tree_mixture")
 
 
 def bastion_calibrate_cost(sample_n, sample_ms, roofline: dict, t_draft, n_max, cost_ms, params, status,

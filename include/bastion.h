@@ -147,6 +147,36 @@ int bastion_build_tree(const float *topk_logit, const int32_t *topk_tok, const d
                        bastion_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Best-first draft tree on a latent-mixture proposal (DBlast, "Methodologie" 1:
+ * q_dep(x_1..b | y) = sum_z q(z|y) prod_i q_i(x_i | y, z), grown with Bastion's
+ * §1-§3 controller).  The prefix score is the mixture probability
+ * rho(x_1..d) = sum_z pi_z prod_{k<=d} q_k^z(x_k); a token outside branch z's
+ * list at position k has q_k^z = 0; the children of a depth-d node are the
+ * union over z of the branches' tokens at position d+1.  Candidates are
+ * ordered by log rho (descending), then depth, token id and parent index
+ * (ascending); the stop rule is bastion_build_tree's.  Scores are fp64
+ * throughout (a parity form: one warp per request, no fixed-point tie rule).
+ *
+ * topk_logit, topk_tok [B, Z, b, K], lse [B, Z, b] (8-byte aligned): step 1
+ *            run per branch.  pi [B, Z] double (8-byte aligned), each row the
+ *            branch weights q(z|y), summing to 1.
+ * root_token, ctx_len, cost_ms, cost_per_request, l_ar: as bastion_build_tree.
+ * Outputs:   as bastion_build_tree without rank: n_nodes [B]; parent, depth,
+ *            pos_id, token, log_rho, a_hat, speedup [B, n_max];
+ *            anc_mask [B, n_max, ceil(n_max/32)].
+ * Limits: 1 <= Z <= 8, 1 <= K <= 64, Z*K <= 256, 1 <= b <= 32,
+ * 1 <= n_max <= 256 (BASTION_ERR_SIZE otherwise); the per-request tables must
+ * fit in 227 KB of shared memory (BASTION_ERR_UNSUPPORTED otherwise).
+ */
+int bastion_build_tree_mixture(const float *topk_logit, const int32_t *topk_tok, const double *lse,
+                               const double *pi, int B, int Z, int b, int K, int n_max,
+                               const int32_t *root_token, const int32_t *ctx_len,
+                               const float *cost_ms, int cost_per_request, const float *l_ar,
+                               int32_t *n_nodes, int32_t *parent, int32_t *depth, int32_t *pos_id,
+                               int32_t *token, float *log_rho, float *a_hat, float *speedup,
+                               uint32_t *anc_mask, int32_t *status, bastion_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Tree-masked GQA attention of the tree's query tokens against the KV cache
  * (the target's parallel verification pass over the whole tree,
  * "Probleemstelling" and Methodologie §2).

@@ -42,7 +42,7 @@ def _header_arg_counts():
 
 def test_binding_argtypes_match_header(L):
     counts = _header_arg_counts()
-    assert len(counts) == 13
+    assert len(counts) == 14
     for name, n in counts.items():
         assert len(getattr(L, name).argtypes) == n, name
 
@@ -85,6 +85,20 @@ def test_host_checks_reject_before_launch(L):
         assert L.bastion_tree_attention(*base) == -2
     base[12], base[5], base[6] = ctypes.c_float(0.1), 24, 8
     assert L.bastion_tree_attention(*base) == -6
+    # mixture tree: Z > 8, Z * K > 256, K > 64; misaligned pi; null pi
+    mx = [fake] * 4 + [1, 9, 4, 8, 16] + [fake] * 3 + [0, fake] + [fake] * 10 + [None]
+    assert L.bastion_build_tree_mixture(*mx) == -2
+    mx[5], mx[7] = 5, 64
+    assert L.bastion_build_tree_mixture(*mx) == -2
+    mx[5], mx[7] = 1, 65
+    assert L.bastion_build_tree_mixture(*mx) == -2
+    mx[7], mx[3] = 8, vp(0x10004)
+    assert L.bastion_build_tree_mixture(*mx) == -4
+    mx[3] = None
+    assert L.bastion_build_tree_mixture(*mx) == -1
+    # mixture tree: tables larger than shared memory -> unsupported
+    mx[3], mx[5], mx[6], mx[7], mx[8] = fake, 8, 32, 32, 256
+    assert L.bastion_build_tree_mixture(*mx) == -6
     # verify: B > 4096
     assert L.bastion_verify_greedy(fake, 1, 5000, 4, 8, 8, 4, fake, fake, fake, fake, fake, fake, fake, ws, 1 << 20, fake, None) == -2
     # stochastic verify: temperature <= 0 or NaN; misaligned uniforms; null uniforms
