@@ -50,7 +50,10 @@ void *scratch_for_current_device() {
   std::lock_guard<std::mutex> lock(g_mutex);
   if (!g_scratch_addr[dev]) {
     void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_verify_scratch) != cudaSuccess || p == nullptr) return nullptr;
+    if (cudaGetSymbolAddress(&p, g_verify_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();  // consume the error: it must not be reported by a later call
+      return nullptr;
+    }
     g_scratch_addr[dev] = p;
   }
   return g_scratch_addr[dev];
@@ -82,8 +85,10 @@ extern "C" int bastion_verify_greedy_noalloc(const void *target_logits, int dtyp
   if (!scratch) return BASTION_ERR_LAUNCH;
   // The array keeps whatever the previous call left; the keys this call uses
   // must start at zero.
-  if (cudaMemsetAsync(scratch, 0, need, (cudaStream_t)stream) != cudaSuccess)
+  if (cudaMemsetAsync(scratch, 0, need, (cudaStream_t)stream) != cudaSuccess) {
+    cudaGetLastError();  // consume the error: it must not be reported by a later call
     return BASTION_ERR_LAUNCH;
+  }
   return bastion::launch_verify(target_logits, dtype, B, n_max, V, ld_row, b, n_nodes, parent,
                                 token, argmax, accept_len, accept_nodes, out_tokens, scratch,
                                 status, (cudaStream_t)stream);

@@ -2,8 +2,9 @@
 allocate device memory (it uses a fixed scratch array inside the library).
 
 Called through the C ABI twice in a row on different inputs; each result must
-equal what the workspace-taking entry point returns for the same inputs
-(integers, so exactly).  This file is named to be collected last.
+equal what the workspace-taking entry point returns for the same inputs, and
+what the CPU oracle returns (integers, so exactly).  This file is named to be
+collected last.
 """
 import ctypes
 
@@ -25,7 +26,8 @@ def _inputs(cid, **over):
     roots, ctx, cost, lar = workload_inputs(w)
     tr = oracle.build_tree(tk.logit, tk.tok, tk.lse, w.n_max, roots, ctx, cost, lar)
     tgt, _ = synth.target_logits(w, tr.n_nodes, tr.depth, tk.tok)
-    return w, tr, tgt
+    vf = oracle.verify_greedy(tgt, w.b, tr.n_nodes, tr.parent, tr.token)
+    return w, tr, tgt, vf
 
 
 def _noalloc(L, td, b, nn, pa, tk):
@@ -48,7 +50,7 @@ def _noalloc(L, td, b, nn, pa, tk):
 def test_noalloc_matches_workspace_entry_point_twice(cuda_lib):
     L = cuda_lib.lib()
     cases = [_inputs(3), _inputs(1), _inputs(2, B=3, seed=99)]
-    for w, tr, tgt in cases:
+    for w, tr, tgt, vf in cases:
         td = to_dev(tgt)
         nn, pa, tk = (to_dev(np.ascontiguousarray(a, np.int32)) for a in (tr.n_nodes, tr.parent, tr.token))
         ref, st_ref = gpu_verify(None, w.b, nn, pa, tk, target_dev=td)
@@ -57,9 +59,14 @@ def test_noalloc_matches_workspace_entry_point_twice(cuda_lib):
         for i in range(w.B):
             n = int(tr.n_nodes[i])
             assert np.array_equal(host(got[0])[i, :n], host(ref.argmax)[i, :n])
+            assert np.array_equal(host(got[0])[i, :n], vf.argmax[i, :n])
         assert np.array_equal(host(got[1]), host(ref.accept_len))
         assert np.array_equal(host(got[2]), host(ref.accept_nodes))
         assert np.array_equal(host(got[3]), host(ref.out_tokens))
+        # and the CPU oracle's walk
+        assert np.array_equal(host(got[1]), vf.accept_len)
+        assert np.array_equal(host(got[2]), vf.accept_nodes)
+        assert np.array_equal(host(got[3]), vf.out_tokens)
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(cuda_lib):
