@@ -22,6 +22,7 @@ STATUS_EMPTY_ROW = 2
 STATUS_BAD_COST = 4
 STATUS_KV_OVERFLOW = 8
 STATUS_BAD_TREE = 16
+STATUS_BAD_WEIGHT = 32
 STATUS_TIMEOUT = 1 << 30
 
 # the exported C symbols, in header order
@@ -180,6 +181,15 @@ def bastion_build_tree_mixture(topk_logit, topk_tok, lse, pi, n_max, root_token,
     for t in (topk_logit, topk_tok, lse, pi):
         if not t.is_contiguous():
             raise BastionError("mixture tree inputs must be contiguous")
+    # the library reads these bytes as the stated types; a wrong dtype would be read as garbage
+    for name, t, dt in (("topk_logit", topk_logit, torch.float32), ("topk_tok", topk_tok, torch.int32),
+                        ("lse", lse, torch.float64), ("pi", pi, torch.float64)):
+        if t.dtype != dt:
+            raise BastionError(f"mixture tree: {name} must be {dt}, got {t.dtype}")
+    if tuple(topk_tok.shape) != (B, Z, b, K) or tuple(lse.shape) != (B, Z, b) or tuple(pi.shape) != (B, Z):
+        raise BastionError("mixture tree: topk_tok [B,Z,b,K], lse [B,Z,b] and pi [B,Z] must match topk_logit")
+    if cost_ms.numel() not in (n_max + 1, B * (n_max + 1)):
+        raise BastionError("mixture tree: cost_ms must hold n_max + 1 entries, or n_max + 1 per request")
     per_req = 1 if (cost_ms.dim() == 2 and cost_ms.shape[0] == B and B > 1) else 0
     rc = lib().bastion_build_tree_mixture(_p(topk_logit), _p(topk_tok), _p(lse), _p(pi), B, Z, b, K,
                                           int(n_max), _p(root_token), _p(ctx_len), _p(cost_ms), per_req,

@@ -73,6 +73,7 @@ const char *bastion_status_string(int code) {
     case BASTION_STATUS_BAD_COST: return "a cost C(N) that is not positive and finite";
     case BASTION_STATUS_KV_OVERFLOW: return "ctx_len + n_nodes exceeds the KV cache capacity";
     case BASTION_STATUS_BAD_TREE: return "n_nodes outside [1, n_max]";
+    case BASTION_STATUS_BAD_WEIGHT: return "a mixture weight is negative or not finite";
     case BASTION_STATUS_TIMEOUT: return "a bounded device wait ran out";
     default: return "unknown code";
   }

@@ -141,7 +141,9 @@ __global__ void __launch_bounds__(32) build_tree_mixture_kernel(MixArgs a) {
       s += lse_r[(size_t)lane * b + d - 1];
       Lam[lane * (b + 1) + d] = s;
     }
-    lpi[lane] = log(a.pi[(size_t)r * Z + lane]);
+    const double w = a.pi[(size_t)r * Z + lane];
+    lpi[lane] = log(w);
+    if (!(w >= 0.0) || isinf(w)) atomicOr(&a.status[r], BASTION_STATUS_BAD_WEIGHT);
   }
   const float *cr = a.cost + (a.cost_per_request ? (size_t)r * (n_max + 1) : 0);
   bool bad = false;
@@ -293,7 +295,9 @@ __global__ void __launch_bounds__(32) build_tree_mixture_kernel(MixArgs a) {
       bt = take ? t2 : bt;
       bn = take ? n2 : bn;
     }
-    if (bn < 0 || bs == kNegInf) break;  // no candidate, or the best has rho = 0
+    // no candidate, or the best has rho = 0 (a NaN score, from a bad weight,
+    // counts as rho = 0 too)
+    if (bn < 0 || !(bs > kNegInf)) break;
     const double rho = exp(bs);
     if ((A + rho) * Lar / (double)C[N + 1] < A * Lar / (double)C[N]) break;  // S would decrease
     const int p = bn, i = N, u = pu[p], dp = dep[p];

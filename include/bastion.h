@@ -64,6 +64,7 @@ enum {
   BASTION_STATUS_BAD_COST = 4,     /* some C(N) <= 0 or not finite */
   BASTION_STATUS_KV_OVERFLOW = 8,  /* ctx_len + n_nodes > L_cap, or ctx_len < 0 */
   BASTION_STATUS_BAD_TREE = 16,    /* n_nodes outside [1, n_max] */
+  BASTION_STATUS_BAD_WEIGHT = 32,  /* a mixture weight pi is negative or not finite */
   BASTION_STATUS_TIMEOUT = 1 << 30 /* a bounded device wait ran out */
 };
 
@@ -159,7 +160,9 @@ int bastion_build_tree(const float *topk_logit, const int32_t *topk_tok, const d
  *
  * topk_logit, topk_tok [B, Z, b, K], lse [B, Z, b] (8-byte aligned): step 1
  *            run per branch.  pi [B, Z] double (8-byte aligned), each row the
- *            branch weights q(z|y), summing to 1.
+ *            branch weights q(z|y), summing to 1.  A weight that is negative,
+ *            NaN or infinite sets BASTION_STATUS_BAD_WEIGHT in status[r], and
+ *            that request's outputs are undefined.
  * root_token, ctx_len, cost_ms, cost_per_request, l_ar: as bastion_build_tree.
  * Outputs:   as bastion_build_tree without rank: n_nodes [B]; parent, depth,
  *            pos_id, token, log_rho, a_hat, speedup [B, n_max];

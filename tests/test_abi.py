@@ -49,7 +49,7 @@ def test_binding_argtypes_match_header(L):
 
 def test_version_and_strings(L):
     assert L.bastion_version().startswith(b"bastion-gb300")
-    for code in (0, -1, -2, -3, -4, -5, -6, -7, 1, 2, 4, 8, 16, 1 << 30):
+    for code in (0, -1, -2, -3, -4, -5, -6, -7, 1, 2, 4, 8, 16, 32, 1 << 30):
         assert L.bastion_status_string(code) != b"unknown code"
 
 
@@ -131,3 +131,30 @@ def test_workspace_queries(L):
     assert L.bastion_verify_sample_workspace_bytes(32, 128, 151936) >= 32 * 128 * (8 + 75 * 16)
     assert L.bastion_verify_sample_workspace_bytes(1, 257, 8) == 0
     assert L.bastion_tree_attention_workspace_bytes(8, 64, 32, 8, 128, 4160) > 0
+
+
+def test_mixture_binding_rejects_wrong_dtypes_and_shapes(L):
+    """The binding checks dtypes and shapes before the library reads the bytes
+    (CPU tensors: the check fails before any pointer is passed)."""
+    import torch
+    from draft_tree_build_gb300 import bastion
+    B, Z, b, K, n_max = 2, 3, 4, 8, 16
+    lg = torch.zeros(B, Z, b, K)
+    tk = torch.zeros(B, Z, b, K, dtype=torch.int32)
+    ls = torch.zeros(B, Z, b, dtype=torch.float64)
+    pi = torch.full((B, Z), 1.0 / Z, dtype=torch.float64)
+    i32 = lambda *s: torch.zeros(*s, dtype=torch.int32)  # noqa: E731
+    f32 = lambda *s: torch.zeros(*s)  # noqa: E731
+    rest = (n_max, i32(B), i32(B), f32(1, n_max + 1), f32(B), i32(B), i32(B, n_max), i32(B, n_max),
+            i32(B, n_max), i32(B, n_max), f32(B, n_max), f32(B, n_max), f32(B, n_max),
+            i32(B, n_max, 1), i32(B))
+    with pytest.raises(bastion.BastionError, match="lse"):
+        bastion.bastion_build_tree_mixture(lg, tk, ls.float(), pi, *rest)
+    with pytest.raises(bastion.BastionError, match="pi"):
+        bastion.bastion_build_tree_mixture(lg, tk, ls, pi.float(), *rest)
+    with pytest.raises(bastion.BastionError, match="topk_tok"):
+        bastion.bastion_build_tree_mixture(lg, tk.long(), ls, pi, *rest)
+    with pytest.raises(bastion.BastionError, match="must match"):
+        bastion.bastion_build_tree_mixture(lg, tk, ls[:, :, :2].contiguous(), pi, *rest)
+    with pytest.raises(bastion.BastionError, match="cost_ms"):
+        bastion.bastion_build_tree_mixture(lg, tk, ls, pi, n_max, i32(B), i32(B), f32(1, n_max), *rest[4:])

@@ -90,3 +90,21 @@ def test_mixture_tree_zero_weight_branch_and_bad_cost(cuda_lib):
     c[0, 7] = 0.0
     _, st = _gpu(lg, tk, ls, pi, n_max, roots, ctx, c, lar)
     assert np.all(st & bastion.STATUS_BAD_COST)
+
+
+def test_mixture_tree_bad_weight_sets_status(cuda_lib):
+    """A negative or NaN branch weight sets the weight status bit on that
+    request only; the others are built as the oracle builds them."""
+    from draft_tree_build_gb300 import bastion
+    B, Z, b, V, K, n_max = 3, 2, 5, 300, 8, 24
+    lg, tk, ls = _branch_topk(B, Z, b, V, K, 21)
+    pi = np.array([[0.5, 0.5], [-0.25, 1.25], [np.nan, 1.0]])
+    roots, ctx, lar = np.zeros(B, np.int32), np.zeros(B, np.int32), np.full(B, 18.0, np.float32)
+    c = np.full((1, n_max + 1), 5.0, np.float32)
+    g, st = _gpu(lg, tk, ls, pi, n_max, roots, ctx, c, lar)
+    assert st[0] == 0
+    assert st[1] & bastion.STATUS_BAD_WEIGHT and st[2] & bastion.STATUS_BAD_WEIGHT
+    ref = oracle.build_tree_mixture(lg[:1], tk[:1], ls[:1], pi[:1], n_max, roots[:1], ctx[:1], c, lar[:1])
+    assert int(g["n_nodes"][0]) == int(ref.n_nodes[0])
+    n = int(ref.n_nodes[0])
+    assert np.array_equal(g["token"][0, :n], ref.token[0, :n])
