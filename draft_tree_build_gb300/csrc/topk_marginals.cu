@@ -427,7 +427,11 @@ __global__ void __launch_bounds__(kT, 5) topk_cluster_kernel(TopkArgs a) {
     xtok = (uint32_t)(s.e0 + e);
   }
   // one thread waits for the copy; the barrier releases the rest
-  if (tid == 0 && s.body && !mbar_wait_bounded(bar, 0)) atomicOr(&a.status[req], BASTION_STATUS_TIMEOUT);
+  bool body_ok = true;
+  if (tid == 0 && s.body) {
+    body_ok = mbar_wait_bounded(bar, 0);
+    if (!body_ok) atomicOr(&a.status[req], BASTION_STATUS_TIMEOUT);
+  }
   __syncthreads();
 
   // ---- pass A: vector maxima and the thread max into the leader's table
@@ -475,7 +479,8 @@ __global__ void __launch_bounds__(kT, 5) topk_cluster_kernel(TopkArgs a) {
     sum *= ex2(-c_err);
     if (has_x) sum += exp_shifted(xs - tmax);
   }
-  if (!mbar_wait_bounded(tab_bar, 0) && lane == 0) atomicOr(&a.status[req], BASTION_STATUS_TIMEOUT);
+  const bool tab_ok = mbar_wait_bounded(tab_bar, 0);
+  if (!tab_ok && lane == 0) atomicOr(&a.status[req], BASTION_STATUS_TIMEOUT);
 
   // ---- the row threshold: the K-th largest prefix of the table, counted by
   // its distance below the largest one (256 bins: 0..254 steps, then "more")
@@ -577,10 +582,18 @@ __global__ void __launch_bounds__(kT, 5) topk_cluster_kernel(TopkArgs a) {
       st_async_v4(dsmem_addr(&sc.part[rank], 0), __float_as_uint(Mc), __float_as_uint(acc.x),
                   __float_as_uint(acc.y), nl, rb);
   }
-  if (rank != 0) return;  // nothing reads or writes a non-leader's shared memory now
+  if (rank != 0) {
+    // Nothing reads or writes a non-leader's shared memory now, unless a wait
+    // above ran out: then its own bulk copy or another CTA's prefixes may
+    // still be landing, and the CTA waits for them (bounded) before it leaves.
+    if (!tab_ok) mbar_wait_bounded(tab_bar, 0);
+    if (!body_ok) mbar_wait_bounded(bar, 0);
+    return;
+  }
 
   // ---- leader: the row's keys, their ranks, and lse (last warp) meanwhile
-  if (!mbar_wait_bounded(row_bar, 0) && lane == 0) atomicOr(&a.status[req], BASTION_STATUS_TIMEOUT);
+  const bool row_ok = mbar_wait_bounded(row_bar, 0);
+  if (!row_ok && lane == 0) atomicOr(&a.status[req], BASTION_STATUS_TIMEOUT);
   uint64_t *list = reinterpret_cast<uint64_t *>(body);  // this CTA's slice is spent
   if (tid == 0) {
     int o = 0, over = 0;
@@ -609,6 +622,11 @@ __global__ void __launch_bounds__(kT, 5) topk_cluster_kernel(TopkArgs a) {
   rank_keys(a, row, list, n, rk);
   __syncthreads();
   write_logq(a, row, list, n, rk, sc.lse);
+  // after a wait that ran out, stores or copies into this CTA may still be in
+  // flight: wait for them (bounded) before leaving
+  if (!row_ok) mbar_wait_bounded(row_bar, 0);
+  if (!tab_ok) mbar_wait_bounded(tab_bar, 0);
+  if (!body_ok) mbar_wait_bounded(bar, 0);
 }
 
 // Rows too wide for the cluster path: one CTA per row, exact selection over
