@@ -1,6 +1,8 @@
 """GPU parity: tree-masked GQA attention (tcgen05 kernel, C ABI) against the
 fp64 oracle; bf16 output within 2e-2 absolute.  Rows past n_nodes untouched."""
 import math
+import os
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 import pytest
@@ -46,10 +48,24 @@ def _trees(B, n_max, seed, flat=True):
                              np.zeros(B, np.int32), cost, np.full(B, 18.0, np.float32))
 
 
-def _check_rows(out, q, k, v, ctx, tr, sel):
+def _oracle_rows(q, k, v, ctx, tr, sel):
+    """The oracle's rows for sel, split over host threads (the oracle is a C
+    function called through ctypes, which releases the GIL while it runs)."""
     D = q.shape[-1]
-    ref = oracle.tree_attention(q, k, v, ctx, tr.n_nodes, tr.anc_mask, 1 / math.sqrt(D), sel=sel)
-    got = np.stack([out[r, i, h] for r, i, h in sel])
+    sel = np.ascontiguousarray(sel, np.int32).reshape(-1, 3)
+    nt = max(1, min(len(sel) // 256, os.cpu_count() or 1))
+    run = lambda s: oracle.tree_attention(q, k, v, ctx, tr.n_nodes, tr.anc_mask,  # noqa: E731
+                                          1 / math.sqrt(D), sel=s)
+    if nt == 1:
+        return run(sel)
+    with ThreadPoolExecutor(nt) as ex:
+        return np.concatenate(list(ex.map(run, np.array_split(sel, nt))))
+
+
+def _check_rows(out, q, k, v, ctx, tr, sel):
+    ref = _oracle_rows(q, k, v, ctx, tr, sel)
+    sel = np.asarray(sel).reshape(-1, 3)
+    got = out[sel[:, 0], sel[:, 1], sel[:, 2]]
     err = np.abs(got - ref).max()
     assert err < TOL, err
 
@@ -116,10 +132,8 @@ def test_attention_full_size_qwen3_layer(cuda_lib):
     q, k, v = synth.attention_inputs(w)
     out, st = _run(q, k, v, ctx, tr.n_nodes, tr.anc_mask)
     assert np.all(st == 0)
-    rng = np.random.default_rng(1)
-    sel = [(int(r), int(i), int(h)) for r, i, h in zip(rng.integers(0, w.B, 200),
-                                                       rng.integers(0, 64, 200), rng.integers(0, 32, 200))]
-    sel += [(0, 0, h) for h in range(32)] + [(7, 63, h) for h in range(32)]
+    # every (request, node, head) row: 128 CTAs of 33 key tiles each
+    sel = [(r, i, h) for r in range(w.B) for i in range(64) for h in range(32)]
     _check_rows(out, q, k, v, ctx, tr, sel)
 
 
@@ -134,7 +148,8 @@ def test_attention_kv_overflow_flag(cuda_lib):
 
 def test_attention_serving_size_sampled_rows(cuda_lib):
     """The serving step's attention shape: 64 requests, 256-node trees, 32/8
-    heads, d=128, a 16,384-token context; sampled rows against the oracle.
+    heads, d=128, a 16,384-token context; sampled rows and every row of one
+    request against the oracle.
     The trees come from the oracle (a small-vocabulary drafter, flat cost)."""
     B, n_max, Hq, Hkv, ctx = 64, 256, 32, 8, 16384
     w = synth.Workload(94, "trees", B=B, b=16, V=1024, K=64, n_max=n_max, dtype="bf16", l_ar_ms=15.0,
@@ -152,6 +167,9 @@ def test_attention_serving_size_sampled_rows(cuda_lib):
     sel = [(int(r), int(i), int(h)) for r, i, h in zip(rng.integers(0, B, 160),
                                                        rng.integers(0, n_max, 160), rng.integers(0, Hq, 160))]
     sel += [(0, 0, h) for h in range(0, 32, 4)] + [(B - 1, n_max - 1, h) for h in range(0, 32, 4)]
+    # and every (node, head) row of one whole request (the CTAs of its 8 KV heads)
+    rw = 37
+    sel += [(rw, i, h) for i in range(n_max) for h in range(Hq)]
     _check_rows(out, q, k, v, np.full(B, ctx, np.int32), tr, sel)
 
 
