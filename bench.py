@@ -157,7 +157,15 @@ def pinned_from(arr: np.ndarray):
 
 # --------------------------------------------------------------------------- our arm
 
-def run_ours(args, ws, rank, local):
+def step_config(w, mean_nodes: float, ws: int) -> dict:
+    """The config dict of a tree-step line (both arms print the same one)."""
+    return {"workload": w.name, "B": w.B, "b": w.b, "V": w.V, "K": w.K, "n_max": w.n_max,
+            "logit_dtype": w.dtype, "seed": w.seed, "mean_tree_nodes": mean_nodes,
+            "l2": "inputs larger than L2, two rotating device copies",
+            "parallelism": f"replicas x{ws}"}
+
+
+def run_ours(args, ws, rank, local, light=False):
     import torch
 
     import synth
@@ -269,6 +277,22 @@ def run_ours(args, ws, rank, local):
     k2 = statistics.mean(evs[p][1].elapsed_time(evs[p][2]) for p in range(P))
     k4 = statistics.mean(evs[p][2].elapsed_time(evs[p][3]) for p in range(P))
     assert int(step.status.abs().sum()) == 0, "device status bits set"
+    hbm, peak_kind = peaks()
+    ms_step = elapsed_ms / args.steps
+    vname = "verify_sample" if sampled else "verify_greedy"
+    kern = {"topk_marginals": {"ms": k1, "bytes": bytes_k1, "gbs": bytes_k1 / (k1 * 1e-3) / 1e9},
+            "build_tree": {"ms": k2, "bytes": w.B * w.b * w.K * 16},
+            vname: {"ms": k4, "bytes": bytes_k4, "gbs": bytes_k4 / (k4 * 1e-3) / 1e9}}
+    dom = max(("topk_marginals", vname), key=lambda k: kern[k]["ms"])
+    if light:  # one line of the workloads table: no end-to-end leg
+        ach = kern[dom]["gbs"]
+        return {"workload": w.name, "value": aggregate_rate(args.steps, elapsed_ms, ws), "unit": UNIT,
+                "steps": args.steps, "ms_per_step": ms_step, "mean_tree_nodes": float(n_nodes.mean()),
+                "roofline": {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": hbm, "unit": "GB/s",
+                             "frac": ach / hbm, "peak_source": f"{peak_kind} copy bandwidth",
+                             "step_frac": bytes_step / (ms_step * 1e-3) / 1e9 / hbm,
+                             "bytes_per_step": bytes_step},
+                "kernels": kern, "clocks": clk}
 
     # end to end through the public API with host buffers (pinned), per step:
     # H2D of the drafter logits; the tree; D2H of its sizes; H2D of the target
@@ -307,8 +331,6 @@ def run_ours(args, ws, rank, local):
     h2d = x_pin.numel() * x_pin.element_size() + int(n_nodes.sum()) * w.V * es
     d2h = out_host.numel() * 4 + acc_host.numel() * 4 + nn_host.numel() * 4
 
-    hbm, peak_kind = peaks()
-    ms_step = elapsed_ms / args.steps
     # the cost model's calibration on the device (1,024 observed samples), timed alone
     cal_n = torch.from_numpy(np.linspace(1, w.n_max, 1024).astype(np.float32)).to(dev)
     cal_t = torch.from_numpy((2.0 + 0.01 * np.linspace(1, w.n_max, 1024)).astype(np.float32)).to(dev)
@@ -327,12 +349,7 @@ def run_ours(args, ws, rank, local):
     k_cal = c0.elapsed_time(c1) / P
     assert int(cal_s.item()) == 0
 
-    vname = "verify_sample" if sampled else "verify_greedy"
-    kern = {"topk_marginals": {"ms": k1, "bytes": bytes_k1, "gbs": bytes_k1 / (k1 * 1e-3) / 1e9},
-            "build_tree": {"ms": k2, "bytes": w.B * w.b * w.K * 16},
-            vname: {"ms": k4, "bytes": bytes_k4, "gbs": bytes_k4 / (k4 * 1e-3) / 1e9},
-            "calibrate_cost": {"ms": k_cal, "samples": 1024, "note": "outside the step"}}
-    dom = max(("topk_marginals", vname), key=lambda k: kern[k]["ms"])
+    kern["calibrate_cost"] = {"ms": k_cal, "samples": 1024, "note": "outside the step"}
     ach = kern[dom]["gbs"]
     res = {
         "metric": (METRIC if not sampled else
@@ -341,10 +358,7 @@ def run_ours(args, ws, rank, local):
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "b": w.b, "V": w.V, "K": w.K, "n_max": w.n_max,
-                   "logit_dtype": w.dtype, "seed": w.seed, "mean_tree_nodes": float(n_nodes.mean()),
-                   "l2": "inputs larger than L2, two rotating device copies",
-                   "parallelism": f"replicas x{ws}"},
+        "config": step_config(w, float(n_nodes.mean()), ws),
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": hbm, "unit": "GB/s",
                      "frac": ach / hbm, "peak_source": f"{peak_kind} copy bandwidth",
                      "traffic": (profiled_traffic(*{"topk_marginals": ("topk_marginals_b32_v151936.md",
@@ -366,7 +380,7 @@ def run_ours(args, ws, rank, local):
     return res
 
 
-def run_with_attention(args, ws, rank, local):
+def run_with_attention(args, ws, rank, local, light=False):
     """Workload 4: one tree-masked GQA attention call per step (8 requests, 32/8
     heads, d 128, ctx 4096, trees of 64 nodes).  Workload 5: the full serving
     step, top-K + tree + attention + verify (64 requests, vocab 128,256, trees of
@@ -485,7 +499,12 @@ def run_with_attention(args, ws, rank, local):
 
     hbm, peak_kind = peaks()
     pk = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if peak_kind == "measured" else {}
-    tf_peak = float(pk.get("bf16_tflops", 1900.0))
+    # a kernel of milliseconds launched back to back runs under the power cap:
+    # the sustained figure; a short one, timed alone: the burst figure
+    long_kernel = t_attn >= 1.0
+    tf_peak = float(pk.get("bf16_tflops_sustained" if long_kernel else "bf16_tflops",
+                           1700.0 if long_kernel else 1900.0))
+    tf_kind = f"{peak_kind} bf16 ({'sustained' if long_kernel else 'burst'})"
     G = w.Hq // w.Hkv
     vis_pairs = 0  # visible (query row, key) pairs per KV head: context + own root path
     for r in range(w.B):
@@ -503,7 +522,7 @@ def run_with_attention(args, ws, rank, local):
                 "peak": hbm, "unit": "GB/s", "peak_source": f"{peak_kind} copy bandwidth"}
     else:
         roof = {"bound": "tensor", "kernel": "tree_attention", "achieved": flops / (t_attn * 1e-3) / 1e12,
-                "peak": tf_peak, "unit": "TFLOP/s", "peak_source": f"{peak_kind} bf16 (burst)"}
+                "peak": tf_peak, "unit": "TFLOP/s", "peak_source": tf_kind}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = (profiled_traffic("tree_attention_b8_ctx4096_n64.md", "tree_attention.cu")
                        if args.workload == 4 else None)
@@ -512,6 +531,11 @@ def run_with_attention(args, ws, rank, local):
     roof["attn_flops"] = flops
     metric = ("tree-attention calls/s (B=8, 32/8 heads, d=128, ctx 4096, N=64)" if args.workload == 4
               else "full tree steps/s (top-K+best-first+attention+verify) B=64 V=128256 ctx 16384 N=256")
+    if light:  # one line of the workloads table
+        return {"workload": w.name, "metric": metric, "value": aggregate_rate(args.steps, elapsed_ms, ws),
+                "unit": "calls/s" if args.workload == 4 else "steps/s", "steps": args.steps,
+                "ms_per_step": ms_step, "mean_tree_nodes": float(n_nodes.mean()), "roofline": roof,
+                "kernels": {"tree_attention": {"ms": t_attn}}, "clocks": clk}
     return {
         "metric": metric, "value": aggregate_rate(args.steps, elapsed_ms, ws),
         "unit": "calls/s" if args.workload == 4 else "steps/s", "n_gpus": ws, "steps": args.steps,
@@ -527,94 +551,146 @@ def run_with_attention(args, ws, rank, local):
 
 # --------------------------------------------------------------------------- oracle legs
 
-def oracle_step(w, req, x, lse_rows=None, pre=None):
-    """The oracle's tree step for one request (top-K of its b rows, its tree,
-    its target rows' argmaxes and accept walk)."""
-    import oracle
-    import synth
-    roots, ctx, cost, lar = pre
-    tk = oracle.topk_marginals(x[req:req + 1], w.K)
-    tr = oracle.build_tree(tk.logit, tk.tok, tk.lse, w.n_max, roots[req:req + 1], ctx[req:req + 1],
-                           cost, lar[req:req + 1])
-    return tk, tr
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
 
 
-def oracle_verify(args, w, tgt, u, r, tr):
-    """The oracle's verification of request r (greedy, or sampled at T > 0)."""
-    import oracle
-    if args.temperature > 0:
-        oracle.verify_sample(tgt[r:r + 1], w.b, args.temperature, u[r:r + 1], tr.n_nodes, tr.parent, tr.token)
-    else:
-        oracle.verify_greedy(tgt[r:r + 1], w.b, tr.n_nodes, tr.parent, tr.token)
+class OracleStep:
+    """The oracle's tree step (top-K of a request's b rows, its tree, the
+    verification of its target rows), request by request.  The target rows are
+    planted at the oracle's own trees, outside any timing.  The oracle is C
+    called through ctypes, which releases the GIL: a thread pool runs requests
+    on several host cores at once."""
+
+    def __init__(self, args, w):
+        import oracle
+        import synth
+        self.args, self.w = args, w
+        self.pre = (synth.root_tokens(w), synth.ctx_lens(w), synth.cost_table(w), synth.l_ar(w))
+        self.x = synth.drafter_logits(w)
+        tk_all = oracle.topk_marginals(self.x, w.K)
+        tr_all = oracle.build_tree(tk_all.logit, tk_all.tok, tk_all.lse, w.n_max, *self.pre)
+        self.mean_nodes = float(tr_all.n_nodes.mean())
+        self.tgt, _ = synth.target_logits(w, tr_all.n_nodes, tr_all.depth, tk_all.tok)
+        self.u = synth.verify_uniforms(w)
+
+    def request(self, r):
+        import oracle
+        w, (roots, ctx, cost, lar) = self.w, self.pre
+        tk = oracle.topk_marginals(self.x[r:r + 1], w.K)
+        tr = oracle.build_tree(tk.logit, tk.tok, tk.lse, w.n_max, roots[r:r + 1], ctx[r:r + 1],
+                               cost, lar[r:r + 1])
+        if self.args.temperature > 0:
+            oracle.verify_sample(self.tgt[r:r + 1], w.b, self.args.temperature, self.u[r:r + 1],
+                                 tr.n_nodes, tr.parent, tr.token)
+        else:
+            oracle.verify_greedy(self.tgt[r:r + 1], w.b, tr.n_nodes, tr.parent, tr.token)
+
+    def step(self, pool=None):
+        """One whole step: every request of the batch."""
+        if pool is None:
+            for r in range(self.w.B):
+                self.request(r)
+        else:
+            list(pool.map(self.request, range(self.w.B)))
 
 
 def cpu_baseline(args, budget_s=12.0):
-    """Times the oracle as it stands on the host (single thread) on a bounded
-    sample: whole requests of the bench workload, cycled until ~budget_s."""
-    import oracle
+    """Times the oracle as it stands on the host cores, on a bounded sample of
+    the bench workload: whole requests on one thread for half the budget, then
+    whole steps with the requests split over every host core for the other
+    half.  The all-cores figure is the line's value."""
+    from concurrent.futures import ThreadPoolExecutor
+
     import synth
     w = synth.workload(args.workload)
-    pre = (synth.root_tokens(w), synth.ctx_lens(w), synth.cost_table(w), synth.l_ar(w))
-    x = synth.drafter_logits(w)
-    # plant the target for the sampled requests from the oracle's own trees (outside the timing)
-    tk_all = oracle.topk_marginals(x, w.K)
-    tr_all = oracle.build_tree(tk_all.logit, tk_all.tok, tk_all.lse, w.n_max, *pre)
-    tgt, _ = synth.target_logits(w, tr_all.n_nodes, tr_all.depth, tk_all.tok)
-    u = synth.verify_uniforms(w)
+    o = OracleStep(args, w)
     t0 = time.perf_counter()
     done = 0
     while True:
-        r = done % w.B
-        tk, tr = oracle_step(w, r, x, pre=pre)
-        oracle_verify(args, w, tgt, u, r, tr)
+        o.request(done % w.B)
         done += 1
-        if time.perf_counter() - t0 > budget_s and done >= 1:
+        if time.perf_counter() - t0 > budget_s / 2:
             break
-    dt = time.perf_counter() - t0
-    per_req = dt / done
-    return {"value": 1.0 / (per_req * w.B), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{done} whole requests (top-K of 16 rows, tree, verify of its rows) of the "
-                      f"{w.name} workload in {dt:.1f} s, scaled to a {w.B}-request step"}
+    dt1 = time.perf_counter() - t0
+    single = 1.0 / (dt1 / done * w.B)
+    n = host_cores()
+    with ThreadPoolExecutor(n) as pool:
+        o.step(pool)
+        t0 = time.perf_counter()
+        steps = 0
+        while True:
+            o.step(pool)
+            steps += 1
+            if time.perf_counter() - t0 > budget_s / 2:
+                break
+        dt = time.perf_counter() - t0
+    return {"value": steps / dt, "unit": UNIT, "cores": n, "kind": "oracle", "nproc": n,
+            "sample": f"{steps} whole {w.B}-request steps (top-K of 16 rows, tree, verify of its rows, "
+                      f"per request) of the {w.name} workload in {dt:.1f} s, requests split over "
+                      f"{n} host threads",
+            "single_thread": {"value": single, "unit": UNIT, "cores": 1,
+                              "sample": f"{done} whole requests in {dt1:.1f} s on one thread, "
+                                        f"scaled to a {w.B}-request step"}}
 
 
 def run_reference(args, ws, rank):
     """Reference arm: the oracle, as it stands, on the host cores; each step is
-    one request of the workload (a bounded sample), scaled to a full step."""
-    import oracle
+    one whole step of the workload (every request), the requests split over
+    all host cores."""
+    from concurrent.futures import ThreadPoolExecutor
+
     import synth
     w = synth.workload(args.workload)
-    pre = (synth.root_tokens(w), synth.ctx_lens(w), synth.cost_table(w), synth.l_ar(w))
-    x = synth.drafter_logits(w)
-    tk_all = oracle.topk_marginals(x, w.K)
-    tr_all = oracle.build_tree(tk_all.logit, tk_all.tok, tk_all.lse, w.n_max, *pre)
-    tgt, _ = synth.target_logits(w, tr_all.n_nodes, tr_all.depth, tk_all.tok)
-
-    u = synth.verify_uniforms(w)
-
-    def one(r):
-        tk, tr = oracle_step(w, r, x, pre=pre)
-        oracle_verify(args, w, tgt, u, r, tr)
-
-    for i in range(args.warmup):
-        one(i % w.B)
-    t0 = time.perf_counter()
-    for i in range(args.steps):
-        one(i % w.B)
-    dt = time.perf_counter() - t0
-    per_full_step = dt / args.steps * w.B
-    val = 1.0 / per_full_step
+    o = OracleStep(args, w)
+    n = host_cores()
+    with ThreadPoolExecutor(n) as pool:
+        for _ in range(args.warmup):
+            o.step(pool)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            o.step(pool)
+        dt = time.perf_counter() - t0
+    val = args.steps / dt
     metric = METRIC if args.temperature <= 0 else METRIC.replace(
         "+verify)", f"+sampled verify, T={args.temperature:g})")
     return {"impl": "reference", "metric": metric, "value": val, "unit": UNIT, "n_gpus": ws,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_full_step * 1e3,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "b": w.b, "V": w.V, "K": w.K, "n_max": w.n_max,
-                       "logit_dtype": w.dtype},
-            "cpu_baseline": {"value": val, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": f"each step one request of {w.B} (top-K, tree, verify), "
-                                       f"scaled by {w.B}"},
+            "data": "synthetic", "config": step_config(w, o.mean_nodes, ws),
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": n, "kind": "oracle", "nproc": n,
+                             "sample": f"each step one whole {w.B}-request step (top-K, tree, verify "
+                                       f"per request), the requests split over {n} host threads"},
             "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# steps and warm-up of each other workload's line: microsecond steps get many
+# repetitions, the millisecond serving step a few
+SUB_STEPS = {1: (500, 20), 2: (500, 20), 4: (200, 10), 5: (10, 3)}
+
+
+def other_workloads(args, ws, rank, local) -> dict:
+    """The other four workloads, each measured like the headline (graph replay,
+    CUDA events, max over ranks) with its dominant kernel's roofline: the
+    latency cases (1, 2), the attention layer (4) and the serving step (5)."""
+    import gc
+
+    import torch
+    out = {}
+    for wid in (1, 2, 4, 5):
+        sub = argparse.Namespace(**vars(args))
+        sub.workload = wid
+        sub.steps, sub.warmup = SUB_STEPS[wid]
+        sub.chunks = 1
+        r = (run_with_attention if wid in (4, 5) else run_ours)(sub, ws, rank, local, light=True)
+        out[str(wid)] = r
+        gc.collect()
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return out
 
 
 def main():
@@ -625,6 +701,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", type=int, default=3, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="the headline line only (no table of the other four workloads)")
     ap.add_argument("--profile-kernel", choices=["topk", "tree", "verify", "step", "attn"],
                     help="launch one kernel (or the step) --launches times and exit, for ncu")
     ap.add_argument("--launches", type=int, default=3)
@@ -650,6 +728,9 @@ def main():
         res = run_with_attention(args, ws, rank, local)
     else:
         res = run_ours(args, ws, rank, local)
+    if (res is not None and args.workload == 3 and not args.no_workloads and not args.profile_kernel
+            and args.temperature <= 0):
+        res["workloads"] = other_workloads(args, ws, rank, local)
     if res is None:
         print("profile launches done", flush=True)
     elif rank == 0:

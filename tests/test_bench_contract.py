@@ -29,6 +29,18 @@ def test_reference_arm_line():
     assert d["n_gpus"] == 1 and d["steps"] == 2 and d["warmup"] == 3
     assert d["higher_is_better"] is True and d["vs_baseline"] is None
     assert d["config"]["workload"] == "tiny-b4-v1024-k8-n16-f32"
+    # the same config dict as the GPU arm's line for this workload
+    sys.path.insert(0, ROOT)
+    import bench
+    import oracle
+    import synth
+    w = synth.workload(1)
+    tk = oracle.topk_marginals(synth.drafter_logits(w), w.K)
+    tr = oracle.build_tree(tk.logit, tk.tok, tk.lse, w.n_max, synth.root_tokens(w), synth.ctx_lens(w),
+                           synth.cost_table(w), synth.l_ar(w))
+    assert d["config"] == bench.step_config(w, float(tr.n_nodes.mean()), 1)
+    # whole steps: the timed steps fit in the run
+    assert d["ms_per_step"] * d["steps"] < 60e3
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
     e2e = d["e2e"]
@@ -41,3 +53,15 @@ def test_reference_arm_other_ranks_are_silent():
                env={"RANK": "1", "WORLD_SIZE": "2"})
     assert r.returncode == 0, r.stderr[-2000:]
     assert r.stdout.strip() == ""
+
+
+def test_cpu_baseline_reports_single_thread_and_all_cores():
+    import argparse
+    sys.path.insert(0, ROOT)
+    import bench
+    args = argparse.Namespace(workload=1, temperature=0.0)
+    cb = bench.cpu_baseline(args, budget_s=0.4)
+    assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["unit"] == bench.UNIT
+    assert cb["cores"] == cb["nproc"] == bench.host_cores() >= 1
+    st = cb["single_thread"]
+    assert st["cores"] == 1 and st["value"] > 0 and st["sample"]
