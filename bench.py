@@ -276,12 +276,22 @@ def run_ours(args, ws, rank, local, light=False):
     k1 = statistics.mean(evs[p][0].elapsed_time(evs[p][1]) for p in range(P))
     k2 = statistics.mean(evs[p][1].elapsed_time(evs[p][2]) for p in range(P))
     k4 = statistics.mean(evs[p][2].elapsed_time(evs[p][3]) for p in range(P))
+    # steps 1-3 as the step runs them (one fused launch where it applies)
+    fev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(P)]
+    for p in range(P):
+        fev[p][0].record(stream)
+        step.draft(xs[p & 1])
+        fev[p][1].record(stream)
+    torch.cuda.synchronize()
+    k12 = statistics.mean(a_.elapsed_time(b_) for a_, b_ in fev)
     assert int(step.status.abs().sum()) == 0, "device status bits set"
     hbm, peak_kind = peaks()
     ms_step = elapsed_ms / args.steps
     vname = "verify_sample" if sampled else "verify_greedy"
     kern = {"topk_marginals": {"ms": k1, "bytes": bytes_k1, "gbs": bytes_k1 / (k1 * 1e-3) / 1e9},
             "build_tree": {"ms": k2, "bytes": w.B * w.b * w.K * 16},
+            "draft_tree": {"ms": k12, "bytes": bytes_k1, "gbs": bytes_k1 / (k12 * 1e-3) / 1e9,
+                           "note": "steps 1-3 as the step launches them"},
             vname: {"ms": k4, "bytes": bytes_k4, "gbs": bytes_k4 / (k4 * 1e-3) / 1e9}}
     dom = max(("topk_marginals", vname), key=lambda k: kern[k]["ms"])
     if light:  # one line of the workloads table: no end-to-end leg

@@ -341,8 +341,8 @@ def alloc_verify(B, n_max, b, device) -> Verify:
 
 class TreeStep:
     """One tree step (top-K marginals -> best-first tree -> greedy verify) over
-    preallocated device buffers; ``capture()`` records the three launches in a
-    CUDA graph so a step replays with one host call."""
+    preallocated device buffers; ``capture()`` records the launches in a CUDA
+    graph so a step replays with one host call."""
 
     def __init__(self, B, b, V, K, n_max, device, root_token, ctx_len, cost_ms, l_ar):
         self.B, self.b, self.V, self.K, self.n_max = B, b, V, K, n_max

@@ -1027,7 +1027,7 @@ struct TopkPlan {
 // Which kernel takes the rows: BASTION_TOPK_PATH=stream|cluster forces one
 // (where it applies), otherwise the stream kernel once there are two rows
 // per SM and four of its CTAs fit on an SM.
-TopkPlan plan_topk(int V, int K, int es, int rows, int sms) {
+TopkPlan plan_topk(int V, int K, int es, int rows, int sms, const void *, int64_t) {
   TopkPlan p;
   p.stream = false;
   p.nst = 0;
@@ -1110,14 +1110,11 @@ size_t topk_workspace_bytes(int, int, int, int, int) { return 256; }
 
 int topk_max_smem_ok(int, int, int) { return 1; }
 
-int launch_topk(const void *logits, int dtype, int B, int b, int V, int64_t ld, int K,
-                float *topk_logq, float *topk_logit, int32_t *topk_tok, double *lse,
-                void *, int32_t *status, cudaStream_t stream) {
-  const int es = dtype == BASTION_F32 ? 4 : 2;
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const TopkPlan p = plan_topk(V, K, es, B * b, sms);
+namespace {
+
+TopkArgs topk_args(const TopkPlan &p, const void *logits, int B, int b, int V, int64_t ld, int K,
+                   float *topk_logq, float *topk_logit, int32_t *topk_tok, double *lse,
+                   int32_t *status) {
   TopkArgs a;
   a.logits = static_cast<const unsigned char *>(logits);
   a.rows = B * b;
@@ -1136,6 +1133,17 @@ int launch_topk(const void *logits, int dtype, int B, int b, int V, int64_t ld, 
   a.topk_tok = topk_tok;
   a.lse = lse;
   a.status = status;
+  return a;
+}
+
+int sm_count() {
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return sms;
+}
+
+cudaError_t launch_plan(const TopkPlan &p, const TopkArgs &a, int es, int sms, cudaStream_t stream) {
   cudaError_t e;
   if (p.stream) {
     auto kern = es == 4 ? topk_stream_kernel<4> : topk_stream_kernel<2>;
@@ -1148,6 +1156,19 @@ int launch_topk(const void *logits, int dtype, int B, int b, int V, int64_t ld, 
   } else {
     e = es == 4 ? launch_cluster<4>(p, a, stream) : launch_cluster<2>(p, a, stream);
   }
+  return e;
+}
+
+}  // namespace
+
+int launch_topk(const void *logits, int dtype, int B, int b, int V, int64_t ld, int K,
+                float *topk_logq, float *topk_logit, int32_t *topk_tok, double *lse,
+                void *, int32_t *status, cudaStream_t stream) {
+  const int es = dtype == BASTION_F32 ? 4 : 2;
+  const int sms = sm_count();
+  const TopkPlan p = plan_topk(V, K, es, B * b, sms, logits, ld);
+  const TopkArgs a = topk_args(p, logits, B, b, V, ld, K, topk_logq, topk_logit, topk_tok, lse, status);
+  const cudaError_t e = launch_plan(p, a, es, sms, stream);
   return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? BASTION_OK : BASTION_ERR_LAUNCH;
 }
 

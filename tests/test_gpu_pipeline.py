@@ -57,6 +57,31 @@ def test_pipeline_batched_qwen3_vocab_graph(cuda_lib):
     assert vf.accept_len.max() >= 1
 
 
+def test_pipeline_graph_replayed_many_times(cuda_lib):
+    """The step replayed 50 times from two graphs on two alternating inputs: the
+    verify workspace returns to zero after every replay, and the results stay
+    the oracle's."""
+    from draft_tree_build_gb300 import bastion
+    w = synth.workload(3)
+    x = synth.drafter_logits(w)
+    x2 = synth.drafter_logits(synth.workload(3, seed=w.seed + 17))
+    roots, ctx, cost, lar = workload_inputs(w)
+    step = bastion.TreeStep(w.B, w.b, w.V, w.K, w.n_max, dev(), torch.from_numpy(roots),
+                            torch.from_numpy(ctx), torch.from_numpy(cost), torch.from_numpy(lar))
+    xs = [to_dev(x), to_dev(x2)]
+    td = torch.zeros((w.B, w.n_max, w.V), dtype=xs[0].dtype, device=dev())
+    graphs = [step.capture(xs[i], td) for i in range(2)]
+    for i in range(50):
+        graphs[i & 1].replay()
+    torch.cuda.synchronize()
+    assert int(step.ws_verify.abs().sum()) == 0
+    assert int(step.status.abs().sum()) == 0
+    tk = oracle.topk_marginals(x2, w.K)   # replay 49 ran on the second input
+    compare_topk(step.topk, tk)
+    ref = oracle_tree_guided(tk.logit, tk.tok, tk.lse, w.n_max, roots, ctx, cost, lar, step.tree)
+    compare_tree(step.tree, ref)
+
+
 def test_pipeline_serving_llama_vocab(cuda_lib):
     """B=64, b=16, V=128256, K=64, N_max=256 (every tree fills the budget)."""
     step, vf = _step(synth.workload(5))
