@@ -18,7 +18,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libbastion.so")
 SOURCES = ["api.cu", "topk_marginals.cu", "build_tree.cu", "verify_greedy.cu", "tree_attention.cu",
            "verify_noalloc.cu", "verify_sample.cu", "calibrate.cu",
-           "build_tree_mixture.cu"]
+           "build_tree_mixture.cu", "lm_head_topk.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

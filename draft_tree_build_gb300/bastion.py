@@ -29,6 +29,7 @@ STATUS_TIMEOUT = 1 << 30
 SYMBOLS = (
     "bastion_version", "bastion_status_string",
     "bastion_topk_marginals_workspace_bytes", "bastion_topk_marginals",
+    "bastion_lm_head_topk_workspace_bytes", "bastion_lm_head_topk",
     "bastion_build_tree", "bastion_build_tree_mixture",
     "bastion_calibrate_cost",
     "bastion_tree_attention_workspace_bytes", "bastion_tree_attention",
@@ -68,6 +69,10 @@ def lib(build_if_missing: bool = True):
     L.bastion_topk_marginals_workspace_bytes.argtypes = [i32, i32, i32, i32]
     L.bastion_topk_marginals.restype = i32
     L.bastion_topk_marginals.argtypes = [vp, i32, i32, i32, i32, i64, i32, vp, vp, vp, vp, vp, sz, vp, vp]
+    L.bastion_lm_head_topk_workspace_bytes.restype = sz
+    L.bastion_lm_head_topk_workspace_bytes.argtypes = [i32, i32, i32, i32]
+    L.bastion_lm_head_topk.restype = i32
+    L.bastion_lm_head_topk.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp, vp]
     L.bastion_build_tree.restype = i32
     L.bastion_build_tree.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, i32, vp] + [vp] * 11 + [vp]
     L.bastion_build_tree_mixture.restype = i32
@@ -159,6 +164,27 @@ def bastion_topk_marginals(logits, K, topk_logq, topk_logit, topk_tok, lse, work
                                       _p(topk_logit), _p(topk_tok), _p(lse), _p(workspace),
                                       workspace.numel() * workspace.element_size(), _p(status), _s(stream))
     _check(rc, "bastion_topk_marginals")
+
+
+def bastion_lm_head_topk_workspace_bytes(B: int, b: int, V: int, K: int) -> int:
+    return int(lib().bastion_lm_head_topk_workspace_bytes(B, b, V, K))
+
+
+def bastion_lm_head_topk(hidden, weight, K, topk_logq, topk_logit, topk_tok, lse, workspace, status,
+                         stream=None):
+    """hidden [B, b, H] and weight [V, H], contiguous bfloat16; outputs as
+    bastion_topk_marginals for the logits hidden . weight^T."""
+    for name, t in (("hidden", hidden), ("weight", weight)):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise BastionError(f"lm head: {name} must be contiguous bfloat16")
+    B, b, H = hidden.shape
+    V = weight.shape[0]
+    if weight.dim() != 2 or weight.shape[1] != H:
+        raise BastionError("lm head: weight must be [V, H] with the hidden size of hidden")
+    rc = lib().bastion_lm_head_topk(_p(hidden), _p(weight), B, b, H, V, int(K), _p(topk_logq),
+                                    _p(topk_logit), _p(topk_tok), _p(lse), _p(workspace),
+                                    workspace.numel() * workspace.element_size(), _p(status), _s(stream))
+    _check(rc, "bastion_lm_head_topk")
 
 
 def bastion_build_tree(topk_logit, topk_tok, lse, n_max, root_token, ctx_len, cost_ms, l_ar,

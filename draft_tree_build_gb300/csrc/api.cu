@@ -12,6 +12,10 @@ int topk_max_smem_ok(int V, int K, int es);
 int launch_topk(const void *logits, int dtype, int B, int b, int V, int64_t ld, int K,
                 float *topk_logq, float *topk_logit, int32_t *topk_tok, double *lse, void *ws,
                 int32_t *status, cudaStream_t stream);
+size_t lm_head_workspace_bytes(int rows, int V, int K);
+int launch_lm_head(const void *hidden, const void *weight, int B, int b, int H, int V, int K,
+                   float *topk_logq, float *topk_logit, int32_t *topk_tok, double *lse, void *ws,
+                   int32_t *status, cudaStream_t stream);
 int launch_build_tree(const float *topk_logit, const int32_t *topk_tok, const double *lse, int B,
                       int b, int K, int n_max, const int32_t *root_token, const int32_t *ctx_len,
                       const float *cost_ms, int cost_per_request, const float *l_ar,
@@ -102,6 +106,28 @@ int bastion_topk_marginals(const void *logits, int dtype, int B, int b, int V, i
   if ((long long)B * b > (1LL << 24)) return BASTION_ERR_SIZE;
   return bastion::launch_topk(logits, dtype, B, b, V, ld_row, K, topk_logq, topk_logit, topk_tok,
                               lse, workspace, status, (cudaStream_t)stream);
+}
+
+size_t bastion_lm_head_topk_workspace_bytes(int B, int b, int V, int K) {
+  if (B < 1 || b < 1 || (long long)B * b > (1LL << 24) || V < 1 || K < 1 || K > 64 || K > V) return 0;
+  return bastion::lm_head_workspace_bytes(B * b, V, K);
+}
+
+int bastion_lm_head_topk(const void *hidden, const void *weight, int B, int b, int H, int V, int K,
+                         float *topk_logq, float *topk_logit, int32_t *topk_tok, double *lse,
+                         void *workspace, size_t workspace_bytes, int32_t *status,
+                         bastion_stream_t stream) {
+  if (!hidden || !weight || !topk_logit || !topk_tok || !lse || !status || !workspace)
+    return BASTION_ERR_NULL;
+  if (B < 1 || b < 1 || (long long)B * b > (1LL << 24) || V < 1 || K < 1 || K > 64 || K > V ||
+      H < 1 || H > (1 << 20))
+    return BASTION_ERR_SIZE;
+  if (H % 64) return BASTION_ERR_UNSUPPORTED;
+  if (!aligned(hidden, 16) || !aligned(weight, 16) || !aligned(workspace, 256) || !aligned(lse, 8))
+    return BASTION_ERR_ALIGN;
+  if (workspace_bytes < bastion_lm_head_topk_workspace_bytes(B, b, V, K)) return BASTION_ERR_WORKSPACE;
+  return bastion::launch_lm_head(hidden, weight, B, b, H, V, K, topk_logq, topk_logit, topk_tok, lse,
+                                 workspace, status, (cudaStream_t)stream);
 }
 
 int bastion_build_tree(const float *topk_logit, const int32_t *topk_tok, const double *lse,

@@ -105,6 +105,35 @@ int bastion_topk_marginals(const void *logits, int dtype, int B, int b, int V, i
                            int32_t *status, bastion_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Step 1 fused with the drafter's output layer: the top-K marginals of the
+ * logits l_k = W h_k, formed on the tensor cores and never written out.
+ * Methodologie §1: one forward pass of the block-diffusion drafter yields the
+ * position-wise marginals q_k = softmax(l_k); W is its output embedding and
+ * h_k the final hidden state of block position k.
+ *
+ * hidden     [B, b, H] bf16, row-major, 16-byte aligned; H a multiple of 64
+ *            (BASTION_ERR_UNSUPPORTED otherwise).
+ * weight     [V, H] bf16, row-major, 16-byte aligned.
+ * Outputs:   as bastion_topk_marginals, for the logits as accumulated (fp32,
+ *            bf16 products summed on the tensor cores): topk_logq (may be
+ *            NULL), topk_logit, topk_tok [B, b, K] in rank order (logit desc,
+ *            token asc), lse [B, b] double, status [B].  Each logit differs
+ *            from the exact dot product by the accumulation's rounding, well
+ *            inside 2^-16 sum_i |W[v,i] h[i]|, so tokens whose exact logits lie
+ *            closer than that may come in either order.
+ * Limits: B, b >= 1, B*b <= 2^24, 1 <= K <= min(V, 64), V < 2^31, H <= 2^20.
+ * Workspace: bastion_lm_head_topk_workspace_bytes(B, b, V, K) bytes, 256-byte
+ * aligned, zero-filled before its first use; every call leaves it so.  Calls
+ * that share a workspace must not overlap on the GPU.  Two launches (the GEMM
+ * with its per-share top-K, then the per-row merge).
+ */
+size_t bastion_lm_head_topk_workspace_bytes(int B, int b, int V, int K);
+int bastion_lm_head_topk(const void *hidden, const void *weight, int B, int b, int H, int V, int K,
+                         float *topk_logq, float *topk_logit, int32_t *topk_tok, double *lse,
+                         void *workspace, size_t workspace_bytes, int32_t *status,
+                         bastion_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Steps 2-3 -- best-first tree expansion under the online budget controller,
  * and the tree arrays.
  * Methodologie §1 ("Pad-scoren": rho = prod q_k), §2 ("Surrogaat-schatting":

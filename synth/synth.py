@@ -43,6 +43,8 @@ S_Q = 9
 S_K = 10
 S_V = 11
 S_VERIFY_U = 12
+S_HIDDEN = 13
+S_WEIGHT = 14
 
 PLANT_VALUE = 12.0  # above any Box-Muller draw (|z| < 8.7 since u1 >= 2^-54)
 
@@ -134,6 +136,17 @@ def fill_normal(ptr: int, n: int, dtype: str, scale: float, seed: int, stream: i
         lib().synth_fill_normal_f32(ptr, n, scale, seed, stream, offset)
     else:
         raise ValueError(dtype)
+
+
+def lm_head_inputs(B: int, b: int, H: int, V: int, seed: int):
+    """Drafter final hidden states [B, b, H] ~ N(0, 1) and an output embedding
+    [V, H] ~ N(0, 4/H), both bf16 bits (uint16): logits of standard deviation
+    about 2, the drafter-logit scale of the batched workloads."""
+    hidden = host_array((B, b, H), "bf16")
+    weight = host_array((V, H), "bf16")
+    fill_normal(hidden.ctypes.data, hidden.size, "bf16", 1.0, seed, S_HIDDEN)
+    fill_normal(weight.ctypes.data, weight.size, "bf16", 2.0 / float(np.sqrt(H)), seed, S_WEIGHT)
+    return hidden, weight
 
 
 def fill_normal_rows(ptr: int, rows: int, cols: int, ld: int, dtype: str, scale: float,

@@ -42,7 +42,7 @@ def _header_arg_counts():
 
 def test_binding_argtypes_match_header(L):
     counts = _header_arg_counts()
-    assert len(counts) == 14
+    assert len(counts) == 16
     for name, n in counts.items():
         assert len(getattr(L, name).argtypes) == n, name
 
@@ -73,6 +73,18 @@ def test_host_checks_reject_before_launch(L):
     # tree: n_max > 256
     args = [fake] * 3 + [1, 4, 8, 257] + [fake] * 3 + [0, fake] + [fake] * 11 + [None]
     assert L.bastion_build_tree(*args) == -2
+    # lm head: H not a multiple of 64 -> unsupported; K > 64 -> size; misaligned weight; small workspace
+    lm = [fake, fake, 2, 4, 4096, 1000, 8, None, fake, fake, fake, ws, 1 << 24, fake, None]
+    lm[4] = 4000
+    assert L.bastion_lm_head_topk(*lm) == -6
+    lm[4], lm[6] = 4096, 65
+    assert L.bastion_lm_head_topk(*lm) == -2
+    lm[6], lm[1] = 8, vp(0x10008)
+    assert L.bastion_lm_head_topk(*lm) == -4
+    lm[1], lm[12] = fake, 16
+    assert L.bastion_lm_head_topk(*lm) == -5
+    lm[12], lm[0] = 1 << 24, None
+    assert L.bastion_lm_head_topk(*lm) == -1
     # attention: D != 128 -> unsupported; Hq % Hkv -> size
     base = [fake, fake, fake, 1, 16, 32, 8, 64, 256, fake, fake, fake, ctypes.c_float(0.1), fake, ws, 1 << 20, fake, None]
     assert L.bastion_tree_attention(*base) == -6
