@@ -10,23 +10,25 @@
 //
 // sm_103a design (one persistent CTA per SM):
 //  * the rows are cut into M-tiles of 128 and the vocabulary into N-tiles of
-//    256; CTA c owns M-tile c % MT and every CPM-th N-tile from c / MT on, so
+//    192; CTA c owns M-tile c % MT and every CPM-th N-tile from c / MT on, so
 //    the MT CTAs that read the same N-tile of W run side by side and W comes
 //    from HBM about once (the other reads hit L2);
-//  * warp 0 streams A (hidden, 128 x 64) and B (W, 256 x 64) tiles through a
-//    3-stage ring with TMA (cp.async.bulk.tensor, 128-byte swizzle, zero fill
+//  * warp 0 streams A (hidden, 128 x 64) and B (W, 192 x 64) tiles through a
+//    4-stage ring with TMA (cp.async.bulk.tensor, 128-byte swizzle, zero fill
 //    past the edges); lane 0 of warp 1 issues tcgen05.mma kind::f16 (bf16 in,
-//    fp32 accumulate, M = 128, N = 256, K = 16, four per 64-column chunk)
-//    into one of two TMEM accumulators of 256 columns, so the epilogue of one
-//    tile overlaps the MMAs of the next;
+//    fp32 accumulate, M = 128, N = 192, K = 16, four per 64-column chunk)
+//    into one of two TMEM accumulators of 192 columns, so the epilogue of one
+//    tile overlaps the MMAs of the next.  (N = 192 rather than 256 leaves
+//    shared memory for a fourth stage next to the heaps; three stages of
+//    N = 256 left the MMAs waiting for operands);
 //  * warps 2-5 are the epilogue, one thread per row (TMEM lane): per 32-column
 //    chunk (tcgen05.ld) the thread updates its row's running max and sum of
 //    2^(l log2(e) - c) (c an integer kept at floor(max log2(e)), the sum
 //    rescaled by exact powers of two) and inserts every logit whose key
 //    (value desc, token asc, one 64-bit integer) beats the root of the row's
-//    min-heap of the K best keys seen (in shared memory, one column of heap
-//    slots per thread; the first K keys are stored as they come and the heap
-//    is built once).  After every tile each share publishes its J-th best key
+//    4-ary min-heap of the K best keys seen (in shared memory, one column of
+//    heap slots per thread; the first K keys are stored as they come and the
+//    heap is built once).  After every tile each share publishes its J-th best key
 //    (J = ceil(K / CPM)) and reads the others': at least K keys of the row lie
 //    at or above the smallest of them, so a key below it cannot be among the
 //    row's K best and is not inserted (without this bound nearly every
@@ -49,17 +51,15 @@ namespace bastion {
 namespace {
 
 constexpr int kLT = 192;  // warp 0 TMA, warp 1 MMA (and TMEM), warps 2-5 epilogue
-constexpr int kBM = 128, kBN = 256, kBK = 64;
-constexpr int kStages = 3;
+constexpr int kBM = 128, kBN = 192, kBK = 64;
+constexpr int kStages = 4;
 constexpr int kMaxK = 64;
 constexpr uint32_t kABytes = kBM * kBK * 2;             // 16 KB
-constexpr uint32_t kBBytes = kBN * kBK * 2;             // 32 KB
-constexpr uint32_t kStageBytes = kABytes + kBBytes;     // 48 KB
+constexpr uint32_t kBBytes = kBN * kBK * 2;             // 24 KB
+constexpr uint32_t kStageBytes = kABytes + kBBytes;     // 40 KB (a multiple of 1 KB)
 constexpr uint32_t kOffHeap = kStages * kStageBytes;    // heaps after the ring
 constexpr uint32_t kHeapBytes = kBM * kMaxK * 8;        // 64 KB
-constexpr uint32_t kOffStage = kOffHeap + kHeapBytes;   // a chunk's logits per row
-constexpr uint32_t kStageVals = kBM * 32 * 4;           // 16 KB
-constexpr uint32_t kOffBar = kOffStage + kStageVals;
+constexpr uint32_t kOffBar = kOffHeap + kHeapBytes;
 constexpr uint32_t kSmem = kOffBar + 256 + 1024;        // + alignment slack
 constexpr float kL2e = 1.4426950216293335f;             // log2(e) rounded to float
 constexpr float kCNone = -1.0e30f;                      // c before the first finite logit
@@ -89,7 +89,7 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
 }
 
 // kind::f16 instruction descriptor: fp32 accumulate, bf16 A and B (both
-// K-major), M = 128, N = 256.
+// K-major), M = 128, N = 192.
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) |
                             ((uint32_t)(kBM >> 4) << 24);
 
@@ -127,6 +127,60 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// tcgen05.ld of 32 columns without waiting, and a wait tied to the
+// destination registers (so no use of them is scheduled before it).
+__device__ __forceinline__ void tmem_ld32_issue(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_tied(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                 "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]),
+                 "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]),
+                 "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]),
+                 "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]),
+                 "+r"(r[31])
+               :
+               : "memory");
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Sum of 2^(x_i k + nc) over four values: two packed f32x2 FMAs, four ex2,
+// one packed add; the pair (s0, s1) accumulates.
+__device__ __forceinline__ void exp4_acc(float x0, float x1, float x2, float x3, float k, float nc,
+                                         float &s0, float &s1) {
+  float t0, t1, t2, t3;
+  asm("{\n .reg .b64 d, e, kk, cc;\n"
+      " mov.b64 d, {%4, %5};\n mov.b64 e, {%6, %7};\n mov.b64 kk, {%9, %9};\n"
+      " mov.b64 cc, {%8, %8};\n fma.rn.f32x2 d, d, kk, cc;\n fma.rn.f32x2 e, e, kk, cc;\n"
+      " mov.b64 {%0, %1}, d;\n mov.b64 {%2, %3}, e;\n}\n"
+      : "=f"(t0), "=f"(t1), "=f"(t2), "=f"(t3)
+      : "f"(x0), "f"(x1), "f"(x2), "f"(x3), "f"(nc), "f"(k));
+  float e0, e1, e2, e3;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(t0));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"(t1));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e2) : "f"(t2));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e3) : "f"(t3));
+  asm("{\n .reg .b64 a, b, c;\n mov.b64 a, {%0, %1};\n mov.b64 b, {%2, %3};\n"
+      " mov.b64 c, {%4, %5};\n add.rn.f32x2 a, a, b;\n add.rn.f32x2 a, a, c;\n"
+      " mov.b64 {%0, %1}, a;\n}\n"
+      : "+f"(s0), "+f"(s1)
+      : "f"(e0), "f"(e1), "f"(e2), "f"(e3));
 }
 
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int c0, int c1,
@@ -187,29 +241,35 @@ __device__ __forceinline__ void hp_st(uint32_t a, uint64_t v) {
   asm volatile("st.shared.u64 [%0], %1;" ::"r"(a), "l"(v) : "memory");
 }
 
-// Sifts key down from slot pos of the heap (slot pos is being replaced).
+// Sifts key down from slot pos of the heap (slot pos is being replaced).  The
+// heap is 4-ary (children of slot p: 4p + 1 .. 4p + 4): three levels for 64
+// keys, the four children of a level loaded together.
 __device__ __forceinline__ void heap_sift(uint32_t hb, int K, int pos, uint64_t key) {
+  constexpr uint32_t kRow = kBM * 8;
   while (true) {
-    int ch = 2 * pos + 1;
-    if (ch >= K) break;
-    uint64_t hc = hp_ld(hb + (uint32_t)ch * (kBM * 8));
-    if (ch + 1 < K) {
-      const uint64_t h2 = hp_ld(hb + (uint32_t)(ch + 1) * (kBM * 8));
-      if (h2 < hc) {
-        hc = h2;
-        ++ch;
+    const int c0 = 4 * pos + 1;
+    if (c0 >= K) break;
+    uint64_t h[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) h[u] = c0 + u < K ? hp_ld(hb + (uint32_t)(c0 + u) * kRow) : ~0ull;
+    int ch = c0;
+    uint64_t hc = h[0];
+#pragma unroll
+    for (int u = 1; u < 4; ++u)
+      if (h[u] < hc) {
+        hc = h[u];
+        ch = c0 + u;
       }
-    }
     if (hc >= key) break;
-    hp_st(hb + (uint32_t)pos * (kBM * 8), hc);
+    hp_st(hb + (uint32_t)pos * kRow, hc);
     pos = ch;
   }
-  hp_st(hb + (uint32_t)pos * (kBM * 8), key);
+  hp_st(hb + (uint32_t)pos * kRow, key);
 }
 
 // Builds thread rl's heap from its K stored slots (once per share).
 __device__ __noinline__ void heap_build(uint32_t hb, int K) {
-  for (int i = K / 2 - 1; i >= 0; --i) heap_sift(hb, K, i, hp_ld(hb + (uint32_t)i * (kBM * 8)));
+  for (int i = (K - 2) / 4; i >= 0; --i) heap_sift(hb, K, i, hp_ld(hb + (uint32_t)i * (kBM * 8)));
 }
 
 __global__ void __launch_bounds__(kLT, 1)
@@ -319,7 +379,6 @@ __global__ void __launch_bounds__(kLT, 1)
     bool bad = false;
     const int K = a.K;
     const uint32_t hb = smem_u32(heap) + (uint32_t)rl * 8u;  // this thread's heap column
-    float *stage_vals = reinterpret_cast<float *>(smem + kOffStage);  // [32][128]
     int filled = 0;  // keys stored before the heap is built (the first K)
     // the J best keys of this share so far (J <= 4; 0 where fewer were seen),
     // and lb: the smallest J-th best over the row's shares, as last read
@@ -327,24 +386,66 @@ __global__ void __launch_bounds__(kLT, 1)
     uint64_t lb = 0ull;
     const int J = a.J;
     uint64_t *pub_row = a.pub + (size_t)(live ? row : 0) * (size_t)((a.CPM + 1) & ~1);
+    // Publishes this share's J-th best and reads the row's bound: at least
+    // J * CPM >= K keys of the row are >= the smallest published J-th best, so
+    // no key below it is among the row's K best (stale or missing values only
+    // lower the bound).  The row's slots are read as 16-byte words, all loads
+    // issued first.
+    auto exchange = [&]() {
+      if (J == 0) return;
+      const uint64_t tj = J == 1 ? top[0] : J == 2 ? top[1] : J == 3 ? top[2] : top[3];
+      __stcg(reinterpret_cast<unsigned long long *>(pub_row + j0), (unsigned long long)tj);
+      uint64_t m2 = ~0ull;
+      const ulonglong2 *pr = reinterpret_cast<const ulonglong2 *>(pub_row);
+#pragma unroll 1
+      for (int q0 = 0; q0 < a.CPM; q0 += 32) {
+        ulonglong2 w[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+          w[u] = q0 + 2 * u < a.CPM ? __ldcg(pr + q0 / 2 + u) : make_ulonglong2(~0ull, ~0ull);
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const uint64_t x0 = w[u].x, x1 = q0 + 2 * u + 1 < a.CPM ? w[u].y : ~0ull;
+          m2 = x0 < m2 ? x0 : m2;
+          m2 = x1 < m2 ? x1 : m2;
+        }
+      }
+      lb = m2 > lb ? m2 : lb;
+    };
     for (int t = 0; t < ntile; ++t) {
       const int buf = t & 1;
       if (!__all_sync(kFull, wait_bar(&bs.acc_full[buf], (uint32_t)(t >> 1) & 1u, abort, st0))) break;
       tc_fence_after();
       const int n = j0 + t * a.CPM;
+      // chunk cc + 1 is loaded from TMEM while chunk cc is processed
+      uint32_t ra[32], rb[32];
+      const uint32_t tbase = lane_base + (uint32_t)buf * kBN;
+      tmem_ld32_issue(tbase, ra);
+      tmem_wait_tied(ra);
       for (int cc = 0; cc < kBN / 32; ++cc) {
+        if (cc + 1 < kBN / 32) tmem_ld32_issue(tbase + (uint32_t)(cc + 1) * 32u, rb);
         float v[32];
-        tmem_ld32(lane_base + (uint32_t)buf * kBN + (uint32_t)cc * 32u, v);
+#pragma unroll
+        for (int q = 0; q < 32; ++q) v[q] = __uint_as_float(ra[q]);
         const int col0 = n * kBN + cc * 32;
         const int nv = min(32, a.V - col0);  // columns past the vocabulary are zero fill
         if (live && nv > 0) {
-          float cm = -INFINITY;
+          // the chunk's max (NaN ignored: a NaN or +inf logit shows in the
+          // sum or the max, checked once at the end)
+          float cm;
+          if (nv == 32) {
+            float m3[11];
 #pragma unroll
-          for (int q = 0; q < 32; ++q)
-            if (q < nv) {
-              cm = fmaxf(cm, v[q]);
-              bad |= (v[q] != v[q]) || v[q] == INFINITY;
-            }
+            for (int q = 0; q < 10; ++q) m3[q] = max3(v[3 * q], v[3 * q + 1], v[3 * q + 2]);
+            m3[10] = fmaxf(v[30], v[31]);
+            cm = max3(max3(m3[0], m3[1], m3[2]), max3(m3[3], m3[4], m3[5]), max3(m3[6], m3[7], m3[8]));
+            cm = max3(cm, m3[9], m3[10]);
+          } else {
+            cm = -INFINITY;
+#pragma unroll
+            for (int q = 0; q < 32; ++q)
+              if (q < nv) cm = fmaxf(cm, v[q]);
+          }
           m = fmaxf(m, cm);
           if (m > -INFINITY && m < INFINITY) {
             const float cn = floorf(m * kL2e);
@@ -355,10 +456,13 @@ __global__ void __launch_bounds__(kLT, 1)
               c = cn;
             }
             float s0 = 0.f, s1 = 0.f;
+            if (nv == 32) {
 #pragma unroll
-            for (int q = 0; q < 32; q += 2) {
-              if (q < nv) s0 += ex2(fmaf(v[q], kL2e, -c));
-              if (q + 1 < nv) s1 += ex2(fmaf(v[q + 1], kL2e, -c));
+              for (int q = 0; q < 32; q += 4) exp4_acc(v[q], v[q + 1], v[q + 2], v[q + 3], kL2e, -c, s0, s1);
+            } else {
+#pragma unroll
+              for (int q = 0; q < 32; ++q)
+                if (q < nv) s0 += ex2(fmaf(v[q], kL2e, -c));
             }
             const float2 ts = two_sum(hi, s0 + s1);
             hi = ts.x;
@@ -369,25 +473,27 @@ __global__ void __launch_bounds__(kLT, 1)
           // fills) and the row's bound.  Such a key may also enter the
           // share's J best (the J-th best is at least both), so one pass over
           // the chunk's passing columns does all the bookkeeping.  The chunk
-          // is staged in shared memory only when a column passes, and the
-          // passing columns are handled in one small loop (a loop unrolled
-          // over the 32 columns with the heap code inlined in each copy ran
-          // several times slower).
+          // is copied to the thread's local memory only when a column passes,
+          // and the passing columns are handled in one small loop (a loop
+          // unrolled over the 32 columns with the heap code inlined in each
+          // copy ran several times slower).
           const float thr = fmaxf(filled < K || root == 0ull ? -INFINITY : key_value(root),
                                   lb == 0ull ? -INFINITY : key_value(lb));
           uint32_t pass = 0u;
+          float stg[32];  // the chunk, copied (to the thread's local memory) only when a column passes
           if (cm >= thr) {
 #pragma unroll
             for (int q = 0; q < 32; ++q) pass |= (q < nv && v[q] >= thr ? 1u : 0u) << q;
+            if (pass) {
 #pragma unroll
-            for (int q = 0; q < 32; ++q)
-              if (pass) stage_vals[q * kBM + rl] = v[q];
+              for (int q = 0; q < 32; ++q) stg[q] = v[q];
+            }
           }
 #pragma unroll 1
           while (pass) {
             const int q = __ffs(pass) - 1;
             pass &= pass - 1u;
-            const uint64_t key = make_key(stage_vals[q * kBM + rl], (uint32_t)(col0 + q));
+            const uint64_t key = make_key(stg[q], (uint32_t)(col0 + q));
             if (key <= lb) continue;
             // the share's J best
             if (J > 0) {
@@ -412,36 +518,22 @@ __global__ void __launch_bounds__(kLT, 1)
             }
           }
         }
+        // the first tile: the bound as soon as two chunks are in (the other
+        // shares are at about the same point), so that the rest of the first
+        // tile already skips most columns
+        if (t == 0 && cc == 1 && live) exchange();
+        if (cc + 1 < kBN / 32) {
+          tmem_wait_tied(rb);
+#pragma unroll
+          for (int q = 0; q < 32; ++q) ra[q] = rb[q];
+        }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bs.acc_empty[buf]);
-      // publish this share's J-th best and read the row's bound: at least
-      // J * CPM >= K keys of the row are >= the smallest published J-th best,
-      // so no key below it is among the row's K best (stale or missing
-      // values only lower the bound)
-      if (J > 0 && live) {
-        const uint64_t tj = J == 1 ? top[0] : J == 2 ? top[1] : J == 3 ? top[2] : top[3];
-        __stcg(reinterpret_cast<unsigned long long *>(pub_row + j0), (unsigned long long)tj);
-        // the row's slots are read as 16-byte words, all loads issued first
-        uint64_t m2 = ~0ull;
-        const ulonglong2 *pr = reinterpret_cast<const ulonglong2 *>(pub_row);
-#pragma unroll 1
-        for (int q0 = 0; q0 < a.CPM; q0 += 32) {
-          ulonglong2 w[16];
-#pragma unroll
-          for (int u = 0; u < 16; ++u)
-            w[u] = q0 + 2 * u < a.CPM ? __ldcg(pr + q0 / 2 + u) : make_ulonglong2(~0ull, ~0ull);
-#pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            const uint64_t x0 = w[u].x, x1 = q0 + 2 * u + 1 < a.CPM ? w[u].y : ~0ull;
-            m2 = x0 < m2 ? x0 : m2;
-            m2 = x1 < m2 ? x1 : m2;
-          }
-        }
-        lb = m2 > lb ? m2 : lb;
-      }
+      if (live) exchange();
     }
+    bad = m == INFINITY || !(hi == hi) || !(lo == lo) || hi == INFINITY;
     if (live) {  // this CTA's share of the row: its K best keys and (max, c, sum)
       if (bad) atomicOr(&a.status[row / a.b], BASTION_STATUS_NONFINITE);
       const size_t slot = (size_t)row * a.CPM + j0;
