@@ -23,6 +23,14 @@ pytestmark = pytest.mark.gpu
 EPS_FRAC = 2.0 ** -16
 
 
+@pytest.fixture(autouse=True, params=["1", "2", "4"])
+def lm_cluster(request, monkeypatch):
+    """Every case with the W tiles loaded per CTA, and multicast to clusters of
+    two and four CTAs (where the M-tiles divide)."""
+    monkeypatch.setenv("BASTION_LMHEAD_CLUSTER", request.param)
+    return request.param
+
+
 def _gpu(hidden, weight, K):
     from draft_tree_build_gb300 import bastion
     B, b, H = hidden.shape
