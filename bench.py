@@ -677,6 +677,71 @@ def run_reference(args, ws, rank):
             "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_lm_head(args, ws, rank, local, light=True):
+    """The fused drafter LM-head + top-K on the batched workload's drafter: the
+    32 x 16 final hidden states (hidden size 4,096, Qwen3-8B) times an output
+    embedding of 151,936 rows, top-64 per row; tensor-bound (0.64 TFLOP per
+    call), against the sustained bf16 peak (a kernel of ~0.6 ms launched back
+    to back runs under the power cap)."""
+    import torch
+
+    import synth
+    from draft_tree_build_gb300 import bastion
+
+    dev = torch.device(f"cuda:{local}")
+    B, b, H, V, K = 32, 16, 4096, 151936, 64
+    hid, w = synth.lm_head_inputs(B, b, H, V, seed=0xBA5710 + 6)
+    hd = torch.from_numpy(hid.view(np.int16)).view(torch.bfloat16).to(dev)
+    wd = torch.from_numpy(w.view(np.int16)).view(torch.bfloat16).to(dev)
+    del hid, w
+    t = bastion.alloc_topk(B, b, K, dev)
+    wsp = bastion.workspace(bastion.bastion_lm_head_topk_workspace_bytes(B, b, V, K), dev)
+    st = torch.zeros(B, dtype=torch.int32, device=dev)
+
+    def call():
+        bastion.bastion_lm_head_topk(hd, wd, K, t.logq, t.logit, t.tok, t.lse, wsp, st)
+
+    if args.profile_kernel:
+        for _ in range(args.launches):
+            call()
+        torch.cuda.synchronize()
+        return None
+    steps, warm = (20, 3) if light else (args.steps, args.warmup)
+    for _ in range(warm):
+        call()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    clocks = Clocks(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    elapsed_ms = max_over_ranks(e0.elapsed_time(e1), ws)
+    clk = clocks.stop()
+    assert int(st.abs().sum()) == 0, "device status bits set"
+    ms = elapsed_ms / steps
+    flops = 2.0 * B * b * H * V
+    pk_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    pk = json.load(open(pk_path)) if os.path.exists(pk_path) else {}
+    peak = float(pk.get("bf16_tflops_sustained", 1700.0))
+    kind = "measured" if pk else "fallback"
+    ach = flops / (ms * 1e-3) / 1e12
+    return {"workload": f"lmhead-b{B}x{b}-h{H}-v{V}-k{K}-bf16",
+            "metric": "fused drafter LM-head + top-K calls/s (512 x 4096 x 151936, top-64)",
+            "value": aggregate_rate(steps, elapsed_ms, ws), "unit": "calls/s", "steps": steps,
+            "ms_per_step": ms,
+            "roofline": {"bound": "tensor", "kernel": "lm_head_topk", "achieved": ach, "peak": peak,
+                         "unit": "TFLOP/s", "frac": ach / peak, "peak_source": f"{kind} bf16 (sustained)",
+                         "flops": flops},
+            "clocks": clk}
+
+
 # steps and warm-up of each other workload's line: microsecond steps get many
 # repetitions, the millisecond serving step a few
 SUB_STEPS = {1: (500, 20), 2: (500, 20), 4: (200, 10), 5: (10, 3)}
@@ -700,6 +765,9 @@ def other_workloads(args, ws, rank, local) -> dict:
         gc.collect()
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
+    out["lm_head"] = run_lm_head(args, ws, rank, local, light=True)
+    gc.collect()
+    torch.cuda.empty_cache()
     return out
 
 
@@ -711,9 +779,11 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", type=int, default=3, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--lm-head", action="store_true",
+                    help="only the fused drafter LM-head + top-K line")
     ap.add_argument("--no-workloads", action="store_true",
                     help="the headline line only (no table of the other four workloads)")
-    ap.add_argument("--profile-kernel", choices=["topk", "tree", "verify", "step", "attn"],
+    ap.add_argument("--profile-kernel", choices=["topk", "tree", "verify", "step", "attn", "lmhead"],
                     help="launch one kernel (or the step) --launches times and exit, for ncu")
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--temperature", type=float, default=0.0,
@@ -734,6 +804,13 @@ def main():
         return
 
     ws, rank, local = dist_setup()
+    if args.lm_head or args.profile_kernel == "lmhead":
+        res = run_lm_head(args, ws, rank, local, light=False)
+        if res is None:
+            print("profile launches done", flush=True)
+        elif rank == 0:
+            print(json.dumps(res), flush=True)
+        return
     if args.workload in (4, 5):
         res = run_with_attention(args, ws, rank, local)
     else:
