@@ -567,19 +567,38 @@ int64_t oracle_tree_attention(const uint16_t* q, const uint16_t* k, const uint16
 //    passes pi summing to 1) and is counted in N and A_hat; the stop rule is
 //    step 2's.
 //
+// Near ties (several correct results).  Unlike the single-proposal tree, two
+// candidates of equal depth are not compared on exact logit sums: log rho is a
+// log-sum-exp over the branches, and an implementation that forms it in
+// single precision is off by a few 1e-6.  So the band is 1e-5 here: a pop is
+// flagged when another candidate is within 1e-5 of the best in log rho, unless
+// it has the same parent and the same logit in every branch (then log rho is
+// the same function of the same numbers on any implementation, and the token
+// order decides); a stop test is flagged when
+// |rho_c C(N) - A_hat (C(N+1) - C(N))| < 1e-5 A_hat |C(N+1) - C(N)|.
+// With a guide (another implementation's tree: n_nodes, and parent and token
+// per node), the oracle follows the guide at a flagged step only, and only
+// when the guide's choice is itself within the band of the oracle's best.
+//
 // Inputs: topk_logit/topk_tok [B, Z, b, K]; lse [B, Z, b]; pi [B, Z];
-// root_token, ctx_len [B]; cost_ms [Bc, n_max+1]; l_ar [B].  Outputs as step 2
-// without rank: n_nodes; parent, depth, pos_id, token, log_rho, a_hat,
-// speedup [B, n_max]; anc_mask [B, n_max, W]; status [B].
+// root_token, ctx_len [B]; cost_ms [Bc, n_max+1]; l_ar [B]; the guide (may be
+// null).  Outputs as step 2 without rank: n_nodes; parent, depth, pos_id,
+// token, log_rho, a_hat, speedup [B, n_max]; anc_mask [B, n_max, W]; status
+// [B]; counters (may be null): flagged pops, flagged stops, guided steps.
 int oracle_build_tree_mixture(const float* topk_logit, const int32_t* topk_tok, const double* lse,
                               const double* pi, int B, int Z, int b, int K, int n_max,
                               const int32_t* root_token, const int32_t* ctx_len,
                               const float* cost_ms, int cost_per_request, const float* l_ar,
+                              const int32_t* guide_n_nodes, const int32_t* guide_parent,
+                              const int32_t* guide_token,
                               int32_t* n_nodes, int32_t* parent, int32_t* depth, int32_t* pos_id,
                               int32_t* token, double* log_rho, double* a_hat, double* speedup,
-                              uint32_t* anc_mask, int32_t* status) {
+                              uint32_t* anc_mask, int32_t* status, int32_t* n_flag_pop,
+                              int32_t* n_flag_stop, int32_t* n_guided) {
   if (B < 0 || Z < 1 || b < 1 || K < 1 || n_max < 1) return -1;
   const int W = (n_max + 31) / 32;
+  const double kBand = 1e-5;
+  int flag_pop = 0, flag_stop = 0, guided = 0;
   for (int r = 0; r < B; ++r) {
     // branch z, position k (0-based), rank j
     auto lg = [&](int z, int k, int j) {
@@ -660,10 +679,37 @@ int oracle_build_tree_mixture(const float* topk_logit, const int32_t* topk_tok, 
       int best = 0;
       for (int c = 1; c < (int)cands.size(); ++c)
         if (better(cands[c], cands[best])) best = c;
-      const Cand& c = cands[best];
+      bool pop_flag = false;
+      for (int c = 0; c < (int)cands.size(); ++c)
+        if (c != best && cands[best].lr - cands[c].lr < kBand &&
+            !(cands[c].p == cands[best].p && cands[c].ls == cands[best].ls))
+          pop_flag = true;
+      if (pop_flag) ++flag_pop;
+      int choice = best;
+      if (pop_flag && guide_parent && guide_n_nodes && n < guide_n_nodes[r]) {
+        const int gp = guide_parent[(int64_t)r * n_max + n];
+        const int gt = guide_token[(int64_t)r * n_max + n];
+        for (int c = 0; c < (int)cands.size(); ++c)
+          if (cands[c].p == gp && cands[c].t == gt && cands[best].lr - cands[c].lr < kBand) {
+            if (c != best) ++guided;
+            choice = c;
+            break;
+          }
+      }
+      const Cand& c = cands[choice];
       if (c.lr == -kInf) break;
       const double rho = std::exp(c.lr);
-      if (S_of(A + rho, n + 1) < S_of(A, n)) break;  // S would decrease: keep T_n
+      bool stop = S_of(A + rho, n + 1) < S_of(A, n);  // S would decrease: keep T_n
+      const double dC = (double)C[n + 1] - (double)C[n];
+      if (dC != 0.0 && std::fabs(rho * (double)C[n] - A * dC) < kBand * A * std::fabs(dC)) {
+        ++flag_stop;
+        if (guide_n_nodes) {
+          const bool gstop = guide_n_nodes[r] == n;
+          if (gstop != stop) ++guided;
+          stop = gstop;
+        }
+      }
+      if (stop) break;
       const int i = n++;
       kids[c.p].push_back(c.t);
       A += rho;
@@ -675,6 +721,9 @@ int oracle_build_tree_mixture(const float* topk_logit, const int32_t* topk_tok, 
     n_nodes[r] = n;
     if (status) status[r] = st;
   }
+  if (n_flag_pop) *n_flag_pop = flag_pop;
+  if (n_flag_stop) *n_flag_stop = flag_stop;
+  if (n_guided) *n_guided = guided;
   return 0;
 }
 

@@ -52,7 +52,7 @@ def lib():
         L.oracle_lm_head_topk.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
         L.oracle_lm_head_topk.restype = i32
         L.oracle_build_tree_mixture.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp,
-                                                i32, vp] + [vp] * 10
+                                                i32, vp, vp, vp, vp] + [vp] * 10 + [vp, vp, vp]
         L.oracle_build_tree_mixture.restype = i32
         L.oracle_build_tree.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, i32, vp, i32,
                                         vp, vp, vp] + [vp] * 11 + [vp, vp, vp]
@@ -118,13 +118,17 @@ class MixTree:
     speedup: np.ndarray
     anc_mask: np.ndarray  # uint32 [B, n_max, W]
     status: np.ndarray
+    flagged_pops: int = 0
+    flagged_stops: int = 0
+    guided: int = 0
 
 
 def build_tree_mixture(topk_logit, topk_tok, lse, pi, n_max: int, root_token, ctx_len, cost_ms,
-                       l_ar) -> MixTree:
+                       l_ar, guide=None) -> MixTree:
     """Best-first tree on the latent-mixture path score.  topk_logit/tok
     [B, Z, b, K]; lse [B, Z, b] fp64; pi [B, Z] (rows summing to 1); cost_ms
-    [Bc, n_max+1] (Bc = 1 or B)."""
+    [Bc, n_max+1] (Bc = 1 or B); guide: optional (n_nodes, parent, token) of
+    another implementation's tree, followed only at near-tie steps."""
     lg = np.ascontiguousarray(topk_logit, dtype=np.float32)
     tk = np.ascontiguousarray(topk_tok, dtype=np.int32)
     ls = np.ascontiguousarray(lse, dtype=np.float64)
@@ -136,15 +140,22 @@ def build_tree_mixture(topk_logit, topk_tok, lse, pi, n_max: int, root_token, ct
                   np.zeros((B, n_max), np.int32), np.zeros((B, n_max), np.int32),
                   np.zeros((B, n_max), np.int32), np.zeros((B, n_max)), np.zeros((B, n_max)),
                   np.zeros((B, n_max)), np.zeros((B, n_max, W), np.uint32), np.zeros(B, np.int32))
+    g = [None, None, None]
+    if guide is not None:
+        g = [np.ascontiguousarray(x, dtype=np.int32) for x in guide]
+    fp, fs, gd = ctypes.c_int32(0), ctypes.c_int32(0), ctypes.c_int32(0)
     rc = lib().oracle_build_tree_mixture(
         _p(lg), _p(tk), _p(ls), _p(pz), B, Z, b, K, n_max,
         _p(np.ascontiguousarray(root_token, dtype=np.int32)),
         _p(np.ascontiguousarray(ctx_len, dtype=np.int32)), _p(cost), int(cost.shape[0] == B and B > 1),
-        _p(np.ascontiguousarray(l_ar, dtype=np.float32)), _p(out.n_nodes), _p(out.parent),
+        _p(np.ascontiguousarray(l_ar, dtype=np.float32)), _p(g[0]), _p(g[1]), _p(g[2]),
+        _p(out.n_nodes), _p(out.parent),
         _p(out.depth), _p(out.pos_id), _p(out.token), _p(out.log_rho), _p(out.a_hat),
-        _p(out.speedup), _p(out.anc_mask), _p(out.status))
+        _p(out.speedup), _p(out.anc_mask), _p(out.status), ctypes.byref(fp), ctypes.byref(fs),
+        ctypes.byref(gd))
     if rc != 0:
         raise ValueError("oracle_build_tree_mixture: bad arguments")
+    out.flagged_pops, out.flagged_stops, out.guided = fp.value, fs.value, gd.value
     return out
 
 

@@ -148,3 +148,83 @@ def test_invariants_and_branch_relabelling():
                                    ctx, _flat(n_max), lar)
     assert np.array_equal(m.parent, m2.parent) and np.array_equal(m.token, m2.token)
     assert np.allclose(m.log_rho, m2.log_rho, rtol=0, atol=1e-12)
+
+
+def _tie_case():
+    """Z = 2, pi = (1/2, 1/2), b = 2, K = 2, logits log p with lse = 0:
+    position 1: branch 0 {10: 1/2, 11: 1/4}, branch 1 {10: 1/2, 12: 1/4};
+    position 2: branch 0 {20: 1/2, 21: 1/2}, branch 1 {20: 1/2, 22: 1/4}.
+    rho: (10) 1/2, (10,20) 1/4, then (11), (12) and (10,21) all 1/8: a tie
+    across depths 1 and 2 and across branches."""
+    tk = np.array([[[[10, 11], [20, 21]], [[10, 12], [20, 22]]]], np.int32)
+    p = np.array([[[[0.5, 0.25], [0.5, 0.5]], [[0.5, 0.25], [0.5, 0.25]]]])
+    lg = np.log(p).astype(np.float32)
+    ls = np.zeros((1, 2, 2))
+    pi = np.array([[0.5, 0.5]])
+    return lg, tk, ls, pi
+
+
+def test_tie_across_depths_is_flagged_and_follows_the_guide():
+    lg, tk, ls, pi = _tie_case()
+    n_max = 6
+    roots, ctx, lar = _common(1)
+    m = oracle.build_tree_mixture(lg, tk, ls, pi, n_max, roots, ctx, _flat(n_max), lar)
+    # own order: the tie goes to the lower depth, then to the lower token
+    assert m.token[0, :6].tolist() == [0, 10, 20, 11, 12, 21]
+    assert m.parent[0, :6].tolist() == [-1, 0, 1, 0, 0, 1]
+    assert np.allclose(np.exp(m.log_rho[0, :6]), [1, 0.5, 0.25, 0.125, 0.125, 0.125], rtol=1e-12)
+    assert m.flagged_pops >= 2 and m.guided == 0
+    # a guide that takes the depth-2 node first is followed at the flagged pop
+    guide = (np.array([6], np.int32), np.array([[-1, 0, 1, 1, 0, 0]], np.int32),
+             np.array([[0, 10, 20, 21, 11, 12]], np.int32))
+    g = oracle.build_tree_mixture(lg, tk, ls, pi, n_max, roots, ctx, _flat(n_max), lar, guide=guide)
+    assert g.guided == 1
+    assert g.parent[0].tolist() == guide[1][0].tolist() and g.token[0].tolist() == guide[2][0].tolist()
+    assert g.a_hat[0, 5] == pytest.approx(m.a_hat[0, 5], rel=1e-12)
+
+
+def test_guide_outside_the_band_is_ignored():
+    lg, tk, ls, pi = _tie_case()
+    n_max = 6
+    roots, ctx, lar = _common(1)
+    m = oracle.build_tree_mixture(lg, tk, ls, pi, n_max, roots, ctx, _flat(n_max), lar)
+    # at the flagged pop the guide names (11, 20), rho 1/16: not a near tie
+    guide = (np.array([6], np.int32), np.array([[-1, 0, 1, 3, 0, 0]], np.int32),
+             np.array([[0, 10, 20, 20, 11, 12]], np.int32))
+    g = oracle.build_tree_mixture(lg, tk, ls, pi, n_max, roots, ctx, _flat(n_max), lar, guide=guide)
+    assert g.guided == 0
+    assert np.array_equal(g.parent, m.parent) and np.array_equal(g.token, m.token)
+
+
+def test_stop_at_the_boundary_is_flagged_and_follows_the_guide():
+    """After the root (A_hat = 1) the best candidate has rho = 1/2; with
+    C(1) = 2 and C(2) = 3 the stop test rho C(1) < A_hat (C(2) - C(1)) is an
+    equality: either tree is correct."""
+    lg, tk, ls, pi = _tie_case()
+    n_max = 4
+    roots, ctx, lar = _common(1)
+    c = np.array([[0.0, 2.0, 3.0, 3.0, 3.0]], np.float32)
+    m = oracle.build_tree_mixture(lg, tk, ls, pi, n_max, roots, ctx, c, lar)
+    assert m.flagged_stops >= 1
+    stop = (np.array([1], np.int32), np.full((1, n_max), -1, np.int32), np.zeros((1, n_max), np.int32))
+    g = oracle.build_tree_mixture(lg, tk, ls, pi, n_max, roots, ctx, c, lar, guide=stop)
+    assert int(g.n_nodes[0]) == 1
+    go = (np.array([4], np.int32), np.array([[-1, 0, 1, 0]], np.int32),
+          np.array([[0, 10, 20, 11]], np.int32))
+    g2 = oracle.build_tree_mixture(lg, tk, ls, pi, n_max, roots, ctx, c, lar, guide=go)
+    assert int(g2.n_nodes[0]) == 4       # C flat after N = 2: nothing else stops it
+    assert g2.token[0, :4].tolist() == [0, 10, 20, 11]
+    assert g.guided + g2.guided == 1     # the oracle's own decision matches one of the two
+
+
+def test_no_flags_on_random_logits_without_ties():
+    """Random fp32 logits: near ties within 1e-5 are rare; identical branch
+    copies tie only within one parent with identical logits, never flagged."""
+    B, Z, b, V, K, n_max = 2, 3, 5, 300, 6, 30
+    lg, tk, ls = _branch_topk(B, 1, b, V, K, 2)
+    rep = lambda a: np.repeat(a, Z, axis=1)
+    pi = np.tile([0.2, 0.3, 0.5], (B, 1))
+    roots, ctx, lar = _common(B)
+    m = oracle.build_tree_mixture(rep(lg), rep(tk), rep(ls), pi, n_max, roots, ctx, _flat(n_max), lar)
+    t = oracle.build_tree(lg[:, 0], tk[:, 0], ls[:, 0], n_max, roots, ctx, _flat(n_max), lar)
+    assert m.flagged_pops == t.flagged_pops == 0
