@@ -742,6 +742,84 @@ def run_lm_head(args, ws, rank, local, light=True):
             "clocks": clk}
 
 
+def run_mixture(args, ws, rank, local, light=True):
+    """Best-first trees on a latent-mixture proposal (DBlast's dependent block
+    proposal, Bastion's controller): B = 32 requests, Z = 4 branches, b = 16
+    positions, the top-64 of each branch's bf16 logits over 151,936 tokens
+    (found by the top-K kernel before the timed region), n_max = 128 and a flat
+    cost table, so every tree fills the budget: the longest build.  The build
+    is one warp's sequence of pops per request, bound by latency; the HBM
+    figure relates the inputs it reads to the call's time."""
+    import torch
+
+    import synth
+    from draft_tree_build_gb300 import bastion
+
+    dev = torch.device(f"cuda:{local}")
+    B, Z, b, V, K, n_max = 32, 4, 16, 151936, 64, 128
+    x, pi = synth.mixture_inputs(B, Z, b, V, seed=0xBA5710 + 7)
+    xd = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev).view(B * Z, b, V)
+    del x
+    t = bastion.alloc_topk(B * Z, b, K, dev)
+    st = torch.zeros(B * Z, dtype=torch.int32, device=dev)
+    wsp = bastion.workspace(bastion.bastion_topk_marginals_workspace_bytes(B * Z, b, V, K), dev)
+    bastion.bastion_topk_marginals(xd, K, t.logq, t.logit, t.tok, t.lse, wsp, st)
+    torch.cuda.synchronize()
+    del xd, wsp
+    lg, tk, ls = t.logit.view(B, Z, b, K), t.tok.view(B, Z, b, K), t.lse.view(B, Z, b)
+    pid = torch.from_numpy(np.ascontiguousarray(pi)).to(dev)
+    w = synth.workload(3)
+    roots = torch.from_numpy(synth.root_tokens(w)).to(dev)
+    ctx = torch.from_numpy(synth.ctx_lens(w)).to(dev)
+    lar = torch.from_numpy(synth.l_ar(w)).to(dev)
+    cost = torch.full((n_max + 1,), 5.0, dtype=torch.float32, device=dev)
+    tr = bastion.alloc_tree(B, n_max, dev)
+
+    def call():
+        bastion.bastion_build_tree_mixture(lg, tk, ls, pid, n_max, roots, ctx, cost, lar, tr.n_nodes,
+                                           tr.parent, tr.depth, tr.pos_id, tr.token, tr.log_rho,
+                                           tr.a_hat, tr.speedup, tr.anc_mask, st[:B])
+
+    if args.profile_kernel:
+        for _ in range(args.launches):
+            call()
+        torch.cuda.synchronize()
+        return None
+    steps, warm = (200, 10) if light else (args.steps, args.warmup)
+    for _ in range(warm):
+        call()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    clocks = Clocks(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    elapsed_ms = max_over_ranks(e0.elapsed_time(e1), ws)
+    clk = clocks.stop()
+    assert int(st.abs().sum()) == 0, "device status bits set"
+    assert int(tr.n_nodes.min()) == n_max
+    ms = elapsed_ms / steps
+    # inputs read per call: logits, tokens (4 B each per entry), lse, pi, cost
+    nbytes = B * Z * b * K * 8 + B * Z * b * 8 + B * Z * 8 + (n_max + 1) * 4
+    hbm, peak_kind = peaks()
+    ach = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": f"mixture-b{B}-z{Z}-b{b}-k{K}-n{n_max}-flat",
+            "metric": "latent-mixture tree builds/s (32 requests, Z=4, K=64, n_max=128, every tree full)",
+            "value": aggregate_rate(steps, elapsed_ms, ws), "unit": "calls/s", "steps": steps,
+            "ms_per_step": ms, "us_per_call": ms * 1e3,
+            "roofline": {"bound": "hbm", "kernel": "build_tree_mixture", "achieved": ach, "peak": hbm,
+                         "unit": "GB/s", "frac": ach / hbm, "peak_source": f"{peak_kind} copy bandwidth",
+                         "note": "one warp's sequential pops per request: latency-bound, not HBM-bound"},
+            "clocks": clk}
+
+
 # steps and warm-up of each other workload's line: microsecond steps get many
 # repetitions, the millisecond serving step a few
 SUB_STEPS = {1: (500, 20), 2: (500, 20), 4: (200, 10), 5: (10, 3)}
@@ -768,6 +846,9 @@ def other_workloads(args, ws, rank, local) -> dict:
     out["lm_head"] = run_lm_head(args, ws, rank, local, light=True)
     gc.collect()
     torch.cuda.empty_cache()
+    out["mixture"] = run_mixture(args, ws, rank, local, light=True)
+    gc.collect()
+    torch.cuda.empty_cache()
     return out
 
 
@@ -783,7 +864,10 @@ def main():
                     help="only the fused drafter LM-head + top-K line")
     ap.add_argument("--no-workloads", action="store_true",
                     help="the headline line only (no table of the other four workloads)")
-    ap.add_argument("--profile-kernel", choices=["topk", "tree", "verify", "step", "attn", "lmhead"],
+    ap.add_argument("--mixture", action="store_true",
+                    help="only the latent-mixture tree line")
+    ap.add_argument("--profile-kernel", choices=["topk", "tree", "verify", "step", "attn", "lmhead",
+                                                 "mixture"],
                     help="launch one kernel (or the step) --launches times and exit, for ncu")
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--temperature", type=float, default=0.0,
@@ -804,6 +888,13 @@ def main():
         return
 
     ws, rank, local = dist_setup()
+    if args.mixture or args.profile_kernel == "mixture":
+        res = run_mixture(args, ws, rank, local, light=False)
+        if res is None:
+            print("profile launches done", flush=True)
+        elif rank == 0:
+            print(json.dumps(res), flush=True)
+        return
     if args.lm_head or args.profile_kernel == "lmhead":
         res = run_lm_head(args, ws, rank, local, light=False)
         if res is None:

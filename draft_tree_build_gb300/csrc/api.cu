@@ -161,8 +161,8 @@ int bastion_build_tree_mixture(const float *topk_logit, const int32_t *topk_tok,
       !n_nodes || !parent || !depth || !pos_id || !token || !log_rho || !a_hat || !speedup ||
       !anc_mask || !status)
     return BASTION_ERR_NULL;
-  if (B < 1 || B > (1 << 24) || Z < 1 || Z > 8 || b < 1 || b > 32 || K < 1 || K > 64 ||
-      Z * K > 256 || n_max < 1 || n_max > 256)
+  if (B < 1 || B > (1 << 24) || Z < 1 || Z > 32 || b < 1 || b > 32 || K < 1 || K > 1024 ||
+      n_max < 1 || n_max > 256)
     return BASTION_ERR_SIZE;
   if (!aligned(lse, 8) || !aligned(pi, 8)) return BASTION_ERR_ALIGN;
   if (bastion::mixture_tree_smem_bytes(Z, b, K, n_max) > (size_t)227 * 1024) return BASTION_ERR_UNSUPPORTED;

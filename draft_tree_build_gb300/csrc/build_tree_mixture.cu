@@ -13,37 +13,89 @@
 // Inputs per request: each branch's K ranked tokens per block position (the
 // top-K step run per branch: logits, tokens, lse) and the branch weights pi.
 // A token outside branch z's list at position k has q_k^z = 0; the children of
-// a depth-d node are the union over z of the branches' tokens at position d+1.
+// a depth-d node are the union U over z of the branches' tokens at position
+// d+1.
 //
-// One warp builds one request's tree (requests are independent CTAs); this is
-// the parity form of the step, in fp64 throughout:
-//  * per position d, the union U_d of the branches' tokens is tabulated once,
-//    with each branch's logit for each union token (-inf where absent);
-//  * node n keeps, per branch, the sum of its path's logits (fp64) and one
-//    pending candidate, its best untaken child under (log rho descending,
-//    token ascending); a child's log rho is log sum_z exp(log pi_z + (logit
-//    sum - lse sum)), with the largest term factored out;
-//  * a pop takes the best pending candidate over the nodes under (log rho
-//    descending, depth, token, parent ascending), runs the stop test
-//    (A_hat + rho) L / C(N+1) < A_hat L / C(N), and then rescans two child
-//    lists with warp-parallel argmaxes: the parent's (its next-best untaken
-//    child) and the new node's.
-// There is no wait of any kind: every loop is bounded by the tree budget or
-// a table size.
+// Arithmetic (no fp64 after the per-request set-up):
+//  * Per node n and branch z, P_z(n) = log pi_z + sum over the path of
+//    (logit - lse) in branch z, a 64-bit fixed-point integer (2^-40 units) as
+//    in the single-proposal tree; -inf where the path leaves branch z's lists.
+//  * Position tables: E = exp(logit - max logit of its row) in fp32 for every
+//    branch-rank entry, stored per union token and branch.
+//  * Node weights: with X_z = P_z(n) + (max logit - lse) of branch z at the
+//    children's position and S_n = max_z X_z, w_z(n) = exp(X_z - S_n) in fp32,
+//    so the best child of n has sum_z w_z E >= 1.  A child u of n then has
+//    rho = exp(S_n) sum_z w_z(n) E_z(u): Z fused multiply-adds in branch order,
+//    no transcendental.  Both exponentials reduce their argument in fixed
+//    point (x = k ln 2 + f) before one expf, so each is within 2.2 2^-23
+//    (relative).
+//  * The child's score is S_n + log of that sum, with the log split into
+//    exponent * ln 2 (fixed point) and logf of a mantissa in [2^-1/2, 2^1/2):
+//    within (5 + Z/2) 2^-23 of the exact log rho (two exponentials, Z
+//    roundings of the sum, the log), about 8e-7 for Z = 4 and 2.5e-6 for
+//    Z = 32, inside the 1e-5 band of the mixture oracle's near-tie flags.
+//  * When a node's best remaining child falls below 2^-100 (its sum loses
+//    precision to fp32 underflow), that node's scan is redone in the log
+//    domain: the largest branch term of each child in fixed point first, then
+//    the sums rescaled by it.
+//
+// Work layout: one CTA per request.  Its 256 threads stage the tables: the
+// request's lists with several loads in flight per thread, the union of each
+// position's tokens by hashing into shared memory and a warp-ballot
+// compaction, then E per (union token, branch).  Node n's pending candidate,
+// its best untaken child, is kept in lane n % 32, register slot n / 32, as a
+// 96-bit key (order-preserving image of the score, then a tie word from depth
+// and node) with its union index and token, and found by three redux.sync per
+// pop.  A pop runs the stop test rho C(N) < A_hat (C(N+1) - C(N)) in fp32 with
+// A_hat summed with Kahan compensation, adds the node (lane z forms its P_z
+// from the branch's rank of the token and the node's weights from P_z), and
+// rescans two child lists: the parent's (its next-best child) and the new
+// node's (its best child).
+//
+// Two forms of the child tables, the same arithmetic in the same order:
+//  * dense (Z <= 8, when the tables fit in shared memory): per union token,
+//    its E and rank in every branch (padded to ZP = 1, 2, 4 or 8 branches).
+//    Four warps run the pops, one per SM sub-partition: each holds the same
+//    pending keys and takes the same decisions, and each scans every fourth
+//    block of 32 union tokens (one vector load and ZP FMAs per token, the
+//    argmax folded in) and owns the taken-bits of those blocks; their four
+//    partial argmaxes meet through shared memory at one named barrier per
+//    pop (double-buffered, so a warp is at most one pop ahead).  A pop on
+//    one warp was bound by instruction issue on a single sub-partition.
+//  * sparse (otherwise): E and union index per branch-rank entry; warp 0 runs
+//    the pops alone, a scan accumulating per-token sums in shared memory one
+//    branch at a time (a branch lists a token at most once, so no two lanes
+//    of a pass collide), then taking the argmax.
+// Every loop is bounded by the tree budget or a table size; the named barrier
+// is reached the same number of times by all four warps (they take identical
+// decisions from identical data), and there are no other waits.
+#include <climits>
 #include <cmath>
 
 #include "common.cuh"
+#include "tree_build.cuh"
 
 namespace bastion {
 
 namespace {
+
+using tb::kInfCut;
+using tb::kNegFix;
+
+constexpr int kMixThreads = 256;
+constexpr int kPopWarps = 4;  // dense form: the warps that run the pops
+constexpr int kEmptySlot = INT_MIN;
+constexpr int64_t kLn2Fix = 762123384786ll;  // ln 2 in 2^-40 units, rounded
+constexpr int64_t kExpCut = -(104ll << 40);  // exp of less is 0 in fp32
+constexpr int64_t kVeryNeg = kNegFix * 2;    // below every finite score
+constexpr float kTiny = 7.888609052210118e-31f;  // 2^-100
 
 struct MixArgs {
   const float *topk_logit;  // [B, Z, b, K]
   const int32_t *topk_tok;  // [B, Z, b, K]
   const double *lse;        // [B, Z, b]
   const double *pi;         // [B, Z]
-  int B, Z, b, K, n_max, W, E, UW;
+  int B, Z, b, K, n_max;
   const int32_t *root_token, *ctx_len;
   const float *cost;
   int cost_per_request;
@@ -54,298 +106,965 @@ struct MixArgs {
   int32_t *status;
 };
 
-// Shared-memory layout for one request (fp64 arrays first, 8-byte aligned).
+// Shared-memory layout for one request.  Region 1 (the position tables) lives
+// through the build; region 2 holds one group of positions' staging arrays
+// while the tables are built and the node arrays afterwards.  Entry
+// e = (d Z + z) K + j is branch z's rank-j token at block position d + 1;
+// union token u of position d + 1 is slot d ZK + u.  ZP = 0: the sparse form.
 struct MixLayout {
-  size_t lam, lpi, ls, plr, lr;                       // double
-  size_t ulg, utok, nu, cost, par, dep, tok, ah, sp;  // 4-byte
-  size_t ptok, pu, mask, taken, etok, efirst, umap;
+  size_t flse, fmax, mq, lg, utok, cost, nu;  // region 1, both forms
+  size_t ue;                                  // region 1, both forms
+  size_t dE, dR;                              // region 1, dense form
+  size_t ee;                                  // region 1, sparse form
+  size_t pn, sn, lrn, acc, wz, an, taken, mask, par, dep, tok, pu, pt, part;  // region 2: nodes
+  size_t rtok, eu, hk;                        // region 2: staging of one group
+  int H, G;  // hash slots per position, positions per staging group
   size_t bytes;
 };
 
-__host__ __device__ inline MixLayout mix_layout(int Z, int b, int E, int n_max, int W, int UW) {
+__host__ __device__ inline MixLayout mix_layout(int Z, int b, int K, int n_max, int ZP) {
   MixLayout l;
+  const size_t ZK = (size_t)Z * K, E = (size_t)b * ZK;
+  const size_t W = (n_max + 31) / 32, UW = (ZK + 31) / 32, n = (size_t)n_max;
+  int H = 64;
+  while ((size_t)H < 2 * ZK) H <<= 1;
   size_t o = 0;
-  auto take = [&](size_t n) { const size_t at = o; o += n; return at; };
-  l.lam = take((size_t)Z * (b + 1) * 8);
-  l.lpi = take((size_t)Z * 8);
-  l.ls = take((size_t)n_max * Z * 8);
-  l.plr = take((size_t)n_max * 8);
-  l.lr = take((size_t)n_max * 8);
-  l.ulg = take((size_t)b * E * Z * 4);
-  l.utok = take((size_t)b * E * 4);
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += (bytes + 15) & ~(size_t)15;
+    return at;
+  };
+  l.flse = take((size_t)b * Z * 8);
+  l.fmax = take((size_t)b * Z * 8);
+  l.mq = take((size_t)b * Z * 8);
+  l.lg = take(E * 4);
+  l.utok = take(E * 4);
+  l.cost = take((n + 1) * 4);
   l.nu = take((size_t)b * 4);
-  l.cost = take((size_t)(n_max + 1) * 4);
-  l.par = take((size_t)n_max * 4);
-  l.dep = take((size_t)n_max * 4);
-  l.tok = take((size_t)n_max * 4);
-  l.ah = take((size_t)n_max * 4);
-  l.sp = take((size_t)n_max * 4);
-  l.ptok = take((size_t)n_max * 4);
-  l.pu = take((size_t)n_max * 4);
-  l.mask = take((size_t)n_max * W * 4);
-  l.taken = take((size_t)n_max * UW * 4);
-  l.etok = take((size_t)E * 4);
-  l.efirst = take((size_t)E * 4);
-  l.umap = take((size_t)E * 4);
-  l.bytes = o;
+  l.dE = l.dR = l.ee = 0;
+  l.ue = take(E * 2);
+  if (ZP > 0) {
+    l.dE = take(E * ZP * 4);
+    l.dR = take(E * ZP * 2);
+  } else {
+    l.ee = take(E * 4);
+  }
+  const size_t r2 = o;
+  const size_t copies = ZP > 0 ? kPopWarps : 1;  // per-warp copies of P, S and w
+  l.pn = take(copies * n * Z * 8);
+  l.sn = take(copies * n * 8);
+  l.lrn = take(n * 8);
+  l.acc = ZP > 0 ? 0 : take(2 * ZK * 4);  // also ZK int64 in the log-domain rescan
+  l.wz = take(copies * n * Z * 4);
+  l.an = take(n * 4);
+  l.taken = take(n * UW * 4);
+  l.mask = take(n * W * 4);
+  l.par = take(n * 4);
+  l.dep = take(n * 4);
+  l.tok = take(n * 4);
+  l.pu = take(copies * n * 4);
+  l.pt = take(copies * n * 4);
+  l.part = ZP > 0 ? take(2 * 2 * kPopWarps * 16) : 0;
+  const size_t node_bytes = o - r2;
+  const size_t per_pos = ((ZK * 4 + 15) & ~(size_t)15) + ((ZK * 2 + 15) & ~(size_t)15) + (size_t)H * 4;
+  const size_t cap = node_bytes > 65536 ? node_bytes : 65536;
+  int G = (int)(cap / per_pos);
+  G = G < 1 ? 1 : (G > b ? b : G);
+  o = r2;
+  l.rtok = take((size_t)G * ZK * 4);
+  l.eu = take((size_t)G * ZK * 2);
+  l.hk = take((size_t)G * H * 4);
+  l.H = H;
+  l.G = G;
+  const size_t stage_bytes = o - r2;
+  l.bytes = r2 + (node_bytes > stage_bytes ? node_bytes : stage_bytes);
   return l;
 }
 
-constexpr double kNegInf = -INFINITY;
-
-// (score, depth, token, node) order: true when a is better than b.
-__device__ __forceinline__ bool mix_better(double sa, int da, int ta, int na, double sb, int db,
-                                           int tb, int nb) {
-  if (sa != sb) return sa > sb;
-  if (da != db) return da < db;
-  if (ta != tb) return ta < tb;
-  return na < nb;
+// The dense width for Z branches (0: the sparse form only).
+__host__ __device__ inline int dense_width(int Z) {
+  return Z == 1 ? 1 : Z == 2 ? 2 : Z <= 4 ? 4 : Z <= 8 ? 8 : 0;
 }
 
-__global__ void __launch_bounds__(32) build_tree_mixture_kernel(MixArgs a) {
+struct MixSm {
+  const int64_t *flse, *fmax, *mq;
+  const float *lg, *C;
+  const int *utok, *nu;
+  const float *dE, *Ee;
+  const int16_t *dR;
+  const uint16_t *ue;
+  int64_t *Pn, *Sn, *lrn;
+  float *acc, *wz, *An;
+  uint32_t *taken, *mask;
+  int *par, *dep, *tok, *pu, *pt;  // pu, pt: the pending child's union index and token
+  int Z, K, ZK, UW, W, b;
+};
+
+// The conversions below use 32-bit converts and integer shifts only: a
+// conversion between a 64-bit integer and a float costs about a hundred
+// cycles on this part, more than the rest of a pop step.
+
+// round(x 2^40) for a logit x, as tb::fix_logit (clamped to 2^17; -inf and
+// NaN give kNegFix), from the float's fields.
+__device__ __forceinline__ int64_t fix_f32(float x) {
+  if (!(x > -INFINITY)) return kNegFix;
+  x = fminf(fmaxf(x, -tb::kMaxLogit), tb::kMaxLogit);
+  const uint32_t bits = __float_as_uint(x);
+  const int ex = (int)((bits >> 23) & 0xFFu);
+  if (ex == 0) return 0;  // zero or subnormal: below 2^-126
+  const int64_t m = (int64_t)((bits & 0x7FFFFFu) | 0x800000u);
+  const int sh = ex - 127 - 23 + 40;  // x 2^40 = m 2^sh, sh <= 34
+  int64_t v;
+  if (sh >= 0) {
+    v = m << sh;
+  } else if (sh < -24) {
+    v = 0;  // below 2^-1
+  } else {  // round half to even
+    const int r = -sh;
+    const int64_t q = m >> r, rem = m & ((1ll << r) - 1), half = 1ll << (r - 1);
+    v = q + ((rem > half || (rem == half && (q & 1))) ? 1 : 0);
+  }
+  return (bits >> 31) ? -v : v;
+}
+
+// exp(D 2^-40) for D <= 0: k = nearest integer to x / ln 2 from an estimate of
+// x within 2^-8, f = D - k ln 2 exactly in fixed point (|f| < 0.36), result
+// 2^k expf(f) with f rounded to 2^-31 first.
+__device__ __forceinline__ float exp_fix(int64_t D) {
+  if (D < kExpCut) return 0.f;
+  const float xa = (float)(int)(D >> 32) * 0.00390625f;
+  const int k = __float2int_rn(xa * 1.4426950408889634f);
+  const int64_t f = D - (int64_t)k * kLn2Fix;
+  const float ff = (float)(int)(f >> 9) * 4.656612873077393e-10f;
+  return ldexpf(expf(ff), k);
+}
+
+// log(v) in 2^-40 units for a normal float v > 0: v = m 2^e with m in
+// [2^-1/2, 2^1/2] from the float's fields, e ln 2 in fixed point, logf(m)
+// (|logf(m)| < 0.35) rounded to 2^-30.
+__device__ __forceinline__ int64_t log_fix(float v) {
+  const uint32_t bits = __float_as_uint(v);
+  int e = (int)(bits >> 23) - 127;
+  float m = __uint_as_float((bits & 0x7FFFFFu) | 0x3F800000u);  // [1, 2)
+  if (m > 1.41421356f) {
+    m *= 0.5f;
+    ++e;
+  }
+  return (int64_t)e * kLn2Fix + ((int64_t)__float2int_rn(logf(m) * 1073741824.f) << 10);
+}
+
+__device__ __forceinline__ int64_t warp_max_i64(int64_t x) {
+  const uint64_t k = tb::key_of(x);
+  const uint32_t h = __reduce_max_sync(kFull, (uint32_t)(k >> 32));
+  const uint32_t l = __reduce_max_sync(kFull, (uint32_t)(k >> 32) == h ? (uint32_t)k : 0u);
+  return (int64_t)((((uint64_t)h << 32) | l) ^ 0x8000000000000000ull);
+}
+
+struct Pick {
+  float v;     // the best untaken child's scaled rho (0: none with a positive sum)
+  int t, u;    // its token and union index
+  bool any;    // some untaken child exists
+};
+
+// The warp's best of the lanes' (value desc, token asc) candidates.
+__device__ __forceinline__ Pick warp_pick(float bv, int bt, int bu, bool any) {
+  const uint32_t vb = __float_as_uint(bv);  // bv >= 0: the bits order as the values
+  const uint32_t m = __reduce_max_sync(kFull, vb);
+  const int tm = __reduce_min_sync(kFull, vb == m ? bt : INT_MAX);
+  const uint32_t who = __ballot_sync(kFull, vb == m && bt == tm);
+  Pick p;
+  p.u = __shfl_sync(kFull, bu, __ffs(who) - 1);
+  p.v = __uint_as_float(m);
+  p.t = tm;
+  p.any = __any_sync(kFull, any);
+  return p;
+}
+
+// A lane's best (value desc, token asc) by value alone; the tokens are read
+// only on an exact tie.
+__device__ __forceinline__ void lane_track(float v, int u, const int *ut, float &bv, int &bu) {
+  if (v > bv) {
+    bv = v;
+    bu = u;
+  } else if (v == bv && v > 0.f && ut[u] < ut[bu]) {
+    bu = u;
+  }
+}
+
+// ---------------------------------------------------------------- dense form
+
+template <int ZP>
+__device__ __forceinline__ void load_e(const float *p, float (&e)[ZP]) {
+  if constexpr (ZP == 1) {
+    e[0] = p[0];
+  } else if constexpr (ZP == 2) {
+    const float2 v = *reinterpret_cast<const float2 *>(p);
+    e[0] = v.x;
+    e[1] = v.y;
+  } else {
+#pragma unroll
+    for (int h = 0; h < ZP / 4; ++h) {
+      const float4 v = reinterpret_cast<const float4 *>(p)[h];
+      e[4 * h] = v.x;
+      e[4 * h + 1] = v.y;
+      e[4 * h + 2] = v.z;
+      e[4 * h + 3] = v.w;
+    }
+  }
+}
+
+// This warp's part of the picks for node qa (row da, taken-bits apply) and
+// for the new node qb (row db, nothing taken; qb = -1 for none): blocks
+// c = warp, warp + 4, ... of 32 union tokens, lane l taking u = 32 c + l.
+template <int ZP>
+__device__ __forceinline__ void part_pick(const MixSm &s, int lane, int warp, int qa, int da,
+                                          const float (&wa)[ZP], int qb, int db,
+                                          const float (&wb)[ZP], Pick &pa, Pick &pb) {
+  const int na = s.nu[da], nb = qb >= 0 ? s.nu[db] : 0, dbb = qb >= 0 ? db : 0;
+  const float *Ea = s.dE + da * s.ZK * ZP, *Eb = s.dE + dbb * s.ZK * ZP;
+  const uint32_t *tk = s.taken + qa * s.UW;
+  const int *uta = s.utok + da * s.ZK, *utb = s.utok + dbb * s.ZK;
+  float bva = 0.f, bvb = 0.f;
+  int bua = -1, bub = -1;
+  bool anya = false;
+  const int nm = na > nb ? na : nb;
+#pragma unroll 2
+  for (int c = warp; c * 32 < nm; c += kPopWarps) {
+    const int u = c * 32 + lane;
+    float va = 0.f, vb = 0.f;
+    uint32_t tw = 1u << lane;  // past the row: as if taken
+    if (u < na) {
+      float e[ZP];
+      load_e<ZP>(Ea + u * ZP, e);
+      tw = tk[c];
+#pragma unroll
+      for (int z = 0; z < ZP; ++z) va = fmaf(wa[z], e[z], va);
+    }
+    if (u < nb) {
+      float e[ZP];
+      load_e<ZP>(Eb + u * ZP, e);
+#pragma unroll
+      for (int z = 0; z < ZP; ++z) vb = fmaf(wb[z], e[z], vb);
+    }
+    if (!((tw >> lane) & 1u)) {
+      anya = true;
+      lane_track(va, u, uta, bva, bua);
+    }
+    if (u < nb) lane_track(vb, u, utb, bvb, bub);
+  }
+  const int bta = bua >= 0 ? uta[bua] : INT_MAX, btb = bub >= 0 ? utb[bub] : INT_MAX;
+  pa = warp_pick(bva, bta, bua, anya);
+  pb = warp_pick(bvb, btb, bub, nb > warp * 32);
+}
+
+// A pick as the four warps exchange it.
+struct Part {
+  float v;
+  int t, u, any;
+};
+
+// The best of the warps' parts: value, then token.
+__device__ __forceinline__ Pick combine(const Part *pp) {
+  Pick b;
+  b.v = 0.f;
+  b.t = INT_MAX;
+  b.u = -1;
+  b.any = false;
+#pragma unroll
+  for (int w = 0; w < kPopWarps; ++w) {
+    const Part q = pp[w];
+    b.any = b.any || q.any != 0;
+    if (q.v > b.v || (q.v == b.v && q.v > 0.f && q.t < b.t)) {
+      b.v = q.v;
+      b.t = q.t;
+      b.u = q.u;
+    }
+  }
+  return b;
+}
+
+__device__ __forceinline__ void pop_barrier() {
+  asm volatile("bar.sync 1, %0;" ::"r"(kPopWarps * 32) : "memory");
+}
+
+// Node q's children (row d) in the log domain: the largest branch term of
+// each untaken child relative to S_q, in fixed point; then the sums rescaled
+// by the largest of those, M.  Sets shift = M.
+template <int ZP>
+__device__ __forceinline__ Pick slow_dense(const MixSm &s, int lane, int q, int d, int64_t &shift) {
+  const int Z = s.Z, K = s.K, n = s.nu[d];
+  const int64_t Sq = s.Sn[q];
+  int64_t base[ZP];
+#pragma unroll
+  for (int z = 0; z < ZP; ++z) {
+    base[z] = kVeryNeg;
+    if (z < Z) {
+      const int64_t P = s.Pn[q * Z + z];
+      if (P > kInfCut) base[z] = P - s.flse[d * Z + z] - Sq;
+    }
+  }
+  const int16_t *R = s.dR + (size_t)d * s.ZK * ZP;
+  const uint32_t *tk = s.taken + q * s.UW;
+  auto term = [&](int u, int z) -> int64_t {
+    const int j = R[(size_t)u * ZP + z];
+    if (j < 0 || base[z] == kVeryNeg) return kVeryNeg;
+    const int64_t fx = fix_f32(s.lg[(d * Z + z) * K + j]);
+    return fx == kNegFix ? kVeryNeg : base[z] + fx;
+  };
+  int64_t best = kVeryNeg;
+  for (int u = lane; u < n; u += 32) {
+    if ((tk[u >> 5] >> lane) & 1u) continue;
+#pragma unroll
+    for (int z = 0; z < ZP; ++z) {
+      const int64_t t = term(u, z);
+      best = t > best ? t : best;
+    }
+  }
+  const int64_t M = warp_max_i64(best);
+  shift = M;
+  float bv = 0.f;
+  int bt = INT_MAX, bu = -1;
+  bool any = false;
+  if (M > kVeryNeg / 2) {
+    const int *ut = s.utok + d * s.ZK;
+    for (int u = lane; u < n; u += 32) {
+      if ((tk[u >> 5] >> lane) & 1u) continue;
+      any = true;
+      float v = 0.f;
+#pragma unroll
+      for (int z = 0; z < ZP; ++z) {
+        const int64_t t = term(u, z);
+        if (t != kVeryNeg) {
+          const int64_t D = t - M;
+          v += exp_fix(D < 0 ? D : 0);
+        }
+      }
+      lane_track(v, u, ut, bv, bu);
+    }
+    bt = bu >= 0 ? ut[bu] : INT_MAX;
+  }
+  return warp_pick(bv, bt, bu, any);
+}
+
+// P_z of node i, the child (union token u of row d - 1) of node p: lane z
+// reads the token's rank in branch z.
+template <int ZP>
+__device__ __forceinline__ int64_t child_p_dense(const MixSm &s, int lane, int p, int d, int u) {
+  int64_t P = kNegFix;
+  if (lane < s.Z) {
+    const int j = s.dR[((size_t)(d - 1) * s.ZK + u) * ZP + lane];
+    const int64_t Pp = s.Pn[p * s.Z + lane];
+    if (j >= 0 && Pp > kInfCut) {
+      const int row = (d - 1) * s.Z + lane;
+      const int64_t fx = fix_f32(s.lg[row * s.K + j]);
+      if (fx != kNegFix) {
+        P = Pp + (fx - s.flse[row]);
+        P = P < kNegFix ? kNegFix : P;
+      }
+    }
+  }
+  return P;
+}
+
+// --------------------------------------------------------------- sparse form
+
+// The scaled sums of node q's children (row d) into acc[0..nu), one branch
+// per pass.
+__device__ __forceinline__ void scan_sparse(const MixSm &s, int lane, int q, int d, float *acc) {
+  const int Z = s.Z, K = s.K, n = s.nu[d];
+  for (int u = lane; u < n; u += 32) acc[u] = 0.f;
+  __syncwarp();
+  for (int z = 0; z < Z; ++z) {
+    const float wv = s.wz[q * Z + z];
+    if (wv == 0.f) continue;  // uniform over the warp
+    const int e0 = (d * Z + z) * K;
+    for (int j = lane; j < K; j += 32) {
+      const int u = s.ue[e0 + j];
+      acc[u] = fmaf(wv, s.Ee[e0 + j], acc[u]);
+    }
+    __syncwarp();
+  }
+}
+
+__device__ __forceinline__ Pick pick_sparse(const MixSm &s, int lane, int q, int d, const float *acc) {
+  const int n = s.nu[d];
+  const uint32_t *tk = s.taken + q * s.UW;
+  const int *ut = s.utok + d * s.ZK;
+  float bv = 0.f;
+  int bt = INT_MAX, bu = -1;
+  bool any = false;
+  for (int u = lane; u < n; u += 32) {
+    if ((tk[u >> 5] >> lane) & 1u) continue;
+    any = true;
+    lane_track(acc[u], u, ut, bv, bu);
+  }
+  bt = bu >= 0 ? ut[bu] : INT_MAX;
+  return warp_pick(bv, bt, bu, any);
+}
+
+__device__ __forceinline__ Pick slow_sparse(const MixSm &s, int lane, int q, int d, int64_t &shift) {
+  const int Z = s.Z, K = s.K, n = s.nu[d];
+  const int64_t Sq = s.Sn[q];
+  int64_t *mx = reinterpret_cast<int64_t *>(s.acc);
+  for (int u = lane; u < n; u += 32) mx[u] = kVeryNeg;
+  __syncwarp();
+  for (int z = 0; z < Z; ++z) {
+    const int64_t P = s.Pn[q * Z + z];
+    if (P <= kInfCut) continue;
+    const int64_t base = P - s.flse[d * Z + z] - Sq;
+    const int e0 = (d * Z + z) * K;
+    for (int j = lane; j < K; j += 32) {
+      const int64_t fx = fix_f32(s.lg[e0 + j]);
+      if (fx == kNegFix) continue;
+      const int u = s.ue[e0 + j];
+      const int64_t v = base + fx;
+      mx[u] = v > mx[u] ? v : mx[u];
+    }
+    __syncwarp();
+  }
+  const uint32_t *tk = s.taken + q * s.UW;
+  int64_t best = kVeryNeg;
+  for (int u = lane; u < n; u += 32)
+    if (!((tk[u >> 5] >> lane) & 1u)) best = mx[u] > best ? mx[u] : best;
+  const int64_t M = warp_max_i64(best);
+  __syncwarp();
+  shift = M;
+  if (M <= kVeryNeg / 2) return warp_pick(0.f, INT_MAX, -1, false);
+  float *acc = s.acc;
+  for (int u = lane; u < n; u += 32) acc[u] = 0.f;
+  __syncwarp();
+  for (int z = 0; z < Z; ++z) {
+    const int64_t P = s.Pn[q * Z + z];
+    if (P <= kInfCut) continue;
+    const int64_t base = P - s.flse[d * Z + z] - Sq - M;
+    const int e0 = (d * Z + z) * K;
+    for (int j = lane; j < K; j += 32) {
+      const int64_t fx = fix_f32(s.lg[e0 + j]);
+      if (fx == kNegFix) continue;
+      const int u = s.ue[e0 + j];
+      const int64_t D = base + fx;
+      acc[u] += exp_fix(D < 0 ? D : 0);
+    }
+    __syncwarp();
+  }
+  return pick_sparse(s, lane, q, d, acc);
+}
+
+// P_z of node i, the child (union token u of row d - 1) of node p: a warp
+// search of the row's entries for u.
+__device__ __forceinline__ int64_t child_p_sparse(const MixSm &s, int lane, int p, int i, int d,
+                                                  int u) {
+  if (lane < s.Z) s.Pn[i * s.Z + lane] = kNegFix;
+  __syncwarp();
+  const int e0 = (d - 1) * s.ZK;
+  for (int e = lane; e < s.ZK; e += 32) {
+    if (s.ue[e0 + e] != u) continue;
+    const int z = e / s.K, row = (d - 1) * s.Z + z;
+    const int64_t Pp = s.Pn[p * s.Z + z], fx = fix_f32(s.lg[e0 + e]);
+    int64_t v = kNegFix;
+    if (Pp > kInfCut && fx != kNegFix) {
+      v = Pp + (fx - s.flse[row]);
+      v = v < kNegFix ? kNegFix : v;
+    }
+    s.Pn[i * s.Z + z] = v;
+  }
+  __syncwarp();
+  return lane < s.Z ? s.Pn[i * s.Z + lane] : kNegFix;
+}
+
+// ----------------------------------------------------------------- both forms
+
+// The sparse form's pending children of node qa (row da) and of the new node
+// qb (row db, or qb = -1), with the log-domain rescan of either where its
+// best falls below 2^-100; shifts sa, sb of their keys.
+__device__ __forceinline__ void pick_sparse2(const MixSm &s, int lane, int qa, int da, int qb, int db,
+                                             Pick &pa, int64_t &sa, Pick &pb, int64_t &sb) {
+  sa = sb = 0;
+  pb.v = 0.f;
+  pb.t = INT_MAX;
+  pb.u = -1;
+  pb.any = false;
+  scan_sparse(s, lane, qa, da, s.acc);
+  if (qb >= 0) scan_sparse(s, lane, qb, db, s.acc + s.ZK);
+  pa = pick_sparse(s, lane, qa, da, s.acc);
+  if (qb >= 0) pb = pick_sparse(s, lane, qb, db, s.acc + s.ZK);
+  __syncwarp();
+  if (pa.v < kTiny && pa.any) {
+    pa = slow_sparse(s, lane, qa, da, sa);
+    __syncwarp();
+  }
+  if (qb >= 0 && pb.v < kTiny && pb.any) {
+    pb = slow_sparse(s, lane, qb, db, sb);
+    __syncwarp();
+  }
+}
+
+// The pending candidate of node q (children at depth dchild) from a pick: its
+// key goes to lane q % 32, slot q / 32 (a zero key when there is none); lane 0
+// records its union index and token in this warp's copy.
+template <int S>
+struct Pending {
+  uint32_t kh[S], kl[S], kt[S];  // the 96-bit key
+
+  __device__ __forceinline__ void clear() {
+#pragma unroll
+    for (int i = 0; i < S; ++i) kh[i] = kl[i] = kt[i] = 0u;
+  }
+  __device__ __forceinline__ void set(const MixSm &s, int lane, int q, int dchild, const Pick &p,
+                                      int64_t score) {
+    const bool ok = p.v > 0.f;
+    uint32_t hi = 0u, lo = 0u, tw = 0u;
+    if (ok) {
+      const uint64_t k = tb::key_of(score);
+      hi = (uint32_t)(k >> 32);
+      lo = (uint32_t)k;
+      tw = 0xFFFFFFFFu - (((uint32_t)dchild << 16) | (uint32_t)q);
+    }
+    const int sl = q >> 5;
+#pragma unroll
+    for (int i = 0; i < S; ++i) {
+      const bool me = lane == (q & 31) && i == sl;
+      kh[i] = me ? hi : kh[i];
+      kl[i] = me ? lo : kl[i];
+      kt[i] = me ? tw : kt[i];
+    }
+    if (lane == 0) {
+      s.pu[q] = p.u;
+      s.pt[q] = p.t;
+    }
+  }
+  // The best key over the warp (all zero: none).
+  __device__ __forceinline__ void best(uint32_t &mh, uint32_t &ml, uint32_t &mt) const {
+    uint32_t bh = kh[0], bl = kl[0], bt = kt[0];
+#pragma unroll
+    for (int i = 1; i < S; ++i) {
+      const bool g = tb::key_gt(kh[i], kl[i], kt[i], bh, bl, bt);
+      bh = g ? kh[i] : bh;
+      bl = g ? kl[i] : bl;
+      bt = g ? kt[i] : bt;
+    }
+    tb::warp_best(bh, bl, bt, mh, ml, mt);
+  }
+};
+
+template <int S, int ZP>
+__global__ void __launch_bounds__(kMixThreads, 1) build_tree_mixture_kernel(MixArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
-  const int r = blockIdx.x, lane = threadIdx.x;
-  const int Z = a.Z, b = a.b, K = a.K, E = a.E, n_max = a.n_max, W = a.W, UW = a.UW;
-  const MixLayout L = mix_layout(Z, b, E, n_max, W, UW);
-  double *Lam = reinterpret_cast<double *>(smem + L.lam);  // [Z][b+1]
-  double *lpi = reinterpret_cast<double *>(smem + L.lpi);  // [Z]
-  double *Ls = reinterpret_cast<double *>(smem + L.ls);    // [n_max][Z] logit sums
-  double *plr = reinterpret_cast<double *>(smem + L.plr);  // [n_max] pending log rho
-  double *lr = reinterpret_cast<double *>(smem + L.lr);    // [n_max] node log rho
-  float *ulg = reinterpret_cast<float *>(smem + L.ulg);    // [b][E][Z] branch logits of U_d
-  int *utok = reinterpret_cast<int *>(smem + L.utok);      // [b][E] tokens of U_d
-  int *nu = reinterpret_cast<int *>(smem + L.nu);          // [b] |U_d|
-  float *C = reinterpret_cast<float *>(smem + L.cost);     // [n_max + 1]
-  int *par = reinterpret_cast<int *>(smem + L.par);
-  int *dep = reinterpret_cast<int *>(smem + L.dep);
-  int *tok = reinterpret_cast<int *>(smem + L.tok);
-  float *ah = reinterpret_cast<float *>(smem + L.ah);
-  float *sp = reinterpret_cast<float *>(smem + L.sp);
-  int *ptok = reinterpret_cast<int *>(smem + L.ptok);     // pending child's token (-1: none)
-  int *pu = reinterpret_cast<int *>(smem + L.pu);         // pending child's union index
-  uint32_t *mask = reinterpret_cast<uint32_t *>(smem + L.mask);    // [n_max][W]
-  uint32_t *taken = reinterpret_cast<uint32_t *>(smem + L.taken);  // [n_max][UW]
-  int *etok = reinterpret_cast<int *>(smem + L.etok);      // [E] one position's entries
-  int *efirst = reinterpret_cast<int *>(smem + L.efirst);  // [E] first entry with that token
-  int *umap = reinterpret_cast<int *>(smem + L.umap);      // [E] union index of a first entry
+  const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int NW = kMixThreads / 32;
+  const int Z = a.Z, b = a.b, K = a.K, n_max = a.n_max, ZK = Z * K;
+  const MixLayout L = mix_layout(Z, b, K, n_max, ZP);
+  int64_t *flse = reinterpret_cast<int64_t *>(smem + L.flse);
+  int64_t *fmax = reinterpret_cast<int64_t *>(smem + L.fmax);
+  int64_t *mq = reinterpret_cast<int64_t *>(smem + L.mq);
+  float *lg = reinterpret_cast<float *>(smem + L.lg);
+  int *utok = reinterpret_cast<int *>(smem + L.utok);
+  float *C = reinterpret_cast<float *>(smem + L.cost);
+  int *nu = reinterpret_cast<int *>(smem + L.nu);
+  float *dE = reinterpret_cast<float *>(smem + L.dE);
+  int16_t *dR = reinterpret_cast<int16_t *>(smem + L.dR);
+  float *Ee = reinterpret_cast<float *>(smem + L.ee);
+  uint16_t *ue = reinterpret_cast<uint16_t *>(smem + L.ue);
+  int *rtok = reinterpret_cast<int *>(smem + L.rtok);
+  uint16_t *eu = reinterpret_cast<uint16_t *>(smem + L.eu);
+  int *hk = reinterpret_cast<int *>(smem + L.hk);
 
   griddep_wait();
   griddep_launch_dependents();
 
-  // ---- tables: lse sums and log pi per branch, the cost row
-  const double *lse_r = a.lse + (size_t)r * Z * b;
-  if (lane < Z) {
-    double s = 0.0;
-    Lam[lane * (b + 1)] = 0.0;
-    for (int d = 1; d <= b; ++d) {
-      s += lse_r[(size_t)lane * b + d - 1];
-      Lam[lane * (b + 1) + d] = s;
-    }
-    const double w = a.pi[(size_t)r * Z + lane];
-    lpi[lane] = log(w);
-    if (!(w >= 0.0) || isinf(w)) atomicOr(&a.status[r], BASTION_STATUS_BAD_WEIGHT);
-  }
+  // ---- the cost row and the fixed-point lse of every (position, branch) row
   const float *cr = a.cost + (a.cost_per_request ? (size_t)r * (n_max + 1) : 0);
   bool bad = false;
-  for (int i = lane; i <= n_max; i += 32) {
-    const float c = cr[i];
+  for (int i = tid; i <= n_max; i += kMixThreads) {
+    const float c = __ldg(cr + i);
     C[i] = c;
     if (i >= 1) bad |= !(c > 0.f) || isinf(c);
   }
-  if (__any_sync(kFull, bad) && lane == 0) atomicOr(&a.status[r], BASTION_STATUS_BAD_COST);
+  for (int q = tid; q < b * Z; q += kMixThreads) {
+    const int d = q / Z, z = q - d * Z;
+    flse[q] = tb::fix_lse(__ldg(a.lse + ((size_t)r * Z + z) * b + d));
+  }
+  const bool bad_cost = __syncthreads_or(bad) != 0;
 
-  // ---- the union of the branches' tokens at each position; entry e is
-  // (branch e / K, rank e % K)
+  // ---- the union U of the branches' tokens at each position, G positions per
+  // staging group
   const size_t rb = (size_t)r * Z * b * K;
-  for (int d = 0; d < b; ++d) {
-    for (int e = lane; e < E; e += 32)
-      etok[e] = a.topk_tok[rb + ((size_t)(e / K) * b + d) * K + (e % K)];
-    __syncwarp();
-    for (int e = lane; e < E; e += 32) {
-      const int t = etok[e];
-      int f = e;
-      for (int e2 = 0; e2 < e; ++e2)
-        if (etok[e2] == t) {
-          f = e2;
-          break;
-        }
-      efirst[e] = f;
-    }
-    __syncwarp();
-    int cnt = 0;
-    for (int base = 0; base < E; base += 32) {
-      const int e = base + lane;
-      const bool first = e < E && efirst[e] == e;
-      const uint32_t bal = __ballot_sync(kFull, first);
-      if (first) {
-        const int u = cnt + __popc(bal & ((1u << lane) - 1u));
-        umap[e] = u;
-        utok[d * E + u] = etok[e];
-      }
-      cnt += __popc(bal);
-    }
-    if (lane == 0) nu[d] = cnt;
-    for (int q = lane; q < cnt * Z; q += 32) ulg[(size_t)d * E * Z + q] = -INFINITY;
-    __syncwarp();
-    for (int e = lane; e < E; e += 32) {
-      const int u = umap[efirst[e]];
-      ulg[((size_t)d * E + u) * Z + e / K] = a.topk_logit[rb + ((size_t)(e / K) * b + d) * K + (e % K)];
-    }
-    __syncwarp();
-  }
-
-  // log rho of child u (position dq of the union) of node q
-  auto child_lr = [&](int q, int dq, int u) -> double {
-    double t[8];
-    double m = kNegInf;
-    for (int z = 0; z < Z; ++z) {
-      const double lv = (double)ulg[((size_t)dq * E + u) * Z + z];
-      const double lq = Ls[q * Z + z];
-      const double ls = (lq == kNegInf || lv == kNegInf) ? kNegInf : lq + lv;
-      t[z] = ls == kNegInf ? kNegInf : lpi[z] + (ls - Lam[z * (b + 1) + dq + 1]);
-      m = t[z] > m ? t[z] : m;
-    }
-    if (m == kNegInf) return kNegInf;
-    double s = 0.0;
-    for (int z = 0; z < Z; ++z) s += exp(t[z] - m);
-    return m + log(s);
-  };
-  // node q's best untaken child -> (plr, ptok, pu); ptok = -1 when none
-  auto rescan = [&](int q) {
-    const int dq = dep[q];
-    double bs = kNegInf;
-    int bt = -1, bu = -1;
-    if (dq < b) {
-      const int n_u = nu[dq];
-      for (int u = lane; u < n_u; u += 32) {
-        if ((taken[q * UW + (u >> 5)] >> (u & 31)) & 1u) continue;
-        const double s = child_lr(q, dq, u);
-        const int t = utok[dq * E + u];
-        if (bt < 0 || s > bs || (s == bs && t < bt)) {
-          bs = s;
-          bt = t;
-          bu = u;
-        }
+  const int H = L.H, G = L.G, hshift = 32 - (31 - __clz(H));
+  for (int g0 = 0; g0 < b; g0 += G) {
+    const int g1 = g0 + G < b ? g0 + G : b, ng = (g1 - g0) * ZK;
+    // the group's logits and tokens (local entry li = (d - g0) ZK + z K + j),
+    // four loads in flight per thread; its hash tables emptied and, in the
+    // dense form, its union slots cleared
+    for (int q = tid; q < (g1 - g0) * H; q += kMixThreads) hk[q] = kEmptySlot;
+    if constexpr (ZP > 0) {
+      for (int q = tid; q < ng * ZP; q += kMixThreads) {
+        dE[(size_t)g0 * ZK * ZP + q] = 0.f;
+        dR[(size_t)g0 * ZK * ZP + q] = -1;
       }
     }
+    constexpr int UL = 4;
+    for (int l0 = tid; l0 < ng; l0 += kMixThreads * UL) {
+      float x[UL];
+      int t[UL];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const double s2 = __shfl_xor_sync(kFull, bs, o);
-      const int t2 = __shfl_xor_sync(kFull, bt, o);
-      const int u2 = __shfl_xor_sync(kFull, bu, o);
-      const bool take = t2 >= 0 && (bt < 0 || s2 > bs || (s2 == bs && t2 < bt));
-      bs = take ? s2 : bs;
-      bt = take ? t2 : bt;
-      bu = take ? u2 : bu;
+      for (int k = 0; k < UL; ++k) {
+        const int li = l0 + k * kMixThreads;
+        if (li < ng) {
+          const int dl = li / ZK, rem = li - dl * ZK, z = rem / K, j = rem - z * K;
+          const size_t gi = rb + ((size_t)z * b + g0 + dl) * K + j;
+          x[k] = __ldg(a.topk_logit + gi);
+          t[k] = __ldg(a.topk_tok + gi);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < UL; ++k) {
+        const int li = l0 + k * kMixThreads;
+        if (li < ng) {
+          lg[(size_t)g0 * ZK + li] = x[k];
+          rtok[li] = t[k];
+        }
+      }
     }
-    if (lane == 0) {
-      plr[q] = bs;
-      ptok[q] = bt;
-      pu[q] = bu;
+    __syncthreads();
+    // one warp per (position, branch) row: its largest logit, and its tokens
+    // into the position's hash table
+    for (int row = g0 * Z + warp; row < g1 * Z; row += NW) {
+      const int d = row / Z;
+      int *h = hk + (d - g0) * H;
+      float mx = -INFINITY;
+      for (int j = lane; j < K; j += 32) {
+        const int li = (row - g0 * Z) * K + j;
+        mx = fmaxf(mx, lg[(size_t)row * K + j]);
+        const int tkn = rtok[li];
+        uint32_t sl = ((uint32_t)tkn * 0x9E3779B1u) >> hshift;
+        for (int it = 0; it < H; ++it) {  // the table is at most half full
+          const int old = atomicCAS(h + sl, kEmptySlot, tkn);
+          if (old == kEmptySlot || old == tkn) break;
+          sl = (sl + 1) & (uint32_t)(H - 1);
+        }
+        eu[li] = (uint16_t)sl;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+      if (lane == 0) {
+        const int64_t fm = fix_f32(mx);
+        fmax[row] = fm;
+        mq[row] = fm == kNegFix ? kNegFix : fm - flse[row];
+      }
     }
-    __syncwarp();
-  };
-
-  // ---- the root
-  const double Lar = (double)a.l_ar[r];
-  if (lane == 0) {
-    par[0] = -1;
-    dep[0] = 0;
-    tok[0] = a.root_token[r];
-    lr[0] = 0.0;
+    __syncthreads();
+    for (int d = g0 + warp; d < g1; d += NW) {  // slot order -> union index
+      int *h = hk + (d - g0) * H;
+      int cnt = 0;
+      for (int s0 = 0; s0 < H; s0 += 32) {
+        const int v = h[s0 + lane];
+        const bool occ = v != kEmptySlot;
+        const uint32_t bal = __ballot_sync(kFull, occ);
+        if (occ) {
+          const int u = cnt + __popc(bal & ((1u << lane) - 1u));
+          utok[d * ZK + u] = v;
+          h[s0 + lane] = u;
+        }
+        cnt += __popc(bal);
+      }
+      if (lane == 0) nu[d] = cnt;
+    }
+    __syncthreads();
+    // each entry's union index and E = exp(logit - its row's largest)
+    for (int li = tid; li < ng; li += kMixThreads) {
+      const int dl = li / ZK, rem = li - dl * ZK, z = rem / K, j = rem - z * K;
+      const int d = g0 + dl, row = d * Z + z;
+      const size_t e = (size_t)g0 * ZK + li;
+      int u = hk[dl * H + eu[li]];
+      u = (unsigned)u < (unsigned)ZK ? u : 0;  // (a token equal to INT32_MIN)
+      const int64_t fm = fmax[row], fx = fix_f32(lg[e]);
+      const float ev = (fm == kNegFix || fx == kNegFix) ? 0.f : exp_fix(fx - fm);
+      ue[e] = (uint16_t)u;
+      if constexpr (ZP > 0) {
+        const size_t slot = ((size_t)d * ZK + u) * ZP + z;
+        dE[slot] = ev;
+        dR[slot] = (int16_t)j;
+      } else {
+        Ee[e] = ev;
+      }
+    }
+    __syncthreads();
   }
-  if (lane < Z) Ls[lane] = 0.0;
-  for (int w = lane; w < W; w += 32) mask[w] = w == 0 ? 1u : 0u;
-  for (int q = lane; q < n_max * UW; q += 32) taken[q] = 0u;
-  __syncwarp();
-  double A = 1.0;
-  if (lane == 0) {
-    ah[0] = 1.f;
-    sp[0] = (float)(A * Lar / (double)C[1]);
-  }
-  __syncwarp();
-  rescan(0);
+  MixSm s;
+  s.flse = flse;
+  s.fmax = fmax;
+  s.mq = mq;
+  s.lg = lg;
+  s.C = C;
+  s.utok = utok;
+  s.nu = nu;
+  s.dE = dE;
+  s.dR = dR;
+  s.Ee = Ee;
+  s.ue = ue;
+  s.Z = Z;
+  s.K = K;
+  s.ZK = ZK;
+  s.UW = (ZK + 31) / 32;
+  s.W = (n_max + 31) / 32;
+  s.b = b;
+  const int W = s.W, UW = s.UW;
+  // this warp's copies of the node state (the dense form keeps one per pop warp)
+  const int cw = ZP > 0 ? (warp < kPopWarps ? warp : 0) : 0;
+  s.Pn = reinterpret_cast<int64_t *>(smem + L.pn) + (size_t)cw * n_max * Z;
+  s.Sn = reinterpret_cast<int64_t *>(smem + L.sn) + (size_t)cw * n_max;
+  s.wz = reinterpret_cast<float *>(smem + L.wz) + (size_t)cw * n_max * Z;
+  s.lrn = reinterpret_cast<int64_t *>(smem + L.lrn);
+  s.acc = reinterpret_cast<float *>(smem + L.acc);
+  s.An = reinterpret_cast<float *>(smem + L.an);
+  s.taken = reinterpret_cast<uint32_t *>(smem + L.taken);
+  s.mask = reinterpret_cast<uint32_t *>(smem + L.mask);
+  s.par = reinterpret_cast<int *>(smem + L.par);
+  s.dep = reinterpret_cast<int *>(smem + L.dep);
+  s.tok = reinterpret_cast<int *>(smem + L.tok);
+  s.pu = reinterpret_cast<int *>(smem + L.pu) + (size_t)cw * n_max;
+  s.pt = reinterpret_cast<int *>(smem + L.pt) + (size_t)cw * n_max;
+  Part *part = reinterpret_cast<Part *>(smem + L.part);  // [2 phases][2 nodes][kPopWarps]
 
+  if constexpr (ZP > 0) {  // every node's taken-bits cleared once
+    for (int q = tid; q < n_max * UW; q += kMixThreads) s.taken[q] = 0u;
+    __syncthreads();
+  }
+  constexpr int kRun = ZP > 0 ? kPopWarps : 1;  // the warps that run the pops
+  if (warp >= kRun) return;
+
+  // ---- the root: P_z = log pi_z (a weight that is negative or not finite
+  // counts as 0 and sets the status bit)
+  bool badw = false;
+  int64_t P0 = kNegFix;
+  if (lane < Z) {
+    const double w = a.pi[(size_t)r * Z + lane];
+    badw = !(w >= 0.0) || isinf(w);
+    if (!badw && w > 0.0) P0 = tb::fix_lse(log(w));
+  }
+  if (__any_sync(kFull, badw) && warp == 0 && lane == 0) atomicOr(&a.status[r], BASTION_STATUS_BAD_WEIGHT);
+  if (warp == 0 && lane == 0) {
+    s.par[0] = -1;
+    s.dep[0] = 0;
+    s.tok[0] = a.root_token[r];
+    s.lrn[0] = 0;
+    s.An[0] = 1.f;
+  }
+  if (warp == 0)
+    for (int q = lane; q < W; q += 32) s.mask[q] = q == 0 ? 1u : 0u;
+
+  Pending<S> pend;
+  pend.clear();
+  float A_hi = 1.f, A_lo = 0.f;  // A_hat with Kahan compensation
   int N = 1;
-  while (N < n_max) {
-    // the best pending candidate over the nodes
-    double bs = kNegInf;
-    int bd = 0, bt = -1, bn = -1;
-    for (int q = lane; q < N; q += 32) {
-      const int t = ptok[q];
-      if (t < 0) continue;
-      const double s = plr[q];
-      const int d = dep[q] + 1;
-      if (bn < 0 || mix_better(s, d, t, q, bs, bd, bt, bn)) {
-        bs = s;
-        bd = d;
-        bt = t;
-        bn = q;
-      }
-    }
+
+  if constexpr (ZP > 0) {
+    // ==== dense form: four warps, identical decisions, a quarter of each scan
+    int ph = 0;
+    // node i's weights (lane z) and scale for its children at row d; false when
+    // no child can have a finite score
+    auto setup = [&](int i, int d, int64_t P, float &wl) -> bool {
+      wl = 0.f;
+      if (lane < Z) s.Pn[i * Z + lane] = P;
+      if (d >= b) return false;
+      const int64_t m = lane < Z ? s.mq[d * Z + lane] : kNegFix;
+      const int64_t X = (lane < Z && P > kInfCut && m > kInfCut) ? P + m : kVeryNeg;
+      const int64_t Smax = warp_max_i64(X);
+      if (Smax <= kInfCut) return false;
+      wl = X <= kInfCut ? 0.f : exp_fix(X - Smax);
+      if (lane < Z) s.wz[i * Z + lane] = wl;
+      if (lane == 0) s.Sn[i] = Smax;
+      return true;
+    };
+    // the pending children of qa (row da) and of the new node qb (row db, its
+    // weights in lanes z: wlb), combined over the warps, and their keys
+    auto scan = [&](int qa, int da, int qb, int db, float wlb, Pick &pa, int64_t &ka, Pick &pb,
+                    int64_t &kb) {
+      float wa[ZP], wb[ZP];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const double s2 = __shfl_xor_sync(kFull, bs, o);
-      const int d2 = __shfl_xor_sync(kFull, bd, o);
-      const int t2 = __shfl_xor_sync(kFull, bt, o);
-      const int n2 = __shfl_xor_sync(kFull, bn, o);
-      const bool take = n2 >= 0 && (bn < 0 || mix_better(s2, d2, t2, n2, bs, bd, bt, bn));
-      bs = take ? s2 : bs;
-      bd = take ? d2 : bd;
-      bt = take ? t2 : bt;
-      bn = take ? n2 : bn;
+      for (int z = 0; z < ZP; ++z) {
+        wa[z] = z < Z ? s.wz[qa * Z + z] : 0.f;
+        wb[z] = __shfl_sync(kFull, wlb, z);
+      }
+      part_pick<ZP>(s, lane, warp, qa, da, wa, qb, db, wb, pa, pb);
+      Part *pp = part + ph * 2 * kPopWarps;
+      if (lane == 0) {
+        pp[warp] = Part{pa.v, pa.t, pa.u, pa.any ? 1 : 0};
+        pp[kPopWarps + warp] = Part{pb.v, pb.t, pb.u, pb.any ? 1 : 0};
+      }
+      pop_barrier();
+      pa = combine(pp);
+      pb = combine(pp + kPopWarps);
+      ph ^= 1;
+      int64_t sa = 0, sb = 0;
+      if (pa.v < kTiny && pa.any) pa = slow_dense<ZP>(s, lane, qa, da, sa);
+      if (qb >= 0 && pb.v < kTiny && pb.any) pb = slow_dense<ZP>(s, lane, qb, db, sb);
+      ka = pa.v > 0.f ? s.Sn[qa] + sa + log_fix(pa.v) : 0;
+      kb = (qb >= 0 && pb.v > 0.f) ? s.Sn[qb] + sb + log_fix(pb.v) : 0;
+    };
+
+    float wl0;
+    if (setup(0, 0, P0, wl0)) {
+      __syncwarp();
+      Pick pa, pb;
+      int64_t ka, kb;
+      scan(0, 0, -1, 0, 0.f, pa, ka, pb, kb);
+      pend.set(s, lane, 0, 1, pa, ka);
+      __syncwarp();
     }
-    // no candidate, or the best has rho = 0 (a NaN score, from a bad weight,
-    // counts as rho = 0 too)
-    if (bn < 0 || !(bs > kNegInf)) break;
-    const double rho = exp(bs);
-    if ((A + rho) * Lar / (double)C[N + 1] < A * Lar / (double)C[N]) break;  // S would decrease
-    const int p = bn, i = N, u = pu[p], dp = dep[p];
-    N = i + 1;
-    A += rho;
-    if (lane < Z) {
-      const double lv = (double)ulg[((size_t)dp * E + u) * Z + lane];
-      const double lq = Ls[p * Z + lane];
-      Ls[i * Z + lane] = (lq == kNegInf || lv == kNegInf) ? kNegInf : lq + lv;
+    while (N < n_max) {
+      uint32_t mh, ml, mt;
+      pend.best(mh, ml, mt);
+      if ((mh | ml | mt) == 0u) break;  // no candidate left
+      const int64_t sc = (int64_t)((((uint64_t)mh << 32) | ml) ^ 0x8000000000000000ull);
+      if (sc < kInfCut) break;  // the best candidate has rho = 0
+      const uint32_t sec = 0xFFFFFFFFu - mt;
+      const int p = (int)(sec & 0xFFFFu), d = (int)(sec >> 16);
+      const float rho = exp_fix(sc);
+      const float Cp = C[N], Cn = C[N + 1];
+      if (rho * Cp < (A_hi + A_lo) * (Cn - Cp)) break;  // S would decrease: keep T_N
+      {
+        const float y = rho - A_lo;
+        const float t = A_hi + y;
+        A_lo = (t - A_hi) - y;
+        A_hi = t;
+      }
+      const int i = N;
+      N = i + 1;
+      const int u = s.pu[p], t = s.pt[p];
+      if (warp == 0) {
+        if (lane == 0) {
+          s.par[i] = p;
+          s.dep[i] = d;
+          s.tok[i] = t;
+          s.lrn[i] = sc;
+          s.An[i] = A_hi + A_lo;
+        }
+        for (int q = lane; q < W; q += 32)
+          s.mask[i * W + q] = s.mask[p * W + q] | (q == (i >> 5) ? (1u << (i & 31)) : 0u);
+      }
+      // the word of the taken child belongs to warp (u / 32) % 4
+      if (lane == 0 && ((u >> 5) & (kPopWarps - 1)) == warp) s.taken[p * UW + (u >> 5)] |= 1u << (u & 31);
+      float wl;
+      const bool kids = setup(i, d, child_p_dense<ZP>(s, lane, p, d, u), wl);
+      __syncwarp();
+      Pick pa, pb;
+      int64_t ka, kb;
+      scan(p, d - 1, kids ? i : -1, d, wl, pa, ka, pb, kb);
+      pend.set(s, lane, p, d, pa, ka);
+      if (kids) pend.set(s, lane, i, d + 1, pb, kb);
+      __syncwarp();  // lane 0's records before the next pop reads them
     }
-    for (int w = lane; w < W; w += 32)
-      mask[i * W + w] = mask[p * W + w] | (w == (i >> 5) ? (1u << (i & 31)) : 0u);
-    if (lane == 0) {
-      par[i] = p;
-      dep[i] = bd;
-      tok[i] = bt;
-      lr[i] = bs;
-      ah[i] = (float)A;
-      sp[i] = (float)(A * Lar / (double)C[N]);
-      taken[p * UW + (u >> 5)] |= 1u << (u & 31);
-    }
+  } else {
+    // ==== sparse form: warp 0 alone
+    if (lane < Z) s.Pn[lane] = P0;
+    for (int q = lane; q < UW; q += 32) s.taken[q] = 0u;
     __syncwarp();
-    rescan(p);
-    rescan(i);
+    auto setup = [&](int i, int d, int64_t P) -> bool {
+      if (lane < Z) s.Pn[i * Z + lane] = P;
+      if (d >= b) return false;
+      const int64_t m = lane < Z ? s.mq[d * Z + lane] : kNegFix;
+      const int64_t X = (lane < Z && P > kInfCut && m > kInfCut) ? P + m : kVeryNeg;
+      const int64_t Smax = warp_max_i64(X);
+      if (Smax <= kInfCut) return false;
+      if (lane < Z) s.wz[i * Z + lane] = X <= kInfCut ? 0.f : exp_fix(X - Smax);
+      for (int q = lane; q < UW; q += 32) s.taken[i * UW + q] = 0u;
+      if (lane == 0) s.Sn[i] = Smax;
+      return true;
+    };
+    auto keyed = [&](int qa, int da, int qb, int db, Pick &pa, int64_t &ka, Pick &pb, int64_t &kb) {
+      __syncwarp();
+      int64_t sa, sb;
+      pick_sparse2(s, lane, qa, da, qb, db, pa, sa, pb, sb);
+      ka = pa.v > 0.f ? s.Sn[qa] + sa + log_fix(pa.v) : 0;
+      kb = (qb >= 0 && pb.v > 0.f) ? s.Sn[qb] + sb + log_fix(pb.v) : 0;
+      __syncwarp();
+    };
+    if (setup(0, 0, P0)) {
+      Pick pa, pb;
+      int64_t ka, kb;
+      keyed(0, 0, -1, 0, pa, ka, pb, kb);
+      pend.set(s, lane, 0, 1, pa, ka);
+      __syncwarp();
+    }
+    while (N < n_max) {
+      uint32_t mh, ml, mt;
+      pend.best(mh, ml, mt);
+      if ((mh | ml | mt) == 0u) break;
+      const int64_t sc = (int64_t)((((uint64_t)mh << 32) | ml) ^ 0x8000000000000000ull);
+      if (sc < kInfCut) break;
+      const uint32_t sec = 0xFFFFFFFFu - mt;
+      const int p = (int)(sec & 0xFFFFu), d = (int)(sec >> 16);
+      const float rho = exp_fix(sc);
+      const float Cp = C[N], Cn = C[N + 1];
+      if (rho * Cp < (A_hi + A_lo) * (Cn - Cp)) break;
+      {
+        const float y = rho - A_lo;
+        const float t = A_hi + y;
+        A_lo = (t - A_hi) - y;
+        A_hi = t;
+      }
+      const int i = N;
+      N = i + 1;
+      const int u = s.pu[p], t = s.pt[p];
+      if (lane == 0) {
+        s.par[i] = p;
+        s.dep[i] = d;
+        s.tok[i] = t;
+        s.lrn[i] = sc;
+        s.An[i] = A_hi + A_lo;
+        s.taken[p * UW + (u >> 5)] |= 1u << (u & 31);
+      }
+      for (int q = lane; q < W; q += 32)
+        s.mask[i * W + q] = s.mask[p * W + q] | (q == (i >> 5) ? (1u << (i & 31)) : 0u);
+      const bool kids = setup(i, d, child_p_sparse(s, lane, p, i, d, u));
+      Pick pa, pb;
+      int64_t ka, kb;
+      keyed(p, d - 1, kids ? i : -1, d, pa, ka, pb, kb);
+      pend.set(s, lane, p, d, pa, ka);
+      if (kids) pend.set(s, lane, i, d + 1, pb, kb);
+      __syncwarp();  // lane 0's records before the next pop reads them
+    }
   }
+  if (warp != 0) return;
   __syncwarp();
 
   // ---- outputs
   const size_t nb = (size_t)r * n_max;
   const int ctx = a.ctx_len[r];
-  if (lane == 0) a.n_nodes[r] = N;
-  for (int i = lane; i < N; i += 32) {
-    a.parent[nb + i] = par[i];
-    a.depth[nb + i] = dep[i];
-    a.pos_id[nb + i] = ctx + dep[i];
-    a.token[nb + i] = tok[i];
-    a.log_rho[nb + i] = (float)lr[i];
-    a.a_hat[nb + i] = ah[i];
-    a.speedup[nb + i] = sp[i];
+  const float L_ar = a.l_ar[r];
+  if (lane == 0) {
+    a.n_nodes[r] = N;
+    if (bad_cost) atomicOr(&a.status[r], BASTION_STATUS_BAD_COST);
   }
-  for (int q = lane; q < N * W; q += 32) a.anc_mask[nb * W + q] = mask[q];
+  for (int i = lane; i < N; i += 32) {
+    const size_t o = nb + i;
+    const float Ah = s.An[i];
+    a.parent[o] = s.par[i];
+    a.depth[o] = s.dep[i];
+    a.pos_id[o] = ctx + s.dep[i];
+    a.token[o] = s.tok[i];
+    a.log_rho[o] = __ll2float_rn(s.lrn[i]) * tb::kUnfix;
+    a.a_hat[o] = Ah;
+    a.speedup[o] = Ah * L_ar / C[i + 1];
+  }
+  for (int q = lane; q < N * W; q += 32) a.anc_mask[nb * W + q] = s.mask[q];
 }
+
+constexpr size_t kSmemCap = 227 * 1024;
 
 }  // namespace
 
+// The dense form's width when its tables fit in shared memory, else 0 (the
+// sparse form).
+int mixture_tree_form(int Z, int b, int K, int n_max) {
+  const int zp = dense_width(Z);
+  if (zp > 0 && mix_layout(Z, b, K, n_max, zp).bytes <= kSmemCap) return zp;
+  return 0;
+}
+
 size_t mixture_tree_smem_bytes(int Z, int b, int K, int n_max) {
-  const int E = Z * K, W = (n_max + 31) / 32, UW = (E + 31) / 32;
-  return mix_layout(Z, b, E, n_max, W, UW).bytes;
+  return mix_layout(Z, b, K, n_max, mixture_tree_form(Z, b, K, n_max)).bytes;
 }
 
 int launch_build_tree_mixture(const float *topk_logit, const int32_t *topk_tok, const double *lse,
@@ -365,9 +1084,6 @@ int launch_build_tree_mixture(const float *topk_logit, const int32_t *topk_tok, 
   a.b = b;
   a.K = K;
   a.n_max = n_max;
-  a.W = (n_max + 31) / 32;
-  a.E = Z * K;
-  a.UW = (a.E + 31) / 32;
   a.root_token = root_token;
   a.ctx_len = ctx_len;
   a.cost = cost_ms;
@@ -383,13 +1099,32 @@ int launch_build_tree_mixture(const float *topk_logit, const int32_t *topk_tok, 
   a.speedup = speedup;
   a.anc_mask = anc_mask;
   a.status = status;
-  const size_t smem = mixture_tree_smem_bytes(Z, b, K, n_max);
-  if (smem > 48 * 1024 &&
-      cudaFuncSetAttribute(build_tree_mixture_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem) != cudaSuccess)
+  const int zp = mixture_tree_form(Z, b, K, n_max);
+  const size_t smem = mix_layout(Z, b, K, n_max, zp).bytes;
+  const int slots = tb::tree_slots(n_max);
+  auto go = [&](auto kern) {
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return cudaErrorInvalidValue;
+    return launch_pdl(kern, dim3(B), dim3(kMixThreads), smem, stream, a);
+  };
+  auto by_slots = [&](auto k1, auto k2, auto k4, auto k8) {
+    return slots == 1 ? go(k1) : slots == 2 ? go(k2) : slots == 4 ? go(k4) : go(k8);
+  };
+#define BASTION_MIX_KERNELS(ZP_)                                                                 \
+  by_slots(build_tree_mixture_kernel<1, ZP_>, build_tree_mixture_kernel<2, ZP_>,                 \
+           build_tree_mixture_kernel<4, ZP_>, build_tree_mixture_kernel<8, ZP_>)
+  const cudaError_t e = zp == 1   ? BASTION_MIX_KERNELS(1)
+                        : zp == 2 ? BASTION_MIX_KERNELS(2)
+                        : zp == 4 ? BASTION_MIX_KERNELS(4)
+                        : zp == 8 ? BASTION_MIX_KERNELS(8)
+                                  : BASTION_MIX_KERNELS(0);
+#undef BASTION_MIX_KERNELS
+  if (e != cudaSuccess) {
+    cudaGetLastError();
     return BASTION_ERR_LAUNCH;
-  const cudaError_t e = launch_pdl(build_tree_mixture_kernel, dim3(B), dim3(32), smem, stream, a);
-  return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? BASTION_OK : BASTION_ERR_LAUNCH;
+  }
+  return cudaGetLastError() == cudaSuccess ? BASTION_OK : BASTION_ERR_LAUNCH;
 }
 
 }  // namespace bastion

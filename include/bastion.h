@@ -183,22 +183,29 @@ int bastion_build_tree(const float *topk_logit, const int32_t *topk_tok, const d
  * rho(x_1..d) = sum_z pi_z prod_{k<=d} q_k^z(x_k); a token outside branch z's
  * list at position k has q_k^z = 0; the children of a depth-d node are the
  * union over z of the branches' tokens at position d+1.  Candidates are
- * ordered by log rho (descending), then depth, token id and parent index
- * (ascending); the stop rule is bastion_build_tree's.  Scores are fp64
- * throughout (a parity form: one warp per request, no fixed-point tie rule).
+ * ordered by log rho (descending), then depth and token id (ascending).  The
+ * stop rule is bastion_build_tree's.  Per-branch path scores are 64-bit fixed
+ * point; the mixture sum over the branches is formed in fp32 with log rho
+ * within about (5 + Z/2) 2^-23 of exact, so where two candidates lie within
+ * 1e-5 of each other in log rho, or a stop test within 1e-5 (relative) of its
+ * boundary, either choice is a correct result.
  *
  * topk_logit, topk_tok [B, Z, b, K], lse [B, Z, b] (8-byte aligned): step 1
- *            run per branch.  pi [B, Z] double (8-byte aligned), each row the
+ *            run per branch; each branch lists a token at most once per
+ *            position (otherwise the results are undefined); no token equals
+ *            INT32_MIN.  pi [B, Z] double (8-byte aligned), each row the
  *            branch weights q(z|y), summing to 1.  A weight that is negative,
- *            NaN or infinite sets BASTION_STATUS_BAD_WEIGHT in status[r], and
- *            that request's outputs are undefined.
+ *            NaN or infinite sets BASTION_STATUS_BAD_WEIGHT in status[r] and
+ *            counts as 0 in that request's tree.
  * root_token, ctx_len, cost_ms, cost_per_request, l_ar: as bastion_build_tree.
  * Outputs:   as bastion_build_tree without rank: n_nodes [B]; parent, depth,
  *            pos_id, token, log_rho, a_hat, speedup [B, n_max];
  *            anc_mask [B, n_max, ceil(n_max/32)].
- * Limits: 1 <= Z <= 8, 1 <= K <= 64, Z*K <= 256, 1 <= b <= 32,
- * 1 <= n_max <= 256 (BASTION_ERR_SIZE otherwise); the per-request tables must
- * fit in 227 KB of shared memory (BASTION_ERR_UNSUPPORTED otherwise).
+ * Limits: 1 <= Z <= 32, 1 <= K <= 1024, 1 <= b <= 32, 1 <= n_max <= 256
+ * (BASTION_ERR_SIZE otherwise); one request's tables, about
+ * 14 b Z K + 16 n_max (Z + 2 + Z K / 32) bytes, must fit in 227 KB of shared
+ * memory (BASTION_ERR_UNSUPPORTED otherwise): b = 16 allows Z K up to about
+ * 700 at n_max = 128, e.g. Z = 4 with K = 128, or Z = 8 with K = 64.
  */
 int bastion_build_tree_mixture(const float *topk_logit, const int32_t *topk_tok, const double *lse,
                                const double *pi, int B, int Z, int b, int K, int n_max,

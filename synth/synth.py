@@ -45,6 +45,9 @@ S_V = 11
 S_VERIFY_U = 12
 S_HIDDEN = 13
 S_WEIGHT = 14
+S_MIX_BASE = 15
+S_MIX_BRANCH = 16
+S_MIX_PI = 17
 
 PLANT_VALUE = 12.0  # above any Box-Muller draw (|z| < 8.7 since u1 >= 2^-54)
 
@@ -147,6 +150,31 @@ def lm_head_inputs(B: int, b: int, H: int, V: int, seed: int):
     fill_normal(hidden.ctypes.data, hidden.size, "bf16", 1.0, seed, S_HIDDEN)
     fill_normal(weight.ctypes.data, weight.size, "bf16", 2.0 / float(np.sqrt(H)), seed, S_WEIGHT)
     return hidden, weight
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 to the nearest bf16 (ties to even), as uint16 bits."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    return ((u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)).astype(np.uint16)
+
+
+def mixture_inputs(B: int, Z: int, b: int, V: int, seed: int):
+    """Per-branch drafter logits of a latent-mixture proposal and its branch
+    weights.  Logits [B, Z, b, V] as bf16 bits: a part shared by the branches,
+    N(0, 2^2) (the drafter-logit scale of the batched workloads), plus a
+    branch part N(0, 1), so that the branches' top lists overlap in part.
+    Weights pi [B, Z] float64: normalised standard exponentials (a flat
+    Dirichlet draw)."""
+    base = np.empty((B, 1, b, V), np.float32)
+    fill_normal(base.ctypes.data, base.size, "f32", 2.0, seed, S_MIX_BASE)
+    dev = np.empty((B, Z, b, V), np.float32)
+    fill_normal(dev.ctypes.data, dev.size, "f32", 1.0, seed, S_MIX_BRANCH)
+    dev += base
+    del base
+    logits = f32_to_bf16_bits(dev)
+    del dev
+    e = -np.log(uniforms(seed, S_MIX_PI, B * Z).reshape(B, Z))
+    return logits, e / e.sum(axis=1, keepdims=True)
 
 
 def fill_normal_rows(ptr: int, rows: int, cols: int, ld: int, dtype: str, scale: float,

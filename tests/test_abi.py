@@ -97,19 +97,21 @@ def test_host_checks_reject_before_launch(L):
         assert L.bastion_tree_attention(*base) == -2
     base[12], base[5], base[6] = ctypes.c_float(0.1), 24, 8
     assert L.bastion_tree_attention(*base) == -6
-    # mixture tree: Z > 8, Z * K > 256, K > 64; misaligned pi; null pi
-    mx = [fake] * 4 + [1, 9, 4, 8, 16] + [fake] * 3 + [0, fake] + [fake] * 10 + [None]
+    # mixture tree: Z > 32, K > 1024, b > 32, n_max > 256; misaligned pi; null pi
+    mx = [fake] * 4 + [1, 33, 4, 8, 16] + [fake] * 3 + [0, fake] + [fake] * 10 + [None]
     assert L.bastion_build_tree_mixture(*mx) == -2
-    mx[5], mx[7] = 5, 64
+    mx[5], mx[7] = 2, 1025
     assert L.bastion_build_tree_mixture(*mx) == -2
-    mx[5], mx[7] = 1, 65
+    mx[7], mx[6] = 8, 33
     assert L.bastion_build_tree_mixture(*mx) == -2
-    mx[7], mx[3] = 8, vp(0x10004)
+    mx[6], mx[8] = 4, 257
+    assert L.bastion_build_tree_mixture(*mx) == -2
+    mx[8], mx[3] = 16, vp(0x10004)
     assert L.bastion_build_tree_mixture(*mx) == -4
     mx[3] = None
     assert L.bastion_build_tree_mixture(*mx) == -1
     # mixture tree: tables larger than shared memory -> unsupported
-    mx[3], mx[5], mx[6], mx[7], mx[8] = fake, 8, 32, 32, 256
+    mx[3], mx[5], mx[6], mx[7], mx[8] = fake, 8, 32, 256, 256
     assert L.bastion_build_tree_mixture(*mx) == -6
     # verify: B > 4096
     assert L.bastion_verify_greedy(fake, 1, 5000, 4, 8, 8, 4, fake, fake, fake, fake, fake, fake, fake, ws, 1 << 20, fake, None) == -2
