@@ -112,12 +112,12 @@ struct MixArgs {
 // e = (d Z + z) K + j is branch z's rank-j token at block position d + 1;
 // union token u of position d + 1 is slot d ZK + u.  ZP = 0: the sparse form.
 struct MixLayout {
-  size_t flse, fmax, mq, lg, utok, cost, nu;  // region 1, both forms
+  size_t flse, fmax, mq, lq, utok, cost, nu;  // region 1, both forms
   size_t ue;                                  // region 1, both forms
   size_t dE, dR;                              // region 1, dense form
   size_t ee;                                  // region 1, sparse form
   size_t pn, sn, lrn, acc, wz, an, taken, mask, par, dep, tok, pu, pt, part;  // region 2: nodes
-  size_t rtok, eu, hk;                        // region 2: staging of one group
+  size_t lgs, eu, hk, rmx;                    // region 2: staging of one group
   int H, G;  // hash slots per position, positions per staging group
   size_t bytes;
 };
@@ -137,7 +137,7 @@ __host__ __device__ inline MixLayout mix_layout(int Z, int b, int K, int n_max, 
   l.flse = take((size_t)b * Z * 8);
   l.fmax = take((size_t)b * Z * 8);
   l.mq = take((size_t)b * Z * 8);
-  l.lg = take(E * 4);
+  l.lq = take(E * 8);
   l.utok = take(E * 4);
   l.cost = take((n + 1) * 4);
   l.nu = take((size_t)b * 4);
@@ -166,14 +166,16 @@ __host__ __device__ inline MixLayout mix_layout(int Z, int b, int K, int n_max, 
   l.pt = take(copies * n * 4);
   l.part = ZP > 0 ? take(2 * 2 * kPopWarps * 16) : 0;
   const size_t node_bytes = o - r2;
-  const size_t per_pos = ((ZK * 4 + 15) & ~(size_t)15) + ((ZK * 2 + 15) & ~(size_t)15) + (size_t)H * 4;
+  const size_t per_pos = ((ZK * 4 + 15) & ~(size_t)15) + ((ZK * 2 + 15) & ~(size_t)15) + (size_t)H * 4 +
+                         (size_t)Z * 4;
   const size_t cap = node_bytes > 65536 ? node_bytes : 65536;
   int G = (int)(cap / per_pos);
   G = G < 1 ? 1 : (G > b ? b : G);
   o = r2;
-  l.rtok = take((size_t)G * ZK * 4);
+  l.lgs = take((size_t)G * ZK * 4);
   l.eu = take((size_t)G * ZK * 2);
   l.hk = take((size_t)G * H * 4);
+  l.rmx = take((size_t)G * Z * 4);
   l.H = H;
   l.G = G;
   const size_t stage_bytes = o - r2;
@@ -188,7 +190,8 @@ __host__ __device__ inline int dense_width(int Z) {
 
 struct MixSm {
   const int64_t *flse, *fmax, *mq;
-  const float *lg, *C;
+  const int64_t *lq;  // per entry: logit - lse in fixed point (kNegFix for a -inf logit)
+  const float *C;
   const int *utok, *nu;
   const float *dE, *Ee;
   const int16_t *dR;
@@ -230,13 +233,14 @@ __device__ __forceinline__ int64_t fix_f32(float x) {
 // exp(D 2^-40) for D <= 0: k = nearest integer to x / ln 2 from an estimate of
 // x within 2^-8, f = D - k ln 2 exactly in fixed point (|f| < 0.36), result
 // 2^k expf(f) with f rounded to 2^-31 first.
-__device__ __forceinline__ float exp_fix(int64_t D) {
-  if (D < kExpCut) return 0.f;
+__device__ __forceinline__ float exp_fix(int64_t D0) {
+  const int64_t D = D0 < kExpCut ? kExpCut : D0;
   const float xa = (float)(int)(D >> 32) * 0.00390625f;
   const int k = __float2int_rn(xa * 1.4426950408889634f);
   const int64_t f = D - (int64_t)k * kLn2Fix;
   const float ff = (float)(int)(f >> 9) * 4.656612873077393e-10f;
-  return ldexpf(expf(ff), k);
+  const float r = ldexpf(expf(ff), k);
+  return D0 < kExpCut ? 0.f : r;
 }
 
 // log(v) in 2^-40 units for a normal float v > 0: v = m 2^e with m in
@@ -266,14 +270,15 @@ struct Pick {
   bool any;    // some untaken child exists
 };
 
-// The warp's best of the lanes' (value desc, token asc) candidates.
+// The warp's best of the lanes' (value desc, token asc) candidates.  A lane's
+// candidates are distinct union tokens, so the winner is one lane's and its
+// union index is the largest among lanes holding (value, token).
 __device__ __forceinline__ Pick warp_pick(float bv, int bt, int bu, bool any) {
   const uint32_t vb = __float_as_uint(bv);  // bv >= 0: the bits order as the values
   const uint32_t m = __reduce_max_sync(kFull, vb);
   const int tm = __reduce_min_sync(kFull, vb == m ? bt : INT_MAX);
-  const uint32_t who = __ballot_sync(kFull, vb == m && bt == tm);
   Pick p;
-  p.u = __shfl_sync(kFull, bu, __ffs(who) - 1);
+  p.u = __reduce_max_sync(kFull, (vb == m && bt == tm) ? bu : -1);
   p.v = __uint_as_float(m);
   p.t = tm;
   p.any = __any_sync(kFull, any);
@@ -400,7 +405,7 @@ __device__ __forceinline__ Pick slow_dense(const MixSm &s, int lane, int q, int 
     base[z] = kVeryNeg;
     if (z < Z) {
       const int64_t P = s.Pn[q * Z + z];
-      if (P > kInfCut) base[z] = P - s.flse[d * Z + z] - Sq;
+      if (P > kInfCut) base[z] = P - Sq;
     }
   }
   const int16_t *R = s.dR + (size_t)d * s.ZK * ZP;
@@ -408,8 +413,8 @@ __device__ __forceinline__ Pick slow_dense(const MixSm &s, int lane, int q, int 
   auto term = [&](int u, int z) -> int64_t {
     const int j = R[(size_t)u * ZP + z];
     if (j < 0 || base[z] == kVeryNeg) return kVeryNeg;
-    const int64_t fx = fix_f32(s.lg[(d * Z + z) * K + j]);
-    return fx == kNegFix ? kVeryNeg : base[z] + fx;
+    const int64_t l = s.lq[(d * Z + z) * K + j];
+    return l <= kInfCut ? kVeryNeg : base[z] + l;
   };
   int64_t best = kVeryNeg;
   for (int u = lane; u < n; u += 32) {
@@ -450,20 +455,13 @@ __device__ __forceinline__ Pick slow_dense(const MixSm &s, int lane, int q, int 
 // reads the token's rank in branch z.
 template <int ZP>
 __device__ __forceinline__ int64_t child_p_dense(const MixSm &s, int lane, int p, int d, int u) {
-  int64_t P = kNegFix;
-  if (lane < s.Z) {
-    const int j = s.dR[((size_t)(d - 1) * s.ZK + u) * ZP + lane];
-    const int64_t Pp = s.Pn[p * s.Z + lane];
-    if (j >= 0 && Pp > kInfCut) {
-      const int row = (d - 1) * s.Z + lane;
-      const int64_t fx = fix_f32(s.lg[row * s.K + j]);
-      if (fx != kNegFix) {
-        P = Pp + (fx - s.flse[row]);
-        P = P < kNegFix ? kNegFix : P;
-      }
-    }
-  }
-  return P;
+  const int z = lane < s.Z ? lane : 0;  // lanes past Z read branch 0 and drop it
+  const int j = s.dR[((d - 1) * s.ZK + u) * ZP + z];
+  const int64_t Pp = s.Pn[p * s.Z + z];
+  const int64_t l = s.lq[((d - 1) * s.Z + z) * s.K + (j >= 0 ? j : 0)];
+  int64_t P = Pp + l;
+  P = P < kNegFix ? kNegFix : P;
+  return (lane < s.Z && j >= 0 && Pp > kInfCut && l > kInfCut) ? P : kNegFix;
 }
 
 // --------------------------------------------------------------- sparse form
@@ -511,13 +509,13 @@ __device__ __forceinline__ Pick slow_sparse(const MixSm &s, int lane, int q, int
   for (int z = 0; z < Z; ++z) {
     const int64_t P = s.Pn[q * Z + z];
     if (P <= kInfCut) continue;
-    const int64_t base = P - s.flse[d * Z + z] - Sq;
+    const int64_t base = P - Sq;
     const int e0 = (d * Z + z) * K;
     for (int j = lane; j < K; j += 32) {
-      const int64_t fx = fix_f32(s.lg[e0 + j]);
-      if (fx == kNegFix) continue;
+      const int64_t l = s.lq[e0 + j];
+      if (l <= kInfCut) continue;
       const int u = s.ue[e0 + j];
-      const int64_t v = base + fx;
+      const int64_t v = base + l;
       mx[u] = v > mx[u] ? v : mx[u];
     }
     __syncwarp();
@@ -536,13 +534,13 @@ __device__ __forceinline__ Pick slow_sparse(const MixSm &s, int lane, int q, int
   for (int z = 0; z < Z; ++z) {
     const int64_t P = s.Pn[q * Z + z];
     if (P <= kInfCut) continue;
-    const int64_t base = P - s.flse[d * Z + z] - Sq - M;
+    const int64_t base = P - Sq - M;
     const int e0 = (d * Z + z) * K;
     for (int j = lane; j < K; j += 32) {
-      const int64_t fx = fix_f32(s.lg[e0 + j]);
-      if (fx == kNegFix) continue;
+      const int64_t l = s.lq[e0 + j];
+      if (l <= kInfCut) continue;
       const int u = s.ue[e0 + j];
-      const int64_t D = base + fx;
+      const int64_t D = base + l;
       acc[u] += exp_fix(D < 0 ? D : 0);
     }
     __syncwarp();
@@ -559,11 +557,11 @@ __device__ __forceinline__ int64_t child_p_sparse(const MixSm &s, int lane, int 
   const int e0 = (d - 1) * s.ZK;
   for (int e = lane; e < s.ZK; e += 32) {
     if (s.ue[e0 + e] != u) continue;
-    const int z = e / s.K, row = (d - 1) * s.Z + z;
-    const int64_t Pp = s.Pn[p * s.Z + z], fx = fix_f32(s.lg[e0 + e]);
+    const int z = e / s.K;
+    const int64_t Pp = s.Pn[p * s.Z + z], l = s.lq[e0 + e];
     int64_t v = kNegFix;
-    if (Pp > kInfCut && fx != kNegFix) {
-      v = Pp + (fx - s.flse[row]);
+    if (Pp > kInfCut && l > kInfCut) {
+      v = Pp + l;
       v = v < kNegFix ? kNegFix : v;
     }
     s.Pn[i * s.Z + z] = v;
@@ -657,7 +655,8 @@ __global__ void __launch_bounds__(kMixThreads, 1) build_tree_mixture_kernel(MixA
   int64_t *flse = reinterpret_cast<int64_t *>(smem + L.flse);
   int64_t *fmax = reinterpret_cast<int64_t *>(smem + L.fmax);
   int64_t *mq = reinterpret_cast<int64_t *>(smem + L.mq);
-  float *lg = reinterpret_cast<float *>(smem + L.lg);
+  int64_t *lq = reinterpret_cast<int64_t *>(smem + L.lq);
+  float *lg = reinterpret_cast<float *>(smem + L.lgs);  // the group's logits, local entry index
   int *utok = reinterpret_cast<int *>(smem + L.utok);
   float *C = reinterpret_cast<float *>(smem + L.cost);
   int *nu = reinterpret_cast<int *>(smem + L.nu);
@@ -665,7 +664,6 @@ __global__ void __launch_bounds__(kMixThreads, 1) build_tree_mixture_kernel(MixA
   int16_t *dR = reinterpret_cast<int16_t *>(smem + L.dR);
   float *Ee = reinterpret_cast<float *>(smem + L.ee);
   uint16_t *ue = reinterpret_cast<uint16_t *>(smem + L.ue);
-  int *rtok = reinterpret_cast<int *>(smem + L.rtok);
   uint16_t *eu = reinterpret_cast<uint16_t *>(smem + L.eu);
   int *hk = reinterpret_cast<int *>(smem + L.hk);
 
@@ -690,102 +688,143 @@ __global__ void __launch_bounds__(kMixThreads, 1) build_tree_mixture_kernel(MixA
   // staging group
   const size_t rb = (size_t)r * Z * b * K;
   const int H = L.H, G = L.G, hshift = 32 - (31 - __clz(H));
-  for (int g0 = 0; g0 < b; g0 += G) {
-    const int g1 = g0 + G < b ? g0 + G : b, ng = (g1 - g0) * ZK;
-    // the group's logits and tokens (local entry li = (d - g0) ZK + z K + j),
-    // four loads in flight per thread; its hash tables emptied and, in the
-    // dense form, its union slots cleared
-    for (int q = tid; q < (g1 - g0) * H; q += kMixThreads) hk[q] = kEmptySlot;
-    if constexpr (ZP > 0) {
-      for (int q = tid; q < ng * ZP; q += kMixThreads) {
-        dE[(size_t)g0 * ZK * ZP + q] = 0.f;
-        dR[(size_t)g0 * ZK * ZP + q] = -1;
-      }
+  uint32_t *rmx = reinterpret_cast<uint32_t *>(smem + L.rmx);  // per row: its largest logit, ordered
+  // token tkn into the hash table h (at most half full): its slot
+  auto insert = [&](int *h, int tkn) -> uint16_t {
+    uint32_t sl = ((uint32_t)tkn * 0x9E3779B1u) >> hshift;
+    for (int it = 0; it < H; ++it) {
+      const int old = atomicCAS(h + sl, kEmptySlot, tkn);
+      if (old == kEmptySlot || old == tkn) break;
+      sl = (sl + 1) & (uint32_t)(H - 1);
     }
-    constexpr int UL = 4;
-    for (int l0 = tid; l0 < ng; l0 += kMixThreads * UL) {
-      float x[UL];
-      int t[UL];
-#pragma unroll
-      for (int k = 0; k < UL; ++k) {
-        const int li = l0 + k * kMixThreads;
-        if (li < ng) {
-          const int dl = li / ZK, rem = li - dl * ZK, z = rem / K, j = rem - z * K;
-          const size_t gi = rb + ((size_t)z * b + g0 + dl) * K + j;
-          x[k] = __ldg(a.topk_logit + gi);
-          t[k] = __ldg(a.topk_tok + gi);
+    return (uint16_t)sl;
+  };
+  // Work items are (row, 64-column block) pairs of the group, one warp each:
+  // lane l takes columns j0 + l and j0 + 32 + l.  One division per item.
+  const int KB = (K + 63) >> 6;
+  for (int g0 = 0; g0 < b; g0 += G) {
+    const int g1 = g0 + G < b ? g0 + G : b, ng = (g1 - g0) * ZK, items = (g1 - g0) * Z * KB;
+    // the group's hash tables emptied, its row maxima reset and, in the dense
+    // form, its union slots cleared
+    for (int q = tid; q < (g1 - g0) * H; q += kMixThreads) hk[q] = kEmptySlot;
+    for (int q = tid; q < (g1 - g0) * Z; q += kMixThreads) rmx[q] = 0u;  // below every ordered value
+    if constexpr (ZP > 0) {
+      float *e0 = dE + (size_t)g0 * ZK * ZP;
+      int16_t *r0 = dR + (size_t)g0 * ZK * ZP;
+      const int nq = ng * ZP;
+      if ((nq & 3) == 0 && ((uintptr_t)e0 & 15) == 0 && ((uintptr_t)r0 & 7) == 0) {
+        for (int q = tid; q < nq / 4; q += kMixThreads) {
+          reinterpret_cast<float4 *>(e0)[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+          reinterpret_cast<uint2 *>(r0)[q] = make_uint2(0xFFFFFFFFu, 0xFFFFFFFFu);
         }
-      }
-#pragma unroll
-      for (int k = 0; k < UL; ++k) {
-        const int li = l0 + k * kMixThreads;
-        if (li < ng) {
-          lg[(size_t)g0 * ZK + li] = x[k];
-          rtok[li] = t[k];
+      } else {
+        for (int q = tid; q < nq; q += kMixThreads) {
+          e0[q] = 0.f;
+          r0[q] = -1;
         }
       }
     }
     __syncthreads();
-    // one warp per (position, branch) row: its largest logit, and its tokens
-    // into the position's hash table
-    for (int row = g0 * Z + warp; row < g1 * Z; row += NW) {
-      const int d = row / Z;
-      int *h = hk + (d - g0) * H;
-      float mx = -INFINITY;
-      for (int j = lane; j < K; j += 32) {
-        const int li = (row - g0 * Z) * K + j;
-        mx = fmaxf(mx, lg[(size_t)row * K + j]);
-        const int tkn = rtok[li];
-        uint32_t sl = ((uint32_t)tkn * 0x9E3779B1u) >> hshift;
-        for (int it = 0; it < H; ++it) {  // the table is at most half full
-          const int old = atomicCAS(h + sl, kEmptySlot, tkn);
-          if (old == kEmptySlot || old == tkn) break;
-          sl = (sl + 1) & (uint32_t)(H - 1);
+    // (A) each item's logits and tokens, four items' loads in flight: the
+    // logits kept, logit - lse in fixed point, the tokens into their
+    // position's table, the row's largest logit
+    constexpr int UI = 4;
+    for (int it0 = warp; it0 < items; it0 += NW * UI) {
+      float x[UI][2];
+      int t[UI][2];
+#pragma unroll
+      for (int k = 0; k < UI; ++k) {
+        const int item = it0 + k * NW;
+        const int rl = item / KB, j0 = (item - rl * KB) << 6;  // row within the group, block
+        const int d = g0 + rl / Z, z = rl % Z;
+        const size_t g = rb + ((size_t)z * b + d) * K;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int j = j0 + 32 * h + lane;
+          const bool ok = item < items && j < K;
+          x[k][h] = ok ? __ldg(a.topk_logit + g + j) : -INFINITY;
+          t[k][h] = ok ? __ldg(a.topk_tok + g + j) : 0;
         }
-        eu[li] = (uint16_t)sl;
       }
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
-      if (lane == 0) {
-        const int64_t fm = fix_f32(mx);
+      for (int k = 0; k < UI; ++k) {
+        const int item = it0 + k * NW;
+        if (item >= items) break;  // uniform over the warp
+        const int rl = item / KB, j0 = (item - rl * KB) << 6;
+        const int dl = rl / Z, row = g0 * Z + rl;
+        int *hq = hk + dl * H;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int j = j0 + 32 * h + lane;
+          if (j < K) {
+            const int li = rl * K + j;  // = dl ZK + z K + j
+            lg[li] = x[k][h];
+            const int64_t fx = fix_f32(x[k][h]);
+            lq[(size_t)row * K + j] = fx == kNegFix ? kNegFix : fx - flse[row];
+            eu[li] = insert(hq, t[k][h]);
+          }
+        }
+        float mx = fmaxf(x[k][0], x[k][1]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+        if (lane == 0) atomicMax(rmx + rl, ord_f32(mx));
+      }
+    }
+    __syncthreads();
+    // (B) one warp per position: its table's used slots -> union indices 0, 1,
+    // ... (lane l owns slots 32 q + l; numbered lane by lane after a warp scan
+    // of the lanes' counts)
+    for (int d = g0 + warp; d < g1; d += NW) {
+      int *h = hk + (d - g0) * H;
+      const int S_ = H >> 5;
+      int cnt = 0;
+      for (int q = 0; q < S_; ++q) cnt += h[32 * q + lane] != kEmptySlot;
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += v;
+      }
+      int u = incl - cnt;
+      for (int q = 0; q < S_; ++q) {
+        const int v = h[32 * q + lane];
+        if (v != kEmptySlot) {
+          utok[d * ZK + u] = v;
+          h[32 * q + lane] = u++;
+        }
+      }
+      if (lane == 31) nu[d] = incl;
+    }
+    __syncthreads();
+    // (C) each entry's union index and E = exp(logit - its row's largest);
+    // the rows' largest logits in fixed point
+    for (int item = warp; item < items; item += NW) {
+      const int rl = item / KB, j0 = (item - rl * KB) << 6;
+      const int dl = rl / Z, z = rl - dl * Z, d = g0 + dl, row = g0 * Z + rl;
+      const int64_t fm = fix_f32(unord_f32(rmx[rl]));
+      if (lane == 0 && j0 == 0) {
         fmax[row] = fm;
         mq[row] = fm == kNegFix ? kNegFix : fm - flse[row];
       }
-    }
-    __syncthreads();
-    for (int d = g0 + warp; d < g1; d += NW) {  // slot order -> union index
-      int *h = hk + (d - g0) * H;
-      int cnt = 0;
-      for (int s0 = 0; s0 < H; s0 += 32) {
-        const int v = h[s0 + lane];
-        const bool occ = v != kEmptySlot;
-        const uint32_t bal = __ballot_sync(kFull, occ);
-        if (occ) {
-          const int u = cnt + __popc(bal & ((1u << lane) - 1u));
-          utok[d * ZK + u] = v;
-          h[s0 + lane] = u;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int j = j0 + 32 * h + lane;
+        if (j < K) {
+          const int li = rl * K + j;
+          const size_t e = (size_t)row * K + j;
+          int u = hk[dl * H + eu[li]];
+          u = (unsigned)u < (unsigned)ZK ? u : 0;  // (a token equal to INT32_MIN)
+          const int64_t l = lq[e];
+          const float ev = (fm == kNegFix || l == kNegFix) ? 0.f : exp_fix(l + flse[row] - fm);
+          ue[e] = (uint16_t)u;
+          if constexpr (ZP > 0) {
+            const size_t slot = ((size_t)d * ZK + u) * ZP + z;
+            dE[slot] = ev;
+            dR[slot] = (int16_t)j;
+          } else {
+            Ee[e] = ev;
+          }
         }
-        cnt += __popc(bal);
-      }
-      if (lane == 0) nu[d] = cnt;
-    }
-    __syncthreads();
-    // each entry's union index and E = exp(logit - its row's largest)
-    for (int li = tid; li < ng; li += kMixThreads) {
-      const int dl = li / ZK, rem = li - dl * ZK, z = rem / K, j = rem - z * K;
-      const int d = g0 + dl, row = d * Z + z;
-      const size_t e = (size_t)g0 * ZK + li;
-      int u = hk[dl * H + eu[li]];
-      u = (unsigned)u < (unsigned)ZK ? u : 0;  // (a token equal to INT32_MIN)
-      const int64_t fm = fmax[row], fx = fix_f32(lg[e]);
-      const float ev = (fm == kNegFix || fx == kNegFix) ? 0.f : exp_fix(fx - fm);
-      ue[e] = (uint16_t)u;
-      if constexpr (ZP > 0) {
-        const size_t slot = ((size_t)d * ZK + u) * ZP + z;
-        dE[slot] = ev;
-        dR[slot] = (int16_t)j;
-      } else {
-        Ee[e] = ev;
       }
     }
     __syncthreads();
@@ -794,7 +833,7 @@ __global__ void __launch_bounds__(kMixThreads, 1) build_tree_mixture_kernel(MixA
   s.flse = flse;
   s.fmax = fmax;
   s.mq = mq;
-  s.lg = lg;
+  s.lq = lq;
   s.C = C;
   s.utok = utok;
   s.nu = nu;
@@ -867,11 +906,11 @@ __global__ void __launch_bounds__(kMixThreads, 1) build_tree_mixture_kernel(MixA
       wl = 0.f;
       if (lane < Z) s.Pn[i * Z + lane] = P;
       if (d >= b) return false;
-      const int64_t m = lane < Z ? s.mq[d * Z + lane] : kNegFix;
+      const int64_t m = s.mq[d * Z + (lane < Z ? lane : 0)];
       const int64_t X = (lane < Z && P > kInfCut && m > kInfCut) ? P + m : kVeryNeg;
       const int64_t Smax = warp_max_i64(X);
       if (Smax <= kInfCut) return false;
-      wl = X <= kInfCut ? 0.f : exp_fix(X - Smax);
+      wl = exp_fix(X - Smax);  // 0 for a -inf branch
       if (lane < Z) s.wz[i * Z + lane] = wl;
       if (lane == 0) s.Sn[i] = Smax;
       return true;
