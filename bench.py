@@ -774,11 +774,12 @@ def run_mixture(args, ws, rank, local, light=True):
     lar = torch.from_numpy(synth.l_ar(w)).to(dev)
     cost = torch.full((n_max + 1,), 5.0, dtype=torch.float32, device=dev)
     tr = bastion.alloc_tree(B, n_max, dev)
+    wsm = bastion.workspace(bastion.bastion_build_tree_mixture_workspace_bytes(B, Z, b, K, n_max), dev)
 
     def call():
         bastion.bastion_build_tree_mixture(lg, tk, ls, pid, n_max, roots, ctx, cost, lar, tr.n_nodes,
                                            tr.parent, tr.depth, tr.pos_id, tr.token, tr.log_rho,
-                                           tr.a_hat, tr.speedup, tr.anc_mask, st[:B])
+                                           tr.a_hat, tr.speedup, tr.anc_mask, wsm, st[:B])
 
     if args.profile_kernel:
         for _ in range(args.launches):

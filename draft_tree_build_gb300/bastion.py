@@ -30,7 +30,7 @@ SYMBOLS = (
     "bastion_version", "bastion_status_string",
     "bastion_topk_marginals_workspace_bytes", "bastion_topk_marginals",
     "bastion_lm_head_topk_workspace_bytes", "bastion_lm_head_topk",
-    "bastion_build_tree", "bastion_build_tree_mixture",
+    "bastion_build_tree", "bastion_build_tree_mixture_workspace_bytes", "bastion_build_tree_mixture",
     "bastion_calibrate_cost",
     "bastion_tree_attention_workspace_bytes", "bastion_tree_attention",
     "bastion_verify_greedy_workspace_bytes", "bastion_verify_greedy",
@@ -75,9 +75,11 @@ def lib(build_if_missing: bool = True):
     L.bastion_lm_head_topk.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp, vp]
     L.bastion_build_tree.restype = i32
     L.bastion_build_tree.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, i32, vp] + [vp] * 11 + [vp]
+    L.bastion_build_tree_mixture_workspace_bytes.restype = sz
+    L.bastion_build_tree_mixture_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
     L.bastion_build_tree_mixture.restype = i32
     L.bastion_build_tree_mixture.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, i32,
-                                             vp] + [vp] * 10 + [vp]
+                                             vp] + [vp] * 9 + [vp, sz, vp, vp]
     L.bastion_calibrate_cost.restype = i32
     L.bastion_calibrate_cost.argtypes = [vp, vp, i32] + [ctypes.c_double] * 7 + [i32, vp, vp, vp, vp]
     L.bastion_tree_attention_workspace_bytes.restype = sz
@@ -199,10 +201,15 @@ def bastion_build_tree(topk_logit, topk_tok, lse, n_max, root_token, ctx_len, co
     _check(rc, "bastion_build_tree")
 
 
+def bastion_build_tree_mixture_workspace_bytes(B: int, Z: int, b: int, K: int, n_max: int) -> int:
+    return int(lib().bastion_build_tree_mixture_workspace_bytes(B, Z, b, K, n_max))
+
+
 def bastion_build_tree_mixture(topk_logit, topk_tok, lse, pi, n_max, root_token, ctx_len, cost_ms, l_ar,
                                n_nodes, parent, depth, pos_id, token, log_rho, a_hat, speedup, anc_mask,
-                               status, stream=None):
-    """topk_logit/tok [B, Z, b, K], lse [B, Z, b] float64, pi [B, Z] float64 (contiguous)."""
+                               workspace, status, stream=None):
+    """topk_logit/tok [B, Z, b, K], lse [B, Z, b] float64, pi [B, Z] float64 (contiguous);
+    workspace: bastion_build_tree_mixture_workspace_bytes(B, Z, b, K, n_max) bytes."""
     B, Z, b, K = topk_logit.shape
     for t in (topk_logit, topk_tok, lse, pi):
         if not t.is_contiguous():
@@ -221,6 +228,7 @@ def bastion_build_tree_mixture(topk_logit, topk_tok, lse, pi, n_max, root_token,
                                           int(n_max), _p(root_token), _p(ctx_len), _p(cost_ms), per_req,
                                           _p(l_ar), _p(n_nodes), _p(parent), _p(depth), _p(pos_id),
                                           _p(token), _p(log_rho), _p(a_hat), _p(speedup), _p(anc_mask),
+                                          _p(workspace), workspace.numel() * workspace.element_size(),
                                           _p(status), _s(stream))
     _check(rc, "bastion_build_tree_mixture")
 

@@ -24,13 +24,15 @@ int launch_build_tree(const float *topk_logit, const int32_t *topk_tok, const do
                       uint32_t *anc_mask, int32_t *status, cudaStream_t stream);
 size_t verify_workspace_bytes(int B, int n_max);
 size_t mixture_tree_smem_bytes(int Z, int b, int K, int n_max);
+size_t mixture_tree_ws_stride(int Z, int b, int K, int n_max);
 int launch_build_tree_mixture(const float *topk_logit, const int32_t *topk_tok, const double *lse,
                               const double *pi, int B, int Z, int b, int K, int n_max,
                               const int32_t *root_token, const int32_t *ctx_len,
                               const float *cost_ms, int cost_per_request, const float *l_ar,
                               int32_t *n_nodes, int32_t *parent, int32_t *depth, int32_t *pos_id,
                               int32_t *token, float *log_rho, float *a_hat, float *speedup,
-                              uint32_t *anc_mask, int32_t *status, cudaStream_t stream);
+                              uint32_t *anc_mask, void *workspace, int32_t *status,
+                              cudaStream_t stream);
 int launch_verify(const void *target, int dtype, int B, int n_max, int V, int64_t ld, int b,
                   const int32_t *n_nodes, const int32_t *parent, const int32_t *token,
                   int32_t *argmax, int32_t *accept_len, int32_t *accept_nodes,
@@ -150,26 +152,38 @@ int bastion_build_tree(const float *topk_logit, const int32_t *topk_tok, const d
                                     status, (cudaStream_t)stream);
 }
 
+static bool mixture_sizes_ok(int B, int Z, int b, int K, int n_max) {
+  return !(B < 1 || B > (1 << 24) || Z < 1 || Z > 32 || b < 1 || b > 32 || K < 1 || K > 1024 ||
+           n_max < 1 || n_max > 256);
+}
+
+size_t bastion_build_tree_mixture_workspace_bytes(int B, int Z, int b, int K, int n_max) {
+  if (!mixture_sizes_ok(B, Z, b, K, n_max)) return 0;
+  return (size_t)B * bastion::mixture_tree_ws_stride(Z, b, K, n_max);
+}
+
 int bastion_build_tree_mixture(const float *topk_logit, const int32_t *topk_tok, const double *lse,
                                const double *pi, int B, int Z, int b, int K, int n_max,
                                const int32_t *root_token, const int32_t *ctx_len,
                                const float *cost_ms, int cost_per_request, const float *l_ar,
                                int32_t *n_nodes, int32_t *parent, int32_t *depth, int32_t *pos_id,
                                int32_t *token, float *log_rho, float *a_hat, float *speedup,
-                               uint32_t *anc_mask, int32_t *status, bastion_stream_t stream) {
+                               uint32_t *anc_mask, void *workspace, size_t workspace_bytes,
+                               int32_t *status, bastion_stream_t stream) {
   if (!topk_logit || !topk_tok || !lse || !pi || !root_token || !ctx_len || !cost_ms || !l_ar ||
       !n_nodes || !parent || !depth || !pos_id || !token || !log_rho || !a_hat || !speedup ||
-      !anc_mask || !status)
+      !anc_mask || !workspace || !status)
     return BASTION_ERR_NULL;
-  if (B < 1 || B > (1 << 24) || Z < 1 || Z > 32 || b < 1 || b > 32 || K < 1 || K > 1024 ||
-      n_max < 1 || n_max > 256)
-    return BASTION_ERR_SIZE;
-  if (!aligned(lse, 8) || !aligned(pi, 8)) return BASTION_ERR_ALIGN;
+  if (!mixture_sizes_ok(B, Z, b, K, n_max)) return BASTION_ERR_SIZE;
+  if (!aligned(lse, 8) || !aligned(pi, 8) || !aligned(workspace, 256)) return BASTION_ERR_ALIGN;
+  if (workspace_bytes < (size_t)B * bastion::mixture_tree_ws_stride(Z, b, K, n_max))
+    return BASTION_ERR_WORKSPACE;
   if (bastion::mixture_tree_smem_bytes(Z, b, K, n_max) > (size_t)227 * 1024) return BASTION_ERR_UNSUPPORTED;
   return bastion::launch_build_tree_mixture(topk_logit, topk_tok, lse, pi, B, Z, b, K, n_max,
                                             root_token, ctx_len, cost_ms, cost_per_request, l_ar,
                                             n_nodes, parent, depth, pos_id, token, log_rho, a_hat,
-                                            speedup, anc_mask, status, (cudaStream_t)stream);
+                                            speedup, anc_mask, workspace, status,
+                                            (cudaStream_t)stream);
 }
 
 size_t bastion_verify_greedy_workspace_bytes(int B, int n_max, int V) {

@@ -104,22 +104,23 @@ struct MixArgs {
   float *log_rho, *a_hat, *speedup;
   uint32_t *anc_mask;
   int32_t *status;
+  unsigned char *ws;  // the requests' tables, ws_stride bytes each
+  size_t ws_stride;
 };
 
-// Shared-memory layout for one request.  Region 1 (the position tables) lives
-// through the build; region 2 holds one group of positions' staging arrays
-// while the tables are built and the node arrays afterwards.  Entry
-// e = (d Z + z) K + j is branch z's rank-j token at block position d + 1;
-// union token u of position d + 1 is slot d ZK + u.  ZP = 0: the sparse form.
+// One request's tables (region 1), built by the staging kernel in the
+// workspace and copied as they are into the pop kernel's shared memory, then
+// the pop kernel's own arrays (region 2).  Entry e = (d Z + z) K + j is branch
+// z's rank-j token at block position d + 1; union token u of position d + 1
+// is slot d ZK + u.  ZP = 0: the sparse form.
 struct MixLayout {
-  size_t flse, fmax, mq, lq, utok, cost, nu;  // region 1, both forms
-  size_t ue;                                  // region 1, both forms
-  size_t dE, dR;                              // region 1, dense form
-  size_t ee;                                  // region 1, sparse form
-  size_t pn, sn, lrn, acc, wz, an, taken, mask, par, dep, tok, pu, pt, part;  // region 2: nodes
-  size_t lgs, eu, hk, rmx;                    // region 2: staging of one group
-  int H, G;  // hash slots per position, positions per staging group
-  size_t bytes;
+  size_t flse, fmax, mq, lq, utok, nu, ue;  // region 1, both forms
+  size_t dE, dR;                            // region 1, dense form
+  size_t ee;                                // region 1, sparse form
+  size_t r1;                                // region 1 bytes
+  size_t cost, pn, sn, lrn, acc, wz, an, taken, mask, par, dep, tok, pu, pt, part;  // region 2
+  size_t bytes;                             // the pop kernel's shared memory
+  int H;                                    // hash slots per position (staging)
 };
 
 __host__ __device__ inline MixLayout mix_layout(int Z, int b, int K, int n_max, int ZP) {
@@ -139,18 +140,18 @@ __host__ __device__ inline MixLayout mix_layout(int Z, int b, int K, int n_max, 
   l.mq = take((size_t)b * Z * 8);
   l.lq = take(E * 8);
   l.utok = take(E * 4);
-  l.cost = take((n + 1) * 4);
   l.nu = take((size_t)b * 4);
-  l.dE = l.dR = l.ee = 0;
   l.ue = take(E * 2);
+  l.dE = l.dR = l.ee = 0;
   if (ZP > 0) {
     l.dE = take(E * ZP * 4);
     l.dR = take(E * ZP * 2);
   } else {
     l.ee = take(E * 4);
   }
-  const size_t r2 = o;
-  const size_t copies = ZP > 0 ? kPopWarps : 1;  // per-warp copies of P, S and w
+  l.r1 = o;
+  const size_t copies = ZP > 0 ? kPopWarps : 1;  // per-warp copies of P, S, w and the pending child
+  l.cost = take((n + 1) * 4);
   l.pn = take(copies * n * Z * 8);
   l.sn = take(copies * n * 8);
   l.lrn = take(n * 8);
@@ -165,21 +166,32 @@ __host__ __device__ inline MixLayout mix_layout(int Z, int b, int K, int n_max, 
   l.pu = take(copies * n * 4);
   l.pt = take(copies * n * 4);
   l.part = ZP > 0 ? take(2 * 2 * kPopWarps * 16) : 0;
-  const size_t node_bytes = o - r2;
-  const size_t per_pos = ((ZK * 4 + 15) & ~(size_t)15) + ((ZK * 2 + 15) & ~(size_t)15) + (size_t)H * 4 +
-                         (size_t)Z * 4;
-  const size_t cap = node_bytes > 65536 ? node_bytes : 65536;
-  int G = (int)(cap / per_pos);
-  G = G < 1 ? 1 : (G > b ? b : G);
-  o = r2;
-  l.lgs = take((size_t)G * ZK * 4);
-  l.eu = take((size_t)G * ZK * 2);
-  l.hk = take((size_t)G * H * 4);
-  l.rmx = take((size_t)G * Z * 4);
+  l.bytes = o;
   l.H = H;
-  l.G = G;
-  const size_t stage_bytes = o - r2;
-  l.bytes = r2 + (node_bytes > stage_bytes ? node_bytes : stage_bytes);
+  return l;
+}
+
+// The staging kernel's shared memory for one position: the logits, each
+// entry's hash slot, the hash table, and per branch row its largest logit
+// (ordered) and fixed-point lse.
+struct StageLayout {
+  size_t lg, eu, hk, rmx, fl, bytes;
+};
+__host__ __device__ inline StageLayout stage_layout(int Z, int K, int H) {
+  StageLayout l;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += (bytes + 15) & ~(size_t)15;
+    return at;
+  };
+  const size_t ZK = (size_t)Z * K;
+  l.fl = take((size_t)Z * 8);
+  l.lg = take(ZK * 4);
+  l.hk = take((size_t)H * 4);
+  l.eu = take(ZK * 2);
+  l.rmx = take((size_t)Z * 4);
+  l.bytes = o;
   return l;
 }
 
@@ -645,32 +657,210 @@ struct Pending {
   }
 };
 
-template <int S, int ZP>
-__global__ void __launch_bounds__(kMixThreads, 1) build_tree_mixture_kernel(MixArgs a) {
+// Staging: one CTA per (block position d + 1, request r) builds that
+// position's tables in the workspace.  Work items are (branch row, 64-column
+// block) pairs, one warp each, lane l taking columns j0 + l and j0 + 32 + l:
+// (A) the logits and tokens, four items' loads in flight: logit - lse in
+// fixed point, each token into the position's hash table (at most half
+// full), the row's largest logit; (B) warp 0 numbers the table's used slots
+// (lane l owns slots 32 q + l; numbered lane by lane after a warp scan), the
+// union of the branches' tokens; (C) each entry's union index and
+// E = exp(logit - its row's largest), scattered to its union token's record
+// in the dense form.
+template <int ZP>
+__global__ void __launch_bounds__(kMixThreads) mixture_stage_kernel(MixArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
-  const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int d = blockIdx.x, r = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int NW = kMixThreads / 32;
-  const int Z = a.Z, b = a.b, K = a.K, n_max = a.n_max, ZK = Z * K;
-  const MixLayout L = mix_layout(Z, b, K, n_max, ZP);
-  int64_t *flse = reinterpret_cast<int64_t *>(smem + L.flse);
-  int64_t *fmax = reinterpret_cast<int64_t *>(smem + L.fmax);
-  int64_t *mq = reinterpret_cast<int64_t *>(smem + L.mq);
-  int64_t *lq = reinterpret_cast<int64_t *>(smem + L.lq);
-  float *lg = reinterpret_cast<float *>(smem + L.lgs);  // the group's logits, local entry index
-  int *utok = reinterpret_cast<int *>(smem + L.utok);
-  float *C = reinterpret_cast<float *>(smem + L.cost);
-  int *nu = reinterpret_cast<int *>(smem + L.nu);
-  float *dE = reinterpret_cast<float *>(smem + L.dE);
-  int16_t *dR = reinterpret_cast<int16_t *>(smem + L.dR);
-  float *Ee = reinterpret_cast<float *>(smem + L.ee);
-  uint16_t *ue = reinterpret_cast<uint16_t *>(smem + L.ue);
-  uint16_t *eu = reinterpret_cast<uint16_t *>(smem + L.eu);
-  int *hk = reinterpret_cast<int *>(smem + L.hk);
+  const int Z = a.Z, b = a.b, K = a.K, ZK = Z * K;
+  const MixLayout L = mix_layout(Z, b, K, a.n_max, ZP);
+  const int H = L.H, hshift = 32 - (31 - __clz(H));
+  const StageLayout SL = stage_layout(Z, K, H);
+  float *lgs = reinterpret_cast<float *>(smem + SL.lg);
+  int *hk = reinterpret_cast<int *>(smem + SL.hk);
+  uint16_t *eu = reinterpret_cast<uint16_t *>(smem + SL.eu);
+  uint32_t *rmx = reinterpret_cast<uint32_t *>(smem + SL.rmx);
+  int64_t *fl = reinterpret_cast<int64_t *>(smem + SL.fl);
+  unsigned char *w = a.ws + (size_t)r * a.ws_stride;
+  int64_t *flse = reinterpret_cast<int64_t *>(w + L.flse) + d * Z;
+  int64_t *fmax = reinterpret_cast<int64_t *>(w + L.fmax) + d * Z;
+  int64_t *mq = reinterpret_cast<int64_t *>(w + L.mq) + d * Z;
+  int64_t *lq = reinterpret_cast<int64_t *>(w + L.lq) + (size_t)d * ZK;
+  int *utok = reinterpret_cast<int *>(w + L.utok) + (size_t)d * ZK;
+  int *nu = reinterpret_cast<int *>(w + L.nu);
+  uint16_t *ue = reinterpret_cast<uint16_t *>(w + L.ue) + (size_t)d * ZK;
+  float *dE = reinterpret_cast<float *>(w + L.dE) + (size_t)d * ZK * ZP;
+  int16_t *dR = reinterpret_cast<int16_t *>(w + L.dR) + (size_t)d * ZK * ZP;
+  float *Ee = reinterpret_cast<float *>(w + L.ee) + (size_t)d * ZK;
 
   griddep_wait();
   griddep_launch_dependents();
 
-  // ---- the cost row and the fixed-point lse of every (position, branch) row
+  for (int q = tid; q < H; q += kMixThreads) hk[q] = kEmptySlot;
+  for (int q = tid; q < Z; q += kMixThreads) {
+    rmx[q] = 0u;  // below every ordered value
+    const int64_t v = tb::fix_lse(__ldg(a.lse + ((size_t)r * Z + q) * b + d));
+    fl[q] = v;
+    flse[q] = v;
+  }
+  if constexpr (ZP > 0) {  // the position's union records cleared (E 0, rank -1)
+    const int nq = ZK * ZP;
+    if ((nq & 3) == 0 && ((uintptr_t)dE & 15) == 0 && ((uintptr_t)dR & 7) == 0) {
+      for (int q = tid; q < nq / 4; q += kMixThreads) {
+        reinterpret_cast<float4 *>(dE)[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+        reinterpret_cast<uint2 *>(dR)[q] = make_uint2(0xFFFFFFFFu, 0xFFFFFFFFu);
+      }
+    } else {
+      for (int q = tid; q < nq; q += kMixThreads) {
+        dE[q] = 0.f;
+        dR[q] = -1;
+      }
+    }
+  }
+  __syncthreads();
+
+  auto insert = [&](int tkn) -> uint16_t {
+    uint32_t sl = ((uint32_t)tkn * 0x9E3779B1u) >> hshift;
+    for (int it = 0; it < H; ++it) {
+      const int old = atomicCAS(hk + sl, kEmptySlot, tkn);
+      if (old == kEmptySlot || old == tkn) break;
+      sl = (sl + 1) & (uint32_t)(H - 1);
+    }
+    return (uint16_t)sl;
+  };
+  const int KB = (K + 63) >> 6, items = Z * KB;
+  const size_t rb = (size_t)r * Z * b * K;
+  constexpr int UI = 4;
+  for (int it0 = warp; it0 < items; it0 += NW * UI) {  // (A)
+    float x[UI][2];
+    int t[UI][2];
+#pragma unroll
+    for (int k = 0; k < UI; ++k) {
+      const int item = it0 + k * NW;
+      const int z = item / KB, j0 = (item - z * KB) << 6;
+      const size_t g = rb + ((size_t)z * b + d) * K;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int j = j0 + 32 * h + lane;
+        const bool ok = item < items && j < K;
+        x[k][h] = ok ? __ldg(a.topk_logit + g + j) : -INFINITY;
+        t[k][h] = ok ? __ldg(a.topk_tok + g + j) : 0;
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < UI; ++k) {
+      const int item = it0 + k * NW;
+      if (item >= items) break;  // uniform over the warp
+      const int z = item / KB, j0 = (item - z * KB) << 6;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int j = j0 + 32 * h + lane;
+        if (j < K) {
+          lgs[z * K + j] = x[k][h];
+          const int64_t fx = fix_f32(x[k][h]);
+          lq[z * K + j] = fx == kNegFix ? kNegFix : fx - fl[z];
+          eu[z * K + j] = insert(t[k][h]);
+        }
+      }
+      float mx = fmaxf(x[k][0], x[k][1]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+      if (lane == 0) atomicMax(rmx + z, ord_f32(mx));
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {  // (B)
+    const int S_ = H >> 5;
+    int cnt = 0;
+    for (int q = 0; q < S_; ++q) cnt += hk[32 * q + lane] != kEmptySlot;
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int u = incl - cnt;
+    for (int q = 0; q < S_; ++q) {
+      const int v = hk[32 * q + lane];
+      if (v != kEmptySlot) {
+        utok[u] = v;
+        hk[32 * q + lane] = u++;
+      }
+    }
+    if (lane == 31) nu[d] = incl;
+  }
+  __syncthreads();
+  for (int item = warp; item < items; item += NW) {  // (C)
+    const int z = item / KB, j0 = (item - z * KB) << 6;
+    const int64_t fm = fix_f32(unord_f32(rmx[z]));
+    if (lane == 0 && j0 == 0) {
+      fmax[z] = fm;
+      mq[z] = fm == kNegFix ? kNegFix : fm - fl[z];
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int j = j0 + 32 * h + lane;
+      if (j < K) {
+        const int e = z * K + j;
+        int u = hk[eu[e]];
+        u = (unsigned)u < (unsigned)ZK ? u : 0;  // (a token equal to INT32_MIN)
+        const int64_t fx = fix_f32(lgs[e]);
+        const float ev = (fm == kNegFix || fx == kNegFix) ? 0.f : exp_fix(fx - fm);
+        ue[e] = (uint16_t)u;
+        if constexpr (ZP > 0) {
+          dE[u * ZP + z] = ev;
+          dR[u * ZP + z] = (int16_t)j;
+        } else {
+          Ee[e] = ev;
+        }
+      }
+    }
+  }
+}
+
+// The pops of request r on its tables (copied from the workspace).
+template <int S, int ZP>
+__global__ void __launch_bounds__(kMixThreads, 1) build_tree_mixture_kernel(MixArgs a) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int Z = a.Z, b = a.b, K = a.K, n_max = a.n_max, ZK = Z * K;
+  const MixLayout L = mix_layout(Z, b, K, n_max, ZP);
+  const int64_t *flse = reinterpret_cast<const int64_t *>(smem + L.flse);
+  const int64_t *fmax = reinterpret_cast<const int64_t *>(smem + L.fmax);
+  const int64_t *mq = reinterpret_cast<const int64_t *>(smem + L.mq);
+  const int64_t *lq = reinterpret_cast<const int64_t *>(smem + L.lq);
+  const int *utok = reinterpret_cast<const int *>(smem + L.utok);
+  const int *nu = reinterpret_cast<const int *>(smem + L.nu);
+  const uint16_t *ue = reinterpret_cast<const uint16_t *>(smem + L.ue);
+  const float *dE = reinterpret_cast<const float *>(smem + L.dE);
+  const int16_t *dR = reinterpret_cast<const int16_t *>(smem + L.dR);
+  const float *Ee = reinterpret_cast<const float *>(smem + L.ee);
+  float *C = reinterpret_cast<float *>(smem + L.cost);
+
+  griddep_wait();  // the staging kernel's tables are complete
+  griddep_launch_dependents();
+
+  // ---- the tables into shared memory (16-byte chunks, several in flight),
+  // and the cost row
+  {
+    const uint4 *src = reinterpret_cast<const uint4 *>(a.ws + (size_t)r * a.ws_stride);
+    uint4 *dst = reinterpret_cast<uint4 *>(smem);
+    const int n16 = (int)(L.r1 >> 4);
+    constexpr int UC = 8;
+    for (int q0 = tid; q0 < n16; q0 += kMixThreads * UC) {
+      uint4 v[UC];
+#pragma unroll
+      for (int k = 0; k < UC; ++k) {
+        const int q = q0 + k * kMixThreads;
+        if (q < n16) v[k] = __ldcg(src + q);
+      }
+#pragma unroll
+      for (int k = 0; k < UC; ++k) {
+        const int q = q0 + k * kMixThreads;
+        if (q < n16) dst[q] = v[k];
+      }
+    }
+  }
   const float *cr = a.cost + (a.cost_per_request ? (size_t)r * (n_max + 1) : 0);
   bool bad = false;
   for (int i = tid; i <= n_max; i += kMixThreads) {
@@ -678,157 +868,8 @@ __global__ void __launch_bounds__(kMixThreads, 1) build_tree_mixture_kernel(MixA
     C[i] = c;
     if (i >= 1) bad |= !(c > 0.f) || isinf(c);
   }
-  for (int q = tid; q < b * Z; q += kMixThreads) {
-    const int d = q / Z, z = q - d * Z;
-    flse[q] = tb::fix_lse(__ldg(a.lse + ((size_t)r * Z + z) * b + d));
-  }
   const bool bad_cost = __syncthreads_or(bad) != 0;
 
-  // ---- the union U of the branches' tokens at each position, G positions per
-  // staging group
-  const size_t rb = (size_t)r * Z * b * K;
-  const int H = L.H, G = L.G, hshift = 32 - (31 - __clz(H));
-  uint32_t *rmx = reinterpret_cast<uint32_t *>(smem + L.rmx);  // per row: its largest logit, ordered
-  // token tkn into the hash table h (at most half full): its slot
-  auto insert = [&](int *h, int tkn) -> uint16_t {
-    uint32_t sl = ((uint32_t)tkn * 0x9E3779B1u) >> hshift;
-    for (int it = 0; it < H; ++it) {
-      const int old = atomicCAS(h + sl, kEmptySlot, tkn);
-      if (old == kEmptySlot || old == tkn) break;
-      sl = (sl + 1) & (uint32_t)(H - 1);
-    }
-    return (uint16_t)sl;
-  };
-  // Work items are (row, 64-column block) pairs of the group, one warp each:
-  // lane l takes columns j0 + l and j0 + 32 + l.  One division per item.
-  const int KB = (K + 63) >> 6;
-  for (int g0 = 0; g0 < b; g0 += G) {
-    const int g1 = g0 + G < b ? g0 + G : b, ng = (g1 - g0) * ZK, items = (g1 - g0) * Z * KB;
-    // the group's hash tables emptied, its row maxima reset and, in the dense
-    // form, its union slots cleared
-    for (int q = tid; q < (g1 - g0) * H; q += kMixThreads) hk[q] = kEmptySlot;
-    for (int q = tid; q < (g1 - g0) * Z; q += kMixThreads) rmx[q] = 0u;  // below every ordered value
-    if constexpr (ZP > 0) {
-      float *e0 = dE + (size_t)g0 * ZK * ZP;
-      int16_t *r0 = dR + (size_t)g0 * ZK * ZP;
-      const int nq = ng * ZP;
-      if ((nq & 3) == 0 && ((uintptr_t)e0 & 15) == 0 && ((uintptr_t)r0 & 7) == 0) {
-        for (int q = tid; q < nq / 4; q += kMixThreads) {
-          reinterpret_cast<float4 *>(e0)[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-          reinterpret_cast<uint2 *>(r0)[q] = make_uint2(0xFFFFFFFFu, 0xFFFFFFFFu);
-        }
-      } else {
-        for (int q = tid; q < nq; q += kMixThreads) {
-          e0[q] = 0.f;
-          r0[q] = -1;
-        }
-      }
-    }
-    __syncthreads();
-    // (A) each item's logits and tokens, four items' loads in flight: the
-    // logits kept, logit - lse in fixed point, the tokens into their
-    // position's table, the row's largest logit
-    constexpr int UI = 4;
-    for (int it0 = warp; it0 < items; it0 += NW * UI) {
-      float x[UI][2];
-      int t[UI][2];
-#pragma unroll
-      for (int k = 0; k < UI; ++k) {
-        const int item = it0 + k * NW;
-        const int rl = item / KB, j0 = (item - rl * KB) << 6;  // row within the group, block
-        const int d = g0 + rl / Z, z = rl % Z;
-        const size_t g = rb + ((size_t)z * b + d) * K;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int j = j0 + 32 * h + lane;
-          const bool ok = item < items && j < K;
-          x[k][h] = ok ? __ldg(a.topk_logit + g + j) : -INFINITY;
-          t[k][h] = ok ? __ldg(a.topk_tok + g + j) : 0;
-        }
-      }
-#pragma unroll
-      for (int k = 0; k < UI; ++k) {
-        const int item = it0 + k * NW;
-        if (item >= items) break;  // uniform over the warp
-        const int rl = item / KB, j0 = (item - rl * KB) << 6;
-        const int dl = rl / Z, row = g0 * Z + rl;
-        int *hq = hk + dl * H;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int j = j0 + 32 * h + lane;
-          if (j < K) {
-            const int li = rl * K + j;  // = dl ZK + z K + j
-            lg[li] = x[k][h];
-            const int64_t fx = fix_f32(x[k][h]);
-            lq[(size_t)row * K + j] = fx == kNegFix ? kNegFix : fx - flse[row];
-            eu[li] = insert(hq, t[k][h]);
-          }
-        }
-        float mx = fmaxf(x[k][0], x[k][1]);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
-        if (lane == 0) atomicMax(rmx + rl, ord_f32(mx));
-      }
-    }
-    __syncthreads();
-    // (B) one warp per position: its table's used slots -> union indices 0, 1,
-    // ... (lane l owns slots 32 q + l; numbered lane by lane after a warp scan
-    // of the lanes' counts)
-    for (int d = g0 + warp; d < g1; d += NW) {
-      int *h = hk + (d - g0) * H;
-      const int S_ = H >> 5;
-      int cnt = 0;
-      for (int q = 0; q < S_; ++q) cnt += h[32 * q + lane] != kEmptySlot;
-      int incl = cnt;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(kFull, incl, o);
-        if (lane >= o) incl += v;
-      }
-      int u = incl - cnt;
-      for (int q = 0; q < S_; ++q) {
-        const int v = h[32 * q + lane];
-        if (v != kEmptySlot) {
-          utok[d * ZK + u] = v;
-          h[32 * q + lane] = u++;
-        }
-      }
-      if (lane == 31) nu[d] = incl;
-    }
-    __syncthreads();
-    // (C) each entry's union index and E = exp(logit - its row's largest);
-    // the rows' largest logits in fixed point
-    for (int item = warp; item < items; item += NW) {
-      const int rl = item / KB, j0 = (item - rl * KB) << 6;
-      const int dl = rl / Z, z = rl - dl * Z, d = g0 + dl, row = g0 * Z + rl;
-      const int64_t fm = fix_f32(unord_f32(rmx[rl]));
-      if (lane == 0 && j0 == 0) {
-        fmax[row] = fm;
-        mq[row] = fm == kNegFix ? kNegFix : fm - flse[row];
-      }
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int j = j0 + 32 * h + lane;
-        if (j < K) {
-          const int li = rl * K + j;
-          const size_t e = (size_t)row * K + j;
-          int u = hk[dl * H + eu[li]];
-          u = (unsigned)u < (unsigned)ZK ? u : 0;  // (a token equal to INT32_MIN)
-          const int64_t l = lq[e];
-          const float ev = (fm == kNegFix || l == kNegFix) ? 0.f : exp_fix(l + flse[row] - fm);
-          ue[e] = (uint16_t)u;
-          if constexpr (ZP > 0) {
-            const size_t slot = ((size_t)d * ZK + u) * ZP + z;
-            dE[slot] = ev;
-            dR[slot] = (int16_t)j;
-          } else {
-            Ee[e] = ev;
-          }
-        }
-      }
-    }
-    __syncthreads();
-  }
   MixSm s;
   s.flse = flse;
   s.fmax = fmax;
@@ -1106,14 +1147,22 @@ size_t mixture_tree_smem_bytes(int Z, int b, int K, int n_max) {
   return mix_layout(Z, b, K, n_max, mixture_tree_form(Z, b, K, n_max)).bytes;
 }
 
+// Workspace bytes of one request's tables (a multiple of 256).
+size_t mixture_tree_ws_stride(int Z, int b, int K, int n_max) {
+  return (mix_layout(Z, b, K, n_max, mixture_tree_form(Z, b, K, n_max)).r1 + 255) & ~(size_t)255;
+}
+
 int launch_build_tree_mixture(const float *topk_logit, const int32_t *topk_tok, const double *lse,
                               const double *pi, int B, int Z, int b, int K, int n_max,
                               const int32_t *root_token, const int32_t *ctx_len,
                               const float *cost_ms, int cost_per_request, const float *l_ar,
                               int32_t *n_nodes, int32_t *parent, int32_t *depth, int32_t *pos_id,
                               int32_t *token, float *log_rho, float *a_hat, float *speedup,
-                              uint32_t *anc_mask, int32_t *status, cudaStream_t stream) {
+                              uint32_t *anc_mask, void *workspace, int32_t *status,
+                              cudaStream_t stream) {
   MixArgs a;
+  a.ws = static_cast<unsigned char *>(workspace);
+  a.ws_stride = mixture_tree_ws_stride(Z, b, K, n_max);
   a.topk_logit = topk_logit;
   a.topk_tok = topk_tok;
   a.lse = lse;
@@ -1139,8 +1188,26 @@ int launch_build_tree_mixture(const float *topk_logit, const int32_t *topk_tok, 
   a.anc_mask = anc_mask;
   a.status = status;
   const int zp = mixture_tree_form(Z, b, K, n_max);
-  const size_t smem = mix_layout(Z, b, K, n_max, zp).bytes;
+  const MixLayout ml = mix_layout(Z, b, K, n_max, zp);
+  const size_t smem = ml.bytes, stage_smem = stage_layout(Z, K, ml.H).bytes;
   const int slots = tb::tree_slots(n_max);
+  // the staging kernel: one CTA per (position, request)
+  auto stage = [&](auto kern) {
+    if (stage_smem > 48 * 1024 &&
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)stage_smem) !=
+            cudaSuccess)
+      return cudaErrorInvalidValue;
+    return launch_pdl(kern, dim3(b, B), dim3(kMixThreads), stage_smem, stream, a);
+  };
+  const cudaError_t e0 = zp == 1   ? stage(mixture_stage_kernel<1>)
+                         : zp == 2 ? stage(mixture_stage_kernel<2>)
+                         : zp == 4 ? stage(mixture_stage_kernel<4>)
+                         : zp == 8 ? stage(mixture_stage_kernel<8>)
+                                   : stage(mixture_stage_kernel<0>);
+  if (e0 != cudaSuccess) {
+    cudaGetLastError();
+    return BASTION_ERR_LAUNCH;
+  }
   auto go = [&](auto kern) {
     if (smem > 48 * 1024 &&
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)

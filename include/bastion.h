@@ -201,19 +201,28 @@ int bastion_build_tree(const float *topk_logit, const int32_t *topk_tok, const d
  * Outputs:   as bastion_build_tree without rank: n_nodes [B]; parent, depth,
  *            pos_id, token, log_rho, a_hat, speedup [B, n_max];
  *            anc_mask [B, n_max, ceil(n_max/32)].
+ * Workspace: bastion_build_tree_mixture_workspace_bytes(B, Z, b, K, n_max)
+ *            bytes, 256-byte aligned: each request's tables, written by a
+ *            staging launch and read by the build launch (two launches on the
+ *            stream; calls sharing a workspace must not overlap on the GPU).
  * Limits: 1 <= Z <= 32, 1 <= K <= 1024, 1 <= b <= 32, 1 <= n_max <= 256
  * (BASTION_ERR_SIZE otherwise); one request's tables, about
- * 14 b Z K + 16 n_max (Z + 2 + Z K / 32) bytes, must fit in 227 KB of shared
- * memory (BASTION_ERR_UNSUPPORTED otherwise): b = 16 allows Z K up to about
- * 700 at n_max = 128, e.g. Z = 4 with K = 128, or Z = 8 with K = 64.
+ * 18 b Z K + 16 n_max (Z + 2 + Z K / 32) bytes (with Z <= 8 and room, a
+ * faster layout of about b Z K (18 + 6 Zp) bytes, Zp = Z rounded up to 1, 2,
+ * 4 or 8), must fit in 227 KB of shared memory (BASTION_ERR_UNSUPPORTED
+ * otherwise): b = 16 allows Z K up to about 600 at n_max = 128, e.g. Z = 4
+ * with K = 128, or Z = 8 with K = 64.
  */
+size_t bastion_build_tree_mixture_workspace_bytes(int B, int Z, int b, int K, int n_max);
+
 int bastion_build_tree_mixture(const float *topk_logit, const int32_t *topk_tok, const double *lse,
                                const double *pi, int B, int Z, int b, int K, int n_max,
                                const int32_t *root_token, const int32_t *ctx_len,
                                const float *cost_ms, int cost_per_request, const float *l_ar,
                                int32_t *n_nodes, int32_t *parent, int32_t *depth, int32_t *pos_id,
                                int32_t *token, float *log_rho, float *a_hat, float *speedup,
-                               uint32_t *anc_mask, int32_t *status, bastion_stream_t stream);
+                               uint32_t *anc_mask, void *workspace, size_t workspace_bytes,
+                               int32_t *status, bastion_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * Tree-masked GQA attention of the tree's query tokens against the KV cache

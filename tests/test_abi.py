@@ -42,7 +42,7 @@ def _header_arg_counts():
 
 def test_binding_argtypes_match_header(L):
     counts = _header_arg_counts()
-    assert len(counts) == 16
+    assert len(counts) == 17
     for name, n in counts.items():
         assert len(getattr(L, name).argtypes) == n, name
 
@@ -98,7 +98,7 @@ def test_host_checks_reject_before_launch(L):
     base[12], base[5], base[6] = ctypes.c_float(0.1), 24, 8
     assert L.bastion_tree_attention(*base) == -6
     # mixture tree: Z > 32, K > 1024, b > 32, n_max > 256; misaligned pi; null pi
-    mx = [fake] * 4 + [1, 33, 4, 8, 16] + [fake] * 3 + [0, fake] + [fake] * 10 + [None]
+    mx = [fake] * 4 + [1, 33, 4, 8, 16] + [fake] * 3 + [0, fake] + [fake] * 9 + [ws, 1 << 30, fake, None]
     assert L.bastion_build_tree_mixture(*mx) == -2
     mx[5], mx[7] = 2, 1025
     assert L.bastion_build_tree_mixture(*mx) == -2
@@ -110,8 +110,22 @@ def test_host_checks_reject_before_launch(L):
     assert L.bastion_build_tree_mixture(*mx) == -4
     mx[3] = None
     assert L.bastion_build_tree_mixture(*mx) == -1
+    # mixture tree: workspace misaligned, too small, null
+    mx[3] = fake
+    mx[23] = vp(0x100010)
+    assert L.bastion_build_tree_mixture(*mx) == -4
+    mx[23], mx[24] = ws, L.bastion_build_tree_mixture_workspace_bytes(1, 2, 4, 8, 16) - 1
+    assert L.bastion_build_tree_mixture(*mx) == -5
+    mx[23], mx[24] = None, 1 << 30
+    assert L.bastion_build_tree_mixture(*mx) == -1
+    mx[23] = ws
+    # the workspace size: per request, none for sizes out of range
+    one = L.bastion_build_tree_mixture_workspace_bytes(1, 4, 16, 64, 128)
+    assert one > 0 and one % 256 == 0
+    assert L.bastion_build_tree_mixture_workspace_bytes(32, 4, 16, 64, 128) == 32 * one
+    assert L.bastion_build_tree_mixture_workspace_bytes(1, 33, 16, 64, 128) == 0
     # mixture tree: tables larger than shared memory -> unsupported
-    mx[3], mx[5], mx[6], mx[7], mx[8] = fake, 8, 32, 256, 256
+    mx[5], mx[6], mx[7], mx[8] = 8, 32, 256, 256
     assert L.bastion_build_tree_mixture(*mx) == -6
     # verify: B > 4096
     assert L.bastion_verify_greedy(fake, 1, 5000, 4, 8, 8, 4, fake, fake, fake, fake, fake, fake, fake, ws, 1 << 20, fake, None) == -2
@@ -161,7 +175,7 @@ def test_mixture_binding_rejects_wrong_dtypes_and_shapes(L):
     f32 = lambda *s: torch.zeros(*s)  # noqa: E731
     rest = (n_max, i32(B), i32(B), f32(1, n_max + 1), f32(B), i32(B), i32(B, n_max), i32(B, n_max),
             i32(B, n_max), i32(B, n_max), f32(B, n_max), f32(B, n_max), f32(B, n_max),
-            i32(B, n_max, 1), i32(B))
+            i32(B, n_max, 1), torch.zeros(1 << 20, dtype=torch.uint8), i32(B))
     with pytest.raises(bastion.BastionError, match="lse"):
         bastion.bastion_build_tree_mixture(lg, tk, ls.float(), pi, *rest)
     with pytest.raises(bastion.BastionError, match="pi"):

@@ -41,11 +41,13 @@ def _gpu(lg, tk, ls, pi, n_max, roots, ctx, cost, lar):
     out["n_nodes"] = torch.zeros(B, dtype=torch.int32, device=dev())
     out["anc_mask"] = torch.zeros((B, n_max, W), dtype=torch.int32, device=dev())
     st = torch.zeros(B, dtype=torch.int32, device=dev())
+    Z, b, K = lg.shape[1:]
+    ws = bastion.workspace(bastion.bastion_build_tree_mixture_workspace_bytes(B, Z, b, K, n_max), dev())
     bastion.bastion_build_tree_mixture(
         to_dev(lg), to_dev(tk), to_dev(ls), to_dev(np.ascontiguousarray(pi, np.float64)), n_max,
         to_dev(roots), to_dev(ctx), to_dev(np.ascontiguousarray(cost, np.float32)), to_dev(lar),
         out["n_nodes"], out["parent"], out["depth"], out["pos_id"], out["token"], out["log_rho"],
-        out["a_hat"], out["speedup"], out["anc_mask"], st)
+        out["a_hat"], out["speedup"], out["anc_mask"], ws, st)
     torch.cuda.synchronize()
     return {k: host(v) for k, v in out.items()}, host(st)
 
