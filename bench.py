@@ -817,7 +817,7 @@ def run_mixture(args, ws, rank, local, light=True):
             "ms_per_step": ms, "us_per_call": ms * 1e3,
             "roofline": {"bound": "hbm", "kernel": "build_tree_mixture", "achieved": ach, "peak": hbm,
                          "unit": "GB/s", "frac": ach / hbm, "peak_source": f"{peak_kind} copy bandwidth",
-                         "note": "one warp's sequential pops per request: latency-bound, not HBM-bound"},
+                         "note": "sequential pops per request on one SM (four warps): latency-bound, not HBM-bound"},
             "clocks": clk}
 
 

@@ -923,14 +923,15 @@ __global__ void __launch_bounds__(kMixThreads, 1) build_tree_mixture_kernel(MixA
     if (!badw && w > 0.0) P0 = tb::fix_lse(log(w));
   }
   if (__any_sync(kFull, badw) && warp == 0 && lane == 0) atomicOr(&a.status[r], BASTION_STATUS_BAD_WEIGHT);
-  if (warp == 0 && lane == 0) {
+  const int rec = kRun - 1;  // the warp that keeps the tree's records
+  if (warp == rec && lane == 0) {
     s.par[0] = -1;
     s.dep[0] = 0;
     s.tok[0] = a.root_token[r];
     s.lrn[0] = 0;
     s.An[0] = 1.f;
   }
-  if (warp == 0)
+  if (warp == rec)
     for (int q = lane; q < W; q += 32) s.mask[q] = q == 0 ? 1u : 0u;
 
   Pending<S> pend;
@@ -1001,18 +1002,18 @@ __global__ void __launch_bounds__(kMixThreads, 1) build_tree_mixture_kernel(MixA
       const uint32_t sec = 0xFFFFFFFFu - mt;
       const int p = (int)(sec & 0xFFFFu), d = (int)(sec >> 16);
       const float rho = exp_fix(sc);
+      const int u = s.pu[p], t = s.pt[p];
       const float Cp = C[N], Cn = C[N + 1];
       if (rho * Cp < (A_hi + A_lo) * (Cn - Cp)) break;  // S would decrease: keep T_N
       {
         const float y = rho - A_lo;
-        const float t = A_hi + y;
-        A_lo = (t - A_hi) - y;
-        A_hi = t;
+        const float tt = A_hi + y;
+        A_lo = (tt - A_hi) - y;
+        A_hi = tt;
       }
       const int i = N;
       N = i + 1;
-      const int u = s.pu[p], t = s.pt[p];
-      if (warp == 0) {
+      if (warp == kPopWarps - 1) {  // the lightest scanner keeps the tree's records
         if (lane == 0) {
           s.par[i] = p;
           s.dep[i] = d;
@@ -1020,8 +1021,7 @@ __global__ void __launch_bounds__(kMixThreads, 1) build_tree_mixture_kernel(MixA
           s.lrn[i] = sc;
           s.An[i] = A_hi + A_lo;
         }
-        for (int q = lane; q < W; q += 32)
-          s.mask[i * W + q] = s.mask[p * W + q] | (q == (i >> 5) ? (1u << (i & 31)) : 0u);
+        if (lane < W) s.mask[i * W + lane] = s.mask[p * W + lane] | (lane == (i >> 5) ? (1u << (i & 31)) : 0u);
       }
       // the word of the taken child belongs to warp (u / 32) % 4
       if (lane == 0 && ((u >> 5) & (kPopWarps - 1)) == warp) s.taken[p * UW + (u >> 5)] |= 1u << (u & 31);
@@ -1106,7 +1106,7 @@ __global__ void __launch_bounds__(kMixThreads, 1) build_tree_mixture_kernel(MixA
       __syncwarp();  // lane 0's records before the next pop reads them
     }
   }
-  if (warp != 0) return;
+  if (warp != rec) return;
   __syncwarp();
 
   // ---- outputs
