@@ -112,6 +112,15 @@ def _p(t):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _p_rows(t):
+    """Target logits: a device tensor, or a pinned (page-locked) host tensor, which
+    the verify kernels read in place over the host link (only the rows of the
+    tree's nodes cross it)."""
+    if t.is_cuda or (t.device.type == "cpu" and t.is_pinned()):
+        return ctypes.c_void_p(t.data_ptr())
+    raise BastionError("target logits must live on a CUDA device or in pinned host memory")
+
+
 def _s(stream):
     st = stream if stream is not None else torch.cuda.current_stream()
     return ctypes.c_void_p(st.cuda_stream)
@@ -270,10 +279,11 @@ def bastion_verify_greedy_workspace_bytes(B: int, n_max: int, V: int) -> int:
 
 def bastion_verify_greedy(target_logits, b, n_nodes, parent, token, argmax, accept_len,
                           accept_nodes, out_tokens, workspace, status, stream=None):
-    """target_logits [B, n_max, V] (fp32/bf16, last dim contiguous)."""
+    """target_logits [B, n_max, V] (fp32/bf16, last dim contiguous), on the device or in
+    pinned host memory."""
     B, n_max, V = target_logits.shape
     ld = _rows_view(target_logits, 3)
-    rc = lib().bastion_verify_greedy(_p(target_logits), _dtype(target_logits), B, n_max, V, ld, int(b),
+    rc = lib().bastion_verify_greedy(_p_rows(target_logits), _dtype(target_logits), B, n_max, V, ld, int(b),
                                      _p(n_nodes), _p(parent), _p(token), _p(argmax), _p(accept_len),
                                      _p(accept_nodes), _p(out_tokens), _p(workspace),
                                      workspace.numel() * workspace.element_size(), _p(status), _s(stream))
@@ -291,7 +301,7 @@ def bastion_verify_sample(target_logits, b, temperature, uniforms, n_nodes, pare
     ld = _rows_view(target_logits, 3)
     if uniforms.dtype != torch.float64 or not uniforms.is_contiguous():
         raise BastionError("uniforms must be a contiguous float64 tensor")
-    rc = lib().bastion_verify_sample(_p(target_logits), _dtype(target_logits), B, n_max, V, ld, int(b),
+    rc = lib().bastion_verify_sample(_p_rows(target_logits), _dtype(target_logits), B, n_max, V, ld, int(b),
                                      float(temperature), _p(uniforms), _p(n_nodes), _p(parent), _p(token),
                                      _p(sampled), _p(accept_len), _p(accept_nodes), _p(out_tokens),
                                      _p(workspace), workspace.numel() * workspace.element_size(),
@@ -307,7 +317,7 @@ def bastion_verify_greedy_noalloc(target_logits, b, n_nodes, parent, token, argm
     on that array."""
     B, n_max, V = target_logits.shape
     ld = _rows_view(target_logits, 3)
-    rc = lib().bastion_verify_greedy_noalloc(_p(target_logits), _dtype(target_logits), B, n_max, V, ld,
+    rc = lib().bastion_verify_greedy_noalloc(_p_rows(target_logits), _dtype(target_logits), B, n_max, V, ld,
                                              int(b), _p(n_nodes), _p(parent), _p(token), _p(argmax),
                                              _p(accept_len), _p(accept_nodes), _p(out_tokens), _p(status),
                                              _s(stream))

@@ -282,7 +282,11 @@ int bastion_calibrate_cost(const float *sample_n, const float *sample_ms, int n_
  * the current node; the walk ends at the first node without such a child, and
  * that node's greedy token is the bonus token.
  *
- * target_logits [B, n_max, V] at row stride ld_row elements, dtype as given.
+ * target_logits [B, n_max, V] at row stride ld_row elements, dtype as given:
+ *            device memory, or pinned (page-locked) host memory, which the
+ *            sweep reads in place over the host link: only the rows of the
+ *            tree's nodes cross it, and no host-side copy or synchronisation
+ *            is needed between building the tree and verifying it.
  * n_nodes [B], parent/token [B, n_max]: the tree of step 3.
  * Outputs: argmax [B, n_max] (rows >= n_nodes untouched); accept_len [B]
  *          (0..b); accept_nodes [B, b+1] (root 0, then the accepted nodes,

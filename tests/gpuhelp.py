@@ -18,6 +18,13 @@ def to_dev(a: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(a)).to(dev())
 
 
+def to_pinned(a: np.ndarray) -> torch.Tensor:
+    """numpy float32 / uint16 (bf16 bits) -> pinned (page-locked) host tensor."""
+    if a.dtype == np.uint16:
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).pin_memory()
+    return torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+
+
 def host(t: torch.Tensor) -> np.ndarray:
     if t.dtype == torch.bfloat16:
         return t.view(torch.int16).cpu().numpy().view(np.uint16)

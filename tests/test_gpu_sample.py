@@ -13,7 +13,7 @@ import torch
 
 import oracle
 import synth
-from gpuhelp import dev, host, to_dev, workload_inputs
+from gpuhelp import dev, host, to_dev, to_pinned, workload_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -136,6 +136,23 @@ def test_sample_batched_qwen3_vocab(cuda_lib):
     ref = oracle.verify_sample(tgt, w.b, 1.0, u, tr.n_nodes, tr.parent, tr.token)
     flagged = check(g, ref, _as_f64(tgt), 1.0, tr.n_nodes, tr.parent, tr.token, w.b)
     assert flagged <= 8
+
+
+def test_sample_reads_pinned_host_target(cuda_lib):
+    """The batched workload with its target logits in pinned host memory, read in
+    place: the draws and walks of the device-resident call."""
+    w = synth.workload(3)
+    x = synth.drafter_logits(w)
+    tk = oracle.topk_marginals(x, w.K)
+    roots, ctx, cost, lar = workload_inputs(w)
+    tr = oracle.build_tree(tk.logit, tk.tok, tk.lse, w.n_max, roots, ctx, cost, lar)
+    tgt, _ = synth.target_logits(w, tr.n_nodes, tr.depth, tk.tok)
+    u = synth.verify_uniforms(w)
+    g_dev, _ = gpu_sample(tgt, w.b, 1.0, u, tr.n_nodes, tr.parent, tr.token)
+    g_host, st = gpu_sample(tgt, w.b, 1.0, u, tr.n_nodes, tr.parent, tr.token, target_dev=to_pinned(tgt))
+    assert np.all(st == 0)
+    for k in g_dev:
+        assert np.array_equal(g_dev[k], g_host[k]), k
 
 
 def test_sample_low_temperature_is_greedy(cuda_lib):

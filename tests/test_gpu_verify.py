@@ -5,7 +5,7 @@ import pytest
 
 import oracle
 import synth
-from gpuhelp import compare_verify, gpu_verify, host, to_dev, workload_inputs
+from gpuhelp import compare_verify, gpu_verify, host, to_dev, to_pinned, workload_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -82,3 +82,25 @@ def test_verify_deterministic_and_reusable_workspace(cuda_lib):
     b_, _ = gpu_verify(None, w.b, tr.n_nodes, tr.parent, tr.token, target_dev=td)
     for f in ("argmax", "accept_len", "accept_nodes", "out_tokens"):
         assert np.array_equal(host(getattr(a, f)), host(getattr(b_, f)))
+
+
+@pytest.mark.parametrize("cid", [1, 3])
+def test_verify_reads_pinned_host_target(cuda_lib, cid):
+    """Target logits left in pinned host memory: the sweep reads the tree's rows
+    in place over the host link, with the results of the device-resident call."""
+    w = synth.workload(cid)
+    tk, tr = _tree(w)
+    tgt, _ = synth.target_logits(w, tr.n_nodes, tr.depth, tk.tok)
+    g, st = gpu_verify(tgt, w.b, tr.n_nodes, tr.parent, tr.token, target_dev=to_pinned(tgt))
+    assert int(st.abs().sum()) == 0
+    compare_verify(g, oracle.verify_greedy(tgt, w.b, tr.n_nodes, tr.parent, tr.token), tr.n_nodes)
+
+
+def test_verify_rejects_pageable_host_target(cuda_lib):
+    """A pageable host tensor is refused by the binding before the library sees it."""
+    import torch
+    from draft_tree_build_gb300 import bastion
+    tgt = np.zeros((1, 4, 64), np.float32)
+    with pytest.raises(bastion.BastionError, match="pinned"):
+        gpu_verify(tgt, 2, np.array([1], np.int32), np.full((1, 4), -1, np.int32),
+                   np.zeros((1, 4), np.int32), target_dev=torch.from_numpy(tgt))
