@@ -80,12 +80,21 @@ __device__ __forceinline__ bool key_gt(uint32_t ah, uint32_t al, uint32_t at, ui
   return (ah > bh) | ((ah == bh) & ((al > bl) | ((al == bl) & (at > bt))));
 }
 
-// rho = exp(score) from the float pair nearest the fixed-point score.
+// rho = exp(score 2^-40).  x = k ln 2 + f with k the nearest integer to x / ln 2
+// (from an estimate of x within 2^-8, the top 32 bits) and f = score - k ln 2
+// exact in fixed point (|f| < 0.36), then 2^k expf(f) with f rounded to 2^-31:
+// within 2.2 2^-23 (relative) of exact, using 32-bit converts only (a
+// conversion between a 64-bit integer and a float costs ~100 cycles here, and
+// the next pop's stop test waits on this value through A_hat).
+constexpr int64_t kLn2Fix = 762123384786ll;  // ln 2 in 2^-40 units, rounded
 __device__ __forceinline__ float rho_of(int64_t score) {
-  const float hi = __ll2float_rn(score) * kUnfix;
-  const float lo = __ll2float_rn(score - __float2ll_rn(hi * kFix)) * kUnfix;
-  const float e = hi < -104.f ? 0.f : expf(hi);
-  return fmaf(e, lo, e);
+  const int64_t D = score < -(104ll << 40) ? -(104ll << 40) : score;
+  const float xa = (float)(int)(D >> 32) * 0.00390625f;
+  const int k = __float2int_rn(xa * 1.4426950408889634f);
+  const int64_t f = D - (int64_t)k * kLn2Fix;
+  const float ff = (float)(int)(f >> 9) * 4.656612873077393e-10f;
+  const float r = ldexpf(expf(ff), k);
+  return score < -(104ll << 40) ? 0.f : r;
 }
 
 // The largest 96-bit key over the warp.
