@@ -335,6 +335,14 @@ def run_ours(args, ws, rank, local, light=False):
     e2e_ms = max_over_ranks(f0.elapsed_time(f1), ws) / E
     h2d = x_pin.numel() * x_pin.element_size() + int(n_nodes.sum()) * w.V * es
     d2h = out_host.numel() * 4 + acc_host.numel() * 4
+    # the host link's own rate: pinned host-to-device copies of the drafter logits
+    l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    l0.record(stream)
+    for _ in range(5):
+        xin.copy_(x_pin, non_blocking=True)
+    l1.record(stream)
+    torch.cuda.synchronize()
+    link_gbs = 5 * x_pin.numel() * x_pin.element_size() / (l0.elapsed_time(l1) * 1e-3) / 1e9
 
     # the cost model's calibration on the device (1,024 observed samples), timed alone
     cal_n = torch.from_numpy(np.linspace(1, w.n_max, 1024).astype(np.float32)).to(dev)
@@ -378,7 +386,9 @@ def run_ours(args, ws, rank, local, light=False):
         "kernels": kern,
         "clocks": clk,
         "e2e": {"value": aggregate_rate(1, e2e_ms, ws), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h, "h2d_gbs": h2d / (e2e_ms * 1e-3) / 1e9,
+                "link_copy_gbs": link_gbs,
+                "note": "target rows read in place from pinned host memory by the verify sweep"},
         # top-K, tree, verify sweep, (sampled: the draws,) verify finish
         "gpu_launches": (5 if sampled else 4) * args.steps,
     }
