@@ -84,6 +84,8 @@ using tb::kNegFix;
 
 constexpr int kMixThreads = 256;
 constexpr int kPopWarps = 4;  // dense form: the warps that run the pops
+constexpr int kRootSort = 512;  // dense form: the root's children are sorted once when at most this many
+constexpr int64_t kBoundSlack = 1ll << 20;  // 2^-20 in the bounds of lazy entries
 constexpr int kEmptySlot = INT_MIN;
 constexpr int64_t kLn2Fix = 762123384786ll;  // ln 2 in 2^-40 units, rounded
 constexpr int64_t kExpCut = -(104ll << 40);  // exp of less is 0 in fp32
@@ -119,6 +121,8 @@ struct MixLayout {
   size_t ee;                                // region 1, sparse form
   size_t r1;                                // region 1 bytes
   size_t cost, pn, sn, lrn, acc, wz, an, taken, mask, par, dep, tok, pu, pt, part;  // region 2
+  size_t rv, rt, ru, rk, lgn;               // region 2, dense form: the root's sorted children
+  int NR;                                   // their capacity (a power of two, 0: none)
   size_t bytes;                             // the pop kernel's shared memory
   int H;                                    // hash slots per position (staging)
 };
@@ -166,6 +170,17 @@ __host__ __device__ inline MixLayout mix_layout(int Z, int b, int K, int n_max, 
   l.pu = take(copies * n * 4);
   l.pt = take(copies * n * 4);
   l.part = ZP > 0 ? take(2 * 2 * kPopWarps * 16) : 0;
+  int NR = 0;
+  if (ZP > 0) {
+    NR = 32;
+    while ((size_t)NR < ZK && NR < kRootSort) NR <<= 1;
+  }
+  l.NR = NR;
+  l.rv = take((size_t)NR * 4);
+  l.rt = take((size_t)NR * 4);
+  l.ru = take((size_t)NR * 4);
+  l.rk = take((size_t)NR * 8);
+  l.lgn = take(ZP > 0 ? 33 * 8 : 0);
   l.bytes = o;
   l.H = H;
   return l;
@@ -372,6 +387,37 @@ __device__ __forceinline__ void part_pick(const MixSm &s, int lane, int warp, in
   const int bta = bua >= 0 ? uta[bua] : INT_MAX, btb = bub >= 0 ? utb[bub] : INT_MAX;
   pa = warp_pick(bva, bta, bua, anya);
   pb = warp_pick(bvb, btb, bub, nb > warp * 32);
+}
+
+// This warp's part of the pick for node q (row d, taken-bits apply).
+template <int ZP>
+__device__ __forceinline__ Pick part_pick1(const MixSm &s, int lane, int warp, int q, int d,
+                                           const float (&w)[ZP]) {
+  const int n = s.nu[d];
+  const float *E = s.dE + d * s.ZK * ZP;
+  const uint32_t *tk = s.taken + q * s.UW;
+  const int *ut = s.utok + d * s.ZK;
+  float bv = 0.f;
+  int bu = -1;
+  bool any = false;
+#pragma unroll 2
+  for (int c = warp; c * 32 < n; c += kPopWarps) {
+    const int u = c * 32 + lane;
+    float v = 0.f;
+    uint32_t tw = 1u << lane;  // past the row: as if taken
+    if (u < n) {
+      float e[ZP];
+      load_e<ZP>(E + u * ZP, e);
+      tw = tk[c];
+#pragma unroll
+      for (int z = 0; z < ZP; ++z) v = fmaf(w[z], e[z], v);
+    }
+    if (!((tw >> lane) & 1u)) {
+      any = true;
+      lane_track(v, u, ut, bv, bu);
+    }
+  }
+  return warp_pick(bv, bu >= 0 ? ut[bu] : INT_MAX, bu, any);
 }
 
 // A pick as the four warps exchange it.
@@ -609,9 +655,22 @@ __device__ __forceinline__ void pick_sparse2(const MixSm &s, int lane, int qa, i
   }
 }
 
-// The pending candidate of node q (children at depth dchild) from a pick: its
-// key goes to lane q % 32, slot q / 32 (a zero key when there is none); lane 0
-// records its union index and token in this warp's copy.
+// The pending entry of node q (children at depth dchild) goes to lane q % 32,
+// slot q / 32, as a 96-bit key: the order image of its score, then the tie
+// word (bit 31: exact, below it 0x7FFFFFFF - (dchild << 16 | q)), so that among
+// equal scores an exact entry comes before a bound (lazy) one, then lower depth
+// and node.  An exact entry is the node's best untaken child; a lazy one an
+// upper bound on all its children's scores.  A zero key: none.
+__device__ __forceinline__ uint32_t tie_word(int q, int dchild, bool exact) {
+  return (exact ? 0x80000000u : 0u) | (0x7FFFFFFFu - (((uint32_t)dchild << 16) | (uint32_t)q));
+}
+__device__ __forceinline__ void untie(uint32_t mt, int &q, int &dchild, bool &exact) {
+  const uint32_t sec = 0x7FFFFFFFu - (mt & 0x7FFFFFFFu);
+  q = (int)(sec & 0xFFFFu);
+  dchild = (int)(sec >> 16);
+  exact = (mt >> 31) != 0u;
+}
+
 template <int S>
 struct Pending {
   uint32_t kh[S], kl[S], kt[S];  // the 96-bit key
@@ -620,15 +679,14 @@ struct Pending {
 #pragma unroll
     for (int i = 0; i < S; ++i) kh[i] = kl[i] = kt[i] = 0u;
   }
-  __device__ __forceinline__ void set(const MixSm &s, int lane, int q, int dchild, const Pick &p,
-                                      int64_t score) {
-    const bool ok = p.v > 0.f;
+  __device__ __forceinline__ void set_key(int lane, int q, int dchild, bool ok, int64_t score,
+                                          bool exact) {
     uint32_t hi = 0u, lo = 0u, tw = 0u;
     if (ok) {
       const uint64_t k = tb::key_of(score);
       hi = (uint32_t)(k >> 32);
       lo = (uint32_t)k;
-      tw = 0xFFFFFFFFu - (((uint32_t)dchild << 16) | (uint32_t)q);
+      tw = tie_word(q, dchild, exact);
     }
     const int sl = q >> 5;
 #pragma unroll
@@ -638,6 +696,12 @@ struct Pending {
       kl[i] = me ? lo : kl[i];
       kt[i] = me ? tw : kt[i];
     }
+  }
+  // node q's best untaken child from a pick, exact; lane 0 records its union
+  // index and token in this warp's copy
+  __device__ __forceinline__ void set(const MixSm &s, int lane, int q, int dchild, const Pick &p,
+                                      int64_t score) {
+    set_key(lane, q, dchild, p.v > 0.f, score, true);
     if (lane == 0) {
       s.pu[q] = p.u;
       s.pt[q] = p.t;
@@ -940,13 +1004,20 @@ __global__ void __launch_bounds__(kMixThreads, 1) build_tree_mixture_kernel(MixA
   int N = 1;
 
   if constexpr (ZP > 0) {
-    // ==== dense form: four warps, identical decisions, a quarter of each scan
+    // ==== dense form: four warps, identical decisions, a quarter of each scan.
+    // A new node's entry starts as a bound on its children's scores (lazy)
+    // and is scanned only if that bound wins a select; the root's children
+    // are sorted once and taken in order.
     int ph = 0;
+    float *rv = reinterpret_cast<float *>(smem + L.rv);
+    int *rt = reinterpret_cast<int *>(smem + L.rt);
+    int *ru = reinterpret_cast<int *>(smem + L.ru);
+    int64_t *rk = reinterpret_cast<int64_t *>(smem + L.rk);
+    int64_t *lgn = reinterpret_cast<int64_t *>(smem + L.lgn);  // log k, k = 1..32
     // node i's weights (lane z) and scale for its children at row d; false when
     // no child can have a finite score
-    auto setup = [&](int i, int d, int64_t P, float &wl) -> bool {
+    auto weights = [&](int i, int d, int64_t P, float &wl) -> bool {
       wl = 0.f;
-      if (lane < Z) s.Pn[i * Z + lane] = P;
       if (d >= b) return false;
       const int64_t m = s.mq[d * Z + (lane < Z ? lane : 0)];
       const int64_t X = (lane < Z && P > kInfCut && m > kInfCut) ? P + m : kVeryNeg;
@@ -957,52 +1028,138 @@ __global__ void __launch_bounds__(kMixThreads, 1) build_tree_mixture_kernel(MixA
       if (lane == 0) s.Sn[i] = Smax;
       return true;
     };
-    // the pending children of qa (row da) and of the new node qb (row db, its
-    // weights in lanes z: wlb), combined over the warps, and their keys
-    auto scan = [&](int qa, int da, int qb, int db, float wlb, Pick &pa, int64_t &ka, Pick &pb,
-                    int64_t &kb) {
-      float wa[ZP], wb[ZP];
+    // node q's best untaken child (row d, its weights in lanes z: wl), over
+    // the four warps, and its key
+    auto scan = [&](int q, int d, float wl, Pick &pa, int64_t &ka) {
+      float wa[ZP];
 #pragma unroll
-      for (int z = 0; z < ZP; ++z) {
-        wa[z] = z < Z ? s.wz[qa * Z + z] : 0.f;
-        wb[z] = __shfl_sync(kFull, wlb, z);
-      }
-      part_pick<ZP>(s, lane, warp, qa, da, wa, qb, db, wb, pa, pb);
+      for (int z = 0; z < ZP; ++z) wa[z] = __shfl_sync(kFull, wl, z);
+      pa = part_pick1<ZP>(s, lane, warp, q, d, wa);
       Part *pp = part + ph * 2 * kPopWarps;
-      if (lane == 0) {
-        pp[warp] = Part{pa.v, pa.t, pa.u, pa.any ? 1 : 0};
-        pp[kPopWarps + warp] = Part{pb.v, pb.t, pb.u, pb.any ? 1 : 0};
-      }
+      if (lane == 0) pp[warp] = Part{pa.v, pa.t, pa.u, pa.any ? 1 : 0};
       pop_barrier();
       pa = combine(pp);
-      pb = combine(pp + kPopWarps);
       ph ^= 1;
-      int64_t sa = 0, sb = 0;
-      if (pa.v < kTiny && pa.any) pa = slow_dense<ZP>(s, lane, qa, da, sa);
-      if (qb >= 0 && pb.v < kTiny && pb.any) pb = slow_dense<ZP>(s, lane, qb, db, sb);
-      ka = pa.v > 0.f ? s.Sn[qa] + sa + log_fix(pa.v) : 0;
-      kb = (qb >= 0 && pb.v > 0.f) ? s.Sn[qb] + sb + log_fix(pb.v) : 0;
+      int64_t sa = 0;
+      if (pa.v < kTiny && pa.any) pa = slow_dense<ZP>(s, lane, q, d, sa);
+      ka = pa.v > 0.f ? s.Sn[q] + sa + log_fix(pa.v) : 0;
+    };
+    // a new node i at depth d with P_z(i) in lane z: its lazy entry, the bound
+    // S + log(number of finite branches) (every weight is at most 1 and every
+    // E at most 1) plus a margin for rounding; no exponentials
+    auto lazy = [&](int i, int d, int64_t P) {
+      if (lane < Z) s.Pn[i * Z + lane] = P;
+      bool ok = false;
+      int64_t ub = 0;
+      if (d < b) {
+        const int64_t m = s.mq[d * Z + (lane < Z ? lane : 0)];
+        const int64_t X = (lane < Z && P > kInfCut && m > kInfCut) ? P + m : kVeryNeg;
+        const int64_t Smax = warp_max_i64(X);
+        ok = Smax > kInfCut;
+        const int nf = __popc(__ballot_sync(kFull, X > kInfCut));
+        ub = Smax + lgn[nf > 0 ? nf : 1] + kBoundSlack;
+      }
+      pend.set_key(lane, i, d + 1, ok, ub, false);
     };
 
+    // ---- the root: its weights, then its children's values sorted once
+    if (warp == 0) lgn[lane + 1] = log_fix((float)(lane + 1));
     float wl0;
-    if (setup(0, 0, P0, wl0)) {
-      __syncwarp();
-      Pick pa, pb;
-      int64_t ka, kb;
-      scan(0, 0, -1, 0, 0.f, pa, ka, pb, kb);
-      pend.set(s, lane, 0, 1, pa, ka);
-      __syncwarp();
+    if (lane < Z) s.Pn[lane] = P0;
+    const bool root_kids = weights(0, 0, P0, wl0);
+    pop_barrier();  // the log table before any warp reads it
+    const int n0 = root_kids ? nu[0] : 0;
+    bool root_sorted = root_kids && n0 <= L.NR;
+    int rc = 0;  // the next root child in sorted order
+    if (root_sorted) {
+      float wa[ZP];
+#pragma unroll
+      for (int z = 0; z < ZP; ++z) wa[z] = __shfl_sync(kFull, wl0, z);
+      const int NR = L.NR;
+      for (int k = tid; k < NR; k += kPopWarps * 32) {
+        float v = -1.f;  // the padding sorts last
+        int t = INT_MAX;
+        if (k < n0) {
+          float e[ZP];
+          load_e<ZP>(dE + k * ZP, e);
+          v = 0.f;
+#pragma unroll
+          for (int z = 0; z < ZP; ++z) v = fmaf(wa[z], e[z], v);
+          t = utok[k];
+        }
+        rv[k] = v;
+        rt[k] = t;
+        ru[k] = k;
+      }
+      pop_barrier();
+      // bitonic sort by (value desc, token asc); tokens of one row are distinct
+      for (int size = 2; size <= NR; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+          for (int k = tid; k < NR / 2; k += kPopWarps * 32) {
+            const int lo = 2 * k - (k & (stride - 1)), hi = lo + stride;
+            const bool desc = (lo & size) == 0;
+            const float va = rv[lo], vb = rv[hi];
+            const int ta = rt[lo], tb = rt[hi];
+            const bool b_first = vb > va || (vb == va && tb < ta);
+            if (b_first == desc) {
+              rv[lo] = vb;
+              rv[hi] = va;
+              rt[lo] = tb;
+              rt[hi] = ta;
+              const int x = ru[lo];
+              ru[lo] = ru[hi];
+              ru[hi] = x;
+            }
+          }
+          pop_barrier();
+        }
+      }
+      for (int k = tid; k < n0; k += kPopWarps * 32)
+        rk[k] = rv[k] >= kTiny ? s.Sn[0] + log_fix(rv[k]) : 0;
+      pop_barrier();
+      const bool ok = n0 > 0 && rv[0] >= kTiny;
+      if (ok) {
+        pend.set_key(lane, 0, 1, true, rk[0], true);
+      } else if (n0 > 0) {  // the largest child is tiny: the root is scanned as any node
+        root_sorted = false;
+        pend.set_key(lane, 0, 1, true, s.Sn[0] + lgn[Z] + kBoundSlack, false);
+      }
+    } else if (root_kids) {
+      pend.set_key(lane, 0, 1, true, s.Sn[0] + lgn[Z] + kBoundSlack, false);
     }
+    __syncwarp();
+
     while (N < n_max) {
       uint32_t mh, ml, mt;
       pend.best(mh, ml, mt);
       if ((mh | ml | mt) == 0u) break;  // no candidate left
       const int64_t sc = (int64_t)((((uint64_t)mh << 32) | ml) ^ 0x8000000000000000ull);
       if (sc < kInfCut) break;  // the best candidate has rho = 0
-      const uint32_t sec = 0xFFFFFFFFu - mt;
-      const int p = (int)(sec & 0xFFFFu), d = (int)(sec >> 16);
+      int p, d;
+      bool exact;
+      untie(mt, p, d, exact);
+      if (!exact) {
+        // a bound won: node p's best untaken child replaces it, then select again
+        float wl;
+        const int64_t Pp = s.Pn[p * Z + (lane < Z ? lane : 0)];
+        Pick pa;
+        int64_t ka = 0;
+        pa.v = 0.f;
+        pa.t = INT_MAX;
+        pa.u = -1;
+        pa.any = false;
+        if (weights(p, d - 1, lane < Z ? Pp : kNegFix, wl)) {
+          __syncwarp();
+          scan(p, d - 1, wl, pa, ka);
+        }
+        pend.set(s, lane, p, d, pa, ka);
+        if (p == 0) root_sorted = false;
+        __syncwarp();
+        continue;
+      }
       const float rho = exp_fix(sc);
-      const int u = s.pu[p], t = s.pt[p];
+      const bool from_list = p == 0 && root_sorted;
+      const int u = from_list ? ru[rc] : s.pu[p], t = from_list ? rt[rc] : s.pt[p];
       const float Cp = C[N], Cn = C[N + 1];
       if (rho * Cp < (A_hi + A_lo) * (Cn - Cp)) break;  // S would decrease: keep T_N
       {
@@ -1025,14 +1182,24 @@ __global__ void __launch_bounds__(kMixThreads, 1) build_tree_mixture_kernel(MixA
       }
       // the word of the taken child belongs to warp (u / 32) % 4
       if (lane == 0 && ((u >> 5) & (kPopWarps - 1)) == warp) s.taken[p * UW + (u >> 5)] |= 1u << (u & 31);
-      float wl;
-      const bool kids = setup(i, d, child_p_dense<ZP>(s, lane, p, d, u), wl);
-      __syncwarp();
-      Pick pa, pb;
-      int64_t ka, kb;
-      scan(p, d - 1, kids ? i : -1, d, wl, pa, ka, pb, kb);
-      pend.set(s, lane, p, d, pa, ka);
-      if (kids) pend.set(s, lane, i, d + 1, pb, kb);
+      lazy(i, d, child_p_dense<ZP>(s, lane, p, d, u));
+      if (from_list) {  // the root's next child in sorted order
+        ++rc;
+        if (rc < n0 && rv[rc] >= kTiny) {
+          pend.set_key(lane, 0, 1, true, rk[rc], true);
+        } else if (rc < n0) {  // the rest are tiny: a bound (the score just taken), then a scan
+          root_sorted = false;
+          pend.set_key(lane, 0, 1, true, sc, false);
+        } else {
+          pend.set_key(lane, 0, 1, false, 0, true);
+        }
+      } else {  // the parent's next-best child
+        __syncwarp();
+        Pick pa;
+        int64_t ka;
+        scan(p, d - 1, lane < Z ? s.wz[p * Z + lane] : 0.f, pa, ka);
+        pend.set(s, lane, p, d, pa, ka);
+      }
       __syncwarp();  // lane 0's records before the next pop reads them
     }
   } else {
@@ -1073,8 +1240,9 @@ __global__ void __launch_bounds__(kMixThreads, 1) build_tree_mixture_kernel(MixA
       if ((mh | ml | mt) == 0u) break;
       const int64_t sc = (int64_t)((((uint64_t)mh << 32) | ml) ^ 0x8000000000000000ull);
       if (sc < kInfCut) break;
-      const uint32_t sec = 0xFFFFFFFFu - mt;
-      const int p = (int)(sec & 0xFFFFu), d = (int)(sec >> 16);
+      int p, d;
+      bool exact;
+      untie(mt, p, d, exact);
       const float rho = exp_fix(sc);
       const float Cp = C[N], Cn = C[N + 1];
       if (rho * Cp < (A_hi + A_lo) * (Cn - Cp)) break;
