@@ -8,12 +8,12 @@
 //
 // Design (HBM-bound sweep over sum_r n_nodes[r] rows of V logits), two kernels
 // chained with programmatic dependent launch:
-//  * sweep: persistent grid sized from the occupancy; every warp works on its
-//    own contiguous run of items with no barrier and no waiting on other
-//    warps.  An item is one
-//    4 KB segment of one tree row (row counts are read on the device, so only
-//    rows < n_nodes[r] are read).  A lane issues its 8 x 16-byte non-allocating
-//    loads at once, keeps the running max (NaN-propagating packed bf16x2 max)
+//  * sweep: persistent grid sized from the occupancy; the items are dealt to
+//    the warps round robin (grid-stride), with no barrier and no waiting on
+//    other warps.  An item is one 4 KB segment of one tree row (row counts
+//    are read on the device, so only rows < n_nodes[r] are read).  A lane
+//    issues its 8 x 16-byte non-allocating loads at once, keeps the running
+//    max (NaN-propagating packed bf16x2 max)
 //    and the first vector that reached it, then finds the lowest token holding
 //    the max in that vector from the registers it already holds.  The segment
 //    winner (value desc, token asc as one 64-bit key, two redux.sync
@@ -165,30 +165,20 @@ __global__ void __launch_bounds__(kVT) verify_kernel(VerifyArgs a) {
   }
   const int total = prefix[a.B];
   const int gw = blockIdx.x * kWarps + warp, nw = gridDim.x * kWarps;
-  // each warp takes a contiguous run of items; its position (request r, row
-  // i, segment sg) is found once and then stepped
-  const int per = (total + nw - 1) / nw;
-  const int it0 = min(total, gw * per), it1 = min(total, it0 + per);
-  int r = 0, i = 0, sg = 0;
-  if (it0 < it1) {
+  // items are dealt to the warps round robin, so that at any moment the grid
+  // reads one contiguous window of the live rows (a contiguous run per warp
+  // scattered the reads over the whole batch and ran ~2% slower)
+  for (int item = gw; item < total; item += nw) {
+    // the item's request (binary search of the prefix), row and segment
     int lo = 0, hi = a.B;
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
-      if (prefix[mid] <= it0) lo = mid; else hi = mid;
+      if (prefix[mid] <= item) lo = mid; else hi = mid;
     }
-    r = lo;
-    const int off = it0 - prefix[r];
-    i = off / a.nseg;
-    sg = off - i * a.nseg;
-  }
-  for (int item = it0; item < it1; ++item) {
-    if (item > it0 && ++sg == a.nseg) {
-      sg = 0;
-      if (++i * a.nseg >= prefix[r + 1] - prefix[r]) {  // next request with items
-        i = 0;
-        do { ++r; } while (prefix[r + 1] == prefix[r]);
-      }
-    }
+    const int r = lo;
+    const int off = item - prefix[r];
+    const int i = off / a.nseg;
+    const int sg = off - i * a.nseg;
     const int e0 = sg * a.SEG;
     const int n = min(a.V - e0, a.SEG);
     const unsigned char *g0 = a.logits + (((size_t)r * a.n_max + i) * (size_t)a.ld + e0) * ES;

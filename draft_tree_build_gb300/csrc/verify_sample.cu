@@ -10,8 +10,8 @@
 // exceeds u times the row's total; the greedy walk then runs over the draws.
 //
 // Design (HBM-bound: one read of every live row, then one 4 KB item per row):
-//  * sweep: persistent warps take contiguous runs of 4 KB items of the live
-//    rows (as the greedy sweep).  Per item a lane sums 2^(l log2(e)/T - c) over
+//  * sweep: persistent warps take the 4 KB items of the live rows round robin
+//    (as the greedy sweep).  Per item a lane sums 2^(l log2(e)/T - c) over
 //    its elements with c = floor(m log2(e)/T) of its max m, so every exponent
 //    is below ~1; the warp scales the lanes' sums to the item's largest c by
 //    exact powers of two and adds them in two-float arithmetic.  The item's
@@ -223,29 +223,18 @@ __global__ void __launch_bounds__(kST, 4) sample_sweep_kernel(SampleArgs a) {
   request_prefix(a.n_nodes, a.B, a.n_max, a.nseg, prefix, s_tot);
   const int total = prefix[a.B];
   const int gw = blockIdx.x * kSW + (threadIdx.x >> 5), nw = gridDim.x * kSW;
-  const int per = (total + nw - 1) / nw;
-  const int it0 = min(total, gw * per), it1 = min(total, it0 + per);
-  if (it0 >= it1) return;
-  int r, i, sg;
-  {
+  // items dealt to the warps round robin: the grid reads one contiguous window
+  for (int item = gw; item < total; item += nw) {
+    // the item's request (binary search of the prefix), row and segment
     int lo = 0, hi = a.B;
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
-      if (prefix[mid] <= it0) lo = mid; else hi = mid;
+      if (prefix[mid] <= item) lo = mid; else hi = mid;
     }
-    r = lo;
-    const int off = it0 - prefix[r];
-    i = off / a.nseg;
-    sg = off - i * a.nseg;
-  }
-  for (int item = it0; item < it1; ++item) {
-    if (item > it0 && ++sg == a.nseg) {
-      sg = 0;
-      if (++i * a.nseg >= prefix[r + 1] - prefix[r]) {
-        i = 0;
-        do { ++r; } while (prefix[r + 1] == prefix[r]);
-      }
-    }
+    const int r = lo;
+    const int off = item - prefix[r];
+    const int i = off / a.nseg;
+    const int sg = off - i * a.nseg;
     const Item t = item_of<ES>(a, r, i, sg);
     uint4 x[kSV];
 #pragma unroll
