@@ -1,8 +1,8 @@
 // Steps 2-3 of the draft-tree path: best-first prefix-tree expansion under the
 // online budget controller, and the emitted tree arrays, as a kernel of its
 // own (one CTA per request) after the top-K step.  The build itself (scores,
-// frontier, stop test, outputs) is the device code of tree_build.cuh, shared
-// with the fused top-K + tree kernel; see there for the design.
+// frontier, stop test, outputs) is the device code of tree_build.cuh; see
+// there for the design.
 //
 // Bastion (gist.science/nl/paper/2605.29727), Methodologie §1-§3.
 #include "tree_build.cuh"
