@@ -61,6 +61,32 @@ def test_verify_f32_and_status(cuda_lib):
     assert host(g.accept_len)[2] == 0 and np.all(host(g.out_tokens)[2] == -1)
 
 
+def test_verify_requests_without_rows_between_others(cuda_lib):
+    """Requests whose tree size is out of range read no rows and get empty
+    results; the items of the others (found by searching the per-request
+    item counts) are still every row of theirs, bit-exact."""
+    from draft_tree_build_gb300 import bastion
+    B, n_max, V, b = 6, 8, 5000, 3
+    rng = np.random.default_rng(11)
+    tgt = synth.f32_to_bf16_bits(rng.normal(size=(B, n_max, V)).astype(np.float32))
+    n_nodes = np.array([0, 5, -1, 0, 8, n_max + 1], np.int32)
+    parent = np.tile(np.array([-1, 0, 0, 1, 1, 2, 2, 3], np.int32), (B, 1))
+    token = rng.integers(0, V, size=(B, n_max)).astype(np.int32)
+    g, st = gpu_verify(tgt, b, n_nodes, parent, token)
+    s = host(st)
+    ok = (n_nodes >= 1) & (n_nodes <= n_max)
+    assert np.all((s[~ok] & bastion.STATUS_BAD_TREE) != 0) and np.all(s[ok] == 0)
+    am, al, an, ot = host(g.argmax), host(g.accept_len), host(g.accept_nodes), host(g.out_tokens)
+    for r in np.flatnonzero(ok):
+        ref = oracle.verify_greedy(tgt[r:r + 1], b, n_nodes[r:r + 1], parent[r:r + 1], token[r:r + 1])
+        n = int(n_nodes[r])
+        assert np.array_equal(am[r, :n], ref.argmax[0, :n]), r
+        assert al[r] == ref.accept_len[0] and np.array_equal(an[r], ref.accept_nodes[0])
+        assert np.array_equal(ot[r], ref.out_tokens[0])
+    for r in np.flatnonzero(~ok):
+        assert al[r] == 0 and np.all(an[r] == -1) and np.all(ot[r] == -1)
+
+
 def test_verify_full_agreement_chain(cuda_lib):
     w = synth.workload(2)
     tk, tr = _tree(w)
