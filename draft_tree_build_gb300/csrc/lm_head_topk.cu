@@ -29,13 +29,17 @@
 //    (value desc, token asc, one 64-bit integer) beats the root of the row's
 //    4-ary min-heap of the K best keys seen (in shared memory, one column of
 //    heap slots per thread; the first K keys are stored as they come and the
-//    heap is built once).  After every tile each share publishes its J-th best key
-//    (J = ceil(K / CPM)) and reads the others': at least K keys of the row lie
-//    at or above the smallest of them, so a key below it cannot be among the
-//    row's K best and is not inserted (without this bound nearly every
-//    column of the first tiles made some thread of a warp sift its heap).  The
-//    heap then holds every key of the share that can be among the row's K
-//    best;
+//    heap is built once) and above the row's bound.  Each share keeps its 4
+//    best keys exactly and publishes the 4th; the bound is the m-th largest
+//    published value, m = ceil(K / 4): m shares hold 4 keys each at or above
+//    it, so a key below it cannot be among the row's K best and is not
+//    inserted.  The first tile is read twice from TMEM: first for the 4 best,
+//    the max and the sum, then, once m shares have published (a bounded wait
+//    of at most ~20 us, while the MMAs fill the other accumulator), for the
+//    heap; the bound is read again after the next tiles.  (Filling the heap
+//    before a bound existed inserted about half of the first tile's columns
+//    and most of the epilogue's time went to heap sifts.)  The heap then holds
+//    every key of the share that can be among the row's K best;
 //  * a merge kernel takes, per row, the CPM heaps (radix selection of the K-th
 //    best key over them, then ranking by counting) and the CPM (max, c, sum)
 //    shares (exact powers of two again), and writes the K best logits, tokens,
@@ -72,7 +76,7 @@ struct LmArgs {
   int CL;  // CTAs of a cluster: M-tiles that share each W tile, loaded once and multicast
   uint64_t *part_keys;  // [rows][CPM][K]
   float4 *part_stat;    // [rows][CPM]: max, c, sum (hi, lo)
-  uint64_t *pub;        // [rows][CPS]: each share's J-th best key so far (0: none yet);
+  uint64_t *pub;        // [rows][CPS]: each share's J-th (4th) best key so far (0: none yet);
                         // CPS = CPM rounded up to even, so each row's slots are 16-byte aligned
   int32_t *status;
 };
@@ -422,157 +426,204 @@ __global__ void __launch_bounds__(kLT, 1)
     const uint32_t hb = smem_u32(heap) + (uint32_t)rl * 8u;  // this thread's heap column
     int filled = 0;  // keys stored before the heap is built (the first K)
     // the J best keys of this share so far (J <= 4; 0 where fewer were seen),
-    // and lb: the smallest J-th best over the row's shares, as last read
+    // and lb: a lower bound on the row's K-th best key, as last read
     uint64_t top[4] = {0ull, 0ull, 0ull, 0ull};
     uint64_t lb = 0ull;
     const int J = a.J;
     uint64_t *pub_row = a.pub + (size_t)(live ? row : 0) * (size_t)((a.CPM + 1) & ~1);
-    // Publishes this share's J-th best and reads the row's bound: at least
-    // J * CPM >= K keys of the row are >= the smallest published J-th best, so
-    // no key below it is among the row's K best (stale or missing values only
-    // lower the bound).  The row's slots are read as 16-byte words, all loads
-    // issued first.
-    auto exchange = [&]() {
-      if (J == 0) return;
-      const uint64_t tj = J == 1 ? top[0] : J == 2 ? top[1] : J == 3 ? top[2] : top[3];
-      __stcg(reinterpret_cast<unsigned long long *>(pub_row + j0), (unsigned long long)tj);
-      uint64_t m2 = ~0ull;
+    // The row's bound from the shares' published J-th best keys: if m =
+    // ceil(K / J) shares have a J-th best >= x, at least K keys of the row are
+    // >= x, so no key below x is among the row's K best.  x = the m-th largest
+    // published value (m <= 16 with J = 4 and K <= 64); a share that has not
+    // published yet reads as 0, so the bound exists once m shares have
+    // published.  The row's slots are read as 16-byte words, all loads issued
+    // first.
+    const int mJ = J > 0 ? (K + J - 1) / J : 1;
+    // The selection runs on the keys' value words (32-bit min / max): the
+    // bound is the m-th largest value with the lowest tie bits, at most the
+    // m-th largest key, so still valid.
+    auto read_bound = [&]() -> uint64_t {
+      uint32_t big[16];  // the largest published values, descending
+#pragma unroll
+      for (int i = 0; i < 16; ++i) big[i] = 0u;
       const ulonglong2 *pr = reinterpret_cast<const ulonglong2 *>(pub_row);
 #pragma unroll 1
       for (int q0 = 0; q0 < a.CPM; q0 += 32) {
         ulonglong2 w[16];
 #pragma unroll
         for (int u = 0; u < 16; ++u)
-          w[u] = q0 + 2 * u < a.CPM ? __ldcg(pr + q0 / 2 + u) : make_ulonglong2(~0ull, ~0ull);
+          w[u] = q0 + 2 * u < a.CPM ? __ldcg(pr + q0 / 2 + u) : make_ulonglong2(0ull, 0ull);
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const uint64_t x0 = w[u].x, x1 = q0 + 2 * u + 1 < a.CPM ? w[u].y : ~0ull;
-          m2 = x0 < m2 ? x0 : m2;
-          m2 = x1 < m2 ? x1 : m2;
+        for (int u = 0; u < 32; ++u) {
+          const uint32_t x = (u & 1) ? (q0 + u < a.CPM ? (uint32_t)(w[u >> 1].y >> 32) : 0u)
+                                     : (uint32_t)(w[u >> 1].x >> 32);
+#pragma unroll
+          for (int i = 15; i > 0; --i) big[i] = max(big[i], min(big[i - 1], x));
+          big[0] = max(big[0], x);
         }
       }
-      lb = m2 > lb ? m2 : lb;
+      uint32_t r = big[0];
+#pragma unroll
+      for (int i = 1; i < 16; ++i) r = i == mJ - 1 ? big[i] : r;
+      return (uint64_t)r << 32;
+    };
+    auto publish = [&]() {
+      const uint64_t tj = J == 1 ? top[0] : J == 2 ? top[1] : J == 3 ? top[2] : top[3];
+      __stcg(reinterpret_cast<unsigned long long *>(pub_row + j0), (unsigned long long)tj);
     };
     for (int t = 0; t < ntile; ++t) {
       const int buf = t & 1;
       if (!__all_sync(kFull, wait_bar(&bs.acc_full[buf], (uint32_t)(t >> 1) & 1u, abort, st0))) break;
       tc_fence_after();
       const int n = j0 + t * a.CPM;
-      // chunk cc + 1 is loaded from TMEM while chunk cc is processed
-      uint32_t ra[32], rb[32];
       const uint32_t tbase = lane_base + (uint32_t)buf * kBN;
-      tmem_ld32_issue(tbase, ra);
-      tmem_wait_tied(ra);
-      for (int cc = 0; cc < kBN / 32; ++cc) {
-        if (cc + 1 < kBN / 32) tmem_ld32_issue(tbase + (uint32_t)(cc + 1) * 32u, rb);
-        float v[32];
+      // The first tile runs twice over its accumulator: first the share's J
+      // best and the row's max and sum only, then (once the other shares have
+      // published theirs: the bound) the heap.  Filling the heap before any
+      // bound existed inserted most of the first tile's columns.
+      const bool split = t == 0 && J > 0;
+      for (int ph = 0; ph < (split ? 2 : 1); ++ph) {
+        const bool sums = ph == 0, track = !split || ph == 0, heap_on = !split || ph == 1;
+        // chunk cc + 1 is loaded from TMEM while chunk cc is processed
+        uint32_t ra[32], rb[32];
+        tmem_ld32_issue(tbase, ra);
+        tmem_wait_tied(ra);
+        for (int cc = 0; cc < kBN / 32; ++cc) {
+          if (cc + 1 < kBN / 32) tmem_ld32_issue(tbase + (uint32_t)(cc + 1) * 32u, rb);
+          float v[32];
 #pragma unroll
-        for (int q = 0; q < 32; ++q) v[q] = __uint_as_float(ra[q]);
-        const int col0 = n * kBN + cc * 32;
-        const int nv = min(32, a.V - col0);  // columns past the vocabulary are zero fill
-        if (live && nv > 0) {
-          // the chunk's max (NaN ignored: a NaN or +inf logit shows in the
-          // sum or the max, checked once at the end)
-          float cm;
-          if (nv == 32) {
-            float m3[11];
-#pragma unroll
-            for (int q = 0; q < 10; ++q) m3[q] = max3(v[3 * q], v[3 * q + 1], v[3 * q + 2]);
-            m3[10] = fmaxf(v[30], v[31]);
-            cm = max3(max3(m3[0], m3[1], m3[2]), max3(m3[3], m3[4], m3[5]), max3(m3[6], m3[7], m3[8]));
-            cm = max3(cm, m3[9], m3[10]);
-          } else {
-            cm = -INFINITY;
-#pragma unroll
-            for (int q = 0; q < 32; ++q)
-              if (q < nv) cm = fmaxf(cm, v[q]);
-          }
-          m = fmaxf(m, cm);
-          if (m > -INFINITY && m < INFINITY) {
-            const float cn = floorf(m * kL2e);
-            if (cn > c) {  // exact rescale of the running sum by 2^(c - cn)
-              const float f = c > kCNone ? pow2_int(c - cn) : 0.f;
-              hi *= f;
-              lo *= f;
-              c = cn;
-            }
-            float s0 = 0.f, s1 = 0.f;
+          for (int q = 0; q < 32; ++q) v[q] = __uint_as_float(ra[q]);
+          const int col0 = n * kBN + cc * 32;
+          const int nv = min(32, a.V - col0);  // columns past the vocabulary are zero fill
+          if (live && nv > 0) {
+            // the chunk's max (NaN ignored: a NaN or +inf logit shows in the
+            // sum or the max, checked once at the end)
+            float cm;
             if (nv == 32) {
+              float m3[11];
 #pragma unroll
-              for (int q = 0; q < 32; q += 4) exp4_acc(v[q], v[q + 1], v[q + 2], v[q + 3], kL2e, -c, s0, s1);
+              for (int q = 0; q < 10; ++q) m3[q] = max3(v[3 * q], v[3 * q + 1], v[3 * q + 2]);
+              m3[10] = fmaxf(v[30], v[31]);
+              cm = max3(max3(m3[0], m3[1], m3[2]), max3(m3[3], m3[4], m3[5]), max3(m3[6], m3[7], m3[8]));
+              cm = max3(cm, m3[9], m3[10]);
             } else {
+              cm = -INFINITY;
 #pragma unroll
               for (int q = 0; q < 32; ++q)
-                if (q < nv) s0 += ex2(fmaf(v[q], kL2e, -c));
+                if (q < nv) cm = fmaxf(cm, v[q]);
             }
-            const float2 ts = two_sum(hi, s0 + s1);
-            hi = ts.x;
-            lo += ts.y;
-          }
-          // The columns that can matter: a key above both the heap's root
-          // (the K-th best of the share so far; nothing while the heap
-          // fills) and the row's bound.  Such a key may also enter the
-          // share's J best (the J-th best is at least both), so one pass over
-          // the chunk's passing columns does all the bookkeeping.  The chunk
-          // is copied to the thread's local memory only when a column passes,
-          // and the passing columns are handled in one small loop (a loop
-          // unrolled over the 32 columns with the heap code inlined in each
-          // copy ran several times slower).
-          const float thr = fmaxf(filled < K || root == 0ull ? -INFINITY : key_value(root),
-                                  lb == 0ull ? -INFINITY : key_value(lb));
-          uint32_t pass = 0u;
-          float stg[32];  // the chunk, copied (to the thread's local memory) only when a column passes
-          if (cm >= thr) {
-#pragma unroll
-            for (int q = 0; q < 32; ++q) pass |= (q < nv && v[q] >= thr ? 1u : 0u) << q;
-            if (pass) {
-#pragma unroll
-              for (int q = 0; q < 32; ++q) stg[q] = v[q];
-            }
-          }
-#pragma unroll 1
-          while (pass) {
-            const int q = __ffs(pass) - 1;
-            pass &= pass - 1u;
-            const uint64_t key = make_key(stg[q], (uint32_t)(col0 + q));
-            if (key <= lb) continue;
-            // the share's J best
-            if (J > 0) {
-              uint64_t x = key;
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-                if (i < J && x > top[i]) {
-                  const uint64_t t = top[i];
-                  top[i] = x;
-                  x = t;
+            if (sums) {
+              m = fmaxf(m, cm);
+              if (m > -INFINITY && m < INFINITY) {
+                const float cn = floorf(m * kL2e);
+                if (cn > c) {  // exact rescale of the running sum by 2^(c - cn)
+                  const float f = c > kCNone ? pow2_int(c - cn) : 0.f;
+                  hi *= f;
+                  lo *= f;
+                  c = cn;
                 }
+                float s0 = 0.f, s1 = 0.f;
+                if (nv == 32) {
+#pragma unroll
+                  for (int q = 0; q < 32; q += 4) exp4_acc(v[q], v[q + 1], v[q + 2], v[q + 3], kL2e, -c, s0, s1);
+                } else {
+#pragma unroll
+                  for (int q = 0; q < 32; ++q)
+                    if (q < nv) s0 += ex2(fmaf(v[q], kL2e, -c));
+                }
+                const float2 ts = two_sum(hi, s0 + s1);
+                hi = ts.x;
+                lo += ts.y;
+              }
             }
-            if (filled < K) {
-              hp_st(hb + (uint32_t)filled * (kBM * 8), key);
-              if (++filled == K) {
-                heap_build(hb, K);
+            // The columns that can matter: for the heap, a key above both
+            // the heap's root (the K-th best of the share so far; nothing
+            // while the heap fills) and the row's bound; for the share's J
+            // best (not in the first tile's second pass), a key above its J-th
+            // best.  One pass over the chunk's passing columns does both.
+            // The chunk is copied to the thread's local memory only when a
+            // column passes, and the passing columns are handled in one small
+            // loop (a loop unrolled over the 32 columns with the heap code
+            // inlined in each copy ran several times slower).
+            // The share's J best are kept exactly (every key above its J-th
+            // best), so the published values keep rising with the bound.
+            const uint64_t tj = J == 1 ? top[0] : J == 2 ? top[1] : J == 3 ? top[2] : top[3];
+            const float thr_h = heap_on ? fmaxf(filled < K || root == 0ull ? -INFINITY : key_value(root),
+                                                lb == 0ull ? -INFINITY : key_value(lb))
+                                        : INFINITY;
+            const float thr_t = track && J > 0 ? (tj == 0ull ? -INFINITY : key_value(tj)) : INFINITY;
+            const float thr = fminf(thr_h, thr_t);
+            uint32_t pass = 0u;
+            float stg[32];  // the chunk, copied (to the thread's local memory) only when a column passes
+            if (cm >= thr) {
+#pragma unroll
+              for (int q = 0; q < 32; ++q) pass |= (q < nv && v[q] >= thr ? 1u : 0u) << q;
+              if (pass) {
+#pragma unroll
+                for (int q = 0; q < 32; ++q) stg[q] = v[q];
+              }
+            }
+#pragma unroll 1
+            while (pass) {
+              const int q = __ffs(pass) - 1;
+              pass &= pass - 1u;
+              const uint64_t key = make_key(stg[q], (uint32_t)(col0 + q));
+              if (track && J > 0) {  // the share's J best
+                uint64_t x = key;
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                  if (i < J && x > top[i]) {
+                    const uint64_t y = top[i];
+                    top[i] = x;
+                    x = y;
+                  }
+              }
+              if (!heap_on || key < lb) continue;  // lb itself is a key of the row: kept
+              if (filled < K) {
+                hp_st(hb + (uint32_t)filled * (kBM * 8), key);
+                if (++filled == K) {
+                  heap_build(hb, K);
+                  root = hp_ld(hb);
+                }
+              } else if (key > root) {
+                heap_sift(hb, K, 0, key);
                 root = hp_ld(hb);
               }
-            } else if (key > root) {
-              heap_sift(hb, K, 0, key);
-              root = hp_ld(hb);
             }
           }
-        }
-        // the first tile: the bound as soon as two chunks are in (the other
-        // shares are at about the same point), so that the rest of the first
-        // tile already skips most columns
-        if (t == 0 && cc == 1 && live) exchange();
-        if (cc + 1 < kBN / 32) {
-          tmem_wait_tied(rb);
+          if (cc + 1 < kBN / 32) {
+            tmem_wait_tied(rb);
 #pragma unroll
-          for (int q = 0; q < 32; ++q) ra[q] = rb[q];
+            for (int q = 0; q < 32; ++q) ra[q] = rb[q];
+          }
+        }
+        if (split && ph == 0 && live) {
+          // publish the first tile's J best, then read the bound; the other
+          // shares finish their first tile at about the same time, so wait
+          // (at most ~20 us, while the MMAs fill the other accumulator) until
+          // m of them have published
+          publish();
+          const uint64_t t_end = global_ns() + 20000ull;
+          for (;;) {
+            const uint64_t x = read_bound();
+            if (x != 0ull || global_ns() > t_end) {
+              lb = x > lb ? x : lb;
+              break;
+            }
+            __nanosleep(256);
+          }
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bs.acc_empty[buf]);
-      if (live) exchange();
+      // later tiles: publish and read the bound after each of the first four
+      // tiles, then after every fourth (it moves little once it is high)
+      if (live && J > 0 && t > 0 && (t < 4 || (t & 3) == 3)) {
+        publish();
+        const uint64_t x = read_bound();
+        lb = x > lb ? x : lb;
+      }
     }
     bad = m == INFINITY || !(hi == hi) || !(lo == lo) || hi == INFINITY;
     if (live) {  // this CTA's share of the row: its K best keys and (max, c, sum)
@@ -849,10 +900,9 @@ int launch_lm_head(const void *hidden, const void *weight, int B, int b, int H, 
   a.part_keys = reinterpret_cast<uint64_t *>(w);
   a.part_stat = reinterpret_cast<float4 *>(w + keys);
   a.pub = reinterpret_cast<uint64_t *>(w + keys + stat);
-  // J = ceil(K / CPM) keys per share reach K over the row's shares; the bound
-  // is kept for J <= 4 (registers per row)
-  a.J = (K + p.CPM - 1) / p.CPM;
-  if (a.J > 4) a.J = 0;
+  // each share publishes its J = 4th best key: the row's bound needs m =
+  // ceil(K / 4) <= 16 shares (K <= 64); none where K > 4 CPM (m > CPM)
+  a.J = (K + 3) / 4 <= p.CPM ? 4 : 0;
   a.status = status;
   cudaError_t e = cudaFuncSetAttribute(lm_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
   if (e == cudaSuccess) {
