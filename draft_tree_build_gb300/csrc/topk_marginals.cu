@@ -676,7 +676,8 @@ __global__ void __launch_bounds__(kT) topk_exact_kernel(TopkArgs a) {
 // --------------------------------------------------------------------------- stream path
 // Many rows (at least two per SM): one CTA per row, all resident at once.  The
 // row streams through a ring of kRing shared-memory stages filled by bulk
-// copies; the warp that frees a stage last refills it.  Per stage a thread
+// copies (with an L2 evict-first policy: the row is read once); the warp that
+// frees a stage last refills it.  Per stage a thread
 // reads its kSV vectors into registers, frees the stage, and then
 //  * keeps the stage's max (a 16-bit order-key prefix) in shared memory;
 //  * adds 2^(l log2(e) - c) over its elements, where c is an integer kept at
@@ -841,6 +842,8 @@ __global__ void __launch_bounds__(kT, 4) topk_stream_kernel(TopkArgs a) {
   uint16_t *smax = reinterpret_cast<uint16_t *>(smem + L.smax);    // [nst][kT] stage maxima
   unsigned char *ring = smem + L.ring;  // [kRing][kStageBytes]; later the row list
   const unsigned char *gbody = reinterpret_cast<const unsigned char *>(s.ga0);
+  // the row is read once: its lines leave L2 first (37.9 against 38.3 us back to back)
+  const uint64_t pol = l2_evict_first_policy();
 
   if (tid == 0) {
     for (int i = 0; i < kRing; ++i) {
@@ -858,7 +861,7 @@ __global__ void __launch_bounds__(kT, 4) topk_stream_kernel(TopkArgs a) {
     for (int st = 0; st < nst && st < kRing; ++st) {
       const uint32_t bytes = (uint32_t)min(kStageBytes, s.body - st * kStageBytes);
       mbar_arrive_expect_tx(&full[st], bytes);
-      bulk_g2s(ring + st * kStageBytes, gbody + (size_t)st * kStageBytes, bytes, &full[st]);
+      bulk_g2s_hint(ring + st * kStageBytes, gbody + (size_t)st * kStageBytes, bytes, &full[st], pol);
     }
   // the unaligned head and tail of the row, one element per thread
   const int nscal = s.nh + (s.n - s.t0);
@@ -903,7 +906,7 @@ __global__ void __launch_bounds__(kT, 4) topk_stream_kernel(TopkArgs a) {
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           const uint32_t bytes = (uint32_t)min(kStageBytes, s.body - nx * kStageBytes);
           mbar_arrive_expect_tx(&full[slot], bytes);
-          bulk_g2s(ring + slot * kStageBytes, gbody + (size_t)nx * kStageBytes, bytes, &full[slot]);
+          bulk_g2s_hint(ring + slot * kStageBytes, gbody + (size_t)nx * kStageBytes, bytes, &full[slot], pol);
         }
       }
     }
