@@ -145,6 +145,16 @@ __device__ __forceinline__ bool stage_request(const TreeArgs &a, int r, const Tr
                                               int nt) {
   const int R = a.R, b = a.b;
   const int nlg = b * R;
+  // the cost row's loads are issued first and used last, so they travel with
+  // the tables' (the cost table is never written by this grid)
+  const float *cr = a.cost + (a.cost_per_request ? (size_t)r * (a.n_max + 1) : 0);
+  constexpr int kCv = 3;
+  float cv[kCv];
+#pragma unroll
+  for (int k = 0; k < kCv; ++k) {
+    const int i = tid + k * nt;
+    cv[k] = i <= a.n_max ? __ldg(cr + i) : 1.f;
+  }
   const float *gl = a.topk_logit + (size_t)r * b * a.K;
   const int32_t *gt = a.topk_tok + (size_t)r * b * a.K;
   const double *gs = a.lse + (size_t)r * b;
@@ -206,12 +216,19 @@ __device__ __forceinline__ bool stage_request(const TreeArgs &a, int r, const Tr
       }
     }
   }
-  const float *cr = a.cost + (a.cost_per_request ? (size_t)r * (a.n_max + 1) : 0);
   bool bad = false;
-  for (int i = tid; i <= a.n_max; i += nt) {
-    const float c = __ldg(cr + i);  // the cost table is never written by this grid
+#pragma unroll
+  for (int k = 0; k < kCv; ++k) {
+    const int i = tid + k * nt;
+    if (i <= a.n_max) {
+      t.C[i] = cv[k];
+      if (i >= 1) bad |= !(cv[k] > 0.f) || isinf(cv[k]);
+    }
+  }
+  for (int i = tid + kCv * nt; i <= a.n_max; i += nt) {
+    const float c = __ldg(cr + i);
     t.C[i] = c;
-    if (i >= 1) bad |= !(c > 0.f) || isinf(c);
+    bad |= !(c > 0.f) || isinf(c);
   }
   for (int w = tid; w < a.W; w += nt) t.mask[w] = w == 0 ? 1u : 0u;
   return bad;
