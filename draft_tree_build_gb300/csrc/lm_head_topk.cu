@@ -617,9 +617,10 @@ __global__ void __launch_bounds__(kLT, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bs.acc_empty[buf]);
-      // later tiles: publish and read the bound after each of the first four
-      // tiles, then after every fourth (it moves little once it is high)
-      if (live && J > 0 && t > 0 && (t < 4 || (t & 3) == 3)) {
+      // later tiles: publish and read the bound after tiles 1, 3, 7 and 15
+      // (each read is a round trip to L2 in the epilogue's path; after
+      // every tile: 608 against ~560 us)
+      if (live && J > 0 && t > 0 && (t & (t + 1)) == 0) {
         publish();
         const uint64_t x = read_bound();
         lb = x > lb ? x : lb;
